@@ -34,8 +34,9 @@
  *    u_acc from word 0 and u_smp from word 1, u = ((w >> 8) + 0.5) * 2^-24.
  *  - inverse CDF in ascending token order: smallest j with C_j > u * sum(w).
  *  - near ties (reported, not hidden): |u_acc - ratio| < 1e-6 for a decision that
- *    matters (its parent lies on an accepted path), or u*sum(w) within 1e-6*sum(w) of
- *    a CDF boundary around the chosen token, or sum(w) == 0 (then sample from p).
+ *    matters (its parent lies on an accepted path), or u*sum(w) within 1e-6 of a CDF
+ *    boundary around the chosen token (w is in probability units: p and q are
+ *    normalised, so the window is absolute), or sum(w) == 0 (then sample from p).
  *
  * Build: gcc -O2 -fPIC -shared -fopenmp -o liboracle.so oracle.c -lm
  */
@@ -298,11 +299,11 @@ static void orc_load_row(const void *base, int dtype, size_t row, int V, double 
 }
 
 /* Inverse CDF in ascending token order: smallest j with C_j > u * sum(w).  Returns
- * the token; *near is set when u*sum(w) lies within 1e-6*sum(w) of C_{j-1} or C_j. */
+ * the token; *near is set when u*sum(w) lies within 1e-6 of C_{j-1} or C_j. */
 static int orc_inverse_cdf(const double *w, int V, double u, int *near) {
   double total = 0.0;
   for (int j = 0; j < V; ++j) total += w[j];
-  double t = u * total, c = 0.0, tol = ORC_NEAR_TIE * total;
+  double t = u * total, c = 0.0, tol = ORC_NEAR_TIE;
   int last_pos = -1;
   for (int j = 0; j < V; ++j) {
     if (w[j] <= 0.0) continue;
