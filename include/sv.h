@@ -1,0 +1,194 @@
+/*
+ * sv.h -- C ABI of the GB300 (sm_103a) verify step of speculative decoding.
+ *
+ * One verify step = tree attention of the flattened candidate tree against the KV
+ * prefix (sv_tree_attention), token acceptance over the vocabulary (sv_accept_chain /
+ * sv_accept_tree) and the KV commit of the accepted path (sv_commit_kv).
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor argument is caller-owned DEVICE memory, dense row-major in the layout
+ *    given next to it, 16-byte aligned.  The library never allocates device memory:
+ *    scratch comes from a caller workspace sized by the matching *_workspace_size().
+ *  - `parent` arguments are HOST arrays: the candidate tree is shared by all sequences
+ *    of the batch (a static Medusa tree or a chain), BFS ordered: parent[0] = -1 and
+ *    0 <= parent[i] < i, at most SV_MAX_TREE_NODES nodes.  They are validated and
+ *    copied at the call, so the host array may be reused as soon as the call returns.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only enqueue
+ *    work and return without synchronising.
+ *  - Arguments are validated on the host before anything is launched; a failed check
+ *    returns SV_ERR_INVALID_ARG / SV_ERR_UNSUPPORTED / SV_ERR_WORKSPACE and launches
+ *    nothing.  A launch failure returns SV_ERR_CUDA.  sv_last_error() gives the
+ *    message of the last failure in the calling thread.
+ *  - Data-dependent problems found on the device (a token id outside [0,V), a block
+ *    id outside the pool, a prefix longer than the cache, a draft with q(x) = 0) never
+ *    trap: the kernel skips the offending access, ORs an SV_DEV_* bit into a sticky
+ *    device status word and carries on.  Read (and clear) it with
+ *    sv_read_device_status().
+ */
+#ifndef SV_H
+#define SV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t sv_status;
+#define SV_OK 0
+#define SV_ERR_INVALID_ARG 1 /* bad pointer, size, tree, temperature or top-k */
+#define SV_ERR_UNSUPPORTED 2 /* valid, but not a compiled shape (dtype, head dim, N) */
+#define SV_ERR_WORKSPACE 3   /* workspace missing or smaller than *_workspace_size() */
+#define SV_ERR_CUDA 4        /* a CUDA call or kernel launch failed */
+
+/* Bits of the device status word. */
+#define SV_DEV_BAD_TOKEN 0x1u      /* a candidate token id outside [0, V) (rejected) */
+#define SV_DEV_BAD_BLOCK 0x2u      /* a block-table entry outside the pool (skipped) */
+#define SV_DEV_BAD_PREFIX 0x4u     /* prefix_len < 0 or beyond the cache (clamped) */
+#define SV_DEV_ZERO_DRAFT_PROB 0x8u /* a draft with q(x) = 0: ratio taken as +inf/0 */
+
+#define SV_MAX_TREE_NODES 64 /* one 64-bit ancestor word per node */
+#define SV_MAX_TOP_K 1024
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+typedef enum { SV_GREEDY = 0, SV_EXACT = 1 } sv_mode;
+/* How the draft distribution q is given: as float32 probabilities used as they are,
+ * or as draft logits (dtype of the target logits) to which the same temperature and
+ * top-k are applied as to the target. */
+typedef enum { SV_Q_PROBS_F32 = 0, SV_Q_LOGITS = 1 } sv_q_kind;
+
+/* The KV prefix cache of one attention layer.
+ *  contiguous (block_table == NULL): k, v are [B, Lmax, Hkv, D]; sequence b's prefix
+ *    occupies positions [0, prefix_len[b]).
+ *  paged (block_table != NULL): k, v are a pool [num_blocks, block_size, Hkv, D];
+ *    position p of sequence b lives in block block_table[b*max_blocks + p/block_size],
+ *    row p % block_size.
+ * prefix_len [B] is read by attention and updated in place by sv_commit_kv. */
+typedef struct {
+  void *k;
+  void *v;
+  int32_t *prefix_len;
+  const int32_t *block_table;
+  int32_t Lmax;
+  int32_t block_size;
+  int32_t max_blocks;
+  int32_t num_blocks;
+} sv_kv_cache;
+
+/* ------------------------------------------------------------------ attention */
+
+/* Tree attention (pages: "推测解码技术详解", section "Tree Attention验证" -- the flattened
+ * candidate tree and its ancestor mask; lpnh.cn Medusa walkthrough section 3.2 -- a
+ * node's context is its root path; qwbw.cn section 3.1.2 -- the prefix KV is reused
+ * and only the candidates' KV is new).
+ * For every sequence b, tree node n and query head h, with KV head g = h / (Hq/Hkv):
+ *   keys  = prefix positions [0, prefix_len[b])  U  tree nodes j on n's root path,
+ *   out   = softmax(scale * q . K^T) V over those keys.
+ * q [B,N,Hq,D]; k_tree, v_tree [B,N,Hkv,D] (the candidates' fresh K/V, root = node 0);
+ * cache as above (read only); parent [N] host; out [B,N,Hq,D].
+ * dt: SV_BF16 (fp32 accumulation, bf16 output) or SV_F32 (fp32 throughout).
+ * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= N <= 64; block_size % 16 == 0 for
+ * paged caches.  Workspace: sv_tree_attention_workspace_size() bytes (may be 0). */
+sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, const void *q,
+                            const void *k_tree, const void *v_tree, sv_kv_cache cache,
+                            const int32_t *parent, float scale, void *out, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/* Workspace bytes sv_tree_attention needs for these sizes; max_prefix is the largest
+ * prefix the cache can hold (Lmax, or max_blocks*block_size when paged). */
+size_t sv_tree_attention_workspace_size(sv_dtype dt, int B, int N, int Hq, int Hkv, int D,
+                                        int max_prefix);
+
+/* ----------------------------------------------------------------- acceptance */
+
+/* Chain acceptance (hncyxsy.com sections 2.1-2.2; jennyma11 blog "先弄清无损验证"):
+ * draft i (1..gamma) is accepted with probability min(1, p_{i-1}(x_i)/q_i(x_i)) using
+ * u_acc(b, i); at the first rejection the next token is sampled from
+ * norm([p_{i-1} - q_i]+), if all pass the bonus is sampled from p_gamma, both with
+ * u_smp(b, node) by inverse CDF in ascending token order.  p and q are the effective
+ * distributions: logits / temperature, top-k (ties keep lower ids), softmax.  Greedy
+ * (or temperature == 0): accept while x_i == argmax row i-1 (lowest id on ties) and
+ * emit that row's argmax.
+ * Uniforms: Philox4x32-10 with key (seed_lo, seed_hi) and counter (node, b, round_lo,
+ * round_hi); u_acc = word0, u_smp = word1, u = ((w >> 8) + 0.5) * 2^-24.
+ * target_logits [B,gamma+1,V] (row i = target distribution after node i); q
+ * [B,gamma,V] (row i-1 = draft distribution of draft i; unused in greedy mode, may be
+ * NULL); draft_tokens [B,gamma] int32.
+ * Outputs: out_tokens [B,gamma+1] (accepted drafts then the sampled token, -1 after),
+ * out_num_emitted [B] (= accepted + 1), out_num_accepted [B], out_near_ties [B] (count
+ * of decisions with |u_acc - ratio| < 1e-6 and samples within 1e-6 of a CDF
+ * boundary: reported, not hidden; may be NULL).
+ * logit_dt: SV_BF16 or SV_F32.  V % 8 == 0, 1 <= gamma <= 63, 0 <= top_k <= 1024
+ * (0 = off).  Workspace: sv_accept_workspace_size(B, gamma+1, V, gamma). */
+sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
+                          const void *target_logits, const void *q, sv_q_kind q_kind,
+                          const int32_t *draft_tokens, float temperature, int top_k,
+                          uint64_t seed, uint64_t round, int32_t *out_tokens,
+                          int32_t *out_num_emitted, int32_t *out_num_accepted,
+                          uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/* Tree acceptance (qwbw.cn section 2.3 -- keep the longest correct path; jennyma11
+ * blog section "Medusa" -- only the contiguous accepted prefix from the root is
+ * committed).  Every non-root node c (parent a, depth d) is decided independently:
+ * accept iff u_acc(b, c) < p_a(x_c) / q_d(x_c) (greedy: x_c == argmax p_a).  The chosen
+ * node a* is the deepest node whose whole root path is accepted (ties: smallest row).
+ * The emitted tokens are those of the path nodes 1..a*, then a token sampled with
+ * u_smp(b, a*) from norm([p_{a*} - q_{d(a*)+1}]+) if a* has children, else from p_{a*}.
+ * parent [N] host; node_tokens [B,N] (column 0, the root, is not read);
+ * target_logits [B,N,V]; q [B,Dq,V] with row d-1 = depth d (Dq >= tree depth).
+ * Outputs (Dmax = tree depth): out_path_nodes [B,Dmax+1] (root..a*, -1 after),
+ * out_tokens [B,Dmax+1], out_num_emitted [B], out_num_accepted [B], out_near_ties [B].
+ * Workspace: sv_accept_workspace_size(B, N, V, Dq). */
+sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
+                         const int32_t *parent, const int32_t *node_tokens,
+                         const void *target_logits, const void *q, sv_q_kind q_kind, int Dq,
+                         float temperature, int top_k, uint64_t seed, uint64_t round,
+                         int32_t *out_path_nodes, int32_t *out_tokens,
+                         int32_t *out_num_emitted, int32_t *out_num_accepted,
+                         uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* Workspace bytes for sv_accept_chain (N = gamma+1, Dq = gamma) / sv_accept_tree. */
+size_t sv_accept_workspace_size(int B, int N, int V, int Dq);
+
+/* --------------------------------------------------------------------- commit */
+
+/* KV commit (qwbw.cn sections 3.1.4 and 6.3; hncyxsy.com section 4.3: keep the KV of
+ * accepted tokens, roll the rest back by the valid length).  For each sequence b the
+ * tree K/V rows of path_nodes[b, 0..num_accepted[b]] (root first, depth order) are
+ * copied to cache positions prefix_len[b] + i, then prefix_len[b] += num_accepted[b]+1.
+ * Rejected rows are simply not copied; nothing is freed (the caller owns the pages,
+ * which must already cover the new positions).
+ * k_tree, v_tree [B,N,Hkv,D]; path_nodes [B,path_stride] int32; num_accepted [B].
+ * dt: element type of the K/V rows (SV_BF16 or SV_F32). */
+sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_tree,
+                       const void *v_tree, const int32_t *path_nodes, int path_stride,
+                       const int32_t *num_accepted, sv_kv_cache cache, void *stream);
+
+/* ---------------------------------------------------------------- tree helper */
+
+/* Host helper: validate a tree and derive per node its ancestor bitmask (bit j set
+ * iff j is the node or one of its ancestors -- the rows of the tree-attention mask)
+ * and its depth; position id of node n = prefix_len + depth[n].  anc/depth may be
+ * NULL.  Returns SV_ERR_INVALID_ARG for an invalid tree. */
+sv_status sv_tree_prepare(int N, const int32_t *parent, uint64_t *anc, int32_t *depth);
+
+/* ---------------------------------------------------------- status and errors */
+
+/* Copy the sticky device status word (SV_DEV_* bits) to *host_out and clear it.
+ * Synchronises `stream`. */
+sv_status sv_read_device_status(uint32_t *host_out, void *stream);
+
+/* Message of the last failed call in this thread ("" if none). */
+const char *sv_last_error(void);
+
+/* Library version string. */
+const char *sv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SV_H */

@@ -1,0 +1,399 @@
+// C ABI of the verify step: argument validation, planning and launches.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "sv_common.cuh"
+#include "sv_internal.h"
+
+#define SV_VERSION_STRING "sv 0.1.0 (sm_103a)"
+
+// Sticky device status word (SV_DEV_* bits); kernels get its address as a parameter.
+__device__ unsigned int g_sv_status;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+sv_status fail(sv_status code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+sv_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(SV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+// Device address of the status word on the current device (looked up once per device).
+unsigned int *status_word() {
+  static unsigned int *addr[kMaxDevices] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sv_status) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned int *>(p);
+  }
+  return addr[dev];
+}
+
+int num_sms() {
+  static int sms[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return 152;
+  }
+  if (!sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 152;
+    }
+    sms[dev] = n;
+  }
+  return sms[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validate a BFS-ordered parent array and fill the tree descriptor.
+sv_status make_tree(int N, const int32_t *parent, sv::Tree *t) {
+  if (parent == nullptr) return fail(SV_ERR_INVALID_ARG, "parent is NULL");
+  if (N < 1 || N > SV_MAX_TREE_NODES)
+    return fail(N < 1 ? SV_ERR_INVALID_ARG : SV_ERR_UNSUPPORTED,
+                "tree has %d nodes (supported 1..%d)", N, SV_MAX_TREE_NODES);
+  if (parent[0] != -1) return fail(SV_ERR_INVALID_ARG, "parent[0] must be -1 (the root)");
+  memset(t, 0, sizeof *t);
+  t->N = N;
+  t->parent[0] = -1;
+  for (int i = 1; i < N; ++i) {
+    if (parent[i] < 0 || parent[i] >= i)
+      return fail(SV_ERR_INVALID_ARG, "parent[%d] = %d is not in [0, %d)", i, parent[i], i);
+    t->parent[i] = (int8_t)parent[i];
+    t->depth[i] = (int8_t)(t->depth[parent[i]] + 1);
+    t->has_child[parent[i]] = 1;
+    if (t->depth[i] > t->Dmax) t->Dmax = t->depth[i];
+  }
+  for (int i = N; i < SV_MAX_TREE_NODES; ++i) t->parent[i] = -1;
+  return SV_OK;
+}
+
+int max_prefix_of(const sv_kv_cache &c) {
+  return c.block_table ? c.max_blocks * c.block_size : c.Lmax;
+}
+
+sv_status check_cache(const sv_kv_cache &c, bool writable) {
+  (void)writable;
+  if (!c.k || !c.v || !c.prefix_len) return fail(SV_ERR_INVALID_ARG, "cache k, v or prefix_len is NULL");
+  if (!aligned16(c.k) || !aligned16(c.v)) return fail(SV_ERR_INVALID_ARG, "cache k/v not 16-byte aligned");
+  if (c.block_table) {
+    if (c.block_size < 1 || c.max_blocks < 1 || c.num_blocks < 1)
+      return fail(SV_ERR_INVALID_ARG, "paged cache needs block_size, max_blocks, num_blocks >= 1");
+  } else if (c.Lmax < 0) {
+    return fail(SV_ERR_INVALID_ARG, "Lmax < 0");
+  }
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *sv_last_error(void) { return g_last_error.c_str(); }
+
+const char *sv_version(void) { return SV_VERSION_STRING; }
+
+sv_status sv_tree_prepare(int N, const int32_t *parent, uint64_t *anc, int32_t *depth) {
+  sv::Tree t;
+  sv_status st = make_tree(N, parent, &t);
+  if (st != SV_OK) return st;
+  for (int n = 0; n < N; ++n) {
+    uint64_t m = 0;
+    for (int a = n; a >= 0; a = t.parent[a]) m |= 1ull << a;
+    if (anc) anc[n] = m;
+    if (depth) depth[n] = t.depth[n];
+  }
+  return SV_OK;
+}
+
+sv_status sv_read_device_status(uint32_t *host_out, void *stream) {
+  if (!host_out) return fail(SV_ERR_INVALID_ARG, "host_out is NULL");
+  unsigned int *w = status_word();
+  if (!w) return fail(SV_ERR_CUDA, "device status word unavailable");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, w, sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w, 0, sizeof v, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  *host_out = v;
+  return SV_OK;
+}
+
+// ------------------------------------------------------------------ attention
+
+size_t sv_tree_attention_workspace_size(sv_dtype dt, int B, int N, int Hq, int Hkv, int D,
+                                        int max_prefix) {
+  if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || max_prefix < 0)
+    return 0;
+  return sv::attn_plan(dt, B, N, Hq, Hkv, D, max_prefix, num_sms()).ws_bytes;
+}
+
+sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, const void *q,
+                            const void *k_tree, const void *v_tree, sv_kv_cache cache,
+                            const int32_t *parent, float scale, void *out, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+  if (dt != SV_F32 && dt != SV_BF16) return fail(SV_ERR_UNSUPPORTED, "dtype %d not supported", (int)dt);
+  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+    return fail(SV_ERR_INVALID_ARG, "bad sizes B=%d Hq=%d Hkv=%d", B, Hq, Hkv);
+  if (D != 64 && D != 128) return fail(SV_ERR_UNSUPPORTED, "head dim %d (supported 64, 128)", D);
+  sv::Tree tree;
+  sv_status st = make_tree(N, parent, &tree);
+  if (st != SV_OK) return st;
+  if (!q || !k_tree || !v_tree || !out) return fail(SV_ERR_INVALID_ARG, "q, k_tree, v_tree or out is NULL");
+  if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(out))
+    return fail(SV_ERR_INVALID_ARG, "q, k_tree, v_tree and out must be 16-byte aligned");
+  if ((st = check_cache(cache, false)) != SV_OK) return st;
+  if (!std::isfinite(scale)) return fail(SV_ERR_INVALID_ARG, "scale is not finite");
+  if (B == 0) return SV_OK;
+  const int max_prefix = max_prefix_of(cache);
+  const sv::AttnPlan plan = sv::attn_plan(dt, B, N, Hq, Hkv, D, max_prefix, num_sms());
+  if (plan.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < plan.ws_bytes)
+      return fail(SV_ERR_WORKSPACE, "attention workspace %zu bytes, need %zu", workspace_bytes,
+                  plan.ws_bytes);
+    if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  }
+  unsigned int *status = status_word();
+  if (!status) return fail(SV_ERR_CUDA, "no CUDA device");
+
+  sv::AttnParams p{};
+  p.q = q;
+  p.k_tree = k_tree;
+  p.v_tree = v_tree;
+  p.cache_k = cache.k;
+  p.cache_v = cache.v;
+  p.prefix_len = cache.prefix_len;
+  p.block_table = cache.block_table;
+  p.out = out;
+  p.status = status;
+  p.B = B;
+  p.N = N;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.D = D;
+  p.Lmax = cache.Lmax;
+  p.block_size = cache.block_size;
+  p.max_blocks = cache.max_blocks;
+  p.num_blocks = cache.num_blocks;
+  p.cap = max_prefix;
+  p.M = N * p.G;
+  p.m_tiles = plan.m_tiles;
+  p.Mpad = plan.Mpad;
+  p.splits = plan.splits;
+  p.chunk = plan.chunk;
+  p.scale = scale;
+  p.scale_log2 = scale * sv::kLog2e;
+  p.tree = tree;
+  if (plan.ws_bytes > 0) {
+    p.part_o = static_cast<float *>(workspace);
+    p.part_ml = p.part_o + (size_t)B * Hkv * plan.splits * plan.Mpad * D;
+  }
+  cudaError_t e = sv::launch_attention(dt, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "tree attention launch");
+  return SV_OK;
+}
+
+// ----------------------------------------------------------------- acceptance
+
+size_t sv_accept_workspace_size(int B, int N, int V, int Dq) {
+  (void)V;
+  if (B <= 0 || N <= 0 || Dq < 0) return 0;
+  return sv::accept_ws_bytes(B, N, Dq);
+}
+
+namespace {
+
+sv_status accept_common(sv_mode mode, sv_dtype dt, int B, int V, const void *target,
+                        const void *q, sv_q_kind q_kind, float temperature, int top_k,
+                        int32_t *out_tokens, int32_t *out_num_emitted,
+                        int32_t *out_num_accepted, bool *greedy) {
+  if (mode != SV_GREEDY && mode != SV_EXACT) return fail(SV_ERR_INVALID_ARG, "mode %d", (int)mode);
+  if (dt != SV_F32 && dt != SV_BF16) return fail(SV_ERR_UNSUPPORTED, "logit dtype %d", (int)dt);
+  if (B < 0) return fail(SV_ERR_INVALID_ARG, "B < 0");
+  if (V < 8 || V % 8 != 0) return fail(SV_ERR_UNSUPPORTED, "V = %d must be a positive multiple of 8", V);
+  if (!(temperature >= 0.f) || !std::isfinite(temperature))
+    return fail(SV_ERR_INVALID_ARG, "temperature must be finite and >= 0");
+  if (top_k < 0 || top_k > SV_MAX_TOP_K)
+    return fail(SV_ERR_INVALID_ARG, "top_k = %d (0..%d)", top_k, SV_MAX_TOP_K);
+  *greedy = mode == SV_GREEDY || temperature == 0.f;
+  if (!target) return fail(SV_ERR_INVALID_ARG, "target_logits is NULL");
+  if (!aligned16(target)) return fail(SV_ERR_INVALID_ARG, "target_logits not 16-byte aligned");
+  if (!*greedy) {
+    if (q_kind != SV_Q_PROBS_F32 && q_kind != SV_Q_LOGITS)
+      return fail(SV_ERR_INVALID_ARG, "q_kind %d", (int)q_kind);
+    if (!q) return fail(SV_ERR_INVALID_ARG, "q is NULL in exact mode");
+    if (!aligned16(q)) return fail(SV_ERR_INVALID_ARG, "q not 16-byte aligned");
+  }
+  if (!out_tokens || !out_num_emitted || !out_num_accepted)
+    return fail(SV_ERR_INVALID_ARG, "an output pointer is NULL");
+  return SV_OK;
+}
+
+sv_status accept_launch(sv_dtype dt, sv::AcceptParams &p, bool greedy, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+  const size_t need = sv::accept_ws_bytes(p.B, p.N, p.Dq);
+  if (!workspace || workspace_bytes < need)
+    return fail(SV_ERR_WORKSPACE, "acceptance workspace %zu bytes, need %zu", workspace_bytes, need);
+  if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  p.status = status_word();
+  if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
+  p.mode = greedy ? SV_GREEDY : SV_EXACT;
+  p.c_log2 = greedy ? 0.f : (float)(1.4426950408889634 / (double)p.temperature);
+  if (p.top_k >= p.V) p.top_k = 0;
+  p.stats = static_cast<sv::RowStat *>(workspace);
+  if (p.B == 0) return SV_OK;
+  cudaError_t e = sv::launch_accept(dt, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "acceptance launch");
+  return SV_OK;
+}
+
+}  // namespace
+
+sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
+                          const void *target_logits, const void *q, sv_q_kind q_kind,
+                          const int32_t *draft_tokens, float temperature, int top_k,
+                          uint64_t seed, uint64_t round, int32_t *out_tokens,
+                          int32_t *out_num_emitted, int32_t *out_num_accepted,
+                          uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+  bool greedy = false;
+  sv_status st = accept_common(mode, logit_dt, B, V, target_logits, q, q_kind, temperature, top_k,
+                               out_tokens, out_num_emitted, out_num_accepted, &greedy);
+  if (st != SV_OK) return st;
+  if (gamma < 1 || gamma >= SV_MAX_TREE_NODES)
+    return fail(SV_ERR_UNSUPPORTED, "gamma = %d (supported 1..%d)", gamma, SV_MAX_TREE_NODES - 1);
+  if (!draft_tokens) return fail(SV_ERR_INVALID_ARG, "draft_tokens is NULL");
+  int32_t parent[SV_MAX_TREE_NODES];
+  for (int i = 0; i <= gamma; ++i) parent[i] = i - 1;
+  sv::AcceptParams p{};
+  if ((st = make_tree(gamma + 1, parent, &p.tree)) != SV_OK) return st;
+  p.B = B;
+  p.N = gamma + 1;
+  p.V = V;
+  p.Dq = gamma;
+  p.q_kind = q_kind;
+  p.target = target_logits;
+  p.q = q;
+  p.tokens = draft_tokens;
+  p.tok_stride = gamma;
+  p.tok_offset = 1;
+  p.temperature = temperature;
+  p.top_k = top_k;
+  p.seed = seed;
+  p.round = round;
+  p.out_path_nodes = nullptr;
+  p.out_tokens = out_tokens;
+  p.out_num_emitted = out_num_emitted;
+  p.out_num_accepted = out_num_accepted;
+  p.out_near_ties = out_near_ties;
+  return accept_launch(logit_dt, p, greedy, workspace, workspace_bytes, stream);
+}
+
+sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
+                         const int32_t *parent, const int32_t *node_tokens,
+                         const void *target_logits, const void *q, sv_q_kind q_kind, int Dq,
+                         float temperature, int top_k, uint64_t seed, uint64_t round,
+                         int32_t *out_path_nodes, int32_t *out_tokens,
+                         int32_t *out_num_emitted, int32_t *out_num_accepted,
+                         uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+  bool greedy = false;
+  sv_status st = accept_common(mode, logit_dt, B, V, target_logits, q, q_kind, temperature, top_k,
+                               out_tokens, out_num_emitted, out_num_accepted, &greedy);
+  if (st != SV_OK) return st;
+  sv::AcceptParams p{};
+  if ((st = make_tree(N, parent, &p.tree)) != SV_OK) return st;
+  if (!node_tokens) return fail(SV_ERR_INVALID_ARG, "node_tokens is NULL");
+  if (!out_path_nodes) return fail(SV_ERR_INVALID_ARG, "out_path_nodes is NULL");
+  if (!greedy && Dq < p.tree.Dmax)
+    return fail(SV_ERR_INVALID_ARG, "q has %d depth rows, the tree is %d deep", Dq, p.tree.Dmax);
+  if (Dq < 0) return fail(SV_ERR_INVALID_ARG, "Dq < 0");
+  p.B = B;
+  p.N = N;
+  p.V = V;
+  p.Dq = greedy ? 0 : Dq;
+  p.q_kind = q_kind;
+  p.target = target_logits;
+  p.q = q;
+  p.tokens = node_tokens;
+  p.tok_stride = N;
+  p.tok_offset = 0;
+  p.temperature = temperature;
+  p.top_k = top_k;
+  p.seed = seed;
+  p.round = round;
+  p.out_path_nodes = out_path_nodes;
+  p.out_tokens = out_tokens;
+  p.out_num_emitted = out_num_emitted;
+  p.out_num_accepted = out_num_accepted;
+  p.out_near_ties = out_near_ties;
+  return accept_launch(logit_dt, p, greedy, workspace, workspace_bytes, stream);
+}
+
+// --------------------------------------------------------------------- commit
+
+sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_tree,
+                       const void *v_tree, const int32_t *path_nodes, int path_stride,
+                       const int32_t *num_accepted, sv_kv_cache cache, void *stream) {
+  if (dt != SV_F32 && dt != SV_BF16) return fail(SV_ERR_UNSUPPORTED, "dtype %d", (int)dt);
+  if (B < 0 || N < 1 || N > SV_MAX_TREE_NODES || Hkv < 1 || D < 1 || path_stride < 1)
+    return fail(SV_ERR_INVALID_ARG, "bad sizes B=%d N=%d Hkv=%d D=%d path_stride=%d", B, N, Hkv, D,
+                path_stride);
+  const int esize = dt == SV_F32 ? 4 : 2;
+  if (((size_t)Hkv * D * esize) % 16 != 0)
+    return fail(SV_ERR_UNSUPPORTED, "Hkv*D*elem bytes must be a multiple of 16");
+  if (!k_tree || !v_tree || !path_nodes || !num_accepted)
+    return fail(SV_ERR_INVALID_ARG, "k_tree, v_tree, path_nodes or num_accepted is NULL");
+  if (!aligned16(k_tree) || !aligned16(v_tree)) return fail(SV_ERR_INVALID_ARG, "k_tree/v_tree not 16-byte aligned");
+  sv_status st = check_cache(cache, true);
+  if (st != SV_OK) return st;
+  if (B == 0) return SV_OK;
+  sv::CommitParams p{};
+  p.k_tree = k_tree;
+  p.v_tree = v_tree;
+  p.path_nodes = path_nodes;
+  p.path_stride = path_stride;
+  p.num_accepted = num_accepted;
+  p.cache_k = cache.k;
+  p.cache_v = cache.v;
+  p.prefix_len = cache.prefix_len;
+  p.block_table = cache.block_table;
+  p.B = B;
+  p.N = N;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.esize = esize;
+  p.Lmax = cache.Lmax;
+  p.block_size = cache.block_size;
+  p.max_blocks = cache.max_blocks;
+  p.num_blocks = cache.num_blocks;
+  p.status = status_word();
+  if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
+  cudaError_t e = sv::launch_commit(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+  return SV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,167 @@
+// Device helpers shared by the verify-step kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sv.h"
+
+namespace sv {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void set_status(unsigned int *status, unsigned int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// ------------------------------------------------------------ element access
+
+// Widen 8 packed bf16 (one 16-byte vector) to float; element i at bits [16i, 16i+16).
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float f[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<bf16> {
+  static constexpr int kVec = 8;  // elements per 16-byte vector
+  __device__ static __forceinline__ void unpack(const uint4 &v, float f[8]) { unpack_bf16x8(v, f); }
+  __device__ static __forceinline__ float load(const bf16 *p) { return __bfloat162float(*p); }
+  // Order-preserving integer key: a larger key is a larger value.
+  __device__ static __forceinline__ uint32_t key(float f) {
+    uint32_t h = __float_as_uint(f) >> 16;
+    return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+  }
+  static constexpr int kKeyBits = 16;
+};
+
+template <>
+struct Elem<float> {
+  static constexpr int kVec = 4;
+  __device__ static __forceinline__ void unpack(const uint4 &v, float f[4]) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ static __forceinline__ float load(const float *p) { return *p; }
+  __device__ static __forceinline__ uint32_t key(float f) {
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  }
+  static constexpr int kKeyBits = 32;
+};
+
+// ------------------------------------------------------------------ Philox
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two 32x32->64
+// multiplies by the Philox multipliers, mixing with the other two words and the key;
+// the key advances by the two Weyl increments after every round.
+__device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t a = c[0], b = c[2];
+    const uint32_t hi0 = __umulhi(0xD2511F53u, a), lo0 = 0xD2511F53u * a;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, b), lo1 = 0xCD9E8D57u * b;
+    const uint32_t n0 = hi1 ^ c[1] ^ k0;
+    const uint32_t n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+}
+
+// Uniforms of (sequence b, node c): u_acc from word 0, u_smp from word 1, each
+// ((w >> 8) + 0.5) * 2^-24, exact in double.
+__device__ __forceinline__ void verify_uniforms(uint64_t seed, uint64_t round, int b, int c,
+                                                double *u_acc, double *u_smp) {
+  uint32_t ctr[4] = {(uint32_t)c, (uint32_t)b, (uint32_t)round, (uint32_t)(round >> 32)};
+  philox4x32_10(ctr, (uint32_t)seed, (uint32_t)(seed >> 32));
+  *u_acc = ((double)(ctr[0] >> 8) + 0.5) * (1.0 / 16777216.0);
+  *u_smp = ((double)(ctr[1] >> 8) + 0.5) * (1.0 / 16777216.0);
+}
+
+// --------------------------------------------------------- warp reductions
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Kahan-compensated accumulation.
+struct KahanF {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float y = x - c;
+    const float t = s + y;
+    c = (t - s) - y;
+    s = t;
+  }
+  __device__ __forceinline__ double value() const { return (double)s - (double)c; }
+};
+
+// ------------------------------------------------------ async copies, MMA
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// 16-byte cp.async; when !valid nothing is read and the destination is zero-filled.
+__device__ __forceinline__ void cp_async_16(void *smem, const void *gmem, bool valid) {
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)),
+               "l"(gmem), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t r[4], const void *p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t r[4], const void *p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+}  // namespace sv

@@ -1,0 +1,103 @@
+// Internal launch parameters of the verify-step kernels (host and device).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "sv.h"
+
+namespace sv {
+
+constexpr int kMaxNodes = SV_MAX_TREE_NODES;
+
+// The candidate tree, passed by value: parent (BFS order, parent[0] = -1) and depth.
+struct Tree {
+  int N;
+  int Dmax;
+  int8_t parent[kMaxNodes];
+  int8_t depth[kMaxNodes];
+  int8_t has_child[kMaxNodes];
+};
+
+// ---------------------------------------------------------------- attention
+
+struct AttnParams {
+  const void *q, *k_tree, *v_tree;  // [B,N,Hq,D], [B,N,Hkv,D] x2
+  const void *cache_k, *cache_v;    // [B,Lmax,Hkv,D] or [num_blocks,block_size,Hkv,D]
+  const int32_t *prefix_len;        // [B]
+  const int32_t *block_table;       // [B,max_blocks] or NULL
+  void *out;                        // [B,N,Hq,D]
+  float *part_o;                    // [B,Hkv,S,Mpad,D] unnormalised partial outputs
+  float *part_ml;                   // [B,Hkv,S,Mpad,2] running max (log2 units) and sum
+  unsigned int *status;
+  int B, N, Hq, Hkv, G, D;
+  int Lmax, block_size, max_blocks, num_blocks, cap;  // cap = largest valid prefix
+  int M, m_tiles, Mpad;  // query rows per (b, kv head) = N*G, tiles of 64 rows
+  int splits, chunk;     // prefix split: split s covers [s*chunk, (s+1)*chunk)
+  float scale_log2;      // softmax scale * log2(e)
+  float scale;
+  Tree tree;
+};
+
+struct AttnPlan {
+  int m_tiles, Mpad, splits, chunk;
+  size_t ws_bytes;
+};
+
+AttnPlan attn_plan(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, int max_prefix,
+                   int num_sms);
+cudaError_t launch_attention(sv_dtype dt, const AttnParams &p, cudaStream_t s);
+
+// --------------------------------------------------------------- acceptance
+
+struct RowStat {
+  float zmax;     // largest logit of the row
+  int32_t argmax; // its lowest index
+  uint32_t key_k; // top-k threshold key (kept: key > key_k, or == key_k and idx <= idx_k)
+  int32_t idx_k;
+  double S;       // sum over kept entries of exp((z - zmax) / T)
+};
+
+struct AcceptParams {
+  int mode;        // SV_GREEDY / SV_EXACT
+  int B, N, V, Dq;
+  int q_kind;      // SV_Q_PROBS_F32 / SV_Q_LOGITS
+  const void *target;        // [B,N,V]
+  const void *q;             // [B,Dq,V]
+  const int32_t *tokens;     // token of node c of seq b = tokens[b*tok_stride + c - tok_offset]
+  int tok_stride, tok_offset;
+  float temperature;
+  float c_log2;              // log2(e) / T
+  int top_k;                 // 0 = off
+  uint64_t seed, round;
+  RowStat *stats;            // [B*N + B*Dq]
+  int32_t *out_path_nodes;   // [B,Dmax+1] or NULL
+  int32_t *out_tokens;       // [B,Dmax+1]
+  int32_t *out_num_emitted, *out_num_accepted;
+  uint32_t *out_near_ties;   // or NULL
+  unsigned int *status;
+  Tree tree;
+};
+
+size_t accept_ws_bytes(int B, int N, int Dq);
+cudaError_t launch_accept(sv_dtype dt, const AcceptParams &p, cudaStream_t s);
+
+// ------------------------------------------------------------------- commit
+
+struct CommitParams {
+  const void *k_tree, *v_tree;
+  const int32_t *path_nodes;
+  int path_stride;
+  const int32_t *num_accepted;
+  void *cache_k, *cache_v;
+  int32_t *prefix_len;
+  const int32_t *block_table;
+  int B, N, Hkv, D, esize;
+  int Lmax, block_size, max_blocks, num_blocks;
+  unsigned int *status;
+};
+
+cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
+
+}  // namespace sv

@@ -1,0 +1,129 @@
+"""The C ABI library loads, exports every symbol include/sv.h declares, and rejects bad
+arguments on the host before any launch (CPU only; no compute call needs a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verify_sv_gb300 as sv
+from speculative_decoding_verify_sv_gb300 import build as svbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    svbuild.build()
+    return sv.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "sv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sv_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("sv_tree_attention", "sv_accept_chain", "sv_accept_tree", "sv_commit_kv",
+              "sv_read_device_status", "sv_last_error", "sv_tree_attention_workspace_size",
+              "sv_accept_workspace_size", "sv_tree_prepare", "sv_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+    assert sv.sv_version().startswith("sv ")
+
+
+def test_tree_prepare_matches_printed_mask(lib):
+    anc, dep = sv.sv_tree_prepare([-1, 0, 0, 1, 1, 2, 2])
+    assert anc == [1, 3, 5, 11, 19, 37, 69]
+    assert dep == [0, 1, 1, 2, 2, 2, 2]
+
+
+@pytest.mark.parametrize("parent", [[0], [-1, 1], [-1, 0, 3], [-1, -1]])
+def test_invalid_trees_are_rejected(lib, parent):
+    with pytest.raises(sv.SVError) as e:
+        sv.sv_tree_prepare(parent)
+    assert e.value.code == sv.SV_ERR_INVALID_ARG
+
+
+def test_too_many_nodes_unsupported(lib):
+    par = (ctypes.c_int32 * 65)(*([-1] + list(range(64))))
+    assert lib.sv_tree_prepare(65, par, None, None) == sv.SV_ERR_UNSUPPORTED
+
+
+def _cache(**kw):
+    c = sv._KVCacheC()
+    c.k = c.v = c.prefix_len = 16
+    c.block_table = None
+    c.Lmax = 128
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_attention_rejects_before_launch(lib):
+    par = (ctypes.c_int32 * 1)(-1)
+    P = ctypes.c_void_p(16)
+    # head dim 96 is not compiled
+    assert lib.sv_tree_attention(1, 1, 1, 4, 4, 96, P, P, P, _cache(), par, 0.1, P, None, 0,
+                                 None) == sv.SV_ERR_UNSUPPORTED
+    # Hq not a multiple of Hkv
+    assert lib.sv_tree_attention(1, 1, 1, 6, 4, 128, P, P, P, _cache(), par, 0.1, P, None, 0,
+                                 None) == sv.SV_ERR_INVALID_ARG
+    # misaligned q
+    assert lib.sv_tree_attention(1, 1, 1, 4, 4, 128, ctypes.c_void_p(18), P, P, _cache(), par,
+                                 0.1, P, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    # NaN scale
+    assert lib.sv_tree_attention(1, 1, 1, 4, 4, 128, P, P, P, _cache(), par, float("nan"), P,
+                                 None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert "scale" in lib.sv_last_error().decode()
+    # missing workspace when the plan needs one (long prefix, small batch -> splits)
+    need = lib.sv_tree_attention_workspace_size(1, 1, 1, 4, 4, 128, 32768)
+    assert need > 0
+    assert lib.sv_tree_attention(1, 1, 1, 4, 4, 128, P, P, P, _cache(Lmax=32768), par, 0.1, P,
+                                 None, 0, None) == sv.SV_ERR_WORKSPACE
+
+
+def test_accept_rejects_before_launch(lib):
+    P = ctypes.c_void_p(16)
+    par = (ctypes.c_int32 * 3)(-1, 0, 0)
+    common = dict(seed=0, round=0)
+    # V not a multiple of 8
+    assert lib.sv_accept_chain(1, 1, 1, 4, 1001, P, P, 1, P, 1.0, 0, 0, 0, P, P, P, P, P, 1 << 20,
+                               None) == sv.SV_ERR_UNSUPPORTED
+    # negative temperature, top_k too large
+    assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, P, 1, P, -1.0, 0, 0, 0, P, P, P, P, P, 1 << 20,
+                               None) == sv.SV_ERR_INVALID_ARG
+    assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, P, 1, P, 1.0, 5000, 0, 0, P, P, P, P, P,
+                               1 << 20, None) == sv.SV_ERR_INVALID_ARG
+    # exact mode needs q
+    assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, None, 1, P, 1.0, 0, 0, 0, P, P, P, P, P,
+                               1 << 20, None) == sv.SV_ERR_INVALID_ARG
+    # q rows must cover the tree depth
+    assert lib.sv_accept_tree(1, 1, 1, 3, 1000, par, P, P, P, 1, 0, 1.0, 0, 0, 0, P, P, P, P, P,
+                              P, 1 << 20, None) == sv.SV_ERR_INVALID_ARG
+    # workspace too small
+    need = lib.sv_accept_workspace_size(2, 3, 1000, 1)
+    assert need > 0
+    assert lib.sv_accept_tree(1, 1, 2, 3, 1000, par, P, P, P, 1, 1, 1.0, 0, 0, 0, P, P, P, P, P,
+                              P, need - 1, None) == sv.SV_ERR_WORKSPACE
+    del common
+
+
+def test_commit_rejects_before_launch(lib):
+    P = ctypes.c_void_p(16)
+    # rows must be whole 16-byte vectors: Hkv*D*2 = 6 bytes
+    assert lib.sv_commit_kv(1, 1, 2, 1, 3, P, P, P, 2, P, _cache(), None) == sv.SV_ERR_UNSUPPORTED
+    assert lib.sv_commit_kv(1, 1, 2, 1, 8, P, P, None, 2, P, _cache(), None) == sv.SV_ERR_INVALID_ARG
+
+
+def test_binding_requires_cuda_tensors(lib):
+    import torch
+    with pytest.raises(TypeError):
+        sv.sv_accept_chain(sv.GREEDY, torch.zeros(1, 2, 8), None, sv.Q_LOGITS,
+                           torch.zeros(1, 1, dtype=torch.int32))

@@ -1,0 +1,191 @@
+"""GPU token acceptance vs the CPU oracle, through the C ABI.
+
+Accepted lengths, paths and emitted token ids must be bit-identical on every sequence
+that neither side reports as a near tie (|u - p/q| < 1e-6 for a decision that
+matters, or a sample within 1e-6 of a CDF boundary); near ties are counted and bounded.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+import oracle
+import speculative_decoding_verify_sv_gb300 as sv
+from speculative_decoding_verify_sv_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare(gpu, ref, keys, max_exempt_frac=0.01):
+    g = {k: v.cpu() for k, v in gpu.items()}
+    exempt = (g["near_ties"] > 0) | (ref["near_ties"] > 0)
+    keep = ~exempt
+    for k in keys:
+        a, b = g[k][keep], ref[k][keep]
+        if not torch.equal(a, b):
+            bad = torch.nonzero((g[k] != ref[k]).reshape(g[k].shape[0], -1).any(1) & keep).flatten()
+            raise AssertionError(f"{k} differs on sequences {bad[:10].tolist()}: "
+                                 f"gpu {g[k][bad[:3]].tolist()} oracle {ref[k][bad[:3]].tolist()}")
+    n_ex = int(exempt.sum())
+    assert n_ex <= max(2, max_exempt_frac * exempt.numel()), f"{n_ex} near-tie sequences"
+    return n_ex
+
+
+def _chain(mode, lg, q_kind=sv.Q_LOGITS, T=1.0, top_k=0, seed=3, rnd=1, q=None):
+    dev = torch.device("cuda")
+    tl = lg["target_logits"].to(dev)
+    qq = (lg["draft_logits"] if q is None else q)
+    qq = None if mode == sv.GREEDY and q is None else qq.to(dev)
+    out = sv.sv_accept_chain(mode, tl, qq, q_kind, lg["draft_tokens"].to(dev), temperature=T,
+                             top_k=top_k, seed=seed, round_=rnd)
+    torch.cuda.synchronize()
+    ref = oracle.accept_chain(mode, lg["target_logits"], None if qq is None else qq.cpu(), q_kind,
+                              lg["draft_tokens"], temperature=T, top_k=top_k, seed=seed, round_=rnd)
+    return out, ref
+
+
+@pytest.mark.parametrize("mode", [sv.GREEDY, sv.EXACT])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("T,top_k", [(1.0, 0), (0.7, 50)])
+def test_chain(cuda_ok, mode, dtype, T, top_k):
+    lg = wl.chain_logits(96, 5, 4000, sigma=3.0, draft_sigma=1.0, dtype=dtype, temperature=T,
+                         top_k=top_k, seed=11)
+    out, ref = _chain(mode, lg, T=T, top_k=top_k)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"])
+    assert sv.sv_read_device_status() == 0
+
+
+def test_chain_q_as_probabilities(cuda_ok):
+    lg = wl.chain_logits(64, 4, 1000, sigma=2.0, draft_sigma=0.5, dtype=torch.float32, seed=12)
+    qp = wl.draft_probs(lg["draft_logits"])
+    out, ref = _chain(sv.EXACT, lg, q_kind=sv.Q_PROBS_F32, q=qp)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"])
+
+
+def test_chain_large_vocab(cuda_ok):
+    lg = wl.chain_logits(16, 4, 152064, sigma=3.0, draft_sigma=1.0, dtype=torch.bfloat16, seed=13)
+    out, ref = _chain(sv.EXACT, lg, seed=9, rnd=4)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"])
+    out, ref = _chain(sv.GREEDY, lg)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"])
+
+
+@pytest.mark.parametrize("parent", [wl.TREE_T26, wl.TREE_T64, wl.TREE_EXAMPLE7])
+@pytest.mark.parametrize("mode", [sv.GREEDY, sv.EXACT])
+def test_tree(cuda_ok, parent, mode):
+    B = 64
+    lg = wl.medusa_logits(B, parent, 2000, sigma=3.0, seed=14, coverage=True, coverage_sigma=0.7)
+    dev = torch.device("cuda")
+    q = lg["draft_logits"].to(dev) if mode == sv.EXACT else None
+    out = sv.sv_accept_tree(mode, lg["target_logits"].to(dev), q, sv.Q_LOGITS, parent,
+                            lg["node_tokens"].to(dev), seed=21, round_=2)
+    torch.cuda.synchronize()
+    ref = oracle.accept_tree(mode, lg["target_logits"], lg["draft_logits"] if q is not None else None,
+                             oracle.Q_LOGITS, parent, lg["node_tokens"], seed=21, round_=2)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted", "path_nodes"])
+    assert int(ref["num_accepted"].sum()) > 0  # paths do get accepted in this variant
+
+
+def test_top_k_tie_fallback(cuda_ok):
+    """Every logit equal: more than 4096 entries tie at the threshold, so the kernel
+    takes its counting path; the kept set is the k lowest ids."""
+    B, gamma, V, k = 4, 3, 8192, 7
+    tl = torch.zeros((B, gamma + 1, V), dtype=torch.bfloat16)
+    ql = torch.zeros((B, gamma, V), dtype=torch.bfloat16)
+    toks = torch.tensor([[0, 3, 6], [1, 7, 2], [6, 6, 9], [5, 4, 3]], dtype=torch.int32)
+    lg = dict(target_logits=tl, draft_logits=ql, draft_tokens=toks)
+    out, ref = _chain(sv.EXACT, lg, T=1.0, top_k=k, seed=2)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"], max_exempt_frac=1.0)
+    assert torch.all(out["tokens"].cpu()[out["tokens"].cpu() >= 0] < 10)
+    st = sv.sv_read_device_status()
+    assert st & sv.SV_DEV_ZERO_DRAFT_PROB  # token 9 lies outside q's top-7
+
+
+def test_bad_token_sets_status(cuda_ok):
+    lg = wl.chain_logits(2, 2, 64, seed=15)
+    lg["draft_tokens"][0, 0] = 64
+    lg["draft_tokens"][1, 1] = -5
+    out, ref = _chain(sv.EXACT, lg)
+    assert sv.sv_read_device_status() & sv.SV_DEV_BAD_TOKEN
+    assert int(out["num_accepted"][0]) == 0 and int(out["num_accepted"][1]) <= 1
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"], max_exempt_frac=1.0)
+
+
+def _log(p):
+    p = np.asarray(p, dtype=np.float64)
+    with np.errstate(divide="ignore"):
+        return np.where(p > 0, np.log(p), -np.inf)
+
+
+def test_chi_square_first_token_gpu(cuda_ok):
+    """(P5) through the GPU: V = 16, gamma = 4, 10^6 sequences; also bit-equal to the oracle."""
+    gamma, V, B = 4, 16, 1_000_000
+    rng = np.random.default_rng(2024)
+    p = rng.dirichlet(np.full(V, 0.7), size=gamma + 1)
+    q = rng.dirichlet(np.full(V, 0.7), size=gamma)
+    tl = torch.from_numpy(_log(p).astype(np.float32)).expand(B, gamma + 1, V).contiguous()
+    qq = torch.from_numpy(q.astype(np.float32)).expand(B, gamma, V).contiguous()
+    toks = np.empty((B, gamma), dtype=np.int32)
+    for i in range(gamma):
+        toks[:, i] = rng.choice(V, size=B, p=q[i] / q[i].sum())
+    lg = dict(target_logits=tl, draft_logits=qq, draft_tokens=torch.from_numpy(toks))
+    out, ref = _chain(sv.EXACT, lg, q_kind=sv.Q_PROBS_F32, q=qq, seed=5, rnd=1)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"], max_exempt_frac=1e-3)
+    first = out["tokens"][:, 0].cpu().numpy()
+    p0 = np.exp(_log(p[0]).astype(np.float32).astype(np.float64))
+    assert stats.chisquare(np.bincount(first, minlength=V), B * p0 / p0.sum()).pvalue > 1e-4
+
+
+def test_closed_form_gpu(cuda_ok):
+    """(P6) through the GPU: alpha = 0.8, gamma = 4 -> mean emitted 3.3616, accepted 2.3616."""
+    alpha, gamma, V, B = 0.8, 4, 16, 1_000_000
+    p = np.zeros((gamma + 1, V))
+    p[:, 0], p[:, 1] = alpha, 1 - alpha
+    q = np.zeros((gamma, V))
+    q[:, 0] = 1.0
+    tl = torch.from_numpy(_log(p).astype(np.float32)).expand(B, gamma + 1, V).contiguous()
+    qq = torch.from_numpy(q.astype(np.float32)).expand(B, gamma, V).contiguous()
+    toks = torch.zeros((B, gamma), dtype=torch.int32)
+    lg = dict(target_logits=tl, draft_logits=qq, draft_tokens=toks)
+    out, ref = _chain(sv.EXACT, lg, q_kind=sv.Q_PROBS_F32, q=qq, seed=99, rnd=0)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"], max_exempt_frac=1e-3)
+    probs = [alpha ** k * (1 - alpha) for k in range(gamma)] + [alpha ** gamma]
+    vals = np.arange(gamma + 1) + 1
+    mean = float(np.dot(probs, vals))
+    sd = math.sqrt(float(np.dot(probs, vals ** 2)) - mean ** 2)
+    em = out["num_emitted"].double().mean().item()
+    assert abs(em - 3.3616) < 4 * sd / math.sqrt(B)
+    assert abs(out["num_accepted"].double().mean().item() - 2.3616) < 4 * sd / math.sqrt(B)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_full_size_workloads(cuda_ok, cfg):
+    """Each workload at full size: every sequence compared with the oracle, in both modes."""
+    w = wl.make_workload(cfg, device="cuda")
+    c = w["cfg"]
+    modes = [sv.EXACT, sv.GREEDY]
+    for mode in modes:
+        if c["kind"] == "chain":
+            out = sv.sv_accept_chain(mode, w["target_logits"], w["draft_logits"], sv.Q_LOGITS,
+                                     w["draft_tokens"], temperature=c["temperature"],
+                                     top_k=c["top_k"], seed=w["seed"], round_=0)
+            torch.cuda.synchronize()
+            ref = oracle.accept_chain(mode, w["target_logits"].cpu(), w["draft_logits"].cpu(),
+                                      oracle.Q_LOGITS, w["draft_tokens"].cpu(),
+                                      temperature=c["temperature"], top_k=c["top_k"],
+                                      seed=w["seed"], round_=0)
+            keys = ["tokens", "num_emitted", "num_accepted"]
+        else:
+            out = sv.sv_accept_tree(mode, w["target_logits"], w["draft_logits"], sv.Q_LOGITS,
+                                    w["parent"], w["node_tokens"], temperature=c["temperature"],
+                                    top_k=c["top_k"], seed=w["seed"], round_=0)
+            torch.cuda.synchronize()
+            ref = oracle.accept_tree(mode, w["target_logits"].cpu(), w["draft_logits"].cpu(),
+                                     oracle.Q_LOGITS, w["parent"], w["node_tokens"].cpu(),
+                                     temperature=c["temperature"], top_k=c["top_k"],
+                                     seed=w["seed"], round_=0)
+            keys = ["tokens", "num_emitted", "num_accepted", "path_nodes"]
+        _compare(out, ref, keys, max_exempt_frac=0.05)
+    assert sv.sv_read_device_status() == 0

@@ -156,8 +156,9 @@ def test_closed_form_expected_tokens(construction):
     tol = 4 * math.sqrt(var / B)
     assert abs(em.mean().item() - mean) < tol
     assert abs(out["num_accepted"].double().mean().item() - (mean - 1)) < tol
-    # |u - 0.8| < 1e-6 happens ~2e-6 per decision (24-bit uniforms): reported, rare
-    assert int(out["near_ties"].sum()) < 60
+    # reported near ties: |u - 0.8| < 1e-6 (~2e-6 per decision) and samples within
+    # 1e-6 of a CDF boundary (~2e-6 / sum(w) per boundary side): tens per 10^6 rounds
+    assert int(out["near_ties"].sum()) < 300
 
 
 # ---------------------------------------------------------- chi-square (P5)
