@@ -1,0 +1,480 @@
+#!/usr/bin/env python
+"""Verify-step benchmark: verified candidate tokens/s on one GB300 (per GPU replica).
+
+A step is one pass of the whole hot path over one batch: tree attention (one layer),
+token acceptance over the vocabulary, and the KV commit of the accepted path.
+Default workload: the 64-node Medusa tree, bf16, B=8, 32 heads x 128, prefix 2048,
+vocab 32000, exact sampling at T=1.
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
+torch.cuda.synchronize() on both sides; each step is timed with CUDA events on the
+stream the kernels run on.  Between steps (outside the events) prefix_len is restored
+and L2 is flushed by writing a buffer of twice its size.  Under torchrun every rank
+runs an independent replica (weak scaling, no collective on the data path); the
+device time is the max over ranks.
+
+--impl reference times the CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "verified candidate tokens/s at 1 GB300; verify-step HBM GB/s vs peak"
+UNIT = "candidate tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- helpers
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, help="workload id 1..5 (default 2)")
+    ap.add_argument("--mode", choices=["exact", "greedy"], default=None)
+    ap.add_argument("--preheat-s", type=float, default=1.0,
+                    help="untimed seconds of steps before warm-up (clock ramp)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target duration of the oracle sample")
+    return ap.parse_args()
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        t = torch.tensor([x], dtype=torch.float64,
+                         device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        t = torch.tensor([x], dtype=torch.float64,
+                         device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled while the GPU works."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[0]), smax=float(parts[1]), util=float(parts[3]),
+                                 hw=parts[4], hwt=parts[5], swt=parts[6], pcap=parts[7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r["util"] > 0] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def committed_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current source of the kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            entries = json.load(f)
+    except (OSError, ValueError):
+        return None
+    src = os.path.join(ROOT, "speculative_decoding_verify_sv_gb300", "csrc", kernel_file)
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    for e in entries:
+        if e.get("workload") == workload and e.get("source_sha") == sha:
+            return e.get("dram_bytes_per_launch")
+    return None
+
+
+def attention_bytes(w) -> int:
+    """Algorithmic bytes of one tree-attention launch: prefix K and V read once, tree
+    Q/K/V read, O written."""
+    c = w["cfg"]
+    es = 4 if c["dtype"] == torch.float32 else 2
+    B, N, Hq, Hkv, D = c["B"], w["N"], c["Hq"], c["Hkv"], c["D"]
+    prefix = int(w["prefix_len"].sum().item()) * Hkv * D * es * 2
+    tree = B * N * (2 * Hq + 2 * Hkv) * D * es
+    return prefix + tree
+
+
+def accept_bytes(w) -> int:
+    """Algorithmic bytes of acceptance: every target row and draft row read once."""
+    c = w["cfg"]
+    es = 4 if c["dtype"] == torch.float32 else 2
+    B, N, V = c["B"], w["N"], c["V"]
+    return B * (N + w["Dmax"]) * V * es
+
+
+def attention_flops(w) -> int:
+    c = w["cfg"]
+    B, N, Hq, D = c["B"], w["N"], c["Hq"], c["D"]
+    keys = int(w["prefix_len"].sum().item()) * N * Hq + B * N * N * Hq
+    return 4 * keys * D
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, dist: Dist):
+    import speculative_decoding_verify_sv_gb300 as sv
+    from speculative_decoding_verify_sv_gb300 import workloads as wl
+    from speculative_decoding_verify_sv_gb300.step import VerifyStep
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    w = wl.make_workload(args.config, device=dev)
+    c = w["cfg"]
+    mode_name = args.mode or c["mode"]
+    mode = sv.EXACT if mode_name == "exact" else sv.GREEDY
+    chain = c["kind"] == "chain"
+    cache = sv.KVCache(w["cache_k"], w["cache_v"], w["prefix_len"], w["block_table"],
+                       w.get("block_size", 16))
+    step = VerifyStep(w["parent"], c["B"], c["Hq"], c["Hkv"], c["D"], c["V"], cache,
+                      dtype=c["dtype"], mode=mode, q_kind=sv.Q_LOGITS,
+                      temperature=c["temperature"], top_k=c["top_k"], chain=chain, device=dev)
+    toks = w["draft_tokens"] if chain else w["node_tokens"]
+    prefix0 = w["prefix_len"].clone()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 1 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    emitted = torch.zeros(c["B"], dtype=torch.int64, device=dev)
+
+    def prepare():
+        cache.prefix_len.copy_(prefix0)
+        flush.zero_()
+
+    def device_step(i, ev=None):
+        if ev:
+            ev[0].record(stream)
+        step.attention(w["q"], w["k_tree"], w["v_tree"], stream)
+        if ev:
+            ev[1].record(stream)
+        step.accept(w["target_logits"], w["draft_logits"], toks, seed=w["seed"], round_=i,
+                    stream=stream)
+        if ev:
+            ev[2].record(stream)
+        step.commit(w["k_tree"], w["v_tree"], stream)
+        if ev:
+            ev[3].record(stream)
+
+    # pre-heat (clock ramp), then the warm-up steps
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    t_end = time.perf_counter() + args.preheat_s
+    i = 0
+    while time.perf_counter() < t_end:
+        prepare()
+        device_step(i)
+        i += 1
+        if i % 20 == 0:
+            torch.cuda.synchronize()
+    for j in range(args.warmup):
+        prepare()
+        device_step(j)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for j in range(K):
+        prepare()
+        device_step(j, evs[j])
+        emitted.add_(step.outs["num_emitted"])
+    torch.cuda.synchronize()
+    dist.barrier()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    status = sv.sv_read_device_status()
+
+    tot = [e[0].elapsed_time(e[3]) for e in evs]
+    att = [e[0].elapsed_time(e[1]) for e in evs]
+    acc = [e[1].elapsed_time(e[2]) for e in evs]
+    com = [e[2].elapsed_time(e[3]) for e in evs]
+    dev_ms = dist.max(sum(tot))
+    cand = c["B"] * (w["N"] - 1)
+    units = dist.sum(cand * K)
+    value = units / (dev_ms / 1e3)
+    emitted_total = dist.sum(float(emitted.sum().item()))
+
+    peak, peak_kind = measured_peaks()
+    a_bytes = attention_bytes(w)
+    a_ms = statistics.mean(att)
+    achieved = a_bytes / (a_ms / 1e3) / 1e9
+    workload_name = f"{c['name']} (config {args.config})"
+    kernel_file = "attention.cu"
+
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": dist.world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": dev_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if c["dtype"] == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {
+            "workload": workload_name,
+            "B": c["B"], "tree_nodes": w["N"], "candidates_per_step": cand,
+            "Hq": c["Hq"], "Hkv": c["Hkv"], "D": c["D"], "V": c["V"],
+            "prefix": c["L"] if not isinstance(c["L"], tuple) else f"U{{{c['L'][0]}..{c['L'][1]}}}",
+            "paged": c["paged"], "mode": mode_name, "temperature": c["temperature"],
+            "top_k": c["top_k"], "l2": "flushed between steps (2x L2 write, outside events)",
+            "timing": "CUDA events per step on the launch stream; sum over K steps",
+            "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU",
+        },
+        "roofline": {
+            "kernel": "tree attention (attn_mma_kernel + split merge)",
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+            "algorithmic_bytes_per_launch": a_bytes,
+            "traffic": committed_traffic(kernel_file, workload_name),
+        },
+        "breakdown_us": {
+            "attention": 1e3 * a_ms, "accept": 1e3 * statistics.mean(acc),
+            "commit": 1e3 * statistics.mean(com),
+            "accept_gbs": accept_bytes(w) / (statistics.mean(acc) / 1e3) / 1e9,
+            "attention_tflops": attention_flops(w) / (a_ms / 1e3) / 1e12,
+        },
+        "emitted_tokens_per_s": emitted_total / (dev_ms / 1e3),
+        "mean_accepted": emitted_total / (c["B"] * K * dist.world) - 1.0,
+        "acceptance_rate": (emitted_total / (c["B"] * K * dist.world) - 1.0) / max(1, w["Dmax"]),
+        "wall_s_timed_region": wall,
+        "gpu_launches": step.kernel_launches() * K,
+        "device_status": status,
+        "clocks": clocks,
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, dist, w, step, prepare, stream, toks, cand)
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, mode)
+    return result
+
+
+def run_e2e(args, dist, w, step, prepare, stream, toks, cand):
+    """Same metric through the public step API with host inputs: every step copies its
+    inputs from pinned host memory and reads the emitted tokens back."""
+    host = {k: w[k].cpu().pin_memory() for k in ("q", "k_tree", "v_tree", "target_logits",
+                                                 "draft_logits")}
+    host["node_tokens"] = toks.cpu().pin_memory()
+    step.alloc_inputs(host)
+    for j in range(max(3, args.warmup)):
+        prepare()
+        step.run_host(host, seed=w["seed"], round_=j, stream=stream)
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    for j in range(K):
+        prepare()
+        evs[j][0].record(stream)
+        step.run_host(host, seed=w["seed"], round_=j, stream=stream)
+        evs[j][1].record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms = dist.max(sum(a.elapsed_time(b) for a, b in evs))
+    units = dist.sum(cand * K)
+    return {"value": units / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": step.h2d_bytes(host),
+            "d2h_bytes_per_step": step.d2h_bytes(), "ms_per_step": ms / K}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, budget_s: float, mode: int, b_limit=None):
+    """Time the oracle on whole sequences (attention of every node and head, acceptance,
+    commit) until the budget is spent; returns (candidates, seconds, sequences)."""
+    import oracle
+    c = w["cfg"]
+    chain = c["kind"] == "chain"
+    B = c["B"] if b_limit is None else min(b_limit, c["B"])
+    cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in w.items()}
+    done, spent = 0, 0.0
+    while done < B and (done == 0 or spent < budget_s):
+        b = done
+        sel = slice(b, b + 1)
+        if cpu["block_table"] is None:
+            ck, cv, bt = cpu["cache_k"][sel], cpu["cache_v"][sel], None
+        else:
+            ck, cv, bt = cpu["cache_k"], cpu["cache_v"], cpu["block_table"][sel]
+        t0 = time.perf_counter()
+        oracle.tree_attention(cpu["q"][sel], cpu["k_tree"][sel], cpu["v_tree"][sel], ck, cv,
+                              cpu["prefix_len"][sel], cpu["parent"], cpu["scale"], block_table=bt,
+                              block_size=w.get("block_size", 16))
+        if chain:
+            r = oracle.accept_chain(mode, cpu["target_logits"][sel], cpu["draft_logits"][sel],
+                                    oracle.Q_LOGITS, cpu["draft_tokens"][sel],
+                                    temperature=c["temperature"], top_k=c["top_k"],
+                                    seed=w["seed"])
+            W = cpu["draft_tokens"].shape[1] + 1
+            path = torch.arange(W, dtype=torch.int32).unsqueeze(0)
+        else:
+            r = oracle.accept_tree(mode, cpu["target_logits"][sel], cpu["draft_logits"][sel],
+                                   oracle.Q_LOGITS, cpu["parent"], cpu["node_tokens"][sel],
+                                   temperature=c["temperature"], top_k=c["top_k"], seed=w["seed"])
+            path = r["path_nodes"]
+        oracle.commit_kv(cpu["k_tree"][sel], cpu["v_tree"][sel], path, r["num_accepted"], ck, cv,
+                         cpu["prefix_len"][sel], block_table=bt, block_size=w.get("block_size", 16))
+        spent += time.perf_counter() - t0
+        done += 1
+    return done * (w["N"] - 1), spent, done
+
+
+def cpu_baseline(w, budget_s, mode):
+    import oracle
+    cand, secs, seqs = oracle_sample(w, budget_s, mode)
+    return {"value": cand / secs, "unit": UNIT, "cores": oracle.get_threads(), "kind": "oracle",
+            "sample": f"{seqs} of {w['cfg']['B']} sequences of the workload (attention of every "
+                      f"node and head over the full prefix, acceptance, commit), {secs:.1f} s"}
+
+
+def run_reference(args, dist: Dist):
+    """The oracle timed on the host cores on the same workload, metric and unit."""
+    import oracle
+    from speculative_decoding_verify_sv_gb300 import workloads as wl
+    if dist.rank != 0:
+        return None
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = wl.make_workload(args.config, device=dev)
+    c = w["cfg"]
+    mode = oracle.EXACT if (args.mode or c["mode"]) == "exact" else oracle.GREEDY
+    # each step: a bounded sample (one sequence), sized so the whole run stays short
+    per_step_budget = max(0.5, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, 0.0, mode, b_limit=1)
+    cand, secs = 0, 0.0
+    for _ in range(args.steps):
+        cnd, s, _ = oracle_sample(w, per_step_budget, mode, b_limit=1)
+        cand += cnd
+        secs += s
+    value = cand / secs
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": f"{c['name']} (config {args.config})", "B": c["B"],
+                   "tree_nodes": w["N"], "candidates_per_step": c["B"] * (w["N"] - 1)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.get_threads(),
+                         "kind": "oracle",
+                         "sample": "one sequence per step (attention of every node and head, "
+                                   "acceptance, commit) of the workload"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, dist)
+        else:
+            res = run_ours(args, dist)
+        if dist.rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,123 @@
+"""One verify step through the C ABI: tree attention, acceptance, KV commit.
+
+``VerifyStep`` owns the device workspaces and output buffers of one workload shape and
+issues the three ABI calls on one stream.  ``run_host`` is the end-to-end form: it
+copies the step's inputs from (pinned) host tensors, runs the step, and copies the
+accepted tokens back.  All arithmetic happens in libsv.so.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import torch
+
+from . import (EXACT, GREEDY, Q_LOGITS, KVCache, sv_accept_chain, sv_accept_tree,
+               sv_accept_workspace_size, sv_commit_kv, sv_tree_attention,
+               sv_tree_attention_workspace_size)
+
+
+def _depths(parent):
+    d = []
+    for p in parent:
+        d.append(0 if p < 0 else d[p] + 1)
+    return d
+
+
+class VerifyStep:
+    """Buffers and calls of one verify step for a fixed batch shape.
+
+    chain=True uses sv_accept_chain (parent must be a chain); otherwise sv_accept_tree.
+    """
+
+    def __init__(self, parent: Sequence[int], B: int, Hq: int, Hkv: int, D: int, V: int,
+                 cache: KVCache, dtype=torch.bfloat16, mode=EXACT, q_kind=Q_LOGITS,
+                 temperature: float = 1.0, top_k: int = 0, chain: bool = False,
+                 device: Optional[torch.device] = None):
+        self.parent = list(parent)
+        self.N = len(self.parent)
+        self.Dmax = max(_depths(self.parent))
+        self.B, self.Hq, self.Hkv, self.D, self.V = B, Hq, Hkv, D, V
+        self.cache, self.dtype, self.mode, self.q_kind = cache, dtype, mode, q_kind
+        self.temperature, self.top_k, self.chain = temperature, top_k, chain
+        self.device = device or cache.k.device
+        self.scale = D ** -0.5
+        ws = sv_tree_attention_workspace_size(dtype, B, self.N, Hq, Hkv, D, cache.max_prefix)
+        self.attn_ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=self.device)
+        self.attn_splits = ws > 0
+        Dq = self.Dmax
+        self.acc_ws = torch.empty(sv_accept_workspace_size(B, self.N, V, Dq), dtype=torch.uint8,
+                                  device=self.device)
+        self.out = torch.empty((B, self.N, Hq, D), dtype=dtype, device=self.device)
+        W = self.Dmax + 1
+        i32 = dict(dtype=torch.int32, device=self.device)
+        self.outs = dict(tokens=torch.empty((B, W), **i32), num_emitted=torch.empty(B, **i32),
+                         num_accepted=torch.empty(B, **i32), near_ties=torch.empty(B, **i32),
+                         path_nodes=torch.empty((B, W), **i32))
+        if chain:
+            pn = torch.arange(W, dtype=torch.int32, device=self.device)
+            self.chain_path = pn.unsqueeze(0).expand(B, W).contiguous()
+
+    def kernel_launches(self) -> int:
+        """Kernels one step launches: attention (+ split merge), two acceptance, commit."""
+        return 1 + int(self.attn_splits) + 2 + 1
+
+    def attention(self, q, k_tree, v_tree, stream=None):
+        return sv_tree_attention(q, k_tree, v_tree, self.cache, self.parent, self.scale,
+                                 out=self.out, workspace=self.attn_ws, stream=stream)
+
+    def accept(self, target_logits, q_draft, node_tokens, seed=0, round_=0, stream=None):
+        if self.chain:
+            toks = node_tokens[:, 1:] if node_tokens.shape[1] == self.N else node_tokens
+            r = sv_accept_chain(self.mode, target_logits, q_draft, self.q_kind,
+                                toks.contiguous() if not toks.is_contiguous() else toks,
+                                temperature=self.temperature, top_k=self.top_k, seed=seed,
+                                round_=round_, outs=self.outs, workspace=self.acc_ws,
+                                stream=stream)
+            # a chain's accepted path is nodes 0..num_accepted
+            return r
+        return sv_accept_tree(self.mode, target_logits, q_draft, self.q_kind, self.parent,
+                              node_tokens, temperature=self.temperature, top_k=self.top_k,
+                              seed=seed, round_=round_, outs=self.outs, workspace=self.acc_ws,
+                              stream=stream)
+
+    def commit(self, k_tree, v_tree, stream=None):
+        path = self.chain_path if self.chain else self.outs["path_nodes"]
+        sv_commit_kv(k_tree, v_tree, path, self.outs["num_accepted"], self.cache, stream=stream)
+
+    def run(self, q, k_tree, v_tree, target_logits, q_draft, node_tokens, seed=0, round_=0,
+            stream=None):
+        self.attention(q, k_tree, v_tree, stream)
+        self.accept(target_logits, q_draft, node_tokens, seed, round_, stream)
+        self.commit(k_tree, v_tree, stream)
+        return self.out, self.outs
+
+    # ------------------------------------------------------------ end to end
+
+    def alloc_inputs(self, like: dict):
+        """Device input buffers shaped like the host tensors in ``like``."""
+        self.dev_in = {k: torch.empty_like(v, device=self.device) for k, v in like.items()}
+        W = self.Dmax + 1
+        pin = dict(dtype=torch.int32, pin_memory=True)
+        self.host_out = dict(tokens=torch.empty((self.B, W), **pin),
+                             num_emitted=torch.empty(self.B, **pin),
+                             num_accepted=torch.empty(self.B, **pin),
+                             near_ties=torch.empty(self.B, **pin))
+        return self.dev_in
+
+    def run_host(self, host_in: dict, seed=0, round_=0, stream=None):
+        """H2D copies of the step inputs (pinned host tensors), the step, and the D2H
+        copy of the emitted tokens and counts; returns the pinned host outputs."""
+        d = self.dev_in
+        for k, v in host_in.items():
+            d[k].copy_(v, non_blocking=True)
+        self.run(d["q"], d["k_tree"], d["v_tree"], d["target_logits"], d["draft_logits"],
+                 d["node_tokens"], seed, round_, stream)
+        for k, v in self.host_out.items():
+            v.copy_(self.outs[k], non_blocking=True)
+        return self.host_out
+
+    def h2d_bytes(self, host_in: dict) -> int:
+        return sum(v.numel() * v.element_size() for v in host_in.values())
+
+    def d2h_bytes(self) -> int:
+        return sum(v.numel() * v.element_size() for v in self.host_out.values())
