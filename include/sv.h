@@ -153,6 +153,28 @@ sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
 /* Workspace bytes for sv_accept_chain (N = gamma+1, Dq = gamma) / sv_accept_tree. */
 size_t sv_accept_workspace_size(int B, int N, int V, int Dq);
 
+/* sv_accept_tree without a workspace argument, for callers that cannot allocate device
+ * memory (no cudaMalloc or allocating library call on their path: fixed-memory
+ * embedded runtimes, callers holding no allocator handle).  No counterpart on the
+ * pages: it is a deployment convenience.  Arguments, outputs and results are those of
+ * sv_accept_tree; the per-row statistics go to a fixed device array inside the library
+ * of SV_NOALLOC_ACCEPT_ROWS rows (24 bytes each, 1.5 MiB), held by every GPU that
+ * loads the library until the process exits.  B*(N+Dq) logit rows (B*N in greedy
+ * mode) must not exceed SV_NOALLOC_ACCEPT_ROWS, else SV_ERR_UNSUPPORTED and nothing is
+ * launched.  The first call on a device looks the array's address up on that device
+ * (make that first call before any stream capture).  Every call shares the one array,
+ * so calls that overlap on the GPU (other streams, other threads) race on it: order
+ * them on one stream.  Each call writes every statistic it reads, so nothing needs
+ * clearing between calls. */
+#define SV_NOALLOC_ACCEPT_ROWS 65536
+sv_status sv_accept_tree_noalloc(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
+                                 const int32_t *parent, const int32_t *node_tokens,
+                                 const void *target_logits, const void *q, sv_q_kind q_kind,
+                                 int Dq, float temperature, int top_k, uint64_t seed,
+                                 uint64_t round, int32_t *out_path_nodes, int32_t *out_tokens,
+                                 int32_t *out_num_emitted, int32_t *out_num_accepted,
+                                 uint32_t *out_near_ties, void *stream);
+
 /* --------------------------------------------------------------------- commit */
 
 /* KV commit (qwbw.cn sections 3.1.4 and 6.3; hncyxsy.com section 4.3: keep the KV of

@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "SVError", "KVCache", "library_path", "load_library", "sv_tree_attention",
     "sv_tree_attention_workspace_size", "sv_accept_chain", "sv_accept_tree",
-    "sv_accept_workspace_size", "sv_commit_kv", "sv_tree_prepare", "sv_read_device_status",
+    "sv_accept_workspace_size", "sv_accept_tree_noalloc", "sv_commit_kv", "sv_tree_prepare", "sv_read_device_status",
     "sv_version", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "SV_MAX_TREE_NODES",
 ]
 
@@ -76,6 +76,8 @@ def load_library():
                                         SZ, P]
         lib.sv_accept_tree.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, U64, U64, P, P, P, P,
                                        P, P, SZ, P]
+        lib.sv_accept_tree_noalloc.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, U64, U64, P,
+                                               P, P, P, P, P]
         lib.sv_accept_workspace_size.argtypes = [I, I, I, I]
         lib.sv_accept_workspace_size.restype = SZ
         lib.sv_commit_kv.argtypes = [I, I, I, I, I, P, P, P, I, P, _KVCacheC, P]
@@ -84,7 +86,7 @@ def load_library():
         lib.sv_last_error.restype = ctypes.c_char_p
         lib.sv_version.restype = ctypes.c_char_p
         for fn in ("sv_tree_attention", "sv_accept_chain", "sv_accept_tree", "sv_commit_kv",
-                   "sv_tree_prepare", "sv_read_device_status"):
+                   "sv_tree_prepare", "sv_read_device_status", "sv_accept_tree_noalloc"):
             getattr(lib, fn).restype = ctypes.c_int32
         _lib = lib
         return lib
@@ -294,6 +296,36 @@ def sv_accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperat
                               _ptr(outs["tokens"]), _ptr(outs["num_emitted"]),
                               _ptr(outs["num_accepted"]), _ptr(outs["near_ties"]),
                               _ptr(workspace), ws_bytes, _stream(stream)))
+    return outs
+
+
+def sv_accept_tree_noalloc(mode, target_logits, q, q_kind, parent, node_tokens,
+                           temperature=1.0, top_k=0, seed=0, round_=0, outs=None,
+                           stream=None) -> dict:
+    """sv_accept_tree without a workspace, for callers that cannot allocate device
+    memory: the library keeps the per-row statistics in a fixed device array.  Calls
+    that overlap on the GPU share that array and race; order them on one stream.  The
+    output buffers are still the caller's (pass them in ``outs`` to avoid allocation)."""
+    lib = load_library()
+    _dev(target_logits, "target_logits", (torch.bfloat16, torch.float32))
+    B, N, V = target_logits.shape
+    _dev(node_tokens, "node_tokens", torch.int32, (B, N))
+    Dq = 0
+    if q is not None:
+        Dq = q.shape[1]
+        _dev(q, "q", target_logits.dtype if q_kind == Q_LOGITS else torch.float32, (B, Dq, V))
+    W = _tree_depth(parent) + 1
+    outs = _accept_outputs(B, W, target_logits.device, outs)
+    outs.setdefault("path_nodes", torch.empty((B, W), dtype=torch.int32, device=target_logits.device))
+    par, n = _parent_arr(parent)
+    if n != N:
+        raise ValueError(f"parent has {n} entries, logits have {N} rows")
+    _check(lib.sv_accept_tree_noalloc(mode, _dt(target_logits), B, N, V, par, _ptr(node_tokens),
+                                      _ptr(target_logits), _ptr(q), q_kind, Dq, float(temperature),
+                                      int(top_k), int(seed), int(round_), _ptr(outs["path_nodes"]),
+                                      _ptr(outs["tokens"]), _ptr(outs["num_emitted"]),
+                                      _ptr(outs["num_accepted"]), _ptr(outs["near_ties"]),
+                                      _stream(stream)))
     return outs
 
 

@@ -397,3 +397,66 @@ sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- acceptance without allocation
+
+// Scratch of sv_accept_tree_noalloc: the per-row statistics (row max, argmax, top-k
+// threshold, softmax sum) that the first acceptance kernel writes and the second
+// reads.  A fixed array in device memory instead of a caller workspace, so that
+// callers which cannot allocate device memory can still run acceptance.  Every GPU
+// that loads this library holds it (SV_NOALLOC_ACCEPT_ROWS rows of 24 bytes) until
+// the process exits.
+static __device__ __align__(256) sv::RowStat g_sv_noalloc_rows[SV_NOALLOC_ACCEPT_ROWS];
+
+namespace {
+
+// Device address of the scratch array on the current device.  Looked up once per
+// device, with that device current; host code must never pass the array's name.
+void *noalloc_rows_address(sv_status *st) {
+  static void *addr[kMaxDevices] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *st = e != cudaSuccess ? cuda_fail(e, "cudaGetDevice") : fail(SV_ERR_CUDA, "device index out of range");
+    return nullptr;
+  }
+  if (!addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_sv_noalloc_rows);
+    if (e != cudaSuccess || p == nullptr) {
+      *st = cuda_fail(e, "cudaGetSymbolAddress of the acceptance scratch array");
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+sv_status sv_accept_tree_noalloc(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
+                                 const int32_t *parent, const int32_t *node_tokens,
+                                 const void *target_logits, const void *q, sv_q_kind q_kind,
+                                 int Dq, float temperature, int top_k, uint64_t seed,
+                                 uint64_t round, int32_t *out_path_nodes, int32_t *out_tokens,
+                                 int32_t *out_num_emitted, int32_t *out_num_accepted,
+                                 uint32_t *out_near_ties, void *stream) {
+  const bool greedy = mode == SV_GREEDY || temperature == 0.f;
+  const long long rows = (long long)B * ((long long)N + (greedy ? 0 : (Dq > 0 ? Dq : 0)));
+  if (rows > SV_NOALLOC_ACCEPT_ROWS)
+    return fail(SV_ERR_UNSUPPORTED,
+                "sv_accept_tree_noalloc: B*(N+Dq) = %lld logit rows exceeds its fixed scratch of "
+                "%d rows; use sv_accept_tree with a workspace",
+                rows, SV_NOALLOC_ACCEPT_ROWS);
+  sv_status st = SV_OK;
+  void *scratch = noalloc_rows_address(&st);
+  if (!scratch) return st;
+  return sv_accept_tree(mode, logit_dt, B, N, V, parent, node_tokens, target_logits, q, q_kind,
+                        Dq, temperature, top_k, seed, round, out_path_nodes, out_tokens,
+                        out_num_emitted, out_num_accepted, out_near_ties, scratch,
+                        sizeof(g_sv_noalloc_rows), stream);
+}
+
+}  // extern "C"
