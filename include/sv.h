@@ -47,6 +47,10 @@ typedef int32_t sv_status;
 #define SV_DEV_BAD_BLOCK 0x2u      /* a block-table entry outside the pool (skipped) */
 #define SV_DEV_BAD_PREFIX 0x4u     /* prefix_len < 0 or beyond the cache (clamped) */
 #define SV_DEV_ZERO_DRAFT_PROB 0x8u /* a draft with q(x) = 0: ratio taken as +inf/0 */
+#define SV_DEV_TIMEOUT 0x10u       /* a pipeline wait gave up after its time limit; the
+                                      outputs of that call are not valid */
+#define SV_DEV_LAYOUT 0x20u        /* shared memory was not 1024-byte aligned; the call
+                                      did nothing (outputs not valid) */
 
 #define SV_MAX_TREE_NODES 64 /* one 64-bit ancestor word per node */
 #define SV_MAX_TOP_K 1024
@@ -89,7 +93,11 @@ typedef struct {
  * cache as above (read only); parent [N] host; out [B,N,Hq,D].
  * dt: SV_BF16 (fp32 accumulation, bf16 output) or SV_F32 (fp32 throughout).
  * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= N <= 64; block_size % 16 == 0 for
- * paged caches.  Workspace: sv_tree_attention_workspace_size() bytes (may be 0). */
+ * paged caches.  Workspace: sv_tree_attention_workspace_size() bytes (may be 0).  The
+ * workspace must be zero-filled before its first use with this function (it keeps a
+ * generation counter and per-piece completion words that later calls rely on); each call
+ * leaves it ready for the next, whatever the shape, including after a call that reported
+ * SV_DEV_TIMEOUT.  Calls sharing one workspace must be stream-ordered. */
 sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, const void *q,
                             const void *k_tree, const void *v_tree, sv_kv_cache cache,
                             const int32_t *parent, float scale, void *out, void *workspace,
@@ -208,6 +216,10 @@ const char *sv_last_error(void);
 
 /* Library version string. */
 const char *sv_version(void);
+
+/* Number of CUDA kernels this library has launched in this process so far (all calls,
+ * all threads); the difference around a region counts the region's launches. */
+uint64_t sv_kernel_launches(void);
 
 #ifdef __cplusplus
 }

@@ -20,7 +20,7 @@ __all__ = [
     "SVError", "KVCache", "library_path", "load_library", "sv_tree_attention",
     "sv_tree_attention_workspace_size", "sv_accept_chain", "sv_accept_tree",
     "sv_accept_workspace_size", "sv_accept_tree_noalloc", "sv_commit_kv", "sv_tree_prepare", "sv_read_device_status",
-    "sv_version", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "SV_MAX_TREE_NODES",
+    "sv_version", "sv_kernel_launches", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "SV_MAX_TREE_NODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -32,6 +32,7 @@ GREEDY, EXACT = 0, 1
 Q_PROBS_F32, Q_LOGITS = 0, 1
 SV_MAX_TREE_NODES = 64
 SV_DEV_BAD_TOKEN, SV_DEV_BAD_BLOCK, SV_DEV_BAD_PREFIX, SV_DEV_ZERO_DRAFT_PROB = 1, 2, 4, 8
+SV_DEV_TIMEOUT, SV_DEV_LAYOUT = 0x10, 0x20
 
 _STATUS_NAMES = {1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_WORKSPACE",
                  4: "SV_ERR_CUDA"}
@@ -85,6 +86,7 @@ def load_library():
         lib.sv_read_device_status.argtypes = [P, P]
         lib.sv_last_error.restype = ctypes.c_char_p
         lib.sv_version.restype = ctypes.c_char_p
+        lib.sv_kernel_launches.restype = ctypes.c_uint64
         for fn in ("sv_tree_attention", "sv_accept_chain", "sv_accept_tree", "sv_commit_kv",
                    "sv_tree_prepare", "sv_read_device_status", "sv_accept_tree_noalloc"):
             getattr(lib, fn).restype = ctypes.c_int32
@@ -99,6 +101,11 @@ def _check(code: int):
 
 def sv_version() -> str:
     return load_library().sv_version().decode()
+
+
+def sv_kernel_launches() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load_library().sv_kernel_launches())
 
 
 # ------------------------------------------------------------------ marshalling
@@ -174,11 +181,11 @@ class KVCache:
         return self.block_table.shape[1] * int(self.block_size)
 
 
-def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor], zero: bool = False):
     if nbytes == 0:
         return workspace, 0
     if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        workspace = (torch.zeros if zero else torch.empty)(nbytes, dtype=torch.uint8, device=device)
     if workspace.numel() * workspace.element_size() < nbytes:
         raise ValueError(f"workspace has {workspace.numel()} bytes, need {nbytes}")
     return workspace, workspace.numel() * workspace.element_size()
@@ -207,7 +214,8 @@ def sv_tree_attention(q, k_tree, v_tree, cache: KVCache, parent, scale, out=None
     _dev(out, "out", q.dtype, q.shape)
     cs = cache.c_struct()
     ws_need = sv_tree_attention_workspace_size(q.dtype, B, N, Hq, Hkv, D, cache.max_prefix)
-    workspace, ws_bytes = _workspace(ws_need, q.device, workspace)
+    # a workspace passed in must have been zero-filled before its first use
+    workspace, ws_bytes = _workspace(ws_need, q.device, workspace, zero=True)
     par, n = _parent_arr(parent)
     if n != N:
         raise ValueError(f"parent has {n} entries, tree has {N} rows")

@@ -1,4 +1,5 @@
 // C ABI of the verify step: argument validation, planning and launches.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -12,6 +13,13 @@
 
 // Sticky device status word (SV_DEV_* bits); kernels get its address as a parameter.
 __device__ unsigned int g_sv_status;
+
+namespace sv {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace sv
 
 namespace {
 
@@ -113,6 +121,8 @@ const char *sv_last_error(void) { return g_last_error.c_str(); }
 
 const char *sv_version(void) { return SV_VERSION_STRING; }
 
+uint64_t sv_kernel_launches(void) { return sv::g_launches.load(std::memory_order_relaxed); }
+
 sv_status sv_tree_prepare(int N, const int32_t *parent, uint64_t *anc, int32_t *depth) {
   sv::Tree t;
   sv_status st = make_tree(N, parent, &t);
@@ -146,7 +156,12 @@ size_t sv_tree_attention_workspace_size(sv_dtype dt, int B, int N, int Hq, int H
                                         int max_prefix) {
   if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || max_prefix < 0)
     return 0;
-  return sv::attn_plan(dt, B, N, Hq, Hkv, D, max_prefix, num_sms()).ws_bytes;
+  size_t ws = sv::attn_plan(dt, B, N, Hq, Hkv, D, max_prefix, num_sms()).ws_bytes;
+  if (dt == SV_BF16 && (D == 64 || D == 128)) {
+    const size_t tc = sv::tc_plan(B, N, Hq, Hkv, D, num_sms()).ws_bytes;
+    if (tc > ws) ws = tc;
+  }
+  return ws;
 }
 
 sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, const void *q,
@@ -168,10 +183,13 @@ sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, c
   if (B == 0) return SV_OK;
   const int max_prefix = max_prefix_of(cache);
   const sv::AttnPlan plan = sv::attn_plan(dt, B, N, Hq, Hkv, D, max_prefix, num_sms());
-  if (plan.ws_bytes > 0) {
-    if (!workspace || workspace_bytes < plan.ws_bytes)
+  const bool use_tc = sv::tc_eligible(dt, N, Hq, Hkv, D, cache);
+  const sv::TcPlan tplan = use_tc ? sv::tc_plan(B, N, Hq, Hkv, D, num_sms()) : sv::TcPlan{};
+  const size_t ws_need = use_tc ? tplan.ws_bytes : plan.ws_bytes;
+  if (ws_need > 0) {
+    if (!workspace || workspace_bytes < ws_need)
       return fail(SV_ERR_WORKSPACE, "attention workspace %zu bytes, need %zu", workspace_bytes,
-                  plan.ws_bytes);
+                  ws_need);
     if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
   }
   unsigned int *status = status_word();
@@ -206,11 +224,18 @@ sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, c
   p.scale = scale;
   p.scale_log2 = scale * sv::kLog2e;
   p.tree = tree;
-  if (plan.ws_bytes > 0) {
-    p.part_o = static_cast<float *>(workspace);
-    p.part_ml = p.part_o + (size_t)B * Hkv * plan.splits * plan.Mpad * D;
+  cudaError_t e;
+  if (use_tc) {
+    e = sv::launch_attention_tc(p, tplan, workspace, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) sv::count_launches(1);
+  } else {
+    if (plan.ws_bytes > 0) {
+      p.part_o = static_cast<float *>(workspace);
+      p.part_ml = p.part_o + (size_t)B * Hkv * plan.splits * plan.Mpad * D;
+    }
+    e = sv::launch_attention(dt, p, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) sv::count_launches(dt == SV_BF16 && plan.splits > 1 ? 2 : 1);
   }
-  cudaError_t e = sv::launch_attention(dt, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "tree attention launch");
   return SV_OK;
 }
@@ -266,6 +291,7 @@ sv_status accept_launch(sv_dtype dt, sv::AcceptParams &p, bool greedy, void *wor
   if (p.B == 0) return SV_OK;
   cudaError_t e = sv::launch_accept(dt, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "acceptance launch");
+  sv::count_launches(2);
   return SV_OK;
 }
 
@@ -393,6 +419,7 @@ sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_
   if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
   cudaError_t e = sv::launch_commit(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+  sv::count_launches(1);
   return SV_OK;
 }
 

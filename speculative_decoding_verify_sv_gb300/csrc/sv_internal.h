@@ -1,6 +1,7 @@
 // Internal launch parameters of the verify-step kernels (host and device).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -48,6 +49,36 @@ struct AttnPlan {
 AttnPlan attn_plan(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, int max_prefix,
                    int num_sms);
 cudaError_t launch_attention(sv_dtype dt, const AttnParams &p, cudaStream_t s);
+
+// Tensor-core (tcgen05) tree attention: persistent CTAs over a stream-K split of the
+// flattened (unit, key tile) space.
+struct TcParams {
+  CUtensorMap tm_q, tm_kt, tm_vt, tm_kc, tm_vc;  // Q, tree K/V, cache K/V (128B swizzle)
+  const int32_t *prefix_len;
+  const int32_t *block_table;
+  void *out;
+  float *part_o;          // [slots, rows, D] fp32 partial outputs of cut units
+  float *part_ml;         // [slots, rows, 2] running max (log2) and sum
+  unsigned long long *hdr;    // [0] generation of the last completed call, [1] low: CTAs done
+  unsigned long long *flags;  // [slots] epoch of the call that published each partial
+  unsigned int *status;
+  int B, N, Hq, Hkv, G, M, m_groups, upb, bn;
+  int Lmax, block_size, max_blocks, num_blocks, cap, paged, page_rows;
+  float scale_log2;
+  Tree tree;
+};
+
+struct TcPlan {
+  int MT, m_groups, grid, CP, BN;
+  size_t off_hdr, off_flags, off_ml, off_o, ws_bytes;
+};
+
+bool tc_eligible(sv_dtype dt, int N, int Hq, int Hkv, int D, const sv_kv_cache &c);
+TcPlan tc_plan(int B, int N, int Hq, int Hkv, int D, int num_sms);
+cudaError_t launch_attention_tc(const AttnParams &p, const TcPlan &pl, void *ws, cudaStream_t s);
+
+// Kernels launched by this library so far (all devices, all threads).
+void count_launches(unsigned n);
 
 // --------------------------------------------------------------- acceptance
 

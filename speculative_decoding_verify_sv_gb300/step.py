@@ -42,7 +42,8 @@ class VerifyStep:
         self.device = device or cache.k.device
         self.scale = D ** -0.5
         ws = sv_tree_attention_workspace_size(dtype, B, self.N, Hq, Hkv, D, cache.max_prefix)
-        self.attn_ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=self.device)
+        # zero before first use: the kernel keeps completion words in it
+        self.attn_ws = torch.zeros(max(ws, 16), dtype=torch.uint8, device=self.device)
         self.attn_splits = ws > 0
         Dq = self.Dmax
         self.acc_ws = torch.empty(sv_accept_workspace_size(B, self.N, V, Dq), dtype=torch.uint8,

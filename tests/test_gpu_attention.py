@@ -138,3 +138,77 @@ def test_full_size_workloads_sampled(cuda_ok, cfg, b_range):
                                 block_table=bt, block_size=w.get("block_size", 16))
     err = (out[sel].double().cpu() - ref).abs().max().item()
     assert err < TOL[dtype], err
+
+
+def test_group_not_dividing_128_uses_general_path(cuda_ok):
+    """GQA group of 3 heads: served by the mma.sync kernel."""
+    par = wl.TREE_T26
+    inp = wl.attention_inputs(2, 26, 12, 4, 128, [300, 1100], dtype=torch.bfloat16, seed=11)
+    _check(inp, par, torch.bfloat16)
+
+
+def test_rows_beyond_two_mma_tiles(cuda_ok):
+    """64 nodes x 8 group heads = 512 rows: two groups of 256 rows per KV head."""
+    par = wl.TREE_T64
+    inp = wl.attention_inputs(2, 64, 16, 2, 128, [500, 77], dtype=torch.bfloat16, seed=12)
+    _check(inp, par, torch.bfloat16)
+
+
+def test_single_unit_cut_across_all_ctas(cuda_ok):
+    """One (sequence, kv head) with a 32K prefix: every CTA holds a piece of it."""
+    par = wl.chain_parent(3)
+    inp = wl.attention_inputs(1, 4, 8, 1, 128, [32768], dtype=torch.bfloat16, seed=13)
+    _check(inp, par, torch.bfloat16)
+
+
+def test_fewer_tiles_than_ctas(cuda_ok):
+    par = wl.chain_parent(1)
+    inp = wl.attention_inputs(1, 2, 4, 1, 64, [10], dtype=torch.bfloat16, seed=14)
+    _check(inp, par, torch.bfloat16)
+
+
+def test_paged_block32_64_128_256(cuda_ok):
+    par = wl.TREE_EXAMPLE7
+    for bs in (32, 64, 128, 256):
+        inp = wl.attention_inputs(3, 7, 16, 4, 128, [700, 33, 130], dtype=torch.bfloat16,
+                                  paged=True, block_size=bs, seed=15 + bs)
+        _check(inp, par, torch.bfloat16, block_size=bs)
+
+
+def test_paged_block128_two_mma_tiles(cuda_ok):
+    """Pages of 128 rows cut into 64-key tiles (the 256-row kernel)."""
+    par = wl.TREE_T26
+    inp = wl.attention_inputs(2, 26, 64, 8, 128, [600, 129], dtype=torch.bfloat16, paged=True,
+                              block_size=128, seed=17)
+    _check(inp, par, torch.bfloat16, block_size=128)
+
+
+def test_workspace_reused_across_calls_and_shapes(cuda_ok):
+    """One zero-filled workspace serves a run of calls of different shapes; every call
+    matches a call with a fresh workspace bit for bit."""
+    cases = [(2, 26, 16, 4, 128, [900, 300], wl.TREE_T26, 21),
+             (1, 4, 8, 1, 128, [32768], wl.chain_parent(3), 22),
+             (3, 7, 16, 4, 128, [700, 33, 130], wl.TREE_EXAMPLE7, 23),
+             (2, 64, 16, 2, 128, [500, 77], wl.TREE_T64, 24)]
+    size = max(sv.sv_tree_attention_workspace_size(torch.bfloat16, B, N, Hq, Hkv, D, max(lens) + 8)
+               for B, N, Hq, Hkv, D, lens, _, _ in cases)
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        for B, N, Hq, Hkv, D, lens, par, seed in cases:
+            inp = wl.attention_inputs(B, N, Hq, Hkv, D, lens, dtype=torch.bfloat16, seed=seed)
+            g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+            cache = sv.KVCache(g["cache_k"], g["cache_v"], g["prefix_len"])
+            out = sv.sv_tree_attention(g["q"], g["k_tree"], g["v_tree"], cache, par,
+                                       1.0 / math.sqrt(D), workspace=ws)
+            torch.cuda.synchronize()
+            assert sv.sv_read_device_status() == 0
+            assert torch.equal(out, _run(inp, par, torch.bfloat16))
+
+
+def test_launch_counter_counts_kernels(cuda_ok):
+    lib = sv.load_library()
+    par = wl.chain_parent(4)
+    inp = wl.attention_inputs(2, 5, 32, 8, 128, [100, 200], dtype=torch.bfloat16, seed=16)
+    before = lib.sv_kernel_launches()
+    _run(inp, par, torch.bfloat16)
+    assert lib.sv_kernel_launches() - before >= 1
