@@ -103,6 +103,12 @@ sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, c
                             const int32_t *parent, float scale, void *out, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* Which kernel sv_tree_attention runs for these sizes: 1 = the tensor-core kernel
+ * (tcgen05 MMA into TMEM, TMA-fed), 0 = the general kernel (mma.sync for bf16, FFMA for
+ * f32), -1 = sizes it rejects.  block_size: the paged cache's block size, 0 for a
+ * contiguous cache.  Host only; no device work. */
+int sv_tree_attention_path(sv_dtype dt, int N, int Hq, int Hkv, int D, int block_size);
+
 /* Workspace bytes sv_tree_attention needs for these sizes; max_prefix is the largest
  * prefix the cache can hold (Lmax, or max_blocks*block_size when paged). */
 size_t sv_tree_attention_workspace_size(sv_dtype dt, int B, int N, int Hq, int Hkv, int D,

@@ -18,7 +18,7 @@ import torch
 
 __all__ = [
     "SVError", "KVCache", "library_path", "load_library", "sv_tree_attention",
-    "sv_tree_attention_workspace_size", "sv_accept_chain", "sv_accept_tree",
+    "sv_tree_attention_workspace_size", "sv_tree_attention_path", "sv_accept_chain", "sv_accept_tree",
     "sv_accept_workspace_size", "sv_accept_tree_noalloc", "sv_commit_kv", "sv_tree_prepare", "sv_read_device_status",
     "sv_version", "sv_kernel_launches", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "SV_MAX_TREE_NODES",
 ]
@@ -72,6 +72,8 @@ def load_library():
         P, I, F, U64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t
         lib.sv_tree_attention.argtypes = [I, I, I, I, I, I, P, P, P, _KVCacheC, P, F, P, P, SZ, P]
         lib.sv_tree_attention_workspace_size.argtypes = [I, I, I, I, I, I, I]
+        lib.sv_tree_attention_path.argtypes = [I, I, I, I, I, I]
+        lib.sv_tree_attention_path.restype = I
         lib.sv_tree_attention_workspace_size.restype = SZ
         lib.sv_accept_chain.argtypes = [I, I, I, I, I, P, P, I, P, F, I, U64, U64, P, P, P, P, P,
                                         SZ, P]
@@ -196,6 +198,12 @@ def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor], zero: boo
 def sv_tree_attention_workspace_size(dtype, B, N, Hq, Hkv, D, max_prefix) -> int:
     dt = SV_BF16 if dtype == torch.bfloat16 else SV_F32
     return int(load_library().sv_tree_attention_workspace_size(dt, B, N, Hq, Hkv, D, max_prefix))
+
+
+def sv_tree_attention_path(dtype, N, Hq, Hkv, D, block_size=0) -> int:
+    """1: the tensor-core kernel serves these sizes; 0: the general kernel; -1: rejected."""
+    dt = SV_BF16 if dtype == torch.bfloat16 else SV_F32
+    return int(load_library().sv_tree_attention_path(dt, N, Hq, Hkv, D, block_size))
 
 
 def sv_tree_attention(q, k_tree, v_tree, cache: KVCache, parent, scale, out=None,

@@ -14,10 +14,12 @@
 // per-thread online accumulation.  With top-k, a second pass gathers the few entries
 // that can be in the top k (those at or above the smallest of k disjoint group
 // maxima) into shared memory, ranks them, and sums the kept ones.
-// Kernel 2 (one CTA per sequence): per-node ratios in double from the row statistics
-// and the two logits of the candidate, the longest accepted path, and the final
-// sample: a coalesced pass summing w = [p - q]+ (or p) per warp segment, then the
-// owning warp re-walks its segment with a warp scan to find the inverse-CDF token.
+// Kernel 2 (one cluster of CTAs per sequence): per-node ratios in double from the row
+// statistics and the two logits of the candidate, the longest accepted path, and the
+// final sample: a coalesced pass summing w = [p - q]+ (or p) per warp segment of each
+// CTA's slice of the vocabulary, slice totals exchanged through distributed shared
+// memory, then the owning warp re-walks its segment with a warp scan to find the
+// inverse-CDF token.
 #include <cfloat>
 #include <climits>
 
@@ -29,7 +31,7 @@ namespace sv {
 namespace {
 
 constexpr int kStatThreads = 512;
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 256;  // two CTAs per SM
 constexpr int kMaxCand = 4096;
 constexpr double kNearTie = 1e-6;
 
@@ -76,21 +78,25 @@ __device__ void block_argmax(float &v, int &i, float *shv, int *shi) {
   __syncthreads();
 }
 
+// Block sum of per-thread float partials: a float tree within each warp, then the warp
+// totals added in double by one thread (FP64 throughput is low on this part, so no
+// per-thread double arithmetic).  Every thread gets the result.
 template <int NT>
-__device__ double block_sum_d(double v, double *sh) {
+__device__ double block_sum_f(float v, double *sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_sum_d(v);
-  if (lane == 0) sh[warp] = v;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  if (lane == 0) sh[warp] = (double)v;
   __syncthreads();
-  if (warp == 0) {
-    v = lane < NT / 32 ? sh[lane] : 0.0;
-    v = warp_sum_d(v);
-    if (lane == 0) sh[0] = v;
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < NT / 32; ++w) t += sh[w];
+    sh[NT / 32] = t;
   }
   __syncthreads();
-  v = sh[0];
+  const double r = sh[NT / 32];
   __syncthreads();
-  return v;
+  return r;
 }
 
 template <int NT>
@@ -139,7 +145,7 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(const Accept
   constexpr int NT = kStatThreads;
   __shared__ float sh_v[32];
   __shared__ int sh_i[32];
-  __shared__ double sh_d[32];
+  __shared__ double sh_d[33];
   __shared__ unsigned sh_u[32];
 
   const int tid = threadIdx.x;
@@ -153,35 +159,58 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(const Accept
 
   float vmax = -INFINITY;
   int imax = INT_MAX;
-  float m = -INFINITY;
+  float m = -INFINITY;  // running maximum the partial sum is taken against
   KahanF acc;
   uint32_t umax[2] = {0u, 0u};  // TOPK: per-unit max key (units: even / odd lanes)
 
-  for (int v = tid; v < nvec; v += NT) {
-    const uint4 raw = __ldg(xv + v);
-    float f[VEC];
-    Elem<T>::unpack(raw, f);
-    float vm = f[0];
+  // each thread takes vectors tid, tid + NT, ... in index order, four at a time, all
+  // four loaded before any is used; vectors past the end read as -inf
+  constexpr int U = 4;
+  const uint4 ninf = make_uint4(Elem<T>::kNegInfWord, Elem<T>::kNegInfWord,
+                                Elem<T>::kNegInfWord, Elem<T>::kNegInfWord);
+  for (int v0 = tid; v0 < nvec; v0 += NT * U) {
+    uint4 raws[U];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      if (f[e] > vmax) vmax = f[e], imax = v * VEC + e;
-      vm = fmaxf(vm, f[e]);
-      if (TOPK) umax[e & 1] = max(umax[e & 1], Elem<T>::key(f[e]));
+    for (int u = 0; u < U; ++u) raws[u] = v0 + u * NT < nvec ? __ldg(xv + v0 + u * NT) : ninf;
+    float f[U][VEC];
+#pragma unroll
+    for (int u = 0; u < U; ++u) Elem<T>::unpack(raws[u], f[u]);
+    // the batch maximum first; the index scan runs only when it beats the running max
+    float mx = f[0][0];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) mx = fmaxf(mx, f[u][e]);
+    if (mx > vmax) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+          if (f[u][e] > vmax) vmax = f[u][e], imax = (v0 + u * NT) * VEC + e;
     }
-    if (!GREEDY && !TOPK) {
-      if (vm > m) {
+    if constexpr (TOPK) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (v0 + u * NT < nvec)
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) umax[e & 1] = max(umax[e & 1], Elem<T>::key(f[u][e]));
+    }
+    if constexpr (!GREEDY && !TOPK) {
+      if (vmax > m) {  // vmax: the largest value this thread has seen
         if (m != -INFINITY) {
-          const float s = exp2f((m - vm) * c);
-          acc.s *= s;
-          acc.c *= s;
+          const float sc = ex2_approx((m - vmax) * c);
+          acc.s *= sc;
+          acc.c *= sc;
         }
-        m = vm;
+        m = vmax;
       }
       if (m != -INFINITY) {
-        float vs = 0.f;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) vs += exp2f((f[e] - m) * c);
-        acc.add(vs);
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) ps[e & 3] += ex2_approx((f[u][e] - m) * c);
+        acc.add((ps[0] + ps[1]) + (ps[2] + ps[3]));
       }
     }
   }
@@ -198,8 +227,8 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(const Accept
   st.S = 0.0;
 
   if constexpr (!GREEDY && !TOPK) {
-    const double part = m == -INFINITY ? 0.0 : acc.value() * (double)exp2f((m - zmax) * c);
-    st.S = block_sum_d<NT>(part, sh_d);
+    const float part = m == -INFINITY ? 0.f : acc.value() * exp2f((m - zmax) * c);
+    st.S = block_sum_f<NT>(part, sh_d);
   }
 
   if constexpr (TOPK) {
@@ -219,15 +248,23 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(const Accept
     __syncthreads();
     const uint32_t tau = tau_sh;
     // gather the entries at or above tau
-    for (int v = tid; v < nvec; v += NT) {
-      const uint4 raw = __ldg(xv + v);
-      float f[VEC];
-      Elem<T>::unpack(raw, f);
+    for (int v0 = tid; v0 < nvec; v0 += NT * U) {
+      uint4 raws[U];
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        if (Elem<T>::key(f[e]) >= tau) {
-          const unsigned slot = atomicAdd(&n_cand, 1u);
-          if (slot < kMaxCand) cand[slot] = Cand{f[e], v * VEC + e};
+      for (int u = 0; u < U; ++u)
+        if (v0 + u * NT < nvec) raws[u] = __ldg(xv + v0 + u * NT);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * NT;
+        if (v >= nvec) break;
+        float f[VEC];
+        Elem<T>::unpack(raws[u], f);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          if (Elem<T>::key(f[e]) >= tau) {
+            const unsigned slot = atomicAdd(&n_cand, 1u);
+            if (slot < kMaxCand) cand[slot] = Cand{f[e], v * VEC + e};
+          }
         }
       }
     }
@@ -237,7 +274,7 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(const Accept
       // rank every candidate: entries beating it (larger value, or equal and lower id)
       __shared__ uint32_t thr_key;
       __shared__ int thr_idx;
-      double part = 0.0;
+      float part = 0.f;
       for (unsigned i = tid; i < nc; i += NT) {
         const Cand ci = cand[i];
         unsigned rank = 0;
@@ -245,13 +282,13 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(const Accept
           const Cand cj = cand[j];
           rank += (cj.z > ci.z || (cj.z == ci.z && cj.idx < ci.idx)) ? 1u : 0u;
         }
-        if (rank < (unsigned)k) part += (double)exp2f((ci.z - zmax) * c);
+        if (rank < (unsigned)k) part += exp2f((ci.z - zmax) * c);
         if (rank == (unsigned)k - 1u) thr_key = Elem<T>::key(ci.z), thr_idx = ci.idx;
       }
       __syncthreads();
       st.key_k = thr_key;
       st.idx_k = thr_idx;
-      st.S = block_sum_d<NT>(part, sh_d);
+      st.S = block_sum_f<NT>(part, sh_d);
     } else {
       // many equal values near the top: find the threshold key bit by bit with counting
       // passes, then the index cut among entries equal to it, then the kept sum
@@ -330,7 +367,7 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(const Accept
           vs += kept<T>(f[e], v * VEC + e, st) ? exp2f((f[e] - zmax) * c) : 0.f;
         s2.add(vs);
       }
-      st.S = block_sum_d<NT>(s2.value(), sh_d);
+      st.S = block_sum_f<NT>(s2.value(), sh_d);
     }
   }
 
@@ -338,20 +375,78 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(const Accept
 }
 
 // ------------------------------------------------------------ kernel 2
+//
+// One thread-block cluster of C CTAs per sequence.  Every CTA takes the node decisions
+// (they are cheap and identical everywhere), so all know the kept path; the final
+// sample's vocabulary pass is split over the cluster: CTA r sums the weights of its
+// slice in chunks of 32 vectors (kept in shared memory), the CTAs read each other's
+// slice totals through distributed shared memory, and in the CTA whose slice holds
+// u * total one warp finds the chunk from the chunk sums and the token inside it.
+// Every CTA runs the same sequence of cluster barriers: each branch that decides a
+// barrier depends only on values that all CTAs of the cluster compute alike.
+// FP64 throughput is low on this part: double arithmetic is kept to a few operations
+// per thread (cumulative sums across chunks, and decisions within 1e-4 of u).
 
-template <typename T, bool GREEDY>
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ unsigned cluster_size() {
+  unsigned n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// Read a double from the same shared-memory variable of CTA `rank` in this cluster.
+__device__ __forceinline__ double ld_peer_f64(const double *local, unsigned rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_incl_scan_f(float v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+constexpr int kMaxCluster = 16;
+constexpr int kMaxChunks = 4096;          // chunk sums one CTA keeps (32 vectors each)
+constexpr double kDecideMargin = 1e-4;    // float ratio this close to u: decide in double
+
+template <typename T, bool GREEDY, bool TOPK>
 __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const AcceptParams p) {
   constexpr int VEC = Elem<T>::kVec;
   constexpr int NW = kSelThreads / 32;
+  constexpr int QV = VEC / 4;  // 16-byte vectors of f32 q probabilities per VEC entries
   __shared__ int8_t s_par[kMaxNodes], s_dep[kMaxNodes], s_hc[kMaxNodes];
   __shared__ uint8_t s_acc[kMaxNodes], s_dnear[kMaxNodes];
   __shared__ int s_best, s_nd;
   __shared__ double seg_sum[NW];
-  __shared__ int s_wstar, s_tok, s_snear, s_found;
+  __shared__ double s_slice[2];  // this CTA's slice total, per attempt (read by peers)
+  __shared__ double s_tots[kMaxCluster];
+  __shared__ float s_chunk[kMaxChunks];
+  __shared__ int s_wstar, s_tok, s_snear, s_rstar;
   __shared__ double s_base, s_t;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.x;
+  const unsigned C = cluster_size(), rank = cluster_rank();
+  const int b = blockIdx.x / (int)C;
   const int N = p.tree.N, V = p.V;
   if (tid < kMaxNodes) {
     s_par[tid] = p.tree.parent[tid];
@@ -366,61 +461,99 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
   const RowStat *qstat = p.stats + (size_t)p.B * N + (size_t)b * p.Dq;
   const double temp = (double)p.temperature;
 
-  // decisions, one thread per non-root node
+  // decisions, one thread per non-root node: accept iff u_acc < p(x)/q(x).  The ratio
+  // is formed in float; when it falls within kDecideMargin (relative) of u it is
+  // recomputed in double, so every decision is the one double precision takes.
   if (tid >= 1 && tid < N) {
     const int cnode = tid, a = s_par[cnode], d = s_dep[cnode];
     const int xt = p.tokens[(size_t)b * p.tok_stride + cnode - p.tok_offset];
     uint8_t acc = 0, dn = 0;
     if (xt < 0 || xt >= V) {
-      set_status(p.status, SV_DEV_BAD_TOKEN);
+      if (rank == 0) set_status(p.status, SV_DEV_BAD_TOKEN);
     } else if (GREEDY) {
       acc = xt == tstat[a].argmax;
     } else {
       const RowStat sa = tstat[a];
       const float zp = Elem<T>::load(row_ptr<T>(p.target, (size_t)b * N + a, V) + xt);
-      const double pp = kept<T>(zp, xt, sa) ? exp(((double)zp - (double)sa.zmax) / temp) / sa.S : 0.0;
-      double qq;
-      if (p.q_kind == SV_Q_LOGITS) {
-        const RowStat sq = qstat[d - 1];
-        const float zq = Elem<T>::load(row_ptr<T>(p.q, (size_t)b * p.Dq + d - 1, V) + xt);
-        qq = kept<T>(zq, xt, sq) ? exp(((double)zq - (double)sq.zmax) / temp) / sq.S : 0.0;
+      const bool kp = kept<T>(zp, xt, sa);
+      bool logits = p.q_kind == SV_Q_LOGITS;
+      RowStat sq{};
+      float zq = 0.f, qprob = 0.f;
+      bool kq = true;
+      if (logits) {
+        sq = qstat[d - 1];
+        zq = Elem<T>::load(row_ptr<T>(p.q, (size_t)b * p.Dq + d - 1, V) + xt);
+        kq = kept<T>(zq, xt, sq);
       } else {
-        qq = (double)(static_cast<const float *>(p.q)[((size_t)b * p.Dq + d - 1) * V + xt]);
-      }
-      double ratio;
-      if (qq > 0.0) {
-        ratio = pp / qq;
-      } else {
-        set_status(p.status, SV_DEV_ZERO_DRAFT_PROB);
-        ratio = pp > 0.0 ? INFINITY : 0.0;
+        qprob = static_cast<const float *>(p.q)[((size_t)b * p.Dq + d - 1) * V + xt];
       }
       double u_acc, u_smp;
       verify_uniforms(p.seed, p.round, b, cnode, &u_acc, &u_smp);
-      acc = u_acc < ratio;
-      dn = fabs(u_acc - ratio) < kNearTie;
+      const bool q_zero = logits ? !kq : !(qprob > 0.f);
+      if (q_zero) {
+        if (rank == 0) set_status(p.status, SV_DEV_ZERO_DRAFT_PROB);
+        acc = kp;  // ratio +inf when p > 0, else 0
+      } else if (!kp) {
+        acc = 0;  // ratio 0
+        dn = u_acc < kNearTie;
+      } else {
+        const float cf = p.c_log2;
+        float rf;
+        if (logits)
+          rf = exp2f(((zp - sa.zmax) - (zq - sq.zmax)) * cf) * (float)(sq.S / sa.S);
+        else
+          rf = exp2f((zp - sa.zmax) * cf) / ((float)sa.S * qprob);
+        const double r = (double)rf;
+        if (fabs(u_acc - r) > kDecideMargin * (1.0 + r)) {
+          acc = u_acc < r;
+        } else {
+          const double pp = exp(((double)zp - (double)sa.zmax) / temp) / sa.S;
+          const double qq = logits ? exp(((double)zq - (double)sq.zmax) / temp) / sq.S : (double)qprob;
+          const double ratio = pp / qq;
+          acc = u_acc < ratio;
+          dn = fabs(u_acc - ratio) < kNearTie;
+        }
+      }
     }
     s_acc[cnode] = acc;
     s_dnear[cnode] = dn;
   }
   __syncthreads();
 
+  // the kept path: node c is on it iff c and all its ancestors were accepted (the root
+  // always is); best = the deepest such node, lowest index among equals.  Threads
+  // 0..63 take one node each: ancestor masks from the parent chain, then ballots.
   if (tid == 0) {
-    uint8_t ok[kMaxNodes];
-    ok[0] = 1;
-    int best = 0, nd = 0;
-    for (int cn = 1; cn < N; ++cn) {
-      const int a = s_par[cn];
-      ok[cn] = ok[a] && s_acc[cn];
-      if (ok[a] && s_dnear[cn]) ++nd;
-      if (ok[cn] && s_dep[cn] > s_dep[best]) best = cn;
-    }
-    s_best = best;
-    s_nd = nd;
+    s_best = 0;
+    s_nd = 0;
     s_snear = 0;
     s_tok = -1;
+    s_wstar = -1;
+    s_rstar = -1;
   }
   __syncthreads();
+  if (tid < kMaxNodes) {
+    const bool live = tid < N;
+    uint64_t anc = 0;
+    if (live)
+      for (int a = tid; a >= 0; a = s_par[a]) anc |= 1ull << a;
+    const bool acc_self = tid == 0 || (live && s_acc[tid]);
+    const unsigned w = __ballot_sync(0xFFFFFFFFu, acc_self);
+    __shared__ unsigned s_accw[2];
+    if (lane == 0) s_accw[warp] = w;
+    // both warps' ballots are needed: warps 0 and 1 meet at a named barrier
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    const uint64_t accm = (uint64_t)s_accw[0] | ((uint64_t)s_accw[1] << 32);
+    const bool ok = live && (anc & ~accm) == 0;
+    const bool ok_par = live && tid > 0 && ((anc & ~(1ull << tid)) & ~accm) == 0;
+    if (ok) atomicMax(&s_best, (s_dep[tid] << 8) | (255 - tid));
+    if (ok_par && s_dnear[tid]) atomicAdd(&s_nd, 1);
+  }
+  __syncthreads();
+  if (tid == 0) s_best = 255 - (s_best & 255);
+  __syncthreads();
   const int best = s_best;
+  bool writer = rank == 0;  // the CTA that writes the sequence's outputs
 
   if constexpr (GREEDY) {
     if (tid == 0) s_tok = tstat[best].argmax;
@@ -430,10 +563,11 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
     const uint4 *pv = reinterpret_cast<const uint4 *>(row_ptr<T>(p.target, (size_t)b * N + best, V));
     bool use_q = s_hc[best] != 0;
     const int qrow = s_dep[best];  // q row of depth d+1
+    const bool q_probs = p.q_kind == SV_Q_PROBS_F32;
     RowStat sq{};
     const uint4 *qv = nullptr;
     if (use_q) {
-      if (p.q_kind == SV_Q_LOGITS) {
+      if (!q_probs) {
         sq = qstat[qrow];
         qv = reinterpret_cast<const uint4 *>(row_ptr<T>(p.q, (size_t)b * p.Dq + qrow, V));
       } else {
@@ -443,124 +577,204 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
     }
     const float c = p.c_log2;
     const float inv_sp = (float)(1.0 / sp.S);
-    const float inv_sq = use_q && p.q_kind == SV_Q_LOGITS ? (float)(1.0 / sq.S) : 0.f;
+    const float inv_sq = use_q && !q_probs ? (float)(1.0 / sq.S) : 0.f;
     const int nvec = V / VEC;
-    const int seg = (nvec + NW - 1) / NW;
-    const int s0 = min(nvec, warp * seg), s1 = min(nvec, s0 + seg);
-    const bool q_probs = p.q_kind == SV_Q_PROBS_F32;
+    // this CTA's slice of the vectors, each warp's segment of the slice, and the
+    // segment's chunks of 32 vectors (chunk k of warp w at s_chunk[w * cpw + k])
+    const int per_cta = (nvec + (int)C - 1) / (int)C;
+    const int c0 = min(nvec, (int)rank * per_cta), c1 = min(nvec, c0 + per_cta);
+    const int seg = (c1 - c0 + NW - 1) / NW;
+    const int s0 = min(c1, c0 + warp * seg), s1 = min(c1, s0 + seg);
+    const int cpw = (seg + 31) / 32;
+    const bool keep_chunks = cpw * NW <= kMaxChunks;  // same in every CTA and warp
 
-    // weights of the VEC entries of vector v
-    auto weights = [&](int v, float w[VEC], bool with_q) {
-      float f[VEC];
-      Elem<T>::unpack(__ldg(pv + v), f);
+    struct Raw {
+      uint4 p, q[QV > 0 ? QV : 1];
+    };
+    auto load_raw = [&](int v, bool with_q) -> Raw {
+      Raw r;
+      r.p = __ldg(pv + v);
+      if (with_q) {
+        if (q_probs) {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e)
-        w[e] = kept<T>(f[e], v * VEC + e, sp) ? exp2f((f[e] - sp.zmax) * c) * inv_sp : 0.f;
+          for (int h = 0; h < QV; ++h) r.q[h] = __ldg(qv + (size_t)v * QV + h);
+        } else {
+          r.q[0] = __ldg(qv + v);
+        }
+      }
+      return r;
+    };
+    // weights of the VEC entries of vector v (top-k membership checked only with top-k)
+    auto weights = [&](int v, const Raw &r, float w[VEC], bool with_q) {
+      float f[VEC];
+      Elem<T>::unpack(r.p, f);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        w[e] = ex2_approx((f[e] - sp.zmax) * c) * inv_sp;
+        if (TOPK && !kept<T>(f[e], v * VEC + e, sp)) w[e] = 0.f;
+      }
       if (with_q) {
         float g[VEC];
         if (q_probs) {
-          // float32 probabilities: a 16-byte vector holds 4, VEC may be 8
 #pragma unroll
-          for (int h = 0; h < VEC / 4; ++h) {
-            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-                                        static_cast<const float *>(p.q) +
-                                        ((size_t)b * p.Dq + qrow) * V) +
-                                    (size_t)v * (VEC / 4) + h);
-            g[4 * h] = __uint_as_float(raw.x);
-            g[4 * h + 1] = __uint_as_float(raw.y);
-            g[4 * h + 2] = __uint_as_float(raw.z);
-            g[4 * h + 3] = __uint_as_float(raw.w);
+          for (int h = 0; h < QV; ++h) {
+            g[4 * h] = __uint_as_float(r.q[h].x);
+            g[4 * h + 1] = __uint_as_float(r.q[h].y);
+            g[4 * h + 2] = __uint_as_float(r.q[h].z);
+            g[4 * h + 3] = __uint_as_float(r.q[h].w);
           }
         } else {
           float fq[VEC];
-          Elem<T>::unpack(__ldg(qv + v), fq);
+          Elem<T>::unpack(r.q[0], fq);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e)
-            g[e] = kept<T>(fq[e], v * VEC + e, sq) ? exp2f((fq[e] - sq.zmax) * c) * inv_sq : 0.f;
+          for (int e = 0; e < VEC; ++e) {
+            g[e] = ex2_approx((fq[e] - sq.zmax) * c) * inv_sq;
+            if (TOPK && !kept<T>(fq[e], v * VEC + e, sq)) g[e] = 0.f;
+          }
         }
 #pragma unroll
         for (int e = 0; e < VEC; ++e) w[e] = fmaxf(w[e] - g[e], 0.f);
       }
+    };
+    auto vec_sum = [&](int v, const Raw &r, bool with_q) -> float {
+      float w[VEC];
+      weights(v, r, w, with_q);
+      float vs = 0.f;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) vs += w[e];
+      return vs;
     };
 
     double u_acc, u_smp;
     verify_uniforms(p.seed, p.round, b, best, &u_acc, &u_smp);
 
     for (int attempt = 0; attempt < 2; ++attempt) {
-      // phase 1: per-warp segment sums (lanes interleave, Kahan per lane)
-      KahanF ls;
-      for (int v = s0 + lane; v < s1; v += 32) {
-        float w[VEC];
-        weights(v, w, use_q);
-        float vs = 0.f;
+      // phase 1: chunk k of the warp's segment = its vectors [s0 + 32k, s0 + 32k + 32),
+      // lane i taking vector s0 + 32k + i; four chunks are loaded before any is used
+      constexpr int U = 4;
+      double wsum = 0.0;  // lane 0: the segment total
+      for (int k0 = 0; s0 + 32 * k0 < s1; k0 += U) {
+        Raw r[U];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) vs += w[e];
-        ls.add(vs);
+        for (int u = 0; u < U; ++u) {
+          const int v = s0 + 32 * (k0 + u) + lane;
+          if (v < s1) r[u] = load_raw(v, use_q);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v0 = s0 + 32 * (k0 + u);
+          if (v0 >= s1) break;
+          const float cs = warp_sum_f(v0 + lane < s1 ? vec_sum(v0 + lane, r[u], use_q) : 0.f);
+          if (lane == 0) {
+            if (keep_chunks) s_chunk[warp * cpw + k0 + u] = cs;
+            wsum += (double)cs;
+          }
+        }
       }
-      const double wsum = warp_sum_d(ls.value());
       if (lane == 0) seg_sum[warp] = wsum;
       __syncthreads();
       if (tid == 0) {
+        double tot = 0.0;
+        for (int w = 0; w < NW; ++w) tot += seg_sum[w];
+        s_slice[attempt] = tot;
+      }
+      cluster_sync_all();
+      if (tid < (int)C) s_tots[tid] = ld_peer_f64(&s_slice[attempt], (unsigned)tid);
+      __syncthreads();
+      if (tid == 0) {
+        // every CTA finds the same slice (same totals, same order)
+        const double *tots = s_tots;
         double total = 0.0;
-        for (int w = 0; w < NW; ++w) total += seg_sum[w];
-        if (!(total > 0.0)) {
-          s_wstar = -1;  // residual has no mass: sample from p instead (reported)
-        } else {
+        for (int r = 0; r < (int)C; ++r) total += tots[r];
+        s_rstar = -1;
+        if (total > 0.0) {
           const double t = u_smp * total;
-          double run = 0.0;
-          int ws = -1, last = -1;
-          double last_base = 0.0;
-          for (int w = 0; w < NW; ++w) {
-            if (seg_sum[w] > 0.0) last = w, last_base = run;
-            if (ws < 0 && run + seg_sum[w] > t) {
-              ws = w;
-              s_base = run;
+          double run = 0.0, last_base = 0.0, base_r = 0.0;
+          int last = -1, rs = -1;
+          for (int r = 0; r < (int)C; ++r) {
+            if (tots[r] > 0.0) last = r, last_base = run;
+            if (rs < 0 && run + tots[r] > t) rs = r, base_r = run;
+            run += tots[r];
+          }
+          if (rs < 0) rs = last, base_r = last_base;  // rounding put t at the very end
+          s_rstar = rs;
+          if ((int)rank == rs) {
+            // the warp segment within this slice
+            double runw = base_r, lastw_base = base_r;
+            int ws = -1, lastw = -1;
+            for (int w = 0; w < NW; ++w) {
+              if (seg_sum[w] > 0.0) lastw = w, lastw_base = runw;
+              if (ws < 0 && runw + seg_sum[w] > t) ws = w, s_base = runw;
+              runw += seg_sum[w];
             }
-            run += seg_sum[w];
+            if (ws < 0) ws = lastw, s_base = lastw_base;
+            s_wstar = ws;
+            s_t = t;
           }
-          if (ws < 0) {  // rounding put t at the very end: last segment with mass
-            ws = last;
-            s_base = last_base;
-          }
-          s_wstar = ws;
-          s_t = t;
         }
       }
       __syncthreads();
-      if (s_wstar >= 0 || attempt == 1) break;
+      if (s_rstar >= 0) break;
+      // the residual has no mass: sample from p instead (reported)
       use_q = false;
       if (tid == 0) s_snear = 1;
-      __syncthreads();
     }
+    const int rstar = s_rstar;
+    writer = (int)rank == (rstar < 0 ? 0 : rstar);
 
-    // phase 2: the owning warp walks its segment in index order
-    if (warp == s_wstar) {
+    // phase 2: the owning warp finds the chunk from the chunk sums, then the token in it
+    if ((int)rank == rstar && warp == s_wstar) {
       const double t = s_t;
       double base = s_base;
       int found = 0, tok = -1, near = 0, last_pos = -1;
-      for (int v0 = s0; v0 < s1 && !found; v0 += 32) {
-        const int v = v0 + lane;
+      const int nch = (s1 - s0 + 31) / 32;
+      int k_first = 0;
+      if (keep_chunks) {
+        // first chunk whose end passes t (else the last one with mass)
+        int kstar = -1, klast = -1;
+        double base_k = base, base_last = base;
+        for (int k0 = 0; k0 < nch && kstar < 0; k0 += 32) {
+          const float x = k0 + lane < nch ? s_chunk[warp * cpw + k0 + lane] : 0.f;
+          const float incl = warp_incl_scan_f(x);
+          const double before = base + (double)(incl - x);
+          const unsigned hit = __ballot_sync(0xFFFFFFFFu, k0 + lane < nch && before + (double)x > t);
+          const unsigned pos = __ballot_sync(0xFFFFFFFFu, k0 + lane < nch && x > 0.f);
+          if (pos) {
+            const int L = 31 - __clz(pos);
+            klast = k0 + L;
+            base_last = __shfl_sync(0xFFFFFFFFu, before, L);
+          }
+          if (hit) {
+            const int L = __ffs(hit) - 1;
+            kstar = k0 + L;
+            base_k = __shfl_sync(0xFFFFFFFFu, before, L);
+          }
+          base += (double)__shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (kstar < 0) kstar = klast, base_k = base_last;
+        if (kstar < 0) kstar = 0, base_k = s_base;
+        k_first = kstar;
+        base = base_k;
+      }
+      for (int k = k_first; k < nch && !found; ++k) {
+        const int v = s0 + 32 * k + lane;
         float w[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) w[e] = 0.f;
-        if (v < s1) weights(v, w, use_q);
+        if (v < s1) weights(v, load_raw(v, use_q), w, use_q);
         float lsum = 0.f;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
           lsum += w[e];
           if (w[e] > 0.f) last_pos = v * VEC + e;
         }
-        double incl = (double)lsum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, base + incl > t);
+        const float incl = warp_incl_scan_f(lsum);
+        const double before = base + (double)(incl - lsum);
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, before + (double)lsum > t);
         if (hit) {
           const int L = __ffs(hit) - 1;
           if (lane == L) {
-            double cum = base + incl - (double)lsum;
+            double cum = before;
             int j = -1, lastp = -1;
             for (int e = 0; e < VEC; ++e) {
               if (w[e] <= 0.f) continue;
@@ -580,7 +794,8 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
           near = __shfl_sync(0xFFFFFFFFu, near, L);
           found = 1;
         }
-        base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        base += (double)__shfl_sync(0xFFFFFFFFu, incl, 31);
+        if (keep_chunks && !found) break;  // rounding: t fell past the chunk's end
       }
       if (!found) {
         int lp = last_pos;
@@ -594,10 +809,12 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
         s_snear |= near;
       }
     }
+    // no CTA leaves while a peer may still read its slice totals
+    cluster_sync_all();
   }
   __syncthreads();
 
-  if (tid == 0) {
+  if (tid == 0 && writer) {
     const int W = p.tree.Dmax + 1;
     const int depth = s_dep[best];
     int32_t *tk = p.out_tokens + (size_t)b * W;
@@ -617,8 +834,45 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
   }
 }
 
+// CTAs per sequence for the final sample: enough clusters to cover the SMs, at most 16.
+int select_cluster(int B, int num_sms) {
+  int C = 1;
+  while (C < kMaxCluster && (long long)B * C * 2 <= num_sms) C *= 2;
+  return C;
+}
+
+template <typename T, bool GREEDY, bool TOPK>
+cudaError_t launch_select(const AcceptParams &p, int num_sms, cudaStream_t s) {
+  auto kern = accept_select_kernel<T, GREEDY, TOPK>;
+  int C = GREEDY ? 1 : select_cluster(p.B, num_sms);
+  if (C > 8) {
+    static bool big_ok[64] = {false}, tried[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !tried[dev]) {
+      tried[dev] = true;
+      big_ok[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                    cudaSuccess;
+      cudaGetLastError();
+    }
+    if (dev < 0 || dev >= 64 || !big_ok[dev]) C = 8;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * C));
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 template <typename T>
-cudaError_t launch_typed(const AcceptParams &p, cudaStream_t s) {
+cudaError_t launch_typed(const AcceptParams &p, int num_sms, cudaStream_t s) {
   const bool greedy = p.mode == SV_GREEDY;
   const bool topk = !greedy && p.top_k > 0 && p.top_k < p.V;
   const int rows = p.B * p.N + ((!greedy && p.q_kind == SV_Q_LOGITS) ? p.B * p.Dq : 0);
@@ -630,11 +884,9 @@ cudaError_t launch_typed(const AcceptParams &p, cudaStream_t s) {
     accept_stats_kernel<T, false, false><<<rows, kStatThreads, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (greedy)
-    accept_select_kernel<T, true><<<p.B, kSelThreads, 0, s>>>(p);
-  else
-    accept_select_kernel<T, false><<<p.B, kSelThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  if (greedy) return launch_select<T, true, false>(p, num_sms, s);
+  return topk ? launch_select<T, false, true>(p, num_sms, s)
+              : launch_select<T, false, false>(p, num_sms, s);
 }
 
 }  // namespace
@@ -643,8 +895,8 @@ size_t accept_ws_bytes(int B, int N, int Dq) {
   return (size_t)B * (size_t)(N + Dq) * sizeof(RowStat);
 }
 
-cudaError_t launch_accept(sv_dtype dt, const AcceptParams &p, cudaStream_t s) {
-  return dt == SV_F32 ? launch_typed<float>(p, s) : launch_typed<bf16>(p, s);
+cudaError_t launch_accept(sv_dtype dt, const AcceptParams &p, int num_sms, cudaStream_t s) {
+  return dt == SV_F32 ? launch_typed<float>(p, num_sms, s) : launch_typed<bf16>(p, num_sms, s);
 }
 
 }  // namespace sv

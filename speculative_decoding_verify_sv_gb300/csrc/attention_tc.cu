@@ -968,13 +968,13 @@ bool map3d(CUtensorMap *m, const void *base, int D, int heads, long long rows, i
 
 }  // namespace
 
-bool tc_eligible(sv_dtype dt, int N, int Hq, int Hkv, int D, const sv_kv_cache &c) {
-  if (dt != SV_BF16 || (D != 64 && D != 128) || N > 64) return false;
+bool tc_eligible(sv_dtype dt, int N, int Hq, int Hkv, int D, int paged_block_size) {
+  if (dt != SV_BF16 || (D != 64 && D != 128) || N > 64 || Hkv < 1 || Hq % Hkv != 0) return false;
   const int G = Hq / Hkv;
   if (G < 1 || G > 128 || 128 % G != 0) return false;
-  if (c.block_table) {
+  if (paged_block_size > 0) {
     // a tile's rows must be whole pages or whole 128-row spans of a page
-    const int bs = c.block_size;
+    const int bs = paged_block_size;
     if (!(bs == 16 || bs == 32 || bs == 64 || (bs >= 128 && bs % 128 == 0))) return false;
   }
   return encoder() != nullptr;

@@ -164,6 +164,13 @@ size_t sv_tree_attention_workspace_size(sv_dtype dt, int B, int N, int Hq, int H
   return ws;
 }
 
+int sv_tree_attention_path(sv_dtype dt, int N, int Hq, int Hkv, int D, int block_size) {
+  if ((dt != SV_F32 && dt != SV_BF16) || N < 1 || N > SV_MAX_TREE_NODES || Hq < 1 || Hkv < 1 ||
+      Hq % Hkv != 0 || (D != 64 && D != 128) || block_size < 0)
+    return -1;
+  return sv::tc_eligible(dt, N, Hq, Hkv, D, block_size) ? 1 : 0;
+}
+
 sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, const void *q,
                             const void *k_tree, const void *v_tree, sv_kv_cache cache,
                             const int32_t *parent, float scale, void *out, void *workspace,
@@ -183,7 +190,7 @@ sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, c
   if (B == 0) return SV_OK;
   const int max_prefix = max_prefix_of(cache);
   const sv::AttnPlan plan = sv::attn_plan(dt, B, N, Hq, Hkv, D, max_prefix, num_sms());
-  const bool use_tc = sv::tc_eligible(dt, N, Hq, Hkv, D, cache);
+  const bool use_tc = sv::tc_eligible(dt, N, Hq, Hkv, D, cache.block_table ? cache.block_size : 0);
   const sv::TcPlan tplan = use_tc ? sv::tc_plan(B, N, Hq, Hkv, D, num_sms()) : sv::TcPlan{};
   const size_t ws_need = use_tc ? tplan.ws_bytes : plan.ws_bytes;
   if (ws_need > 0) {
@@ -289,7 +296,7 @@ sv_status accept_launch(sv_dtype dt, sv::AcceptParams &p, bool greedy, void *wor
   if (p.top_k >= p.V) p.top_k = 0;
   p.stats = static_cast<sv::RowStat *>(workspace);
   if (p.B == 0) return SV_OK;
-  cudaError_t e = sv::launch_accept(dt, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = sv::launch_accept(dt, p, num_sms(), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "acceptance launch");
   sv::count_launches(2);
   return SV_OK;

@@ -43,6 +43,7 @@ struct Elem<bf16> {
     return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
   }
   static constexpr int kKeyBits = 16;
+  static constexpr uint32_t kNegInfWord = 0xFF80FF80u;  // two bf16 -inf
 };
 
 template <>
@@ -60,7 +61,16 @@ struct Elem<float> {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   }
   static constexpr int kKeyBits = 32;
+  static constexpr uint32_t kNegInfWord = 0xFF800000u;
 };
+
+// 2^x by the hardware's approximate exponential (one MUFU op, subnormal results
+// flushed to zero); relative error about 2^-22.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // ------------------------------------------------------------------ Philox
 

@@ -73,7 +73,8 @@ struct TcPlan {
   size_t off_hdr, off_flags, off_ml, off_o, ws_bytes;
 };
 
-bool tc_eligible(sv_dtype dt, int N, int Hq, int Hkv, int D, const sv_kv_cache &c);
+// paged_block_size: the cache's block size, or 0 for a contiguous cache
+bool tc_eligible(sv_dtype dt, int N, int Hq, int Hkv, int D, int paged_block_size);
 TcPlan tc_plan(int B, int N, int Hq, int Hkv, int D, int num_sms);
 cudaError_t launch_attention_tc(const AttnParams &p, const TcPlan &pl, void *ws, cudaStream_t s);
 
@@ -112,7 +113,7 @@ struct AcceptParams {
 };
 
 size_t accept_ws_bytes(int B, int N, int Dq);
-cudaError_t launch_accept(sv_dtype dt, const AcceptParams &p, cudaStream_t s);
+cudaError_t launch_accept(sv_dtype dt, const AcceptParams &p, int num_sms, cudaStream_t s);
 
 // ------------------------------------------------------------------- commit
 
