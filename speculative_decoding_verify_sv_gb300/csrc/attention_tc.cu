@@ -334,6 +334,9 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
     };
     int g = 0, gv = 0, nq = 0;  // K tiles, V tiles and Q pieces issued
     bool ok = true;
+    // the cache is streamed once: its lines go first when L2 needs room, which keeps
+    // the partial outputs of cut units resident until they are merged
+    const uint64_t stream_policy = l2_policy_evict_first();
     // lane 0 waits; the outcome is shared with the warp
     auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
       int r = 1;
@@ -352,8 +355,13 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
       if (src.kind != 2) {
         if (lane == 0) {
           mbar_expect_tx(full, Lay::KV_BYTES);
-          for (int kb = 0; kb < Lay::KB; ++kb)
-            tma_load_3d(dst + kb * Lay::KV_BLOCK, map, kb * 64, src.kvh, src.row, full);
+          for (int kb = 0; kb < Lay::KB; ++kb) {
+            if (src.kind == 0)
+              tma_load_3d(dst + kb * Lay::KV_BLOCK, map, kb * 64, src.kvh, src.row, full);
+            else
+              tma_load_3d_hint(dst + kb * Lay::KV_BLOCK, map, kb * 64, src.kvh, src.row, full,
+                               stream_policy);
+          }
         }
       } else {
         const bool mine = lane < src.npg;
@@ -367,8 +375,8 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
           const int pos = src.pos0 + lane * p.page_rows;
           const int prow = src.blk * p.block_size + pos % p.block_size;
           for (int kb = 0; kb < Lay::KB; ++kb)
-            tma_load_3d(dst + kb * Lay::KV_BLOCK + lane * p.page_rows * 128, map, kb * 64,
-                        src.kvh, prow, full);
+            tma_load_3d_hint(dst + kb * Lay::KV_BLOCK + lane * p.page_rows * 128, map, kb * 64,
+                             src.kvh, prow, full, stream_policy);
         }
       }
       return true;
@@ -402,18 +410,10 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
     Src pend;
     bool have_pend = false;
     Piece pc;
+    // per piece: K of its first tile and the previous tile's V go out before the wait
+    // for the Q buffer (held until the previous piece's last S completes)
     while (ok && piece_next(it, p, pc)) {
-      const int qb = nq % QBUF;
-      if (nq >= QBUF && !wait_all(&q_empty[qb], ((nq / QBUF) - 1) & 1)) break;
-      if (lane == 0) {
-        mbar_expect_tx(&q_full[qb], Lay::Q_BYTES);
-        for (int cp = 0; cp < CP; ++cp)  // the same rows in each of the CP row copies
-          for (int kb = 0; kb < Lay::KB; ++kb)
-            tma_load_3d(sQ + qb * Lay::Q_BYTES + kb * Lay::Q_BLOCK + cp * (kRows / CP) * 128,
-                        &p.tm_q, kb * 64, pc.kvh * p.G, pc.b * p.N + pc.mg * (MT * kRows / p.G),
-                        &q_full[qb]);
-      }
-      ++nq;
+      bool q_pending = true;
       Src nxt = make_src(pc, pc.t0);
       for (int t = pc.t0; t < pc.t1; ++t) {
         const Src src = nxt;
@@ -432,6 +432,23 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
         }
         pend = src;
         have_pend = true;
+        if (q_pending) {
+          const int qb = nq % QBUF;
+          if (nq >= QBUF && !wait_all(&q_empty[qb], ((nq / QBUF) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_expect_tx(&q_full[qb], Lay::Q_BYTES);
+            for (int cp = 0; cp < CP; ++cp)  // the same rows in each of the CP row copies
+              for (int kb = 0; kb < Lay::KB; ++kb)
+                tma_load_3d(sQ + qb * Lay::Q_BYTES + kb * Lay::Q_BLOCK + cp * (kRows / CP) * 128,
+                            &p.tm_q, kb * 64, pc.kvh * p.G,
+                            pc.b * p.N + pc.mg * (MT * kRows / p.G), &q_full[qb]);
+          }
+          ++nq;
+          q_pending = false;
+        }
       }
     }
     if (ok && have_pend && load(pend, gv, true)) ++gv;
@@ -800,42 +817,90 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
         const int hq = pc.kvh * p.G + (valid_row ? R % p.G : 0);
         bf16 *dst = static_cast<bf16 *>(p.out) + (((size_t)pc.b * p.N + node) * p.Hq + hq) * D;
         float w_own = 1.f, inv = l > 0.f ? 1.f / l : 0.f;
-        if (head && valid_row) {
-          // wait for the later pieces, then weigh every piece by 2^(m_piece - M)
-          float M = m_ref;
+        // producers of a head piece: the later CTAs c2 whose share overlaps the unit; the
+        // first kPre are kept in registers (slot and weight) and the first one's partial
+        // O is prefetched a chunk ahead; any further ones are read in place
+        constexpr int kPre = 4;
+        int np = 0;
+        long long pslot[kPre];
+        float pw[kPre];
+        auto for_producers = [&](auto &&fn) {
+          int j = 0;
           for (int c2 = blockIdx.x + 1; c2 < P; ++c2) {
             const long long fa = cta_first(W, c2, P);
             if (fa >= U_end) break;
             if (fa == cta_first(W, c2 + 1, P)) continue;
-            const unsigned long long *flag = p.flags + pc.unit + c2;
+            if (!fn(j++, pc.unit + c2)) break;
+          }
+        };
+        if (head && valid_row) {
+          // wait for the later pieces, then weigh every piece by 2^(m_piece - M)
+          float M = m_ref;
+          float pm[kPre], pl[kPre];
+          for_producers([&](int j, long long sl) -> bool {
+            const unsigned long long *flag = p.flags + sl;
             const unsigned long long t0 = global_ns();
             while (ld_acquire_u64(flag) != epoch) {
               if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
                 *abort_flag = 1;
-                break;
+                return false;
               }
             }
-            M = fmaxf(M, __ldcg(p.part_ml + ((size_t)(pc.unit + c2) * ROWS + R_local) * 2));
-          }
+            const float2 ml =
+                __ldcg(reinterpret_cast<const float2 *>(p.part_ml + ((size_t)sl * ROWS + R_local) * 2));
+#pragma unroll
+            for (int k = 0; k < kPre; ++k)
+              if (k == j) pslot[k] = sl, pm[k] = ml.x, pl[k] = ml.y;
+            M = fmaxf(M, ml.x);
+            np = j + 1;
+            return true;
+          });
           if (*abort_flag) break;
           w_own = m_ref == -INFINITY ? 0.f : exp2f(m_ref - M);
           float L = l * w_own;
-          for (int c2 = blockIdx.x + 1; c2 < P; ++c2) {
-            const long long fa = cta_first(W, c2, P);
-            if (fa >= U_end) break;
-            if (fa == cta_first(W, c2 + 1, P)) continue;
-            const float *ml = p.part_ml + ((size_t)(pc.unit + c2) * ROWS + R_local) * 2;
-            const float m2 = __ldcg(ml);
-            if (m2 != -INFINITY) L += exp2f(m2 - M) * __ldcg(ml + 1);
+#pragma unroll
+          for (int k = 0; k < kPre; ++k) {
+            pw[k] = 0.f;
+            if (k < np && pm[k] != -INFINITY) {
+              pw[k] = exp2f(pm[k] - M);
+              L += pw[k] * pl[k];
+            }
           }
+          if (np > kPre)
+            for_producers([&](int j, long long sl) -> bool {
+              if (j < kPre) return true;
+              const float2 ml =
+                  __ldcg(reinterpret_cast<const float2 *>(p.part_ml + ((size_t)sl * ROWS + R_local) * 2));
+              if (ml.x != -INFINITY) L += exp2f(ml.x - M) * ml.y;
+              return true;
+            });
           inv = L > 0.f ? 1.f / L : 0.f;
           m_ref = M;  // the weights below are 2^(m_piece - M)
+        }
+        // The first producer's partial row is copied whole into shared memory, which is
+        // free by now: this is the CTA's last piece and its last P V has completed.
+        // 16-byte unit i of row r sits at r * (D / 4) + (i ^ (r % (D / 4))) (no bank
+        // conflicts when a warp reads one unit of 32 rows).  Single-tile units only.
+        float4 *stage = nullptr;
+        if (MT == 1 && head && valid_row && np > 0) {
+          static_assert(MT > 1 || kRows * D * 4 <= 2 * STAGES * Lay::KV_BYTES, "staging room");
+          stage = reinterpret_cast<float4 *>(sK) + (size_t)R_local * (D / 4);
+          const float4 *src = reinterpret_cast<const float4 *>(p.part_o + ((size_t)pslot[0] * ROWS + R_local) * D);
+#pragma unroll
+          for (int i = 0; i < D / 4; ++i) cp_async_16(stage + (i ^ (R_local % (D / 4))), src + i, true);
+          cp_async_commit();
+          cp_async_wait<0>();
         }
         __syncwarp();  // tcgen05.ld below is warp-collective
         const long long slot = pc.unit + blockIdx.x;
         float *pdst = p.part_o + ((size_t)slot * ROWS + R_local) * D;
 #pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
+          float4 cur[8];
+          if (stage) {
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) cur[c4] = stage[(ch * 8 + c4) ^ (R_local % (D / 4))];
+          }
           float o[32];
           tmem_ld32(t_lane + (uint32_t)(Lay::S_COLS + mt * D + ch * 32), o);
           tmem_wait_ld();
@@ -848,26 +913,43 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
             continue;
           }
           if (head) {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] *= w_own;
-            for (int c2 = blockIdx.x + 1; c2 < P; ++c2) {
-              const long long fa = cta_first(W, c2, P);
-              if (fa >= U_end) break;
-              if (fa == cta_first(W, c2 + 1, P)) continue;
-              const size_t row = (size_t)(pc.unit + c2) * ROWS + R_local;
-              const float m2 = __ldcg(p.part_ml + row * 2);
-              if (m2 == -INFINITY) continue;
-              const float w2 = exp2f(m2 - m_ref);
-              const float4 *src = reinterpret_cast<const float4 *>(p.part_o + row * D + ch * 32);
+            auto add = [&](float w2, const float4 *src) {
 #pragma unroll
               for (int c4 = 0; c4 < 8; ++c4) {
-                const float4 x = __ldcg(src + c4);
+                const float4 x = src[c4];
                 o[c4 * 4 + 0] += w2 * x.x;
                 o[c4 * 4 + 1] += w2 * x.y;
                 o[c4 * 4 + 2] += w2 * x.z;
                 o[c4 * 4 + 3] += w2 * x.w;
               }
+            };
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] *= w_own;
+            if (stage) add(pw[0], cur);
+#pragma unroll
+            for (int k = stage ? 1 : 0; k < kPre; ++k) {
+              if (k < np) {
+                const float4 *src =
+                    reinterpret_cast<const float4 *>(p.part_o + ((size_t)pslot[k] * ROWS + R_local) * D + ch * 32);
+                float4 x[8];
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) x[c4] = __ldcg(src + c4);
+                add(pw[k], x);
+              }
             }
+            if (np > kPre)
+              for_producers([&](int j, long long sl) -> bool {
+                if (j < kPre) return true;
+                const size_t row = (size_t)sl * ROWS + R_local;
+                const float m2 = __ldcg(p.part_ml + row * 2);
+                if (m2 == -INFINITY) return true;
+                const float4 *src = reinterpret_cast<const float4 *>(p.part_o + row * D + ch * 32);
+                float4 x[8];
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) x[c4] = __ldcg(src + c4);
+                add(exp2f(m2 - m_ref), x);
+                return true;
+              });
           }
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8) {
