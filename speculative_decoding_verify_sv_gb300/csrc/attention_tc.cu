@@ -669,12 +669,8 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
           return r <= 0 ? 0u : (r >= CH ? kAll : (1u << r) - 1u);
         };
 
-        // pass 1: the row maximum of the raw scores over this warp's columns
-        float pmax = -INFINITY;
-#pragma unroll 1
-        for (int h = 0; h < NCH; ++h) {
-          float v[CH];
-          read_chunk(ta0 + h * CH, v);
+        // the row maximum over chunk h's visible columns
+        auto chunk_max = [&](int h, const float (&v)[CH]) -> float {
           const uint32_t km = visible(h);
           float mx[8];
 #pragma unroll
@@ -686,8 +682,36 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
 #pragma unroll
             for (int c = 0; c < CH; ++c) mx[c & 7] = fmaxf(mx[c & 7], ((km >> c) & 1u) ? v[c] : -INFINITY);
           }
+          return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        };
+        // With two M tiles (a 64-column slice per warp) the slice is read from TMEM once,
+        // into registers, and the S buffer is released at once.  Otherwise it is read twice
+        // (max, then P) and S is released with P: releasing it early lets the next S take
+        // the tensor pipe ahead of this tile's P V, which costs more than it gains there.
+        constexpr bool kOnePass = MT == 2 && CW <= 64;
+        float vs[kOnePass ? CW : 1];
+        auto vchunk = [&](int h) -> float (&)[CH] { return *reinterpret_cast<float(*)[CH]>(vs + h * CH); };
+        float pmax = -INFINITY;
+        if constexpr (kOnePass) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) pmax = fmaxf(pmax, mx[i]);
+          for (int h = 0; h < NCH; ++h) {
+            if constexpr (CH == 32) tmem_ld32(ta0 + h * CH, vchunk(h));
+            else tmem_ld16(ta0 + h * CH, vchunk(h));
+          }
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[j]);
+#pragma unroll
+          for (int h = 0; h < NCH; ++h) pmax = fmaxf(pmax, chunk_max(h, vchunk(h)));
+        } else {
+#pragma unroll 1
+          for (int h = 0; h < NCH; ++h) {
+            float v[CH];
+            read_chunk(ta0 + h * CH, v);
+            pmax = fmaxf(pmax, chunk_max(h, v));
+          }
         }
         if constexpr (CP > 1) {
           // the row's maximum over all copies' columns
@@ -741,13 +765,9 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
           ok = false;
           break;
         }
-        // pass 2: P = 2^(s*scale - max) in bf16 into this warp's slice of the P row
+        // P = 2^(s*scale - max) in bf16 into this warp's slice of the P row
         uint8_t *ptile = sP + pb * Lay::P_BYTES + mt * Lay::P_TILE;
-        float rsum = 0.f;
-#pragma unroll 1
-        for (int h = 0; h < NCH; ++h) {
-          float v[CH];
-          read_chunk(ta0 + h * CH, v);
+        auto chunk_exp = [&](int h, float (&v)[CH]) -> float {
           const uint32_t km = visible(h);
           float rs[4] = {0.f, 0.f, 0.f, 0.f};
           if (km == kAll) {
@@ -763,7 +783,6 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
               rs[c & 3] += v[c];
             }
           }
-          rsum += (rs[0] + rs[1]) + (rs[2] + rs[3]);
 #pragma unroll
           for (int c8 = 0; c8 < CH / 8; ++c8) {
             const int a = (col0 + h * CH) / 8 + c8;  // 8-key chunk index in the row
@@ -775,6 +794,19 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
             *reinterpret_cast<uint4 *>(ptile + (a >> 3) * Lay::P_BLOCK +
                                        sw128_offset((uint32_t)row, (uint32_t)(a & 7))) = w;
           }
+          return (rs[0] + rs[1]) + (rs[2] + rs[3]);
+        };
+        float rsum = 0.f;
+        if constexpr (kOnePass) {
+#pragma unroll
+          for (int h = 0; h < NCH; ++h) rsum += chunk_exp(h, vchunk(h));
+        } else {
+#pragma unroll 1
+          for (int h = 0; h < NCH; ++h) {
+            float v[CH];
+            read_chunk(ta0 + h * CH, v);
+            rsum += chunk_exp(h, v);
+          }
         }
         l = l * alpha + rsum;
         if (!zero_v_tail()) {
@@ -785,7 +817,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&s_free[j]);
+          if (!kOnePass) mbar_arrive(&s_free[j]);
           mbar_arrive(&p_full[pb]);
         }
       }
