@@ -38,6 +38,7 @@ using namespace tc;
 
 constexpr int kRows = 128;                // rows per MMA (one M tile)
 constexpr float kRescaleThreshold = 8.f;  // log2 units
+constexpr unsigned kPollSleepNs = 32;     // MMA issuer's back-off between idle polls
 
 // 2^x by the hardware's approximate exponential (one MUFU op; 2^-inf = +0).  P is
 // rounded to bf16 for the tensor core, far coarser than this instruction's error.
@@ -47,7 +48,7 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int D, int MT, int CP, int BN, int STAGES, int QBUF>
+template <int D, int MT, int CP, int BN, int STAGES, int QBUF, int PBUF>
 struct TcLayout {
   static constexpr int KB = D / 64;                      // 64-element column blocks of Q/K/V
   static constexpr int Q_BLOCK = MT * kRows * 128;       // one column block of Q
@@ -57,12 +58,12 @@ struct TcLayout {
   static constexpr int PB = BN / 64;                     // 64-key column blocks of P
   static constexpr int P_BLOCK = kRows * 128;
   static constexpr int P_TILE = PB * P_BLOCK;            // P of one M tile
-  static constexpr int P_BYTES = MT * P_TILE;            // one P buffer (two are used)
+  static constexpr int P_BYTES = MT * P_TILE;            // one P buffer (PBUF are used)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + QBUF * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_BAR = OFF_P + PBUF * P_BYTES;
   // k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], s_free[2], p_full[2], p_free[2], o_free, drain,
   // xch_full[2], xl_full, pub, q_full[QBUF], q_empty[QBUF]
   static constexpr int NBAR = 4 * STAGES + 14 + 2 * QBUF;
@@ -160,11 +161,12 @@ __device__ __forceinline__ long long block_scan(long long x, long long *red, lon
   return before + x;
 }
 
-template <int D, int MT, int CP, int BN, int STAGES, int QBUF>
-__global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS, 1)
+template <int D, int MT, int CP, int BN, int STAGES, int QBUF, int PBUF>
+__global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ TcParams p) {
   static_assert(CP == 1 || MT == 1, "row copies need a single M tile");
-  using Lay = TcLayout<D, MT, CP, BN, STAGES, QBUF>;
+  static_assert(PBUF == 1 || PBUF == 2, "P buffers");
+  using Lay = TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>;
   constexpr int NSW = Lay::NSW;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw;
@@ -491,10 +493,10 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
       while (true) {
         bool prog = false;
         if (gp < gs) {
-          const int gk = gp, s = gk % STAGES, pb = gk & 1;
+          const int gk = gp, s = gk % STAGES, pb = gk % PBUF;
           const bool first = m_first[gk & 3];
           const int qi = m_qi[gk & 3];
-          if (mbar_test(&p_full[pb], (gk >> 1) & 1) &&
+          if (mbar_test(&p_full[pb], (gk / PBUF) & 1) &&
               (!first || qi == 0 || mbar_test(o_free, (qi - 1) & 1)) &&
               mbar_test(&v_full[s], (gk / STAGES) & 1)) {
             tc_fence_after();
@@ -567,6 +569,9 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
             break;
           }
         }
+        // a short sleep keeps the poll from taking issue slots from the softmax warp
+        // that shares this SM sub-partition
+        __nanosleep(kPollSleepNs);
       }
       // every MMA issued must complete before TMEM is released
       umma_commit(drain);
@@ -617,7 +622,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
       const int L = clamp_len(p, pc.b);
       float m_ref = -INFINITY, l = 0.f;
       for (int k = 0; k < n; ++k) {
-        const int gk = g + k, j = gk & 1, s = gk % STAGES, t = pc.t0 + k, pb = gk & 1;
+        const int gk = g + k, j = gk & 1, s = gk % STAGES, t = pc.t0 + k, pb = gk % PBUF;
         const bool tree = t == 0;
         const int nvalid = tree ? p.N : min(BN, L - (t - 1) * BN);
         if (!mbar_wait(&s_full[j], (gk >> 1) & 1, abort_flag)) {
@@ -641,6 +646,12 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
         };
         if (warp_idle) {  // every row of this warp is padding: nothing to compute or write
           if (!zero_v_tail()) {
+            ok = false;
+            break;
+          }
+          // with one P buffer, arrive for this tile only after the previous tile's P V
+          // (so the arrival cannot count toward the previous phase)
+          if (PBUF == 1 && gk >= 1 && !mbar_wait(&p_free[0], (gk - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -743,7 +754,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
         // this piece must have finished first (P V runs in order, so waiting for the
         // previous tile's buffer release is enough)
         if (owner && __any_sync(0xFFFFFFFFu, rescale)) {
-          if (!mbar_wait(&p_free[(gk - 1) & 1], ((gk - 1) >> 1) & 1, abort_flag)) {
+          if (!mbar_wait(&p_free[(gk - 1) % PBUF], ((gk - 1) / PBUF) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -761,7 +772,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
           tmem_wait_st();
         }
         // P buffer gk&1 is free once the P V of tile gk-2 has finished
-        if (gk >= 2 && !mbar_wait(&p_free[pb], ((gk >> 1) - 1) & 1, abort_flag)) {
+        if (gk >= PBUF && !mbar_wait(&p_free[pb], ((gk / PBUF) - 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -844,7 +855,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
       const long long U_end = pc.fs - pc.t0 + pc.T;
       constexpr int ROWS = MT * kRows;
       if (owner && !warp_idle) {
-        if (!mbar_wait(&p_free[gl & 1], (gl >> 1) & 1, abort_flag)) break;
+        if (!mbar_wait(&p_free[gl % PBUF], (gl / PBUF) & 1, abort_flag)) break;
         tc_fence_after();
         const int hq = pc.kvh * p.G + (valid_row ? R % p.G : 0);
         bf16 *dst = static_cast<bf16 *>(p.out) + (((size_t)pc.b * p.N + node) * p.Hq + hq) * D;
@@ -1025,15 +1036,15 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF>::THREADS
   finish();
 }
 
-template <int D, int MT, int CP, int BN, int STAGES, int QBUF>
+template <int D, int MT, int CP, int BN, int STAGES, int QBUF, int PBUF>
 cudaError_t launch_tc_typed(const TcParams &p, int grid, cudaStream_t s) {
-  using Lay = TcLayout<D, MT, CP, BN, STAGES, QBUF>;
+  using Lay = TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>;
   static_assert(Lay::SMEM <= 232448, "shared memory layout exceeds 227 KB");
   static bool attr[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, MT, CP, BN, STAGES, QBUF>,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, MT, CP, BN, STAGES, QBUF, PBUF>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::SMEM);
     if (e != cudaSuccess) return e;
     attr[dev] = true;
@@ -1049,7 +1060,7 @@ cudaError_t launch_tc_typed(const TcParams &p, int grid, cudaStream_t s) {
   at[0].val.cooperative = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, MT, CP, BN, STAGES, QBUF>, p);
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, MT, CP, BN, STAGES, QBUF, PBUF>, p);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -1168,15 +1179,17 @@ cudaError_t launch_attention_tc(const AttnParams &a, const TcPlan &pl, void *ws,
   p.scale_log2 = a.scale_log2;
   p.tree = a.tree;
   if (a.D == 128) {
-    if (pl.MT == 2) return launch_tc_typed<128, 2, 1, 64, 3, 1>(p, pl.grid, s);
-    if (pl.CP == 4) return launch_tc_typed<128, 1, 4, 128, 2, 1>(p, pl.grid, s);
-    if (pl.CP == 2) return launch_tc_typed<128, 1, 2, 128, 2, 1>(p, pl.grid, s);
-    return launch_tc_typed<128, 1, 1, 128, 2, 1>(p, pl.grid, s);
+    // (two Q buffers paid for with one P buffer measured slower: the softmax then
+    // waits for every P V before writing the next P)
+    if (pl.MT == 2) return launch_tc_typed<128, 2, 1, 64, 3, 1, 2>(p, pl.grid, s);
+    if (pl.CP == 4) return launch_tc_typed<128, 1, 4, 128, 2, 1, 2>(p, pl.grid, s);
+    if (pl.CP == 2) return launch_tc_typed<128, 1, 2, 128, 2, 1, 2>(p, pl.grid, s);
+    return launch_tc_typed<128, 1, 1, 128, 2, 1, 2>(p, pl.grid, s);
   }
-  if (pl.MT == 2) return launch_tc_typed<64, 2, 1, 64, 4, 2>(p, pl.grid, s);
-  if (pl.CP == 4) return launch_tc_typed<64, 1, 4, 128, 3, 2>(p, pl.grid, s);
-  if (pl.CP == 2) return launch_tc_typed<64, 1, 2, 128, 3, 2>(p, pl.grid, s);
-  return launch_tc_typed<64, 1, 1, 128, 3, 2>(p, pl.grid, s);
+  if (pl.MT == 2) return launch_tc_typed<64, 2, 1, 64, 4, 2, 2>(p, pl.grid, s);
+  if (pl.CP == 4) return launch_tc_typed<64, 1, 4, 128, 3, 2, 2>(p, pl.grid, s);
+  if (pl.CP == 2) return launch_tc_typed<64, 1, 2, 128, 3, 2, 2>(p, pl.grid, s);
+  return launch_tc_typed<64, 1, 1, 128, 3, 2, 2>(p, pl.grid, s);
 }
 
 }  // namespace sv
