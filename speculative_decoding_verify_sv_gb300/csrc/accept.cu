@@ -140,7 +140,7 @@ __device__ __forceinline__ bool kept(float z, int j, const RowStat &st) {
 // ------------------------------------------------------------ kernel 1
 
 template <typename T, bool GREEDY, bool TOPK>
-__global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(const AcceptParams p) {
+__global__ void __launch_bounds__(kStatThreads, 2) accept_stats_kernel(const AcceptParams p) {
   constexpr int VEC = Elem<T>::kVec;
   constexpr int NT = kStatThreads;
   __shared__ float sh_v[32];
@@ -163,15 +163,23 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(const Accept
   KahanF acc;
   uint32_t umax[2] = {0u, 0u};  // TOPK: per-unit max key (units: even / odd lanes)
 
-  // each thread takes vectors tid, tid + NT, ... in index order, four at a time, all
-  // four loaded before any is used; vectors past the end read as -inf
+  // each thread takes vectors tid, tid + NT, ... in index order, four at a time; the
+  // next four are loaded while the current four are worked on (two batches in flight);
+  // vectors past the end read as -inf
   constexpr int U = 4;
   const uint4 ninf = make_uint4(Elem<T>::kNegInfWord, Elem<T>::kNegInfWord,
                                 Elem<T>::kNegInfWord, Elem<T>::kNegInfWord);
+  auto load_batch = [&](int v0, uint4 (&r)[U]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) r[u] = v0 + u * NT < nvec ? __ldg(xv + v0 + u * NT) : ninf;
+  };
+  uint4 nxt[U];
+  load_batch(tid, nxt);
   for (int v0 = tid; v0 < nvec; v0 += NT * U) {
     uint4 raws[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) raws[u] = v0 + u * NT < nvec ? __ldg(xv + v0 + u * NT) : ninf;
+    for (int u = 0; u < U; ++u) raws[u] = nxt[u];
+    if (v0 + NT * U < nvec) load_batch(v0 + NT * U, nxt);
     float f[U][VEC];
 #pragma unroll
     for (int u = 0; u < U; ++u) Elem<T>::unpack(raws[u], f[u]);
@@ -400,6 +408,32 @@ __device__ __forceinline__ unsigned cluster_size() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n"
                "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// First lane (0..n-1) whose exclusive prefix + own value exceeds t, with that prefix; if
+// none does (rounding put t at the very end), the last lane with a positive value.
+// Warp-wide: lane i holds x (0 for i >= n); base is added to every prefix.
+__device__ __forceinline__ int warp_find_cdf(double x, int n, double base, double t,
+                                             double *before_out) {
+  const int lane = threadIdx.x & 31;
+  double incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const double before = base + (incl - x);
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < n && before + x > t);
+  const unsigned pos = __ballot_sync(0xFFFFFFFFu, lane < n && x > 0.0);
+  const int L = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+  *before_out = __shfl_sync(0xFFFFFFFFu, before, L < 0 ? 0 : L);
+  return L;
 }
 // Read a double from the same shared-memory variable of CTA `rank` in this cluster.
 __device__ __forceinline__ double ld_peer_f64(const double *local, unsigned rank) {
@@ -679,39 +713,26 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
         s_slice[attempt] = tot;
       }
       cluster_sync_all();
-      if (tid < (int)C) s_tots[tid] = ld_peer_f64(&s_slice[attempt], (unsigned)tid);
-      __syncthreads();
-      if (tid == 0) {
-        // every CTA finds the same slice (same totals, same order)
-        const double *tots = s_tots;
-        double total = 0.0;
-        for (int r = 0; r < (int)C; ++r) total += tots[r];
-        s_rstar = -1;
+      if (warp == 0) {
+        // every CTA finds the same slice (same totals, same scan): lane r reads CTA r's
+        // slice total through distributed shared memory
+        const double tr = lane < (int)C ? ld_peer_f64(&s_slice[attempt], (unsigned)lane) : 0.0;
+        double total = tr;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
+        int rs = -1;
+        double base_r = 0.0, t = 0.0;
         if (total > 0.0) {
-          const double t = u_smp * total;
-          double run = 0.0, last_base = 0.0, base_r = 0.0;
-          int last = -1, rs = -1;
-          for (int r = 0; r < (int)C; ++r) {
-            if (tots[r] > 0.0) last = r, last_base = run;
-            if (rs < 0 && run + tots[r] > t) rs = r, base_r = run;
-            run += tots[r];
-          }
-          if (rs < 0) rs = last, base_r = last_base;  // rounding put t at the very end
-          s_rstar = rs;
-          if ((int)rank == rs) {
-            // the warp segment within this slice
-            double runw = base_r, lastw_base = base_r;
-            int ws = -1, lastw = -1;
-            for (int w = 0; w < NW; ++w) {
-              if (seg_sum[w] > 0.0) lastw = w, lastw_base = runw;
-              if (ws < 0 && runw + seg_sum[w] > t) ws = w, s_base = runw;
-              runw += seg_sum[w];
-            }
-            if (ws < 0) ws = lastw, s_base = lastw_base;
-            s_wstar = ws;
-            s_t = t;
-          }
+          t = u_smp * total;
+          rs = warp_find_cdf(tr, (int)C, 0.0, t, &base_r);
         }
+        if ((int)rank == rs) {
+          // the warp segment within this slice
+          double base_w;
+          const int ws = warp_find_cdf(lane < NW ? seg_sum[lane] : 0.0, NW, base_r, t, &base_w);
+          if (lane == 0) s_wstar = ws, s_base = base_w, s_t = t;
+        }
+        if (lane == 0) s_rstar = rs;
       }
       __syncthreads();
       if (s_rstar >= 0) break;
@@ -719,6 +740,8 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
       use_q = false;
       if (tid == 0) s_snear = 1;
     }
+    // this CTA has read its peers' totals for the last time: let them go once all have
+    cluster_arrive();
     const int rstar = s_rstar;
     writer = (int)rank == (rstar < 0 ? 0 : rstar);
 
@@ -810,7 +833,7 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
       }
     }
     // no CTA leaves while a peer may still read its slice totals
-    cluster_sync_all();
+    cluster_wait();
   }
   __syncthreads();
 

@@ -39,6 +39,11 @@ using namespace tc;
 constexpr int kRows = 128;                // rows per MMA (one M tile)
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 constexpr unsigned kPollSleepNs = 32;     // MMA issuer's back-off between idle polls
+// Slots of the flattened work space that stand for the start of a unit (its Q load,
+// the previous piece's O readout and, for a cut unit, the merge).  Charged only when a
+// CTA holds few units (then the number of unit starts per CTA varies by one or two and
+// decides which CTA finishes last); with many units per CTA the costs average out.
+constexpr int kUnitStartSlots = 4;
 
 // 2^x by the hardware's approximate exponential (one MUFU op; 2^-inf = +0).  P is
 // rounded to bf16 for the tensor core, far coarser than this instruction's error.
@@ -104,28 +109,39 @@ __device__ __forceinline__ int unit_tiles(const TcParams &p, int b) {
   return 1 + (clamp_len(p, b) + p.bn - 1) / p.bn;
 }
 
+// Each unit occupies vt + T slots of the flattened space: vt empty slots that stand for
+// the fixed cost of starting a unit (the CTA that holds a unit's start is charged for
+// it and gets that many fewer tiles), then its T tiles.  it.t runs over the slots;
+// pieces are reported in tile coordinates and pieces without tiles are skipped.
 __device__ __forceinline__ bool piece_next(PieceIter &it, const TcParams &p, Piece &pc) {
-  if (it.f >= it.end) return false;
-  pc.b = it.b;
-  pc.kvh = it.ul / p.m_groups;
-  pc.mg = it.ul % p.m_groups;
-  pc.T = it.T;
-  pc.t0 = it.t;
-  const long long rem = it.end - it.f;
-  pc.t1 = (int)min((long long)it.T, (long long)it.t + rem);
-  pc.unit = (long long)it.b * p.upb + it.ul;
-  pc.fs = it.f;
-  it.f += pc.t1 - pc.t0;
-  it.t = pc.t1;
-  if (it.t == it.T) {
-    it.t = 0;
-    if (++it.ul == p.upb) {
-      it.ul = 0;
-      ++it.b;
-      if (it.f < it.end) it.T = unit_tiles(p, it.b);
+  while (it.f < it.end) {
+    const int span = it.T + p.vt;
+    const int s0 = it.t;
+    const int s1 = (int)min((long long)span, (long long)it.t + (it.end - it.f));
+    const long long f_s0 = it.f;
+    pc.b = it.b;
+    pc.kvh = it.ul / p.m_groups;
+    pc.mg = it.ul % p.m_groups;
+    pc.T = it.T;
+    pc.unit = (long long)it.b * p.upb + it.ul;
+    it.f += s1 - s0;
+    it.t = s1;
+    if (it.t == span) {
+      it.t = 0;
+      if (++it.ul == p.upb) {
+        it.ul = 0;
+        ++it.b;
+        if (it.f < it.end) it.T = unit_tiles(p, it.b);
+      }
+    }
+    pc.t0 = max(0, s0 - p.vt);
+    pc.t1 = max(0, s1 - p.vt);
+    if (pc.t1 > pc.t0) {
+      pc.fs = f_s0 + (pc.t0 + p.vt - s0);  // flattened index of tile t0
+      return true;
     }
   }
-  return true;
+  return false;
 }
 
 // Flattened tile at which CTA c of P starts (CTA P starts at W: the end).
@@ -217,36 +233,51 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
   long long *red = reinterpret_cast<long long *>(sm + Lay::OFF_RED);
 
   // ---- this CTA's share of the flattened (unit, tile) space: an equal split of the
-  // total W, computed alike by every CTA from the prefix lengths
-  long long W;
-  {
+  // total W, computed alike by every CTA from the prefix lengths; then the sequence
+  // holding its first slot f0 (b_start) and the slots before that sequence (base_start)
+  long long W, f0, f1;
+  int b_start = 0;
+  long long base_start = 0;
+  if (p.B <= (int)blockDim.x) {
+    // one scan: thread b holds sequence b
+    const int b = threadIdx.x;
+    long long w = 0;
+    if (b < p.B) {
+      if (blockIdx.x == 0) {
+        const int L = p.prefix_len[b];
+        if (L < 0 || L > p.cap) set_status(p.status, SV_DEV_BAD_PREFIX);
+      }
+      w = (long long)(unit_tiles(p, b) + p.vt) * p.upb;
+    }
+    long long total;
+    const long long incl = block_scan(w, red, total);
+    W = total;
+    f0 = cta_first(W, blockIdx.x, P);
+    f1 = cta_first(W, blockIdx.x + 1, P);
+    if (b < p.B && incl - w <= f0 && f0 < incl) {
+      red[14] = b;
+      red[15] = incl - w;
+    }
+    __syncthreads();
+  } else {
     long long part = 0;
     for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
       if (blockIdx.x == 0) {
         const int L = p.prefix_len[b];
         if (L < 0 || L > p.cap) set_status(p.status, SV_DEV_BAD_PREFIX);
       }
-      part += unit_tiles(p, b);
+      part += unit_tiles(p, b) + p.vt;
     }
     long long total;
     block_scan(part, red, total);
     W = total * p.upb;
-  }
-  const long long f0 = cta_first(W, blockIdx.x, P), f1 = cta_first(W, blockIdx.x + 1, P);
-  if (f0 >= f1) {  // no work for this CTA (uniform)
-    finish();
-    return;
-  }
-  // the sequence holding tile f0, and the tiles before it
-  int b_start = 0;
-  long long base_start = 0;
-  {
+    f0 = cta_first(W, blockIdx.x, P);
+    f1 = cta_first(W, blockIdx.x + 1, P);
     long long carry = 0;
-    bool found = false;
+    bool found = f0 >= f1;
     for (int b0 = 0; b0 < p.B && !found; b0 += blockDim.x) {
       const int b = b0 + threadIdx.x;
-      const long long w = b < p.B ? (long long)unit_tiles(p, b) * p.upb : 0;
-      long long total;
+      const long long w = b < p.B ? (long long)(unit_tiles(p, b) + p.vt) * p.upb : 0;
       const long long incl = block_scan(w, red, total);
       const long long excl = carry + incl - w;
       if (b < p.B && excl <= f0 && f0 < excl + w) {
@@ -257,9 +288,13 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       carry += total;
       found = carry > f0;
     }
-    b_start = (int)red[14];
-    base_start = red[15];
   }
+  if (f0 >= f1) {  // no work for this CTA (uniform)
+    finish();
+    return;
+  }
+  b_start = (int)red[14];
+  base_start = red[15];
 
   if (threadIdx.x < kMaxNodes)
     sPar[threadIdx.x] = threadIdx.x < p.tree.N ? (int)p.tree.parent[threadIdx.x] : -1;
@@ -316,8 +351,8 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
   it.end = f1;
   it.b = b_start;
   it.T = unit_tiles(p, b_start);
-  it.ul = (int)((f0 - base_start) / it.T);
-  it.t = (int)((f0 - base_start) % it.T);
+  it.ul = (int)((f0 - base_start) / (it.T + p.vt));
+  it.t = (int)((f0 - base_start) % (it.T + p.vt));
 
   uint8_t *const sQ = sm + Lay::OFF_Q;
   uint8_t *const sK = sm + Lay::OFF_K;
@@ -1171,6 +1206,7 @@ cudaError_t launch_attention_tc(const AttnParams &a, const TcPlan &pl, void *ws,
   p.m_groups = pl.m_groups;
   p.upb = a.Hkv * pl.m_groups;
   p.bn = BN;
+  p.vt = (long long)a.B * p.upb <= 2LL * pl.grid ? kUnitStartSlots : 0;
   p.Lmax = a.Lmax;
   p.block_size = a.block_size;
   p.max_blocks = a.max_blocks;

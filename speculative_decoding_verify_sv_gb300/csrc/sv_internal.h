@@ -63,6 +63,7 @@ struct TcParams {
   unsigned long long *flags;  // [slots] epoch of the call that published each partial
   unsigned int *status;
   int B, N, Hq, Hkv, G, M, m_groups, upb, bn;
+  int vt;  // empty slots charged for the start of each unit in the work split
   int Lmax, block_size, max_blocks, num_blocks, cap, paged, page_rows;
   float scale_log2;
   Tree tree;
