@@ -11,7 +11,8 @@ torch.cuda.synchronize() on both sides; each step is timed with CUDA events on t
 stream the kernels run on.  Between steps (outside the events) prefix_len is restored
 and L2 is flushed by writing a buffer of twice its size, then reading another one of
 that size (so that no dirty lines are left for the timed kernels to write back).  Each stage of the step
-(attention, acceptance, commit) is captured once into a CUDA graph and replayed, so
+(attention; acceptance with the KV commit fused into it) is captured once into a CUDA
+graph and replayed, so
 that host launch overhead does not open gaps inside the timed windows (--eager times
 the plain launches instead).  Under torchrun every rank
 runs an independent replica (weak scaling, no collective on the data path); the
@@ -249,13 +250,10 @@ def run_ours(args, dist: Dist):
         step.attention(w["q"], w["k_tree"], w["v_tree"], stream)
         if ev:
             ev[1].record(stream)
-        step.accept(w["target_logits"], w["draft_logits"], toks, seed=w["seed"], round_=i,
-                    stream=stream)
+        step.accept_commit(w["target_logits"], w["draft_logits"], toks, w["k_tree"], w["v_tree"],
+                           seed=w["seed"], round_=i, stream=stream)
         if ev:
             ev[2].record(stream)
-        step.commit(w["k_tree"], w["v_tree"], stream)
-        if ev:
-            ev[3].record(stream)
 
     # pre-heat (clock ramp), then the warm-up steps
     sampler = ClockSampler(dev.index)
@@ -281,9 +279,9 @@ def run_ours(args, dist: Dist):
             n0 = sv.sv_kernel_launches()
             graphs = []
             for fn in (lambda st: step.attention(w["q"], w["k_tree"], w["v_tree"], st),
-                       lambda st: step.accept(w["target_logits"], w["draft_logits"], toks,
-                                              seed=w["seed"], round_=0, stream=st),
-                       lambda st: step.commit(w["k_tree"], w["v_tree"], st)):
+                       lambda st: step.accept_commit(w["target_logits"], w["draft_logits"], toks,
+                                                     w["k_tree"], w["v_tree"], seed=w["seed"],
+                                                     round_=0, stream=st)):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, capture_error_mode="relaxed"):
                     fn(torch.cuda.current_stream())
@@ -307,10 +305,10 @@ def run_ours(args, dist: Dist):
         for k, g in enumerate(graphs):
             ev[k].record(stream)
             g.replay()
-        ev[3].record(stream)
+        ev[2].record(stream)
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     dist.barrier()
     torch.cuda.synchronize()
     launches0 = sv.sv_kernel_launches()
@@ -328,10 +326,9 @@ def run_ours(args, dist: Dist):
     clocks = sampler.stop()
     status = sv.sv_read_device_status()
 
-    tot = [e[0].elapsed_time(e[3]) for e in evs]
+    tot = [e[0].elapsed_time(e[2]) for e in evs]
     att = [e[0].elapsed_time(e[1]) for e in evs]
     acc = [e[1].elapsed_time(e[2]) for e in evs]
-    com = [e[2].elapsed_time(e[3]) for e in evs]
     dev_ms = dist.max(sum(tot))
     cand = c["B"] * (w["N"] - 1)
     units = dist.sum(cand * K)
@@ -381,8 +378,7 @@ def run_ours(args, dist: Dist):
             "traffic": committed_traffic(kernel_file, workload_name),
         },
         "breakdown_us": {
-            "attention": 1e3 * a_ms, "accept": 1e3 * statistics.mean(acc),
-            "commit": 1e3 * statistics.mean(com),
+            "attention": 1e3 * a_ms, "accept_and_commit": 1e3 * statistics.mean(acc),
             "accept_gbs": accept_bytes(w) / (statistics.mean(acc) / 1e3) / 1e9,
             "attention_tflops": attention_flops(w) / (a_ms / 1e3) / 1e12,
         },

@@ -203,6 +203,34 @@ sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_
                        const void *v_tree, const int32_t *path_nodes, int path_stride,
                        const int32_t *num_accepted, sv_kv_cache cache, void *stream);
 
+/* Acceptance and the KV commit of its kept path in one call: the same results as
+ * sv_accept_tree (resp. sv_accept_chain) followed by sv_commit_kv with path_nodes =
+ * out_path_nodes (resp. nodes 0..accepted), path_stride = tree depth + 1 and
+ * num_accepted = out_num_accepted (qwbw.cn sections 3.1.4 and 6.3 for the commit).
+ * The commit runs inside the acceptance's second kernel, split over the CTAs that
+ * already hold the sequence, so it costs no launch of its own.  kv_dt, Hkv, D, k_tree,
+ * v_tree and cache are the sv_commit_kv arguments (same layout, ownership and
+ * checks); the acceptance arguments, outputs and workspace are those of the separate
+ * call.  prefix_len[b] is read before any K/V is written and advanced once, after. */
+sv_status sv_accept_tree_commit(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
+                                const int32_t *parent, const int32_t *node_tokens,
+                                const void *target_logits, const void *q, sv_q_kind q_kind,
+                                int Dq, float temperature, int top_k, uint64_t seed,
+                                uint64_t round, sv_dtype kv_dt, int Hkv, int D,
+                                const void *k_tree, const void *v_tree, sv_kv_cache cache,
+                                int32_t *out_path_nodes, int32_t *out_tokens,
+                                int32_t *out_num_emitted, int32_t *out_num_accepted,
+                                uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
+                                void *stream);
+sv_status sv_accept_chain_commit(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
+                                 const void *target_logits, const void *q, sv_q_kind q_kind,
+                                 const int32_t *draft_tokens, float temperature, int top_k,
+                                 uint64_t seed, uint64_t round, sv_dtype kv_dt, int Hkv, int D,
+                                 const void *k_tree, const void *v_tree, sv_kv_cache cache,
+                                 int32_t *out_tokens, int32_t *out_num_emitted,
+                                 int32_t *out_num_accepted, uint32_t *out_near_ties,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
 /* ---------------------------------------------------------------- tree helper */
 
 /* Host helper: validate a tree and derive per node its ancestor bitmask (bit j set

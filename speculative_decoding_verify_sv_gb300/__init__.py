@@ -19,7 +19,8 @@ import torch
 __all__ = [
     "SVError", "KVCache", "library_path", "load_library", "sv_tree_attention",
     "sv_tree_attention_workspace_size", "sv_tree_attention_path", "sv_accept_chain", "sv_accept_tree",
-    "sv_accept_workspace_size", "sv_accept_tree_noalloc", "sv_commit_kv", "sv_tree_prepare", "sv_read_device_status",
+    "sv_accept_workspace_size", "sv_accept_tree_noalloc", "sv_commit_kv", "sv_accept_tree_commit",
+    "sv_accept_chain_commit", "sv_tree_prepare", "sv_read_device_status",
     "sv_version", "sv_kernel_launches", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "SV_MAX_TREE_NODES",
 ]
 
@@ -84,13 +85,18 @@ def load_library():
         lib.sv_accept_workspace_size.argtypes = [I, I, I, I]
         lib.sv_accept_workspace_size.restype = SZ
         lib.sv_commit_kv.argtypes = [I, I, I, I, I, P, P, P, I, P, _KVCacheC, P]
+        lib.sv_accept_tree_commit.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, U64, U64,
+                                              I, I, I, P, P, _KVCacheC, P, P, P, P, P, P, SZ, P]
+        lib.sv_accept_chain_commit.argtypes = [I, I, I, I, I, P, P, I, P, F, I, U64, U64,
+                                               I, I, I, P, P, _KVCacheC, P, P, P, P, P, SZ, P]
         lib.sv_tree_prepare.argtypes = [I, P, P, P]
         lib.sv_read_device_status.argtypes = [P, P]
         lib.sv_last_error.restype = ctypes.c_char_p
         lib.sv_version.restype = ctypes.c_char_p
         lib.sv_kernel_launches.restype = ctypes.c_uint64
         for fn in ("sv_tree_attention", "sv_accept_chain", "sv_accept_tree", "sv_commit_kv",
-                   "sv_tree_prepare", "sv_read_device_status", "sv_accept_tree_noalloc"):
+                   "sv_tree_prepare", "sv_read_device_status", "sv_accept_tree_noalloc",
+                   "sv_accept_tree_commit", "sv_accept_chain_commit"):
             getattr(lib, fn).restype = ctypes.c_int32
         _lib = lib
         return lib
@@ -360,6 +366,74 @@ def sv_commit_kv(k_tree, v_tree, path_nodes, num_accepted, cache: KVCache, strea
     _check(lib.sv_commit_kv(_dt(k_tree), B, N, Hkv, D, _ptr(k_tree), _ptr(v_tree),
                             _ptr(path_nodes), path_nodes.shape[1], _ptr(num_accepted),
                             cache.c_struct(), _stream(stream)))
+
+
+def _kv_args(k_tree, v_tree, cache: KVCache):
+    _dev(k_tree, "k_tree", (torch.bfloat16, torch.float32))
+    _dev(v_tree, "v_tree", k_tree.dtype, k_tree.shape)
+    return _dt(k_tree), k_tree.shape[2], k_tree.shape[3], cache.c_struct()
+
+
+def sv_accept_chain_commit(mode, target_logits, q, q_kind, draft_tokens, k_tree, v_tree,
+                           cache: KVCache, temperature=1.0, top_k=0, seed=0, round_=0,
+                           outs=None, workspace=None, stream=None) -> dict:
+    """sv_accept_chain, then the commit of nodes 0..accepted of k_tree/v_tree
+    [B,gamma+1,Hkv,D] into the cache, in the same launches."""
+    lib = load_library()
+    _dev(target_logits, "target_logits", (torch.bfloat16, torch.float32))
+    B, W, V = target_logits.shape
+    gamma = W - 1
+    _dev(draft_tokens, "draft_tokens", torch.int32, (B, gamma))
+    if q is not None:
+        _dev(q, "q", target_logits.dtype if q_kind == Q_LOGITS else torch.float32, (B, gamma, V))
+    if k_tree.shape[:2] != (B, W):
+        raise ValueError("k_tree must be [B, gamma+1, Hkv, D]")
+    kv_dt, Hkv, D, cs = _kv_args(k_tree, v_tree, cache)
+    outs = _accept_outputs(B, W, target_logits.device, outs)
+    workspace, ws_bytes = _workspace(sv_accept_workspace_size(B, W, V, gamma), target_logits.device,
+                                     workspace)
+    _check(lib.sv_accept_chain_commit(mode, _dt(target_logits), B, gamma, V, _ptr(target_logits),
+                                      _ptr(q), q_kind, _ptr(draft_tokens), float(temperature),
+                                      int(top_k), int(seed), int(round_), kv_dt, Hkv, D,
+                                      _ptr(k_tree), _ptr(v_tree), cs, _ptr(outs["tokens"]),
+                                      _ptr(outs["num_emitted"]), _ptr(outs["num_accepted"]),
+                                      _ptr(outs["near_ties"]), _ptr(workspace), ws_bytes,
+                                      _stream(stream)))
+    return outs
+
+
+def sv_accept_tree_commit(mode, target_logits, q, q_kind, parent, node_tokens, k_tree, v_tree,
+                          cache: KVCache, temperature=1.0, top_k=0, seed=0, round_=0, outs=None,
+                          workspace=None, stream=None) -> dict:
+    """sv_accept_tree, then the commit of the kept path of k_tree/v_tree [B,N,Hkv,D] into
+    the cache, in the same launches."""
+    lib = load_library()
+    _dev(target_logits, "target_logits", (torch.bfloat16, torch.float32))
+    B, N, V = target_logits.shape
+    _dev(node_tokens, "node_tokens", torch.int32, (B, N))
+    Dq = 0
+    if q is not None:
+        Dq = q.shape[1]
+        _dev(q, "q", target_logits.dtype if q_kind == Q_LOGITS else torch.float32, (B, Dq, V))
+    if k_tree.shape[:2] != (B, N):
+        raise ValueError("k_tree must be [B, N, Hkv, D]")
+    kv_dt, Hkv, D, cs = _kv_args(k_tree, v_tree, cache)
+    W = _tree_depth(parent) + 1
+    outs = _accept_outputs(B, W, target_logits.device, outs)
+    outs.setdefault("path_nodes", torch.empty((B, W), dtype=torch.int32, device=target_logits.device))
+    workspace, ws_bytes = _workspace(sv_accept_workspace_size(B, N, V, Dq), target_logits.device,
+                                     workspace)
+    par, n = _parent_arr(parent)
+    if n != N:
+        raise ValueError(f"parent has {n} entries, logits have {N} rows")
+    _check(lib.sv_accept_tree_commit(mode, _dt(target_logits), B, N, V, par, _ptr(node_tokens),
+                                     _ptr(target_logits), _ptr(q), q_kind, Dq, float(temperature),
+                                     int(top_k), int(seed), int(round_), kv_dt, Hkv, D,
+                                     _ptr(k_tree), _ptr(v_tree), cs, _ptr(outs["path_nodes"]),
+                                     _ptr(outs["tokens"]), _ptr(outs["num_emitted"]),
+                                     _ptr(outs["num_accepted"]), _ptr(outs["near_ties"]),
+                                     _ptr(workspace), ws_bytes, _stream(stream)))
+    return outs
 
 
 # ------------------------------------------------------------------ tree, status

@@ -460,6 +460,62 @@ __device__ __forceinline__ float warp_incl_scan_f(float v) {
 }
 
 constexpr int kMaxCluster = 16;
+
+// Commit of the kept path inside the select kernel (the work of the commit kernel): the
+// tree K/V rows of path nodes path[0..count) (root first) go to cache positions L..L+count-1.
+// The rows' 16-byte vectors are split over the `parts` CTAs of the cluster; loads are
+// issued four at a time before the stores.  Bad block ids and positions past the cache
+// are reported (by CTA 0) and skipped.
+__device__ void commit_path_slice(const CommitParams &cm, int b, int L, const int8_t *path,
+                                  int count, unsigned part, unsigned parts) {
+  const long long row_vec = (long long)cm.Hkv * cm.D * cm.esize / 16;
+  const long long total = (long long)count * row_vec;
+  const long long i0 = total * part / parts, i1 = total * (part + 1) / parts;
+  const uint4 *__restrict__ kt = static_cast<const uint4 *>(cm.k_tree);
+  const uint4 *__restrict__ vt = static_cast<const uint4 *>(cm.v_tree);
+  uint4 *__restrict__ ck = static_cast<uint4 *>(cm.cache_k);
+  uint4 *__restrict__ cv = static_cast<uint4 *>(cm.cache_v);
+  constexpr int U = 4;
+  for (long long i = i0 + threadIdx.x; i < i1; i += (long long)blockDim.x * U) {
+    uint4 kk[U], vv[U];
+    long long dst[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      dst[u] = -1;
+      const long long ii = i + (long long)u * blockDim.x;
+      if (ii >= i1) continue;
+      const int k = (int)(ii / row_vec);
+      const long long e = ii % row_vec;
+      const int node = path[k], pos = L + k;
+      long long dst_row;
+      if (cm.block_table) {
+        const int bi = pos / cm.block_size;
+        const int blk = bi < cm.max_blocks ? cm.block_table[(size_t)b * cm.max_blocks + bi] : -1;
+        if (blk < 0 || blk >= cm.num_blocks) {
+          if (e == 0) set_status(cm.status, SV_DEV_BAD_BLOCK);
+          continue;
+        }
+        dst_row = (long long)blk * cm.block_size + pos % cm.block_size;
+      } else {
+        if (pos >= cm.Lmax) {
+          if (e == 0) set_status(cm.status, SV_DEV_BAD_PREFIX);
+          continue;
+        }
+        dst_row = (long long)b * cm.Lmax + pos;
+      }
+      const long long src = ((long long)b * cm.N + node) * row_vec + e;
+      kk[u] = kt[src];
+      vv[u] = vt[src];
+      dst[u] = dst_row * row_vec + e;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (dst[u] >= 0) {
+        ck[dst[u]] = kk[u];
+        cv[dst[u]] = vv[u];
+      }
+  }
+}
 constexpr int kMaxChunks = 4096;          // chunk sums one CTA keeps (32 vectors each)
 constexpr double kDecideMargin = 1e-4;    // float ratio this close to u: decide in double
 
@@ -477,6 +533,7 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
   __shared__ float s_chunk[kMaxChunks];
   __shared__ int s_wstar, s_tok, s_snear, s_rstar;
   __shared__ double s_base, s_t;
+  __shared__ int8_t s_path[kMaxNodes];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned C = cluster_size(), rank = cluster_rank();
@@ -588,6 +645,22 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
   __syncthreads();
   const int best = s_best;
   bool writer = rank == 0;  // the CTA that writes the sequence's outputs
+
+  // commit of the kept path, split over the cluster.  Every CTA reads prefix_len[b]
+  // here; the writer advances it at the very end, after the last cluster barrier
+  // (the non-greedy path) or alone (greedy: one CTA per sequence).
+  int commit_L = -1;
+  const int commit_count = s_dep[best] + 1;
+  if (p.commit) {
+    if (tid == 0)
+      for (int a = best, i = s_dep[best]; a >= 0; a = s_par[a], --i) s_path[i] = (int8_t)a;
+    commit_L = p.cm.prefix_len[b];
+    __syncthreads();
+    if (commit_L >= 0)
+      commit_path_slice(p.cm, b, commit_L, s_path, commit_count, rank, C);
+    else if (tid == 0 && rank == 0)
+      set_status(p.status, SV_DEV_BAD_PREFIX);
+  }
 
   if constexpr (GREEDY) {
     if (tid == 0) s_tok = tstat[best].argmax;
@@ -854,6 +927,7 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
     p.out_num_emitted[b] = depth + 1;
     p.out_num_accepted[b] = depth;
     if (p.out_near_ties) p.out_near_ties[b] = (uint32_t)(s_nd + s_snear);
+    if (p.commit && commit_L >= 0) p.cm.prefix_len[b] = commit_L + commit_count;
   }
 }
 

@@ -304,23 +304,23 @@ sv_status accept_launch(sv_dtype dt, sv::AcceptParams &p, bool greedy, void *wor
 
 }  // namespace
 
-sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
-                          const void *target_logits, const void *q, sv_q_kind q_kind,
-                          const int32_t *draft_tokens, float temperature, int top_k,
-                          uint64_t seed, uint64_t round, int32_t *out_tokens,
-                          int32_t *out_num_emitted, int32_t *out_num_accepted,
-                          uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
-                          void *stream) {
-  bool greedy = false;
+namespace {
+
+sv_status chain_params(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
+                       const void *target_logits, const void *q, sv_q_kind q_kind,
+                       const int32_t *draft_tokens, float temperature, int top_k, uint64_t seed,
+                       uint64_t round, int32_t *out_tokens, int32_t *out_num_emitted,
+                       int32_t *out_num_accepted, uint32_t *out_near_ties, sv::AcceptParams &p,
+                       bool *greedy) {
   sv_status st = accept_common(mode, logit_dt, B, V, target_logits, q, q_kind, temperature, top_k,
-                               out_tokens, out_num_emitted, out_num_accepted, &greedy);
+                               out_tokens, out_num_emitted, out_num_accepted, greedy);
   if (st != SV_OK) return st;
   if (gamma < 1 || gamma >= SV_MAX_TREE_NODES)
     return fail(SV_ERR_UNSUPPORTED, "gamma = %d (supported 1..%d)", gamma, SV_MAX_TREE_NODES - 1);
   if (!draft_tokens) return fail(SV_ERR_INVALID_ARG, "draft_tokens is NULL");
   int32_t parent[SV_MAX_TREE_NODES];
   for (int i = 0; i <= gamma; ++i) parent[i] = i - 1;
-  sv::AcceptParams p{};
+  p = sv::AcceptParams{};
   if ((st = make_tree(gamma + 1, parent, &p.tree)) != SV_OK) return st;
   p.B = B;
   p.N = gamma + 1;
@@ -341,32 +341,29 @@ sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int
   p.out_num_emitted = out_num_emitted;
   p.out_num_accepted = out_num_accepted;
   p.out_near_ties = out_near_ties;
-  return accept_launch(logit_dt, p, greedy, workspace, workspace_bytes, stream);
+  return SV_OK;
 }
 
-sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
-                         const int32_t *parent, const int32_t *node_tokens,
-                         const void *target_logits, const void *q, sv_q_kind q_kind, int Dq,
-                         float temperature, int top_k, uint64_t seed, uint64_t round,
-                         int32_t *out_path_nodes, int32_t *out_tokens,
-                         int32_t *out_num_emitted, int32_t *out_num_accepted,
-                         uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
-                         void *stream) {
-  bool greedy = false;
+sv_status tree_params(sv_mode mode, sv_dtype logit_dt, int B, int N, int V, const int32_t *parent,
+                      const int32_t *node_tokens, const void *target_logits, const void *q,
+                      sv_q_kind q_kind, int Dq, float temperature, int top_k, uint64_t seed,
+                      uint64_t round, int32_t *out_path_nodes, int32_t *out_tokens,
+                      int32_t *out_num_emitted, int32_t *out_num_accepted,
+                      uint32_t *out_near_ties, sv::AcceptParams &p, bool *greedy) {
   sv_status st = accept_common(mode, logit_dt, B, V, target_logits, q, q_kind, temperature, top_k,
-                               out_tokens, out_num_emitted, out_num_accepted, &greedy);
+                               out_tokens, out_num_emitted, out_num_accepted, greedy);
   if (st != SV_OK) return st;
-  sv::AcceptParams p{};
+  p = sv::AcceptParams{};
   if ((st = make_tree(N, parent, &p.tree)) != SV_OK) return st;
   if (!node_tokens) return fail(SV_ERR_INVALID_ARG, "node_tokens is NULL");
   if (!out_path_nodes) return fail(SV_ERR_INVALID_ARG, "out_path_nodes is NULL");
-  if (!greedy && Dq < p.tree.Dmax)
+  if (!*greedy && Dq < p.tree.Dmax)
     return fail(SV_ERR_INVALID_ARG, "q has %d depth rows, the tree is %d deep", Dq, p.tree.Dmax);
   if (Dq < 0) return fail(SV_ERR_INVALID_ARG, "Dq < 0");
   p.B = B;
   p.N = N;
   p.V = V;
-  p.Dq = greedy ? 0 : Dq;
+  p.Dq = *greedy ? 0 : Dq;
   p.q_kind = q_kind;
   p.target = target_logits;
   p.q = q;
@@ -382,33 +379,26 @@ sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
   p.out_num_emitted = out_num_emitted;
   p.out_num_accepted = out_num_accepted;
   p.out_near_ties = out_near_ties;
-  return accept_launch(logit_dt, p, greedy, workspace, workspace_bytes, stream);
+  return SV_OK;
 }
 
-// --------------------------------------------------------------------- commit
-
-sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_tree,
-                       const void *v_tree, const int32_t *path_nodes, int path_stride,
-                       const int32_t *num_accepted, sv_kv_cache cache, void *stream) {
+// Validation of a commit's cache and tree K/V, shared by sv_commit_kv and the fused
+// acceptance + commit calls; fills everything but the path.
+sv_status commit_params(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_tree,
+                        const void *v_tree, const sv_kv_cache &cache, sv::CommitParams &p) {
   if (dt != SV_F32 && dt != SV_BF16) return fail(SV_ERR_UNSUPPORTED, "dtype %d", (int)dt);
-  if (B < 0 || N < 1 || N > SV_MAX_TREE_NODES || Hkv < 1 || D < 1 || path_stride < 1)
-    return fail(SV_ERR_INVALID_ARG, "bad sizes B=%d N=%d Hkv=%d D=%d path_stride=%d", B, N, Hkv, D,
-                path_stride);
+  if (B < 0 || N < 1 || N > SV_MAX_TREE_NODES || Hkv < 1 || D < 1)
+    return fail(SV_ERR_INVALID_ARG, "bad sizes B=%d N=%d Hkv=%d D=%d", B, N, Hkv, D);
   const int esize = dt == SV_F32 ? 4 : 2;
   if (((size_t)Hkv * D * esize) % 16 != 0)
     return fail(SV_ERR_UNSUPPORTED, "Hkv*D*elem bytes must be a multiple of 16");
-  if (!k_tree || !v_tree || !path_nodes || !num_accepted)
-    return fail(SV_ERR_INVALID_ARG, "k_tree, v_tree, path_nodes or num_accepted is NULL");
+  if (!k_tree || !v_tree) return fail(SV_ERR_INVALID_ARG, "k_tree or v_tree is NULL");
   if (!aligned16(k_tree) || !aligned16(v_tree)) return fail(SV_ERR_INVALID_ARG, "k_tree/v_tree not 16-byte aligned");
   sv_status st = check_cache(cache, true);
   if (st != SV_OK) return st;
-  if (B == 0) return SV_OK;
-  sv::CommitParams p{};
+  p = sv::CommitParams{};
   p.k_tree = k_tree;
   p.v_tree = v_tree;
-  p.path_nodes = path_nodes;
-  p.path_stride = path_stride;
-  p.num_accepted = num_accepted;
   p.cache_k = cache.k;
   p.cache_v = cache.v;
   p.prefix_len = cache.prefix_len;
@@ -424,6 +414,101 @@ sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_
   p.num_blocks = cache.num_blocks;
   p.status = status_word();
   if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
+  return SV_OK;
+}
+
+}  // namespace
+
+sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
+                          const void *target_logits, const void *q, sv_q_kind q_kind,
+                          const int32_t *draft_tokens, float temperature, int top_k,
+                          uint64_t seed, uint64_t round, int32_t *out_tokens,
+                          int32_t *out_num_emitted, int32_t *out_num_accepted,
+                          uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+  sv::AcceptParams p;
+  bool greedy = false;
+  sv_status st = chain_params(mode, logit_dt, B, gamma, V, target_logits, q, q_kind, draft_tokens,
+                              temperature, top_k, seed, round, out_tokens, out_num_emitted,
+                              out_num_accepted, out_near_ties, p, &greedy);
+  if (st != SV_OK) return st;
+  return accept_launch(logit_dt, p, greedy, workspace, workspace_bytes, stream);
+}
+
+sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
+                         const int32_t *parent, const int32_t *node_tokens,
+                         const void *target_logits, const void *q, sv_q_kind q_kind, int Dq,
+                         float temperature, int top_k, uint64_t seed, uint64_t round,
+                         int32_t *out_path_nodes, int32_t *out_tokens,
+                         int32_t *out_num_emitted, int32_t *out_num_accepted,
+                         uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+  sv::AcceptParams p;
+  bool greedy = false;
+  sv_status st = tree_params(mode, logit_dt, B, N, V, parent, node_tokens, target_logits, q,
+                             q_kind, Dq, temperature, top_k, seed, round, out_path_nodes,
+                             out_tokens, out_num_emitted, out_num_accepted, out_near_ties, p,
+                             &greedy);
+  if (st != SV_OK) return st;
+  return accept_launch(logit_dt, p, greedy, workspace, workspace_bytes, stream);
+}
+
+sv_status sv_accept_chain_commit(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
+                                 const void *target_logits, const void *q, sv_q_kind q_kind,
+                                 const int32_t *draft_tokens, float temperature, int top_k,
+                                 uint64_t seed, uint64_t round, sv_dtype kv_dt, int Hkv, int D,
+                                 const void *k_tree, const void *v_tree, sv_kv_cache cache,
+                                 int32_t *out_tokens, int32_t *out_num_emitted,
+                                 int32_t *out_num_accepted, uint32_t *out_near_ties,
+                                 void *workspace, size_t workspace_bytes, void *stream) {
+  sv::AcceptParams p;
+  bool greedy = false;
+  sv_status st = chain_params(mode, logit_dt, B, gamma, V, target_logits, q, q_kind, draft_tokens,
+                              temperature, top_k, seed, round, out_tokens, out_num_emitted,
+                              out_num_accepted, out_near_ties, p, &greedy);
+  if (st != SV_OK) return st;
+  if ((st = commit_params(kv_dt, B, gamma + 1, Hkv, D, k_tree, v_tree, cache, p.cm)) != SV_OK)
+    return st;
+  p.commit = 1;
+  return accept_launch(logit_dt, p, greedy, workspace, workspace_bytes, stream);
+}
+
+sv_status sv_accept_tree_commit(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
+                                const int32_t *parent, const int32_t *node_tokens,
+                                const void *target_logits, const void *q, sv_q_kind q_kind,
+                                int Dq, float temperature, int top_k, uint64_t seed,
+                                uint64_t round, sv_dtype kv_dt, int Hkv, int D,
+                                const void *k_tree, const void *v_tree, sv_kv_cache cache,
+                                int32_t *out_path_nodes, int32_t *out_tokens,
+                                int32_t *out_num_emitted, int32_t *out_num_accepted,
+                                uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+  sv::AcceptParams p;
+  bool greedy = false;
+  sv_status st = tree_params(mode, logit_dt, B, N, V, parent, node_tokens, target_logits, q,
+                             q_kind, Dq, temperature, top_k, seed, round, out_path_nodes,
+                             out_tokens, out_num_emitted, out_num_accepted, out_near_ties, p,
+                             &greedy);
+  if (st != SV_OK) return st;
+  if ((st = commit_params(kv_dt, B, N, Hkv, D, k_tree, v_tree, cache, p.cm)) != SV_OK) return st;
+  p.commit = 1;
+  return accept_launch(logit_dt, p, greedy, workspace, workspace_bytes, stream);
+}
+
+// --------------------------------------------------------------------- commit
+
+sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_tree,
+                       const void *v_tree, const int32_t *path_nodes, int path_stride,
+                       const int32_t *num_accepted, sv_kv_cache cache, void *stream) {
+  if (path_stride < 1) return fail(SV_ERR_INVALID_ARG, "path_stride = %d", path_stride);
+  if (!path_nodes || !num_accepted) return fail(SV_ERR_INVALID_ARG, "path_nodes or num_accepted is NULL");
+  sv::CommitParams p;
+  sv_status st = commit_params(dt, B, N, Hkv, D, k_tree, v_tree, cache, p);
+  if (st != SV_OK) return st;
+  if (B == 0) return SV_OK;
+  p.path_nodes = path_nodes;
+  p.path_stride = path_stride;
+  p.num_accepted = num_accepted;
   cudaError_t e = sv::launch_commit(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "commit launch");
   sv::count_launches(1);

@@ -92,6 +92,21 @@ struct RowStat {
   double S;       // sum over kept entries of exp((z - zmax) / T)
 };
 
+// ------------------------------------------------------------------- commit
+
+struct CommitParams {
+  const void *k_tree, *v_tree;
+  const int32_t *path_nodes;
+  int path_stride;
+  const int32_t *num_accepted;
+  void *cache_k, *cache_v;
+  int32_t *prefix_len;
+  const int32_t *block_table;
+  int B, N, Hkv, D, esize;
+  int Lmax, block_size, max_blocks, num_blocks;
+  unsigned int *status;
+};
+
 struct AcceptParams {
   int mode;        // SV_GREEDY / SV_EXACT
   int B, N, V, Dq;
@@ -111,25 +126,14 @@ struct AcceptParams {
   uint32_t *out_near_ties;   // or NULL
   unsigned int *status;
   Tree tree;
+  // commit of the kept path in the same launch (commit != 0): cm's cache, tree K/V and
+  // sizes are used; its path_nodes / num_accepted are the kernel's own results
+  int commit;
+  CommitParams cm;
 };
 
 size_t accept_ws_bytes(int B, int N, int Dq);
 cudaError_t launch_accept(sv_dtype dt, const AcceptParams &p, int num_sms, cudaStream_t s);
-
-// ------------------------------------------------------------------- commit
-
-struct CommitParams {
-  const void *k_tree, *v_tree;
-  const int32_t *path_nodes;
-  int path_stride;
-  const int32_t *num_accepted;
-  void *cache_k, *cache_v;
-  int32_t *prefix_len;
-  const int32_t *block_table;
-  int B, N, Hkv, D, esize;
-  int Lmax, block_size, max_blocks, num_blocks;
-  unsigned int *status;
-};
 
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
 

@@ -1,7 +1,9 @@
 """One verify step through the C ABI: tree attention, acceptance, KV commit.
 
 ``VerifyStep`` owns the device workspaces and output buffers of one workload shape and
-issues the three ABI calls on one stream.  ``run_host`` is the end-to-end form: it
+issues the ABI calls on one stream: attention, then acceptance with the commit of the
+kept path fused into it (``accept_commit``; ``accept`` and ``commit`` are the separate
+calls).  ``run_host`` is the end-to-end form: it
 copies the step's inputs from (pinned) host tensors, runs the step, and copies the
 accepted tokens back.  All arithmetic happens in libsv.so.
 """
@@ -11,9 +13,9 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (EXACT, GREEDY, Q_LOGITS, KVCache, sv_accept_chain, sv_accept_tree,
-               sv_accept_workspace_size, sv_commit_kv, sv_tree_attention,
-               sv_tree_attention_workspace_size)
+from . import (EXACT, GREEDY, Q_LOGITS, KVCache, sv_accept_chain, sv_accept_chain_commit,
+               sv_accept_tree, sv_accept_tree_commit, sv_accept_workspace_size, sv_commit_kv,
+               sv_tree_attention, sv_tree_attention_workspace_size)
 
 
 def _depths(parent):
@@ -59,8 +61,9 @@ class VerifyStep:
             self.chain_path = pn.unsqueeze(0).expand(B, W).contiguous()
 
     def kernel_launches(self) -> int:
-        """Kernels one step launches: attention (+ split merge), two acceptance, commit."""
-        return 1 + int(self.attn_splits) + 2 + 1
+        """Kernels one step launches: attention, then the two acceptance kernels (the
+        commit runs inside the second)."""
+        return 1 + 2
 
     def attention(self, q, k_tree, v_tree, stream=None):
         return sv_tree_attention(q, k_tree, v_tree, self.cache, self.parent, self.scale,
@@ -85,11 +88,27 @@ class VerifyStep:
         path = self.chain_path if self.chain else self.outs["path_nodes"]
         sv_commit_kv(k_tree, v_tree, path, self.outs["num_accepted"], self.cache, stream=stream)
 
+    def accept_commit(self, target_logits, q_draft, node_tokens, k_tree, v_tree, seed=0,
+                      round_=0, stream=None):
+        """Acceptance and the commit of the kept path in one call."""
+        if self.chain:
+            toks = node_tokens[:, 1:] if node_tokens.shape[1] == self.N else node_tokens
+            return sv_accept_chain_commit(
+                self.mode, target_logits, q_draft, self.q_kind,
+                toks.contiguous() if not toks.is_contiguous() else toks, k_tree, v_tree,
+                self.cache, temperature=self.temperature, top_k=self.top_k, seed=seed,
+                round_=round_, outs=self.outs, workspace=self.acc_ws, stream=stream)
+        return sv_accept_tree_commit(self.mode, target_logits, q_draft, self.q_kind, self.parent,
+                                     node_tokens, k_tree, v_tree, self.cache,
+                                     temperature=self.temperature, top_k=self.top_k, seed=seed,
+                                     round_=round_, outs=self.outs, workspace=self.acc_ws,
+                                     stream=stream)
+
     def run(self, q, k_tree, v_tree, target_logits, q_draft, node_tokens, seed=0, round_=0,
             stream=None):
         self.attention(q, k_tree, v_tree, stream)
-        self.accept(target_logits, q_draft, node_tokens, seed, round_, stream)
-        self.commit(k_tree, v_tree, stream)
+        self.accept_commit(target_logits, q_draft, node_tokens, k_tree, v_tree, seed, round_,
+                           stream)
         return self.out, self.outs
 
     # ------------------------------------------------------------ end to end

@@ -122,6 +122,24 @@ def test_commit_rejects_before_launch(lib):
     assert lib.sv_commit_kv(1, 1, 2, 1, 8, P, P, None, 2, P, _cache(), None) == sv.SV_ERR_INVALID_ARG
 
 
+def test_fused_accept_commit_rejects_before_launch(lib):
+    P = ctypes.c_void_p(16)
+    par = (ctypes.c_int32 * 3)(-1, 0, 0)
+    # a bad acceptance argument (V not a multiple of 8) is reported as by sv_accept_tree
+    assert lib.sv_accept_tree_commit(1, 1, 1, 3, 1001, par, P, P, P, 1, 2, 1.0, 0, 0, 0,
+                                     1, 4, 128, P, P, _cache(), P, P, P, P, P, P, 1 << 20,
+                                     None) == sv.SV_ERR_UNSUPPORTED
+    # a bad commit argument (missing tree V) is reported as by sv_commit_kv
+    assert lib.sv_accept_tree_commit(1, 1, 1, 3, 1000, par, P, P, P, 1, 2, 1.0, 0, 0, 0,
+                                     1, 4, 128, P, None, _cache(), P, P, P, P, P, P, 1 << 20,
+                                     None) == sv.SV_ERR_INVALID_ARG
+    assert "v_tree" in lib.sv_last_error().decode()
+    # rows must be whole 16-byte vectors
+    assert lib.sv_accept_chain_commit(1, 1, 1, 2, 1000, P, P, 1, P, 1.0, 0, 0, 0,
+                                      1, 1, 3, P, P, _cache(), P, P, P, P, P, 1 << 20,
+                                      None) == sv.SV_ERR_UNSUPPORTED
+
+
 def test_binding_requires_cuda_tensors(lib):
     import torch
     with pytest.raises(TypeError):
