@@ -30,7 +30,11 @@ namespace sv {
 
 namespace {
 
-constexpr int kStatThreads = 512;
+// Threads per row of the statistics kernel: 256 (four CTAs per SM, so that a batch's
+// rows are in flight together), 512 with top-k (its k groups of maxima need 2 units per
+// thread for k up to SV_MAX_TOP_K).
+template <bool TOPK>
+__host__ __device__ constexpr int stat_threads() { return TOPK ? 512 : 256; }
 constexpr int kSelThreads = 256;  // two CTAs per SM
 constexpr int kMaxCand = 4096;
 constexpr double kNearTie = 1e-6;
@@ -140,9 +144,12 @@ __device__ __forceinline__ bool kept(float z, int j, const RowStat &st) {
 // ------------------------------------------------------------ kernel 1
 
 template <typename T, bool GREEDY, bool TOPK>
-__global__ void __launch_bounds__(kStatThreads, 2) accept_stats_kernel(const AcceptParams p) {
+__global__ void __launch_bounds__(stat_threads<TOPK>(), TOPK ? 2 : 4) accept_stats_kernel(const AcceptParams p) {
+  // the select kernel may be scheduled now; it waits for this grid before reading the
+  // statistics (programmatic dependent launch)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int VEC = Elem<T>::kVec;
-  constexpr int NT = kStatThreads;
+  constexpr int NT = stat_threads<TOPK>();
   __shared__ float sh_v[32];
   __shared__ int sh_i[32];
   __shared__ double sh_d[33];
@@ -548,6 +555,9 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
   }
   __syncthreads();
 
+  // the row statistics come from the previous kernel (launched as its programmatic
+  // dependent): wait for that grid and its memory
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const RowStat *tstat = p.stats + (size_t)b * N;
   const RowStat *qstat = p.stats + (size_t)p.B * N + (size_t)b * p.Dq;
   const double temp = (double)p.temperature;
@@ -958,13 +968,16 @@ cudaError_t launch_select(const AcceptParams &p, int num_sms, cudaStream_t s) {
   cfg.gridDim = dim3((unsigned)(p.B * C));
   cfg.blockDim = dim3(kSelThreads);
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = (unsigned)C;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  // its launch and prologue overlap the statistics kernel's tail
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -974,11 +987,11 @@ cudaError_t launch_typed(const AcceptParams &p, int num_sms, cudaStream_t s) {
   const bool topk = !greedy && p.top_k > 0 && p.top_k < p.V;
   const int rows = p.B * p.N + ((!greedy && p.q_kind == SV_Q_LOGITS) ? p.B * p.Dq : 0);
   if (greedy)
-    accept_stats_kernel<T, true, false><<<rows, kStatThreads, 0, s>>>(p);
+    accept_stats_kernel<T, true, false><<<rows, stat_threads<false>(), 0, s>>>(p);
   else if (topk)
-    accept_stats_kernel<T, false, true><<<rows, kStatThreads, 0, s>>>(p);
+    accept_stats_kernel<T, false, true><<<rows, stat_threads<true>(), 0, s>>>(p);
   else
-    accept_stats_kernel<T, false, false><<<rows, kStatThreads, 0, s>>>(p);
+    accept_stats_kernel<T, false, false><<<rows, stat_threads<false>(), 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (greedy) return launch_select<T, true, false>(p, num_sms, s);
