@@ -20,6 +20,7 @@
 // CTA's slice of the vocabulary, slice totals exchanged through distributed shared
 // memory, then the owning warp re-walks its segment with a warp scan to find the
 // inverse-CDF token.
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 
@@ -135,6 +136,17 @@ __device__ __forceinline__ float key_to_value<float>(uint32_t key) {
 }
 
 // Is entry (value z, index j) inside the row's top-k set?
+// Row statistics written by other CTAs of the same launch: read from L2, not L1.
+__device__ __forceinline__ RowStat load_stat(const RowStat *s) {
+  RowStat r;
+  r.zmax = __ldcg(&s->zmax);
+  r.argmax = __ldcg(&s->argmax);
+  r.key_k = __ldcg(&s->key_k);
+  r.idx_k = __ldcg(&s->idx_k);
+  r.S = __ldcg(&s->S);
+  return r;
+}
+
 template <typename T>
 __device__ __forceinline__ bool kept(float z, int j, const RowStat &st) {
   const uint32_t k = Elem<T>::key(z);
@@ -143,20 +155,19 @@ __device__ __forceinline__ bool kept(float z, int j, const RowStat &st) {
 
 // ------------------------------------------------------------ kernel 1
 
-template <typename T, bool GREEDY, bool TOPK>
-__global__ void __launch_bounds__(stat_threads<TOPK>(), TOPK ? 2 : 4) accept_stats_kernel(const AcceptParams p) {
-  // the select kernel may be scheduled now; it waits for this grid before reading the
-  // statistics (programmatic dependent launch)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+// Statistics of one logit row (all NT threads of the CTA): row max and its lowest index,
+// the top-k threshold, and the softmax sum over the kept entries.  Thread 0 writes
+// p.stats[row].  Rows 0..B*N-1 are target rows, then the q rows.
+template <typename T, bool GREEDY, bool TOPK, int NT>
+__device__ void row_stats(const AcceptParams &p, size_t row) {
   constexpr int VEC = Elem<T>::kVec;
-  constexpr int NT = stat_threads<TOPK>();
   __shared__ float sh_v[32];
   __shared__ int sh_i[32];
   __shared__ double sh_d[33];
   __shared__ unsigned sh_u[32];
+  __syncthreads();  // the shared scratch may still be read for the previous row
 
   const int tid = threadIdx.x;
-  const size_t row = blockIdx.x;
   const size_t nt_rows = (size_t)p.B * p.N;
   const T *x = row < nt_rows ? row_ptr<T>(p.target, row, p.V)
                              : row_ptr<T>(p.q, row - nt_rows, p.V);
@@ -389,6 +400,14 @@ __global__ void __launch_bounds__(stat_threads<TOPK>(), TOPK ? 2 : 4) accept_sta
   if (tid == 0) p.stats[row] = st;
 }
 
+template <typename T, bool GREEDY, bool TOPK>
+__global__ void __launch_bounds__(stat_threads<TOPK>(), TOPK ? 2 : 4) accept_stats_kernel(const AcceptParams p) {
+  // the select kernel may be scheduled now; it waits for this grid before reading the
+  // statistics (programmatic dependent launch)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  row_stats<T, GREEDY, TOPK, stat_threads<TOPK>()>(p, blockIdx.x);
+}
+
 // ------------------------------------------------------------ kernel 2
 //
 // One thread-block cluster of C CTAs per sequence.  Every CTA takes the node decisions
@@ -526,10 +545,13 @@ __device__ void commit_path_slice(const CommitParams &cm, int b, int L, const in
 constexpr int kMaxChunks = 4096;          // chunk sums one CTA keeps (32 vectors each)
 constexpr double kDecideMargin = 1e-4;    // float ratio this close to u: decide in double
 
-template <typename T, bool GREEDY, bool TOPK>
-__global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const AcceptParams p) {
+// Decisions, path, optional commit and final sample of sequence b by the CTA of rank
+// `rank` in a thread-block cluster of C CTAs that split the vocabulary pass and exchange
+// their slice totals through distributed shared memory (C = 1: one CTA, no exchange).
+template <typename T, bool GREEDY, bool TOPK, int NT>
+__device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned C) {
   constexpr int VEC = Elem<T>::kVec;
-  constexpr int NW = kSelThreads / 32;
+  constexpr int NW = NT / 32;
   constexpr int QV = VEC / 4;  // 16-byte vectors of f32 q probabilities per VEC entries
   __shared__ int8_t s_par[kMaxNodes], s_dep[kMaxNodes], s_hc[kMaxNodes];
   __shared__ uint8_t s_acc[kMaxNodes], s_dnear[kMaxNodes];
@@ -543,9 +565,8 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
   __shared__ int8_t s_path[kMaxNodes];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const unsigned C = cluster_size(), rank = cluster_rank();
-  const int b = blockIdx.x / (int)C;
   const int N = p.tree.N, V = p.V;
+  __syncthreads();  // the shared state may still be read for the previous sequence
   if (tid < kMaxNodes) {
     s_par[tid] = p.tree.parent[tid];
     s_dep[tid] = p.tree.depth[tid];
@@ -555,9 +576,6 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
   }
   __syncthreads();
 
-  // the row statistics come from the previous kernel (launched as its programmatic
-  // dependent): wait for that grid and its memory
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const RowStat *tstat = p.stats + (size_t)b * N;
   const RowStat *qstat = p.stats + (size_t)p.B * N + (size_t)b * p.Dq;
   const double temp = (double)p.temperature;
@@ -572,9 +590,9 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
     if (xt < 0 || xt >= V) {
       if (rank == 0) set_status(p.status, SV_DEV_BAD_TOKEN);
     } else if (GREEDY) {
-      acc = xt == tstat[a].argmax;
+      acc = xt == __ldcg(&tstat[a].argmax);
     } else {
-      const RowStat sa = tstat[a];
+      const RowStat sa = load_stat(tstat + a);
       const float zp = Elem<T>::load(row_ptr<T>(p.target, (size_t)b * N + a, V) + xt);
       const bool kp = kept<T>(zp, xt, sa);
       bool logits = p.q_kind == SV_Q_LOGITS;
@@ -582,7 +600,7 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
       float zq = 0.f, qprob = 0.f;
       bool kq = true;
       if (logits) {
-        sq = qstat[d - 1];
+        sq = load_stat(qstat + (d - 1));
         zq = Elem<T>::load(row_ptr<T>(p.q, (size_t)b * p.Dq + d - 1, V) + xt);
         kq = kept<T>(zq, xt, sq);
       } else {
@@ -673,10 +691,10 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
   }
 
   if constexpr (GREEDY) {
-    if (tid == 0) s_tok = tstat[best].argmax;
+    if (tid == 0) s_tok = __ldcg(&tstat[best].argmax);
   } else {
     // final sample: w = [p_best - q_{d+1}]+ if best has children, else p_best
-    const RowStat sp = tstat[best];
+    const RowStat sp = load_stat(tstat + best);
     const uint4 *pv = reinterpret_cast<const uint4 *>(row_ptr<T>(p.target, (size_t)b * N + best, V));
     bool use_q = s_hc[best] != 0;
     const int qrow = s_dep[best];  // q row of depth d+1
@@ -685,7 +703,7 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
     const uint4 *qv = nullptr;
     if (use_q) {
       if (!q_probs) {
-        sq = qstat[qrow];
+        sq = load_stat(qstat + qrow);
         qv = reinterpret_cast<const uint4 *>(row_ptr<T>(p.q, (size_t)b * p.Dq + qrow, V));
       } else {
         qv = reinterpret_cast<const uint4 *>(static_cast<const float *>(p.q) +
@@ -697,10 +715,12 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
     const float inv_sq = use_q && !q_probs ? (float)(1.0 / sq.S) : 0.f;
     const int nvec = V / VEC;
     // this CTA's slice of the vectors, each warp's segment of the slice, and the
-    // segment's chunks of 32 vectors (chunk k of warp w at s_chunk[w * cpw + k])
-    const int per_cta = (nvec + (int)C - 1) / (int)C;
+    // segment's chunks of 32 vectors (chunk k of warp w at s_chunk[w * cpw + k]).  Slices
+    // and segments start at multiples of 32 vectors, so that every chunk is the same 32
+    // vectors (and its float sum the same) however many CTAs share the pass.
+    const int per_cta = ((nvec + (int)C - 1) / (int)C + 31) / 32 * 32;
     const int c0 = min(nvec, (int)rank * per_cta), c1 = min(nvec, c0 + per_cta);
-    const int seg = (c1 - c0 + NW - 1) / NW;
+    const int seg = ((c1 - c0 + NW - 1) / NW + 31) / 32 * 32;
     const int s0 = min(c1, c0 + warp * seg), s1 = min(c1, s0 + seg);
     const int cpw = (seg + 31) / 32;
     const bool keep_chunks = cpw * NW <= kMaxChunks;  // same in every CTA and warp
@@ -795,11 +815,14 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
         for (int w = 0; w < NW; ++w) tot += seg_sum[w];
         s_slice[attempt] = tot;
       }
-      cluster_sync_all();
+      if (C > 1) cluster_sync_all();
+      else __syncthreads();
       if (warp == 0) {
         // every CTA finds the same slice (same totals, same scan): lane r reads CTA r's
         // slice total through distributed shared memory
-        const double tr = lane < (int)C ? ld_peer_f64(&s_slice[attempt], (unsigned)lane) : 0.0;
+        const double tr = lane < (int)C ? (C > 1 ? ld_peer_f64(&s_slice[attempt], (unsigned)lane)
+                                                 : s_slice[attempt])
+                                        : 0.0;
         double total = tr;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
@@ -824,7 +847,7 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
       if (tid == 0) s_snear = 1;
     }
     // this CTA has read its peers' totals for the last time: let them go once all have
-    cluster_arrive();
+    if (C > 1) cluster_arrive();
     const int rstar = s_rstar;
     writer = (int)rank == (rstar < 0 ? 0 : rstar);
 
@@ -840,11 +863,17 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
         int kstar = -1, klast = -1;
         double base_k = base, base_last = base;
         for (int k0 = 0; k0 < nch && kstar < 0; k0 += 32) {
-          const float x = k0 + lane < nch ? s_chunk[warp * cpw + k0 + lane] : 0.f;
-          const float incl = warp_incl_scan_f(x);
-          const double before = base + (double)(incl - x);
-          const unsigned hit = __ballot_sync(0xFFFFFFFFu, k0 + lane < nch && before + (double)x > t);
-          const unsigned pos = __ballot_sync(0xFFFFFFFFu, k0 + lane < nch && x > 0.f);
+          // (the prefix over chunks in double: only the chunk sums themselves are float)
+          const double x = k0 + lane < nch ? (double)s_chunk[warp * cpw + k0 + lane] : 0.0;
+          double incl = x;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const double before = base + (incl - x);
+          const unsigned hit = __ballot_sync(0xFFFFFFFFu, k0 + lane < nch && before + x > t);
+          const unsigned pos = __ballot_sync(0xFFFFFFFFu, k0 + lane < nch && x > 0.0);
           if (pos) {
             const int L = 31 - __clz(pos);
             klast = k0 + L;
@@ -855,7 +884,7 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
             kstar = k0 + L;
             base_k = __shfl_sync(0xFFFFFFFFu, before, L);
           }
-          base += (double)__shfl_sync(0xFFFFFFFFu, incl, 31);
+          base += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
         if (kstar < 0) kstar = klast, base_k = base_last;
         if (kstar < 0) kstar = 0, base_k = s_base;
@@ -916,7 +945,7 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
       }
     }
     // no CTA leaves while a peer may still read its slice totals
-    cluster_wait();
+    if (C > 1) cluster_wait();
   }
   __syncthreads();
 
@@ -940,6 +969,16 @@ __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const Accept
     if (p.commit && commit_L >= 0) p.cm.prefix_len[b] = commit_L + commit_count;
   }
 }
+
+template <typename T, bool GREEDY, bool TOPK>
+__global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const AcceptParams p) {
+  const unsigned C = cluster_size(), rank = cluster_rank();
+  // the row statistics come from the previous kernel (launched as its programmatic
+  // dependent): wait for that grid and its memory
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  select_seq<T, GREEDY, TOPK, kSelThreads>(p, blockIdx.x / (int)C, rank, C);
+}
+
 
 // CTAs per sequence for the final sample: enough clusters to cover the SMs, at most 16.
 int select_cluster(int B, int num_sms) {

@@ -111,7 +111,7 @@ def test_accept_rejects_before_launch(lib):
     need = lib.sv_accept_workspace_size(2, 3, 1000, 1)
     assert need > 0
     assert lib.sv_accept_tree(1, 1, 2, 3, 1000, par, P, P, P, 1, 1, 1.0, 0, 0, 0, P, P, P, P, P,
-                              P, need - 1, None) == sv.SV_ERR_WORKSPACE
+                              P, 16, None) == sv.SV_ERR_WORKSPACE
     del common
 
 
