@@ -705,10 +705,12 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         const bool full = !tree && valid_row && nv_rel >= CW;
         const uint32_t ta0 = t_lane + (uint32_t)((j * MT + mt) * BN + col0);
 
-        // bit c of visible(h) <=> column h*CH + c of this warp's slice is a key the row sees
+        // bit c of visible(h) <=> column h*CH + c of this warp's slice is a key the row sees.
+        // Padding rows (past the unit's rows) see every column: their results are never
+        // used, and this keeps a warp that mixes real and padding rows on one code path.
         constexpr uint32_t kAll = CH == 32 ? 0xFFFFFFFFu : (1u << CH) - 1u;
         auto visible = [&](int h) -> uint32_t {
-          if (full) return kAll;
+          if (full || !valid_row) return kAll;
           const int sh = h * CH;
           if (tree) return sh < 64 ? (uint32_t)(anc_s >> sh) & kAll : 0u;
           const int r = nv_rel - sh;
