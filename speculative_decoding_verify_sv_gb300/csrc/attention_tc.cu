@@ -684,9 +684,10 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
             ok = false;
             break;
           }
-          // with one P buffer, arrive for this tile only after the previous tile's P V
-          // (so the arrival cannot count toward the previous phase)
-          if (PBUF == 1 && gk >= 1 && !mbar_wait(&p_free[0], (gk - 1) & 1, abort_flag)) {
+          // arrive for this tile only once the P V that last used buffer pb has finished:
+          // its p_full phase is then complete, so this arrival cannot count toward it
+          // (this warp writes no P whose own wait would order it)
+          if (gk >= PBUF && !mbar_wait(&p_free[pb], ((gk / PBUF) - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -1057,6 +1058,9 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           st_release_u64(p.flags + pc.unit + blockIdx.x, epoch);
         }
       }
+      // a warp of padding rows reads no O: it arrives for this piece only once every warp
+      // has arrived for the previous one, so that no arrival counts toward an earlier phase
+      if (warp_idle && qi > 0 && !mbar_wait(o_free, (qi - 1) & 1, abort_flag)) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
