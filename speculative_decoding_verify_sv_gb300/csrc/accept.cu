@@ -39,6 +39,49 @@ __host__ __device__ constexpr int stat_threads() { return TOPK ? 512 : 256; }
 constexpr int kSelThreads = 256;  // two CTAs per SM
 constexpr int kMaxCand = 4096;
 constexpr double kNearTie = 1e-6;
+constexpr float kNearTieF = 1e-6f;
+
+// ------------------------------------------------- float-pair arithmetic
+//
+// FP64 instructions have a latency of hundreds of cycles on this part, so the running
+// sums and prefixes that need more than float precision (the inverse-CDF search) carry
+// a value as an unevaluated sum hi + lo of two floats (Knuth's TwoSum, then a
+// renormalising Fast2Sum): about 2^-44 relative, from a few FP32 operations.
+struct F2 {
+  float hi, lo;
+};
+__device__ __forceinline__ F2 f2(float x) { return F2{x, 0.f}; }
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  float e = (a.hi - (s - bb)) + (b.hi - bb);  // exact error of s
+  e += a.lo + b.lo;
+  const float hi = s + e;
+  return F2{hi, e - (hi - s)};
+}
+__device__ __forceinline__ F2 f2_add(F2 a, float b) { return f2_add(a, f2(b)); }
+__device__ __forceinline__ F2 f2_neg(F2 a) { return F2{-a.hi, -a.lo}; }
+__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) { return f2_add(a, f2_neg(b)); }
+// a > b for normalised pairs
+__device__ __forceinline__ bool f2_gt(F2 a, F2 b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+__device__ __forceinline__ float f2_val(F2 a) { return a.hi + a.lo; }
+// (k + 0.5) * 2^-24 * t for a 24-bit k: k * 2^-24 and 2^-25 are exact floats, and the
+// product k * 2^-24 * t.hi is split exactly with an FMA
+__device__ __forceinline__ F2 f2_uniform_times(uint32_t k, F2 t) {
+  const float uh = (float)k * (1.f / 16777216.f);
+  const float p = uh * t.hi;
+  const float pe = fmaf(uh, t.hi, -p);
+  return f2_add(F2{p, 0.f}, f2_add(f2(pe), f2(fmaf(uh, t.lo, t.hi * (1.f / 33554432.f)))));
+}
+__device__ __forceinline__ F2 shfl_up_f2(F2 v, int o) {
+  return F2{__shfl_up_sync(0xFFFFFFFFu, v.hi, o), __shfl_up_sync(0xFFFFFFFFu, v.lo, o)};
+}
+__device__ __forceinline__ F2 shfl_f2(F2 v, int src) {
+  return F2{__shfl_sync(0xFFFFFFFFu, v.hi, src), __shfl_sync(0xFFFFFFFFu, v.lo, src)};
+}
+__device__ __forceinline__ F2 shfl_xor_f2(F2 v, int o) {
+  return F2{__shfl_xor_sync(0xFFFFFFFFu, v.hi, o), __shfl_xor_sync(0xFFFFFFFFu, v.lo, o)};
+}
 
 struct Cand {
   float z;
@@ -83,23 +126,35 @@ __device__ void block_argmax(float &v, int &i, float *shv, int *shi) {
   __syncthreads();
 }
 
-// Block sum of per-thread float partials: a float tree within each warp, then the warp
-// totals added in double by one thread (FP64 throughput is low on this part, so no
-// per-thread double arithmetic).  Every thread gets the result.
-template <int NT>
-__device__ double block_sum_f(float v, double *sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Block sum of per-thread float partials: a butterfly of float additions whose rounding
+// errors (TwoSum, exact) are summed alongside, within each warp and then over the warp
+// totals.  Every thread gets the result.
+__device__ __forceinline__ void warp_sum_c(float &v, float &c) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  if (lane == 0) sh[warp] = (double)v;
+  for (int o = 16; o > 0; o >>= 1) {
+    const float y = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    const float yc = __shfl_xor_sync(0xFFFFFFFFu, c, o);
+    const float s = v + y;
+    const float bb = s - v;
+    const float e = (v - (s - bb)) + (y - bb);
+    v = s;
+    c = (c + yc) + e;
+  }
+}
+template <int NT>
+__device__ float block_sum_f(float v, float *sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float c = 0.f;
+  warp_sum_c(v, c);
+  if (lane == 0) sh[warp] = v, sh[NT / 32 + warp] = c;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    double t = 0.0;
-    for (int w = 0; w < NT / 32; ++w) t += sh[w];
-    sh[NT / 32] = t;
+  if (warp == 0) {
+    float w = lane < NT / 32 ? sh[lane] : 0.f, wc = lane < NT / 32 ? sh[NT / 32 + lane] : 0.f;
+    warp_sum_c(w, wc);
+    if (lane == 0) sh[2 * (NT / 32)] = w + wc;
   }
   __syncthreads();
-  const double r = sh[NT / 32];
+  const float r = sh[2 * (NT / 32)];
   __syncthreads();
   return r;
 }
@@ -163,7 +218,7 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
   constexpr int VEC = Elem<T>::kVec;
   __shared__ float sh_v[32];
   __shared__ int sh_i[32];
-  __shared__ double sh_d[33];
+  __shared__ float sh_d[2 * (NT / 32) + 1];
   __shared__ unsigned sh_u[32];
   __syncthreads();  // the shared scratch may still be read for the previous row
 
@@ -250,7 +305,7 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
   st.argmax = amax;
   st.key_k = 0u;
   st.idx_k = INT_MAX;
-  st.S = 0.0;
+  st.S = 0.f;
 
   if constexpr (!GREEDY && !TOPK) {
     const float part = m == -INFINITY ? 0.f : acc.value() * exp2f((m - zmax) * c);
@@ -445,28 +500,27 @@ __device__ __forceinline__ void cluster_wait() {
 // First lane (0..n-1) whose exclusive prefix + own value exceeds t, with that prefix; if
 // none does (rounding put t at the very end), the last lane with a positive value.
 // Warp-wide: lane i holds x (0 for i >= n); base is added to every prefix.
-__device__ __forceinline__ int warp_find_cdf(double x, int n, double base, double t,
-                                             double *before_out) {
+__device__ __forceinline__ int warp_find_cdf(F2 x, int n, F2 base, F2 t, F2 *before_out) {
   const int lane = threadIdx.x & 31;
-  double incl = x;
-#pragma unroll
+  F2 incl = x;
+#pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += y;
+    const F2 y = shfl_up_f2(incl, o);
+    if (lane >= o) incl = f2_add(incl, y);
   }
-  const double before = base + (incl - x);
-  const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < n && before + x > t);
-  const unsigned pos = __ballot_sync(0xFFFFFFFFu, lane < n && x > 0.0);
+  const F2 before = f2_add(base, f2_sub(incl, x));
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < n && f2_gt(f2_add(before, x), t));
+  const unsigned pos = __ballot_sync(0xFFFFFFFFu, lane < n && x.hi > 0.f);
   const int L = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
-  *before_out = __shfl_sync(0xFFFFFFFFu, before, L < 0 ? 0 : L);
+  *before_out = shfl_f2(before, L < 0 ? 0 : L);
   return L;
 }
-// Read a double from the same shared-memory variable of CTA `rank` in this cluster.
-__device__ __forceinline__ double ld_peer_f64(const double *local, unsigned rank) {
+// Read a float pair from the same shared-memory variable of CTA `rank` in this cluster.
+__device__ __forceinline__ F2 ld_peer_f2(const F2 *local, unsigned rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  double v;
-  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(remote) : "memory");
+  F2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.hi), "=f"(v.lo) : "r"(remote) : "memory");
   return v;
 }
 
@@ -542,8 +596,37 @@ __device__ void commit_path_slice(const CommitParams &cm, int b, int L, const in
       }
   }
 }
+// Requests into L2 the tree K/V rows that commit_path_slice(.., part, parts) will copy.
+__device__ void commit_prefetch_slice(const CommitParams &cm, int b, const int8_t *path, int count,
+                                      unsigned part, unsigned parts) {
+  const long long row_vec = (long long)cm.Hkv * cm.D * cm.esize / 16;
+  const long long total = (long long)count * row_vec;
+  const long long i0 = total * part / parts, i1 = total * (part + 1) / parts;
+  const uint4 *kt = static_cast<const uint4 *>(cm.k_tree);
+  const uint4 *vt = static_cast<const uint4 *>(cm.v_tree);
+  // one request per 128-byte line (8 vectors) of the slice
+  for (long long i = (i0 & ~7ll) + 8ll * threadIdx.x; i < i1; i += 8ll * blockDim.x) {
+    const long long ii = i < i0 ? i0 : i;
+    const int k = (int)(ii / row_vec);
+    const long long src = ((long long)b * cm.N + path[k]) * row_vec + ii % row_vec;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(kt + src));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(vt + src));
+  }
+}
 constexpr int kMaxChunks = 4096;          // chunk sums one CTA keeps (32 vectors each)
-constexpr double kDecideMargin = 1e-4;    // float ratio this close to u: decide in double
+constexpr float kDecideMarginF = 1e-4f;   // float ratio this close to u: decide in double
+
+// The decision of a node whose float ratio fell within kDecideMarginF of u, in double
+// (out of line: it is rarely taken).  Bit 0: accepted; bit 1: |u - ratio| < kNearTie.
+__device__ __noinline__ int decide_double(uint32_t k_node, float zp, RowStat sa, bool logits, float zq,
+                                          RowStat sq, float qprob, float temperature) {
+  const double temp = (double)temperature;
+  const double u_acc = ((double)k_node + 0.5) * (1.0 / 16777216.0);
+  const double pp = exp(((double)zp - (double)sa.zmax) / temp) / (double)sa.S;
+  const double qq = logits ? exp(((double)zq - (double)sq.zmax) / temp) / (double)sq.S : (double)qprob;
+  const double ratio = pp / qq;
+  return (u_acc < ratio ? 1 : 0) | (fabs(u_acc - ratio) < kNearTie ? 2 : 0);
+}
 
 // Decisions, path, optional commit and final sample of sequence b by the CTA of rank
 // `rank` in a thread-block cluster of C CTAs that split the vocabulary pass and exchange
@@ -556,12 +639,11 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
   __shared__ int8_t s_par[kMaxNodes], s_dep[kMaxNodes], s_hc[kMaxNodes];
   __shared__ uint8_t s_acc[kMaxNodes], s_dnear[kMaxNodes];
   __shared__ int s_best, s_nd;
-  __shared__ double seg_sum[NW];
-  __shared__ double s_slice[2];  // this CTA's slice total, per attempt (read by peers)
-  __shared__ double s_tots[kMaxCluster];
+  __shared__ F2 seg_sum[NW];
+  __shared__ F2 s_slice[2];  // this CTA's slice total, per attempt (read by peers)
   __shared__ float s_chunk[kMaxChunks];
   __shared__ int s_wstar, s_tok, s_snear, s_rstar;
-  __shared__ double s_base, s_t;
+  __shared__ F2 s_base, s_t;
   __shared__ int8_t s_path[kMaxNodes];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -578,65 +660,83 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
 
   const RowStat *tstat = p.stats + (size_t)b * N;
   const RowStat *qstat = p.stats + (size_t)p.B * N + (size_t)b * p.Dq;
-  const double temp = (double)p.temperature;
+
+  // Inputs that do not come from the statistics kernel are read before waiting for it:
+  // the candidate token of each non-root node, the two logits at it (the parent's target
+  // row, the q row of the node's depth), its uniforms, and the cache length for the commit.
+  const bool has_node = tid >= 1 && tid < N;
+  const int cnode = tid, a_par = has_node ? s_par[cnode] : 0, d_node = has_node ? s_dep[cnode] : 1;
+  const int xt = has_node ? p.tokens[(size_t)b * p.tok_stride + cnode - p.tok_offset] : -1;
+  const bool tok_ok = xt >= 0 && xt < V;
+  const bool logits = p.q_kind == SV_Q_LOGITS;
+  float zp = 0.f, zq = 0.f, qprob = 0.f;
+  uint32_t k_node = 0u, k_unused = 0u;
+  if (!GREEDY && has_node && tok_ok) {
+    zp = Elem<T>::load(row_ptr<T>(p.target, (size_t)b * N + a_par, V) + xt);
+    if (logits)
+      zq = Elem<T>::load(row_ptr<T>(p.q, (size_t)b * p.Dq + d_node - 1, V) + xt);
+    else
+      qprob = static_cast<const float *>(p.q)[((size_t)b * p.Dq + d_node - 1) * V + xt];
+    verify_uniform_ints(p.seed, p.round, b, cnode, &k_node, &k_unused);
+  }
+  const int commit_L = p.commit ? p.cm.prefix_len[b] : -1;
+
+  // the row statistics come from the previous kernel (launched as its programmatic
+  // dependent): wait for that grid and its memory
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Threads of a warp took different branches above (the root has no node): reconverge
+  // them here, before the warp-wide work that follows.  (Left diverged, later full-warp
+  // shuffles were measured to cost several hundred cycles each.)
+  __syncwarp();
 
   // decisions, one thread per non-root node: accept iff u_acc < p(x)/q(x).  The ratio
-  // is formed in float; when it falls within kDecideMargin (relative) of u it is
-  // recomputed in double, so every decision is the one double precision takes.
-  if (tid >= 1 && tid < N) {
-    const int cnode = tid, a = s_par[cnode], d = s_dep[cnode];
-    const int xt = p.tokens[(size_t)b * p.tok_stride + cnode - p.tok_offset];
+  // and u are formed in float; when the ratio falls within kDecideMargin (relative) of u
+  // both are recomputed in double, so every decision is the one double precision takes.
+  if (has_node) {
+    const int a = a_par, d = d_node;
     uint8_t acc = 0, dn = 0;
-    if (xt < 0 || xt >= V) {
+    if (!tok_ok) {
       if (rank == 0) set_status(p.status, SV_DEV_BAD_TOKEN);
     } else if (GREEDY) {
       acc = xt == __ldcg(&tstat[a].argmax);
     } else {
+      // u = (k + 0.5) 2^-24 in float (within 2^-25; exact for the k near kNearTie)
+      const float u_f = ((float)k_node + 0.5f) * (1.f / 16777216.f);
       const RowStat sa = load_stat(tstat + a);
-      const float zp = Elem<T>::load(row_ptr<T>(p.target, (size_t)b * N + a, V) + xt);
       const bool kp = kept<T>(zp, xt, sa);
-      bool logits = p.q_kind == SV_Q_LOGITS;
       RowStat sq{};
-      float zq = 0.f, qprob = 0.f;
       bool kq = true;
       if (logits) {
         sq = load_stat(qstat + (d - 1));
-        zq = Elem<T>::load(row_ptr<T>(p.q, (size_t)b * p.Dq + d - 1, V) + xt);
         kq = kept<T>(zq, xt, sq);
-      } else {
-        qprob = static_cast<const float *>(p.q)[((size_t)b * p.Dq + d - 1) * V + xt];
       }
-      double u_acc, u_smp;
-      verify_uniforms(p.seed, p.round, b, cnode, &u_acc, &u_smp);
       const bool q_zero = logits ? !kq : !(qprob > 0.f);
       if (q_zero) {
         if (rank == 0) set_status(p.status, SV_DEV_ZERO_DRAFT_PROB);
         acc = kp;  // ratio +inf when p > 0, else 0
       } else if (!kp) {
         acc = 0;  // ratio 0
-        dn = u_acc < kNearTie;
+        dn = u_f < kNearTieF;
       } else {
         const float cf = p.c_log2;
         float rf;
         if (logits)
-          rf = exp2f(((zp - sa.zmax) - (zq - sq.zmax)) * cf) * (float)(sq.S / sa.S);
+          rf = exp2f(((zp - sa.zmax) - (zq - sq.zmax)) * cf) * (sq.S / sa.S);
         else
-          rf = exp2f((zp - sa.zmax) * cf) / ((float)sa.S * qprob);
-        const double r = (double)rf;
-        if (fabs(u_acc - r) > kDecideMargin * (1.0 + r)) {
-          acc = u_acc < r;
+          rf = exp2f((zp - sa.zmax) * cf) / (sa.S * qprob);
+        if (fabsf(u_f - rf) > kDecideMarginF * (1.f + rf)) {
+          acc = u_f < rf;
         } else {
-          const double pp = exp(((double)zp - (double)sa.zmax) / temp) / sa.S;
-          const double qq = logits ? exp(((double)zq - (double)sq.zmax) / temp) / sq.S : (double)qprob;
-          const double ratio = pp / qq;
-          acc = u_acc < ratio;
-          dn = fabs(u_acc - ratio) < kNearTie;
+          const int r = decide_double(k_node, zp, sa, logits, zq, sq, qprob, p.temperature);
+          acc = r & 1;
+          dn = r >> 1;
         }
       }
     }
     s_acc[cnode] = acc;
     s_dnear[cnode] = dn;
   }
+  __syncwarp();
   __syncthreads();
 
   // the kept path: node c is on it iff c and all its ancestors were accepted (the root
@@ -674,20 +774,16 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
   const int best = s_best;
   bool writer = rank == 0;  // the CTA that writes the sequence's outputs
 
-  // commit of the kept path, split over the cluster.  Every CTA reads prefix_len[b]
-  // here; the writer advances it at the very end, after the last cluster barrier
-  // (the non-greedy path) or alone (greedy: one CTA per sequence).
-  int commit_L = -1;
+  // commit of the kept path, split over the cluster: its tree K/V rows are requested into
+  // L2 now and copied after the final sample.  Every CTA read prefix_len[b] before the
+  // wait; the writer advances it at the very end, after the last cluster barrier (the
+  // non-greedy path) or alone (greedy: one CTA per sequence).
   const int commit_count = s_dep[best] + 1;
   if (p.commit) {
     if (tid == 0)
       for (int a = best, i = s_dep[best]; a >= 0; a = s_par[a], --i) s_path[i] = (int8_t)a;
-    commit_L = p.cm.prefix_len[b];
     __syncthreads();
-    if (commit_L >= 0)
-      commit_path_slice(p.cm, b, commit_L, s_path, commit_count, rank, C);
-    else if (tid == 0 && rank == 0)
-      set_status(p.status, SV_DEV_BAD_PREFIX);
+    if (commit_L >= 0) commit_prefetch_slice(p.cm, b, s_path, commit_count, rank, C);
   }
 
   if constexpr (GREEDY) {
@@ -711,8 +807,8 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
       }
     }
     const float c = p.c_log2;
-    const float inv_sp = (float)(1.0 / sp.S);
-    const float inv_sq = use_q && !q_probs ? (float)(1.0 / sq.S) : 0.f;
+    const float inv_sp = 1.f / sp.S;
+    const float inv_sq = use_q && !q_probs ? 1.f / sq.S : 0.f;
     const int nvec = V / VEC;
     // this CTA's slice of the vectors, each warp's segment of the slice, and the
     // segment's chunks of 32 vectors (chunk k of warp w at s_chunk[w * cpw + k]).  Slices
@@ -782,14 +878,14 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
       return vs;
     };
 
-    double u_acc, u_smp;
-    verify_uniforms(p.seed, p.round, b, best, &u_acc, &u_smp);
+    uint32_t k_acc, k_smp;  // u_smp = (k_smp + 0.5) 2^-24
+    verify_uniform_ints(p.seed, p.round, b, best, &k_acc, &k_smp);
 
     for (int attempt = 0; attempt < 2; ++attempt) {
       // phase 1: chunk k of the warp's segment = its vectors [s0 + 32k, s0 + 32k + 32),
       // lane i taking vector s0 + 32k + i; four chunks are loaded before any is used
       constexpr int U = 4;
-      double wsum = 0.0;  // lane 0: the segment total
+      F2 wsum = f2(0.f);  // lane 0: the segment total
       for (int k0 = 0; s0 + 32 * k0 < s1; k0 += U) {
         Raw r[U];
 #pragma unroll
@@ -804,38 +900,41 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
           const float cs = warp_sum_f(v0 + lane < s1 ? vec_sum(v0 + lane, r[u], use_q) : 0.f);
           if (lane == 0) {
             if (keep_chunks) s_chunk[warp * cpw + k0 + u] = cs;
-            wsum += (double)cs;
+            wsum = f2_add(wsum, cs);
           }
         }
       }
       if (lane == 0) seg_sum[warp] = wsum;
       __syncthreads();
       if (tid == 0) {
-        double tot = 0.0;
-        for (int w = 0; w < NW; ++w) tot += seg_sum[w];
+        F2 tot = f2(0.f);
+        for (int w = 0; w < NW; ++w) tot = f2_add(tot, seg_sum[w]);
         s_slice[attempt] = tot;
       }
       if (C > 1) cluster_sync_all();
       else __syncthreads();
       if (warp == 0) {
+        __syncwarp();
         // every CTA finds the same slice (same totals, same scan): lane r reads CTA r's
         // slice total through distributed shared memory
-        const double tr = lane < (int)C ? (C > 1 ? ld_peer_f64(&s_slice[attempt], (unsigned)lane)
-                                                 : s_slice[attempt])
-                                        : 0.0;
-        double total = tr;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
+        const F2 tr = lane < (int)C ? (C > 1 ? ld_peer_f2(&s_slice[attempt], (unsigned)lane)
+                                             : s_slice[attempt])
+                                    : f2(0.f);
+        // the cluster total, summed alike in every lane (a butterfly of float-pair adds)
+        F2 total = tr;
+#pragma unroll 1
+        for (int o = 16; o > 0; o >>= 1) total = f2_add(total, shfl_xor_f2(total, o));
+        total = shfl_f2(total, 0);
         int rs = -1;
-        double base_r = 0.0, t = 0.0;
-        if (total > 0.0) {
-          t = u_smp * total;
-          rs = warp_find_cdf(tr, (int)C, 0.0, t, &base_r);
+        F2 base_r = f2(0.f), t = f2(0.f);
+        if (total.hi > 0.f) {
+          t = f2_uniform_times(k_smp, total);
+          rs = warp_find_cdf(tr, (int)C, f2(0.f), t, &base_r);
         }
         if ((int)rank == rs) {
           // the warp segment within this slice
-          double base_w;
-          const int ws = warp_find_cdf(lane < NW ? seg_sum[lane] : 0.0, NW, base_r, t, &base_w);
+          F2 base_w;
+          const int ws = warp_find_cdf(lane < NW ? seg_sum[lane] : f2(0.f), NW, base_r, t, &base_w);
           if (lane == 0) s_wstar = ws, s_base = base_w, s_t = t;
         }
         if (lane == 0) s_rstar = rs;
@@ -853,38 +952,39 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
 
     // phase 2: the owning warp finds the chunk from the chunk sums, then the token in it
     if ((int)rank == rstar && warp == s_wstar) {
-      const double t = s_t;
-      double base = s_base;
+      __syncwarp();
+      const F2 t = s_t;
+      F2 base = s_base;
       int found = 0, tok = -1, near = 0, last_pos = -1;
       const int nch = (s1 - s0 + 31) / 32;
       int k_first = 0;
       if (keep_chunks) {
-        // first chunk whose end passes t (else the last one with mass)
+        // first chunk whose end passes t (else the last one with mass); the prefix over
+        // chunks is a float-pair sum, only the chunk sums themselves are float
         int kstar = -1, klast = -1;
-        double base_k = base, base_last = base;
+        F2 base_k = base, base_last = base;
         for (int k0 = 0; k0 < nch && kstar < 0; k0 += 32) {
-          // (the prefix over chunks in double: only the chunk sums themselves are float)
-          const double x = k0 + lane < nch ? (double)s_chunk[warp * cpw + k0 + lane] : 0.0;
-          double incl = x;
-#pragma unroll
+          const F2 x = f2(k0 + lane < nch ? s_chunk[warp * cpw + k0 + lane] : 0.f);
+          F2 incl = x;
+#pragma unroll 1
           for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += y;
+            const F2 y = shfl_up_f2(incl, o);
+            if (lane >= o) incl = f2_add(incl, y);
           }
-          const double before = base + (incl - x);
-          const unsigned hit = __ballot_sync(0xFFFFFFFFu, k0 + lane < nch && before + x > t);
-          const unsigned pos = __ballot_sync(0xFFFFFFFFu, k0 + lane < nch && x > 0.0);
+          const F2 before = f2_add(base, f2_sub(incl, x));
+          const unsigned hit = __ballot_sync(0xFFFFFFFFu, k0 + lane < nch && f2_gt(f2_add(before, x), t));
+          const unsigned pos = __ballot_sync(0xFFFFFFFFu, k0 + lane < nch && x.hi > 0.f);
           if (pos) {
             const int L = 31 - __clz(pos);
             klast = k0 + L;
-            base_last = __shfl_sync(0xFFFFFFFFu, before, L);
+            base_last = shfl_f2(before, L);
           }
           if (hit) {
             const int L = __ffs(hit) - 1;
             kstar = k0 + L;
-            base_k = __shfl_sync(0xFFFFFFFFu, before, L);
+            base_k = shfl_f2(before, L);
           }
-          base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+          base = f2_add(base, shfl_f2(incl, 31));
         }
         if (kstar < 0) kstar = klast, base_k = base_last;
         if (kstar < 0) kstar = 0, base_k = s_base;
@@ -904,21 +1004,21 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
           if (w[e] > 0.f) last_pos = v * VEC + e;
         }
         const float incl = warp_incl_scan_f(lsum);
-        const double before = base + (double)(incl - lsum);
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, before + (double)lsum > t);
+        const F2 before = f2_add(base, incl - lsum);
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, f2_gt(f2_add(before, lsum), t));
         if (hit) {
           const int L = __ffs(hit) - 1;
           if (lane == L) {
-            double cum = before;
+            F2 cum = before;
             int j = -1, lastp = -1;
             for (int e = 0; e < VEC; ++e) {
               if (w[e] <= 0.f) continue;
-              const double prev = cum;
-              cum += (double)w[e];
+              const F2 prev = cum;
+              cum = f2_add(cum, w[e]);
               lastp = v * VEC + e;
-              if (cum > t) {
+              if (f2_gt(cum, t)) {
                 j = v * VEC + e;
-                near = (t - prev < kNearTie) || (cum - t < kNearTie);
+                near = (f2_val(f2_sub(t, prev)) < kNearTieF) || (f2_val(f2_sub(cum, t)) < kNearTieF);
                 break;
               }
             }
@@ -929,7 +1029,7 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
           near = __shfl_sync(0xFFFFFFFFu, near, L);
           found = 1;
         }
-        base += (double)__shfl_sync(0xFFFFFFFFu, incl, 31);
+        base = f2_add(base, __shfl_sync(0xFFFFFFFFu, incl, 31));
         if (keep_chunks && !found) break;  // rounding: t fell past the chunk's end
       }
       if (!found) {
@@ -946,6 +1046,12 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
     }
     // no CTA leaves while a peer may still read its slice totals
     if (C > 1) cluster_wait();
+  }
+  if (p.commit) {
+    if (commit_L >= 0)
+      commit_path_slice(p.cm, b, commit_L, s_path, commit_count, rank, C);
+    else if (tid == 0 && rank == 0)
+      set_status(p.status, SV_DEV_BAD_PREFIX);
   }
   __syncthreads();
 
@@ -973,17 +1079,16 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
 template <typename T, bool GREEDY, bool TOPK>
 __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const AcceptParams p) {
   const unsigned C = cluster_size(), rank = cluster_rank();
-  // the row statistics come from the previous kernel (launched as its programmatic
-  // dependent): wait for that grid and its memory
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // (select_seq waits for the statistics kernel once it has read its other inputs)
   select_seq<T, GREEDY, TOPK, kSelThreads>(p, blockIdx.x / (int)C, rank, C);
 }
 
 
-// CTAs per sequence for the final sample: enough clusters to cover the SMs, at most 16.
+// CTAs per sequence for the final sample: as many as keep the select grid within two CTAs
+// per SM (the pass over two rows per sequence is split among them), at most 16.
 int select_cluster(int B, int num_sms) {
   int C = 1;
-  while (C < kMaxCluster && (long long)B * C * 2 <= num_sms) C *= 2;
+  while (C < kMaxCluster && (long long)B * C * 2 <= 2ll * num_sms) C *= 2;
   return C;
 }
 

@@ -177,6 +177,50 @@ __device__ __forceinline__ long long block_scan(long long x, long long *red, lon
   return before + x;
 }
 
+// One piece (n tiles from tile counter g, the piece's index qi in this CTA) of a softmax
+// warp whose rows are all padding.  It reads no S and writes no P or O, but takes its part
+// in every barrier and in zeroing the V rows past the prefix end.  Each arrival waits for
+// the previous phase of its barrier to be complete, since no write of this warp orders
+// it.  Kept out of line so that the row loop's code stays small.  False if a wait gave up.
+template <class Lay, int BN, int STAGES, int PBUF>
+__device__ __noinline__ bool idle_piece(int N, int t0, int n, bool publish, int g, int qi, int L,
+                                        uint64_t *s_full, uint64_t *s_free, uint64_t *v_full,
+                                        uint64_t *p_full, uint64_t *o_free, uint64_t *pub, uint8_t *sV,
+                                        volatile int *abort_flag) {
+  const int lane = threadIdx.x & 31;
+  for (int k = 0; k < n; ++k) {
+    const int gk = g + k, j = gk & 1, s = gk % STAGES, t = t0 + k, pb = gk % PBUF;
+    if (!mbar_wait(&s_full[j], (gk >> 1) & 1, abort_flag)) return false;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_free[j]);
+    const int nvalid = t == 0 ? N : min(BN, L - (t - 1) * BN);
+    if (t != 0 && nvalid < BN) {  // this warp's share of zeroing the V tail (see the row loop)
+      if (!mbar_wait(&v_full[s], (gk / STAGES) & 1, abort_flag)) return false;
+      uint8_t *vt = sV + s * Lay::KV_BYTES;
+      constexpr int per_row = Lay::KB * 8;
+      for (int i = threadIdx.x; i < (BN - nvalid) * per_row; i += 32 * Lay::NSW) {
+        const int r = nvalid + i / per_row, rem = i % per_row;
+        *reinterpret_cast<uint4 *>(vt + (rem >> 3) * Lay::KV_BLOCK + r * 128 + (rem & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (gk >= PBUF && !mbar_wait(&p_full[pb], ((gk / PBUF) - 1) & 1, abort_flag)) return false;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&p_full[pb]);
+  }
+  if (publish) {
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(pub);
+  }
+  if (qi > 0 && !mbar_wait(o_free, (qi - 1) & 1, abort_flag)) return false;
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(o_free);
+  return true;
+}
+
 template <int D, int MT, int CP, int BN, int STAGES, int QBUF, int PBUF>
 __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ TcParams p) {
@@ -655,6 +699,16 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       const uint64_t anc = valid_row ? sAnc[node] : 0ull;
       const bool warp_idle = CP == 1 && __all_sync(0xFFFFFFFFu, !valid_row);
       const int L = clamp_len(p, pc.b);
+      if (warp_idle) {  // every row of this warp is padding: barriers only
+        if (!idle_piece<Lay, BN, STAGES, PBUF>(p.N, pc.t0, n, pc.t0 > 0, g, qi, L, s_full, s_free, v_full,
+                                              p_full, o_free, pub, sV, abort_flag)) {
+          ok = false;
+          break;
+        }
+        g += n;
+        ++qi;
+        continue;
+      }
       float m_ref = -INFINITY, l = 0.f;
       for (int k = 0; k < n; ++k) {
         const int gk = g + k, j = gk & 1, s = gk % STAGES, t = pc.t0 + k, pb = gk % PBUF;
@@ -679,26 +733,6 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           }
           return true;
         };
-        if (warp_idle) {  // every row of this warp is padding: nothing to compute or write
-          if (!zero_v_tail()) {
-            ok = false;
-            break;
-          }
-          // arrive for this tile only once the P V that last used buffer pb has finished:
-          // its p_full phase is then complete, so this arrival cannot count toward it
-          // (this warp writes no P whose own wait would order it)
-          if (gk >= PBUF && !mbar_wait(&p_free[pb], ((gk / PBUF) - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&s_free[j]);
-            mbar_arrive(&p_full[pb]);
-          }
-          continue;
-        }
         // visible columns of this warp's slice: tree tile -> ancestor bits, prefix
         // tile -> columns before the prefix end
         const uint64_t anc_s = (tree && valid_row && col0 < 64) ? (anc >> col0) : 0ull;
@@ -1058,9 +1092,6 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           st_release_u64(p.flags + pc.unit + blockIdx.x, epoch);
         }
       }
-      // a warp of padding rows reads no O: it arrives for this piece only once every warp
-      // has arrived for the previous one, so that no arrival counts toward an earlier phase
-      if (warp_idle && qi > 0 && !mbar_wait(o_free, (qi - 1) & 1, abort_flag)) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);

@@ -104,6 +104,15 @@ __device__ __forceinline__ void verify_uniforms(uint64_t seed, uint64_t round, i
   *u_smp = ((double)(ctr[1] >> 8) + 0.5) * (1.0 / 16777216.0);
 }
 
+// The same uniforms as their 24-bit integers k: u = (k + 0.5) * 2^-24.
+__device__ __forceinline__ void verify_uniform_ints(uint64_t seed, uint64_t round, int b, int c,
+                                                    uint32_t *k_acc, uint32_t *k_smp) {
+  uint32_t ctr[4] = {(uint32_t)c, (uint32_t)b, (uint32_t)round, (uint32_t)(round >> 32)};
+  philox4x32_10(ctr, (uint32_t)seed, (uint32_t)(seed >> 32));
+  *k_acc = ctr[0] >> 8;
+  *k_smp = ctr[1] >> 8;
+}
+
 // --------------------------------------------------------- warp reductions
 
 __device__ __forceinline__ double warp_sum_d(double v) {
@@ -127,7 +136,7 @@ struct KahanF {
     c = (t - s) - y;
     s = t;
   }
-  __device__ __forceinline__ double value() const { return (double)s - (double)c; }
+  __device__ __forceinline__ float value() const { return s - c; }
 };
 
 // ------------------------------------------------------ async copies, MMA

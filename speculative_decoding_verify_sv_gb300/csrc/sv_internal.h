@@ -89,7 +89,7 @@ struct RowStat {
   int32_t argmax; // its lowest index
   uint32_t key_k; // top-k threshold key (kept: key > key_k, or == key_k and idx <= idx_k)
   int32_t idx_k;
-  double S;       // sum over kept entries of exp((z - zmax) / T)
+  float S;        // sum over kept entries of exp((z - zmax) / T)
 };
 
 // ------------------------------------------------------------------- commit
