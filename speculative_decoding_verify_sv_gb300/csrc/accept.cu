@@ -257,11 +257,25 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
 #pragma unroll
     for (int u = 0; u < U; ++u) Elem<T>::unpack(raws[u], f[u]);
     // the batch maximum first; the index scan runs only when it beats the running max
-    float mx = f[0][0];
+    // (bf16: lane-wise maxima of the packed words, exact)
+    float mx;
+    if constexpr (VEC == 8) {
+      uint32_t hm = raws[0].x;
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+      for (int u = 0; u < U; ++u) {
+        hm = max_bf16x2(hm, raws[u].x);
+        hm = max_bf16x2(hm, raws[u].y);
+        hm = max_bf16x2(hm, raws[u].z);
+        hm = max_bf16x2(hm, raws[u].w);
+      }
+      mx = fmaxf(__uint_as_float(hm << 16), __uint_as_float(hm & 0xFFFF0000u));
+    } else {
+      mx = f[0][0];
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) mx = fmaxf(mx, f[u][e]);
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) mx = fmaxf(mx, f[u][e]);
+    }
     if (mx > vmax) {
 #pragma unroll
       for (int u = 0; u < U; ++u)
@@ -286,12 +300,20 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
         m = vmax;
       }
       if (m != -INFINITY) {
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        // partial sums ps[e & 3] in lane pairs: (z - m) * c and the sums as packed f32x2
+        // (the same roundings and order as the scalar form)
+        float2 ps01 = make_float2(0.f, 0.f), ps23 = make_float2(0.f, 0.f);
+        const float2 m2 = make_float2(m, m), c2 = make_float2(c, c);
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) ps[e & 3] += ex2_approx((f[u][e] - m) * c);
-        acc.add((ps[0] + ps[1]) + (ps[2] + ps[3]));
+          for (int e = 0; e < VEC; e += 2) {
+            const float2 t = mul2(sub2(make_float2(f[u][e], f[u][e + 1]), m2), c2);
+            const float2 x = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            if (e & 2) ps23 = add2(ps23, x);
+            else ps01 = add2(ps01, x);
+          }
+        acc.add((ps01.x + ps01.y) + (ps23.x + ps23.y));
       }
     }
   }
@@ -838,13 +860,23 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
       return r;
     };
     // weights of the VEC entries of vector v (top-k membership checked only with top-k)
+    // (the arguments and scalings as packed f32x2: the same roundings as the scalar form)
+    const float2 c2 = make_float2(c, c), zp2 = make_float2(sp.zmax, sp.zmax);
+    const float2 ip2 = make_float2(inv_sp, inv_sp);
     auto weights = [&](int v, const Raw &r, float w[VEC], bool with_q) {
       float f[VEC];
       Elem<T>::unpack(r.p, f);
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        w[e] = ex2_approx((f[e] - sp.zmax) * c) * inv_sp;
-        if (TOPK && !kept<T>(f[e], v * VEC + e, sp)) w[e] = 0.f;
+      for (int e = 0; e < VEC; e += 2) {
+        const float2 t = mul2(sub2(make_float2(f[e], f[e + 1]), zp2), c2);
+        const float2 x = mul2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), ip2);
+        w[e] = x.x;
+        w[e + 1] = x.y;
+      }
+      if (TOPK) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+          if (!kept<T>(f[e], v * VEC + e, sp)) w[e] = 0.f;
       }
       if (with_q) {
         float g[VEC];
@@ -859,14 +891,26 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
         } else {
           float fq[VEC];
           Elem<T>::unpack(r.q[0], fq);
+          const float2 zq2 = make_float2(sq.zmax, sq.zmax), iq2 = make_float2(inv_sq, inv_sq);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            g[e] = ex2_approx((fq[e] - sq.zmax) * c) * inv_sq;
-            if (TOPK && !kept<T>(fq[e], v * VEC + e, sq)) g[e] = 0.f;
+          for (int e = 0; e < VEC; e += 2) {
+            const float2 t = mul2(sub2(make_float2(fq[e], fq[e + 1]), zq2), c2);
+            const float2 x = mul2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), iq2);
+            g[e] = x.x;
+            g[e + 1] = x.y;
+          }
+          if (TOPK) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+              if (!kept<T>(fq[e], v * VEC + e, sq)) g[e] = 0.f;
           }
         }
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) w[e] = fmaxf(w[e] - g[e], 0.f);
+        for (int e = 0; e < VEC; e += 2) {
+          const float2 d = sub2(make_float2(w[e], w[e + 1]), make_float2(g[e], g[e + 1]));
+          w[e] = fmaxf(d.x, 0.f);
+          w[e + 1] = fmaxf(d.y, 0.f);
+        }
       }
     };
     auto vec_sum = [&](int v, const Raw &r, bool with_q) -> float {
