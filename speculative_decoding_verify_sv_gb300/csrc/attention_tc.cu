@@ -70,8 +70,8 @@ struct TcLayout {
   static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_P + PBUF * P_BYTES;
   // k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], s_free[2], p_full[2], p_free[2], o_free, drain,
-  // xch_full[2], xl_full, pub, q_full[QBUF], q_empty[QBUF]
-  static constexpr int NBAR = 4 * STAGES + 14 + 2 * QBUF;
+  // xch_full[2], xl_full, pub, q_full[QBUF], q_empty[QBUF], stage_full (one M tile only)
+  static constexpr int NBAR = 4 * STAGES + 14 + 2 * QBUF + (MT == 1 ? 1 : 0);
   // row copies exchange partial row maxima [2][4][32] and row sums [4][32] (f32)
   static constexpr int OFF_XCH = OFF_BAR + NBAR * 8;
   static constexpr int OFF_XL = OFF_XCH + (CP > 1 ? 2 * 4 * 32 * 4 : 0);
@@ -231,8 +231,8 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = smem_raw;
   const int P = gridDim.x;
-  // Completion counting: every CTA reads the call's epoch first and counts itself
-  // out at its end; the last one out advances the workspace's generation.
+  // Completion counting: every CTA reads the call's epoch first and then counts itself
+  // out; the last one to do so advances the workspace's generation for the next call.
   unsigned long long *gen = p.hdr;
   unsigned int *done = reinterpret_cast<unsigned int *>(p.hdr + 1);
   const unsigned long long epoch = *reinterpret_cast<volatile unsigned long long *>(gen) + 1ull;
@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
   uint64_t *pub = xl_full + 1;
   uint64_t *q_full = pub + 1;
   uint64_t *q_empty = q_full + QBUF;
+  uint64_t *stage_full = q_empty + QBUF;  // a head piece's first producer, staged
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Lay::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + Lay::OFF_MISC + 4);
   uint64_t *sAnc = reinterpret_cast<uint64_t *>(sm + Lay::OFF_ANC);
@@ -360,6 +361,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
     mbar_init(drain, 1);
     mbar_init(xl_full, NSW);
     mbar_init(pub, NSW);
+    if (MT == 1) mbar_init(stage_full, 32);
     for (int i = 0; i < QBUF; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
@@ -389,6 +391,9 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // this CTA has read the epoch: count it out now (the count only advances the generation
+  // for the next call, which starts after this grid has ended); with two M tiles at the end
+  if (MT == 1) finish();
 
   PieceIter it;
   it.f = f0;
@@ -493,7 +498,13 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
     Piece pc;
     // per piece: K of its first tile and the previous tile's V go out before the wait
     // for the Q buffer (held until the previous piece's last S completes)
+    Piece last;
+    bool have_last = false;
     while (ok && piece_next(it, p, pc)) {
+      if constexpr (MT == 1) {
+        last = pc;
+        have_last = true;
+      }
       bool q_pending = true;
       Src nxt = make_src(pc, pc.t0);
       for (int t = pc.t0; t < pc.t1; ++t) {
@@ -533,6 +544,54 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       }
     }
     if (ok && have_pend && load(pend, gv, true)) ++gv;
+    // The CTA's last piece is a head (it holds the first tiles of a unit that later CTAs
+    // continue; one M tile): once the first of those CTAs has published its partial
+    // result and the last S has freed the K stages and Q, this warp copies that partial
+    // O into the K area (the layout the merge reads) and its row maxima and sums into
+    // the Q area, while the softmax warps finish the last tile.
+    if constexpr (MT == 1) {
+      if (ok && have_last && last.t0 == 0 && last.t1 < last.T) {
+        const long long U_end = last.fs - last.t0 + last.T;
+        long long sl0 = -1;
+        for (int c2 = blockIdx.x + 1; c2 < P; ++c2) {
+          const long long fa = cta_first(W, c2, P);
+          if (fa >= U_end) break;
+          if (fa == cta_first(W, c2 + 1, P)) continue;
+          sl0 = last.unit + c2;
+          break;
+        }
+        if (sl0 >= 0) {
+          int r = 1;
+          if (lane == 0) {
+            const unsigned long long t0 = global_ns();
+            while (ld_acquire_u64(p.flags + sl0) != epoch) {
+              if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                r = 0;
+                break;
+              }
+            }
+            if (r && !mbar_wait(&k_empty[(g - 1) % STAGES], ((g - 1) / STAGES) & 1, abort_flag)) r = 0;
+            if (r && !mbar_wait(&q_empty[(nq - 1) % QBUF], ((nq - 1) / QBUF) & 1, abort_flag)) r = 0;
+          }
+          if (__shfl_sync(0xFFFFFFFFu, r, 0)) {
+            (void)ld_acquire_u64(p.flags + sl0);  // each lane's own acquire of the published rows
+            float4 *stage = reinterpret_cast<float4 *>(sK);
+            float2 *mls = reinterpret_cast<float2 *>(sQ);
+            static_assert(MT > 1 || kRows * D * 4 <= STAGES * Lay::KV_BYTES, "staging room");
+            for (int row = lane; row < kRows; row += 32) {
+              // 16-byte unit i of row r at r * (D / 4) + (i ^ (r % (D / 4))): a warp reading
+              // one unit of 32 rows meets no bank conflict
+              const float4 *src = reinterpret_cast<const float4 *>(p.part_o + ((size_t)sl0 * kRows + row) * D);
+              for (int i = 0; i < D / 4; ++i)
+                cp_async_16(stage + (size_t)row * (D / 4) + (i ^ (row % (D / 4))), src + i, true);
+              cp_async_8(mls + row, p.part_ml + ((size_t)sl0 * kRows + row) * 2);
+            }
+            cp_async_mbar_arrive(stage_full);
+          }
+        }
+      }
+    }
     if (lane == 0 && *abort_flag) {
       // let copies already in flight land before the CTA retires
       const unsigned long long t0 = global_ns();
@@ -953,16 +1012,22 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           float M = m_ref;
           float pm[kPre], pl[kPre];
           for_producers([&](int j, long long sl) -> bool {
-            const unsigned long long *flag = p.flags + sl;
-            const unsigned long long t0 = global_ns();
-            while (ld_acquire_u64(flag) != epoch) {
-              if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
-                *abort_flag = 1;
-                return false;
+            float2 ml;
+            if (MT == 1 && j == 0) {
+              // staged by the producer warp (after it saw the flag)
+              if (!mbar_wait(stage_full, 0, abort_flag)) return false;
+              ml = reinterpret_cast<const float2 *>(sQ)[R_local];
+            } else {
+              const unsigned long long *flag = p.flags + sl;
+              const unsigned long long t0 = global_ns();
+              while (ld_acquire_u64(flag) != epoch) {
+                if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
+                  *abort_flag = 1;
+                  return false;
+                }
               }
+              ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + ((size_t)sl * ROWS + R_local) * 2));
             }
-            const float2 ml =
-                __ldcg(reinterpret_cast<const float2 *>(p.part_ml + ((size_t)sl * ROWS + R_local) * 2));
 #pragma unroll
             for (int k = 0; k < kPre; ++k)
               if (k == j) pslot[k] = sl, pm[k] = ml.x, pl[k] = ml.y;
@@ -992,20 +1057,11 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           inv = L > 0.f ? 1.f / L : 0.f;
           m_ref = M;  // the weights below are 2^(m_piece - M)
         }
-        // The first producer's partial row is copied whole into shared memory, which is
-        // free by now: this is the CTA's last piece and its last P V has completed.
-        // 16-byte unit i of row r sits at r * (D / 4) + (i ^ (r % (D / 4))) (no bank
-        // conflicts when a warp reads one unit of 32 rows).  Single-tile units only.
+        // The first producer's partial rows were staged in shared memory by the producer
+        // warp (one M tile only); 16-byte unit i of row r at r * (D / 4) + (i ^ (r % (D / 4))).
         float4 *stage = nullptr;
-        if (MT == 1 && head && valid_row && np > 0) {
-          static_assert(MT > 1 || kRows * D * 4 <= 2 * STAGES * Lay::KV_BYTES, "staging room");
+        if (MT == 1 && head && valid_row && np > 0)
           stage = reinterpret_cast<float4 *>(sK) + (size_t)R_local * (D / 4);
-          const float4 *src = reinterpret_cast<const float4 *>(p.part_o + ((size_t)pslot[0] * ROWS + R_local) * D);
-#pragma unroll
-          for (int i = 0; i < D / 4; ++i) cp_async_16(stage + (i ^ (R_local % (D / 4))), src + i, true);
-          cp_async_commit();
-          cp_async_wait<0>();
-        }
         __syncwarp();  // tcgen05.ld below is warp-collective
         const long long slot = pc.unit + blockIdx.x;
         float *pdst = p.part_o + ((size_t)slot * ROWS + R_local) * D;
@@ -1105,7 +1161,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, Lay::TMEM_COLS);
   if (threadIdx.x == 0 && *abort_flag) set_status(p.status, SV_DEV_TIMEOUT);
-  finish();
+  if (MT == 2) finish();
 }
 
 template <int D, int MT, int CP, int BN, int STAGES, int QBUF, int PBUF>
