@@ -31,13 +31,19 @@ namespace sv {
 
 namespace {
 
-// Threads per row of the statistics kernel: 256 (four CTAs per SM, so that a batch's
-// rows are in flight together), 512 with top-k (its k groups of maxima need 2 units per
-// thread for k up to SV_MAX_TOP_K).
+// Threads per row of the statistics kernel: 256, four CTAs per SM, so that a batch's rows
+// are in flight together and one row's top-k work overlaps the others' reads (with top-k
+// each thread keeps 4 units, enough groups for k up to SV_MAX_TOP_K).
 template <bool TOPK>
-__host__ __device__ constexpr int stat_threads() { return TOPK ? 512 : 256; }
+__host__ __device__ constexpr int stat_threads() { return 256; }
 constexpr int kSelThreads = 256;  // two CTAs per SM
-constexpr int kMaxCand = 4096;
+constexpr int kMaxCand = 2048;
+// Batches (of 4 vectors per thread) whose maximum the top-k statistics remember: rows of up
+// to 32 * 256 * 4 * 8 = 262,144 bf16 entries; later batches are always re-read.
+constexpr int kMaxTopkBatches = 32;
+// Batches the top-k gather lists for its cooperative re-read (else each thread re-reads
+// its own).
+constexpr int kMaxGatherList = 2048;
 constexpr double kNearTie = 1e-6;
 constexpr float kNearTieF = 1e-6f;
 
@@ -190,6 +196,18 @@ __device__ __forceinline__ float key_to_value<float>(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
+// Largest entry of one 16-byte vector (bf16: packed maxima, exact).
+template <typename T>
+__device__ __forceinline__ float vec_max(const uint4 &r) {
+  if constexpr (Elem<T>::kVec == 8) {
+    const uint32_t hm = max_bf16x2(max_bf16x2(r.x, r.y), max_bf16x2(r.z, r.w));
+    return fmaxf(__uint_as_float(hm << 16), __uint_as_float(hm & 0xFFFF0000u));
+  } else {
+    return fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
+                 fmaxf(__uint_as_float(r.z), __uint_as_float(r.w)));
+  }
+}
+
 // Is entry (value z, index j) inside the row's top-k set?
 // Row statistics written by other CTAs of the same launch: read from L2, not L1.
 __device__ __forceinline__ RowStat load_stat(const RowStat *s) {
@@ -234,7 +252,14 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
   int imax = INT_MAX;
   float m = -INFINITY;  // running maximum the partial sum is taken against
   KahanF acc;
-  uint32_t umax[2] = {0u, 0u};  // TOPK: per-unit max key (units: even / odd lanes)
+  // TOPK: the maxima of this thread's 4 units (fp32: units = element lanes 0..3 of each
+  // vector; bf16: the low and high halves of words x, z and of words y, w, kept as two
+  // packed pairs), and the top 16 bits of the key of each batch's maximum, so that the
+  // gather re-reads only the batches that can hold an entry of the top k
+  uint32_t umax[4] = {0u, 0u, 0u, 0u};
+  uint32_t umw[2] = {Elem<T>::kNegInfWord, Elem<T>::kNegInfWord};
+  constexpr int kKeyShift = Elem<T>::kKeyBits - 16;
+  __shared__ uint16_t s_bkey[TOPK ? kMaxTopkBatches * NT : 1];
 
   // each thread takes vectors tid, tid + NT, ... in index order, four at a time; the
   // next four are loaded while the current four are worked on (two batches in flight);
@@ -248,7 +273,7 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
   };
   uint4 nxt[U];
   load_batch(tid, nxt);
-  for (int v0 = tid; v0 < nvec; v0 += NT * U) {
+  for (int v0 = tid, jb = 0; v0 < nvec; v0 += NT * U, ++jb) {
     uint4 raws[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) raws[u] = nxt[u];
@@ -260,15 +285,18 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
     // (bf16: lane-wise maxima of the packed words, exact)
     float mx;
     if constexpr (VEC == 8) {
-      uint32_t hm = raws[0].x;
+      uint32_t h0 = max_bf16x2(raws[0].x, raws[0].z), h1 = max_bf16x2(raws[0].y, raws[0].w);
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        hm = max_bf16x2(hm, raws[u].x);
-        hm = max_bf16x2(hm, raws[u].y);
-        hm = max_bf16x2(hm, raws[u].z);
-        hm = max_bf16x2(hm, raws[u].w);
+      for (int u = 1; u < U; ++u) {
+        h0 = max_bf16x2(h0, max_bf16x2(raws[u].x, raws[u].z));
+        h1 = max_bf16x2(h1, max_bf16x2(raws[u].y, raws[u].w));
       }
+      const uint32_t hm = max_bf16x2(h0, h1);
       mx = fmaxf(__uint_as_float(hm << 16), __uint_as_float(hm & 0xFFFF0000u));
+      if constexpr (TOPK) {
+        umw[0] = max_bf16x2(umw[0], h0);
+        umw[1] = max_bf16x2(umw[1], h1);
+      }
     } else {
       mx = f[0][0];
 #pragma unroll
@@ -276,6 +304,8 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) mx = fmaxf(mx, f[u][e]);
     }
+    if constexpr (TOPK)
+      if (jb < kMaxTopkBatches) s_bkey[jb * NT + tid] = (uint16_t)(Elem<T>::key(mx) >> kKeyShift);
     if (mx > vmax) {
 #pragma unroll
       for (int u = 0; u < U; ++u)
@@ -283,12 +313,12 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
         for (int e = 0; e < VEC; ++e)
           if (f[u][e] > vmax) vmax = f[u][e], imax = (v0 + u * NT) * VEC + e;
     }
-    if constexpr (TOPK) {
+    if constexpr (TOPK && VEC != 8) {
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (v0 + u * NT < nvec)
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) umax[e & 1] = max(umax[e & 1], Elem<T>::key(f[u][e]));
+          for (int e = 0; e < VEC; ++e) umax[e & 3] = max(umax[e & 3], Elem<T>::key(f[u][e]));
     }
     if constexpr (!GREEDY && !TOPK) {
       if (vmax > m) {  // vmax: the largest value this thread has seen
@@ -337,56 +367,119 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
   if constexpr (TOPK) {
     __shared__ uint32_t gmax[SV_MAX_TOP_K];
     __shared__ Cand cand[kMaxCand];
-    __shared__ unsigned n_cand;
+    __shared__ uint32_t s_glist[kMaxGatherList];
+    __shared__ unsigned n_cand, n_glist;
     __shared__ uint32_t tau_sh;
     const int k = p.top_k;
     for (int g = tid; g < k; g += NT) gmax[g] = 0u;
-    if (tid == 0) n_cand = 0u, tau_sh = 0xFFFFFFFFu;
+    if (tid == 0) n_cand = 0u, n_glist = 0u, tau_sh = 0xFFFFFFFFu;
     __syncthreads();
+    if constexpr (VEC == 8) {
+      umax[0] = Elem<T>::key(__uint_as_float(umw[0] << 16));
+      umax[1] = Elem<T>::key(__uint_as_float(umw[0] & 0xFFFF0000u));
+      umax[2] = Elem<T>::key(__uint_as_float(umw[1] << 16));
+      umax[3] = Elem<T>::key(__uint_as_float(umw[1] & 0xFFFF0000u));
+    }
     // k disjoint groups of units; the smallest group maximum bounds the k-th largest
 #pragma unroll
-    for (int u = 0; u < 2; ++u) atomicMax(&gmax[(2 * tid + u) % k], umax[u]);
+    for (int u = 0; u < 4; ++u) atomicMax(&gmax[(4 * tid + u) % k], umax[u]);
     __syncthreads();
     for (int g = tid; g < k; g += NT) atomicMin(&tau_sh, gmax[g]);
     __syncthreads();
     const uint32_t tau = tau_sh;
-    // gather the entries at or above tau
-    for (int v0 = tid; v0 < nvec; v0 += NT * U) {
-      uint4 raws[U];
+    // the batches whose maximum reaches tau (those past the remembered ones always), as
+    // a list; then the whole CTA re-reads the listed vectors with all loads in flight
+    const uint32_t tau16 = tau >> kKeyShift;
+    for (int v0 = tid, jb = 0; v0 < nvec; v0 += NT * U, ++jb) {
+      if (jb < kMaxTopkBatches && (uint32_t)s_bkey[jb * NT + tid] < tau16) continue;
+      const unsigned slot = atomicAdd(&n_glist, 1u);
+      if (slot < kMaxGatherList) s_glist[slot] = (uint32_t)(jb * NT + tid);
+    }
+    __syncthreads();
+    const unsigned nl = n_glist;
+    auto gather_vec = [&](const uint4 &raw, int v) {
+      float f[VEC];
+      Elem<T>::unpack(raw, f);
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (v0 + u * NT < nvec) raws[u] = __ldg(xv + v0 + u * NT);
+      for (int e = 0; e < VEC; ++e) {
+        if (Elem<T>::key(f[e]) >= tau) {
+          const unsigned slot = atomicAdd(&n_cand, 1u);
+          if (slot < kMaxCand) cand[slot] = Cand{f[e], v * VEC + e};
+        }
+      }
+    };
+    if (nl <= (unsigned)kMaxGatherList) {
+      // item i: vector i % U of listed batch i / U
+      const int items = (int)nl * U;
+      constexpr int R = 4;
+      for (int i0 = tid; i0 < items; i0 += NT * R) {
+        uint4 raws[R];
+        int vv[R];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + u * NT;
-        if (v >= nvec) break;
-        float f[VEC];
-        Elem<T>::unpack(raws[u], f);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          if (Elem<T>::key(f[e]) >= tau) {
-            const unsigned slot = atomicAdd(&n_cand, 1u);
-            if (slot < kMaxCand) cand[slot] = Cand{f[e], v * VEC + e};
+        for (int r = 0; r < R; ++r) {
+          const int i = i0 + r * NT;
+          vv[r] = -1;
+          if (i < items) {
+            const uint32_t e = s_glist[i / U];
+            const int v = (int)(e % NT) + (int)(e / NT) * NT * U + (i % U) * NT;
+            if (v < nvec) {
+              vv[r] = v;
+              raws[r] = __ldg(xv + v);
+            }
           }
         }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (vv[r] >= 0) gather_vec(raws[r], vv[r]);
+      }
+    } else {
+      for (int v0 = tid, jb = 0; v0 < nvec; v0 += NT * U, ++jb) {
+        if (jb < kMaxTopkBatches && (uint32_t)s_bkey[jb * NT + tid] < tau16) continue;
+        uint4 raws[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (v0 + u * NT < nvec) raws[u] = __ldg(xv + v0 + u * NT);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (v0 + u * NT < nvec) gather_vec(raws[u], v0 + u * NT);
       }
     }
     __syncthreads();
     const unsigned nc = n_cand;
     if (nc <= kMaxCand) {
-      // rank every candidate: entries beating it (larger value, or equal and lower id)
+      // rank every candidate: entries beating it (larger value, or equal and lower id);
+      // each candidate's comparisons are split over tpc adjacent threads (a power of two,
+      // the same in every thread), whose counts are summed by shuffles
       __shared__ uint32_t thr_key;
       __shared__ int thr_idx;
+      int tpc = 1;
+      while (tpc < 32 && nc * (unsigned)tpc * 2u <= (unsigned)NT) tpc *= 2;
+      const int per_round = NT / tpc, sub = tid & (tpc - 1);
       float part = 0.f;
-      for (unsigned i = tid; i < nc; i += NT) {
-        const Cand ci = cand[i];
+      for (unsigned base = 0; base < nc; base += (unsigned)per_round) {
+        const unsigned i = base + (unsigned)(tid / tpc);
         unsigned rank = 0;
-        for (unsigned j = 0; j < nc; ++j) {
-          const Cand cj = cand[j];
-          rank += (cj.z > ci.z || (cj.z == ci.z && cj.idx < ci.idx)) ? 1u : 0u;
+        Cand ci{0.f, 0};
+        if (i < nc) {
+          ci = cand[i];
+          unsigned j = (unsigned)sub;
+          for (; j + 3u * tpc < nc; j += 4u * tpc) {
+            const Cand c0 = cand[j], c1 = cand[j + tpc], c2 = cand[j + 2 * tpc], c3 = cand[j + 3 * tpc];
+            rank += (c0.z > ci.z || (c0.z == ci.z && c0.idx < ci.idx)) ? 1u : 0u;
+            rank += (c1.z > ci.z || (c1.z == ci.z && c1.idx < ci.idx)) ? 1u : 0u;
+            rank += (c2.z > ci.z || (c2.z == ci.z && c2.idx < ci.idx)) ? 1u : 0u;
+            rank += (c3.z > ci.z || (c3.z == ci.z && c3.idx < ci.idx)) ? 1u : 0u;
+          }
+          for (; j < nc; j += tpc) {
+            const Cand cj = cand[j];
+            rank += (cj.z > ci.z || (cj.z == ci.z && cj.idx < ci.idx)) ? 1u : 0u;
+          }
         }
-        if (rank < (unsigned)k) part += exp2f((ci.z - zmax) * c);
-        if (rank == (unsigned)k - 1u) thr_key = Elem<T>::key(ci.z), thr_idx = ci.idx;
+        for (int o = 1; o < tpc; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+        if (i < nc && sub == 0) {
+          if (rank < (unsigned)k) part += exp2f((ci.z - zmax) * c);
+          if (rank == (unsigned)k - 1u) thr_key = Elem<T>::key(ci.z), thr_idx = ci.idx;
+        }
       }
       __syncthreads();
       st.key_k = thr_key;
@@ -478,7 +571,7 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
 }
 
 template <typename T, bool GREEDY, bool TOPK>
-__global__ void __launch_bounds__(stat_threads<TOPK>(), TOPK ? 2 : 4) accept_stats_kernel(const AcceptParams p) {
+__global__ void __launch_bounds__(stat_threads<TOPK>(), 4) accept_stats_kernel(const AcceptParams p) {
   // the select kernel may be scheduled now; it waits for this grid before reading the
   // statistics (programmatic dependent launch)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -829,6 +922,8 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
       }
     }
     const float c = p.c_log2;
+    // TOPK: the value of the row's k-th entry (a vector below it holds no kept entry)
+    const float thr_p = TOPK && sp.key_k != 0u ? key_to_value<T>(sp.key_k) : -INFINITY;
     const float inv_sp = 1.f / sp.S;
     const float inv_sq = use_q && !q_probs ? 1.f / sq.S : 0.f;
     const int nvec = V / VEC;
@@ -932,16 +1027,34 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
       F2 wsum = f2(0.f);  // lane 0: the segment total
       for (int k0 = 0; s0 + 32 * k0 < s1; k0 += U) {
         Raw r[U];
+        bool live[U];
+        if constexpr (TOPK) {
+          // with top-k, w is zero wherever p is: a vector whose largest logit is below the
+          // row's k-th value has weight 0 (its q is not read)
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int v = s0 + 32 * (k0 + u) + lane;
-          if (v < s1) r[u] = load_raw(v, use_q);
+          for (int u = 0; u < U; ++u) {
+            const int v = s0 + 32 * (k0 + u) + lane;
+            if (v < s1) r[u].p = __ldg(pv + v);
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int v = s0 + 32 * (k0 + u) + lane;
+            live[u] = v < s1 && vec_max<T>(r[u].p) >= thr_p;
+            if (live[u] && use_q) r[u] = load_raw(v, true);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int v = s0 + 32 * (k0 + u) + lane;
+            live[u] = v < s1;
+            if (live[u]) r[u] = load_raw(v, use_q);
+          }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v0 = s0 + 32 * (k0 + u);
           if (v0 >= s1) break;
-          const float cs = warp_sum_f(v0 + lane < s1 ? vec_sum(v0 + lane, r[u], use_q) : 0.f);
+          const float cs = warp_sum_f(live[u] ? vec_sum(v0 + lane, r[u], use_q) : 0.f);
           if (lane == 0) {
             if (keep_chunks) s_chunk[warp * cpw + k0 + u] = cs;
             wsum = f2_add(wsum, cs);

@@ -94,8 +94,22 @@ def test_tree(cuda_ok, parent, mode):
     assert int(ref["num_accepted"].sum()) > 0  # paths do get accepted in this variant
 
 
+@pytest.mark.parametrize("V,B", [(128256, 24), (270336, 4)])
+def test_chain_large_vocab_top_k(cuda_ok, V, B):
+    """Top-k 50 at T = 0.7 on long rows: the statistics remember each batch's maximum for
+    rows up to 262,144 entries and re-read only the batches that can hold a kept entry
+    (the second size has batches past that limit, which are always re-read); the final
+    sample skips vectors below the k-th value."""
+    lg = wl.chain_logits(B, 4, V, sigma=3.0, draft_sigma=1.0, dtype=torch.bfloat16,
+                         temperature=0.7, top_k=50, seed=16)
+    for mode in (sv.EXACT, sv.GREEDY):
+        out, ref = _chain(mode, lg, T=0.7, top_k=50, seed=5, rnd=2)
+        _compare(out, ref, ["tokens", "num_emitted", "num_accepted"])
+    assert sv.sv_read_device_status() == 0
+
+
 def test_top_k_tie_fallback(cuda_ok):
-    """Every logit equal: more than 4096 entries tie at the threshold, so the kernel
+    """Every logit equal: more than 3072 entries tie at the threshold, so the kernel
     takes its counting path; the kept set is the k lowest ids."""
     B, gamma, V, k = 4, 3, 8192, 7
     tl = torch.zeros((B, gamma + 1, V), dtype=torch.bfloat16)
