@@ -26,6 +26,7 @@
 
 #include "sv_common.cuh"
 #include "sv_internal.h"
+#include "tc_primitives.cuh"
 
 namespace sv {
 
@@ -728,7 +729,45 @@ __device__ void commit_prefetch_slice(const CommitParams &cm, int b, const int8_
     asm volatile("prefetch.global.L2 [%0];" ::"l"(vt + src));
   }
 }
-constexpr int kMaxChunks = 4096;          // chunk sums one CTA keeps (32 vectors each)
+constexpr int kMaxChunks = 2048;          // chunk sums one CTA keeps (32 vectors each)
+// Without top-k, the final sample's pass streams each CTA's slice of the p and q rows
+// when its slice is long, through a ring of up to kRingStages shared-memory stages of
+// kRingVec vectors (as many as the slice fills), filled by bulk asynchronous copies (up to
+// 96 KB with q as logits) without holding them in registers.  A stage
+// has 32 chunks; warp w sums chunks w, w + 8, w + 16, w + 24 together, so that their
+// reductions overlap.
+constexpr int kRingVec = 1024;
+constexpr int kRingStages = 3;
+constexpr int kRingMinVec = 2 * kRingVec;  // slices at least this long use the ring
+constexpr int kRingChunks = kRingVec / 32;                    // chunks per stage
+constexpr int kChunksPerWarp = kRingChunks / (kSelThreads / 32);
+static_assert(kChunksPerWarp * (kSelThreads / 32) == kRingChunks, "whole chunks per warp");
+
+// Bytes of one ring stage: kRingVec vectors of p and the matching q (one vector of
+// logits, or VEC/4 vectors of f32 probabilities, per p vector).
+template <typename T>
+__host__ __device__ constexpr uint32_t ring_stage_bytes(bool q_probs) {
+  return (uint32_t)kRingVec * 16u * (1u + (q_probs ? (uint32_t)(Elem<T>::kVec / 4) : 1u));
+}
+
+// One-dimensional bulk copy global -> shared, completing on an mbarrier (both addresses
+// 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Wait for a phase with a fresh time limit of its own (used to let copies in flight land
+// after a wait gave up).  False if the limit passed.
+__device__ __noinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+  const unsigned long long t0 = tc::global_ns();
+  while (!tc::mbar_try_wait(bar, parity))
+    if (tc::global_ns() - t0 > tc::kWaitLimitNs) return false;
+  return true;
+}
 constexpr float kDecideMarginF = 1e-4f;   // float ratio this close to u: decide in double
 
 // The decision of a node whose float ratio fell within kDecideMarginF of u, in double
@@ -746,7 +785,7 @@ __device__ __noinline__ int decide_double(uint32_t k_node, float zp, RowStat sa,
 // Decisions, path, optional commit and final sample of sequence b by the CTA of rank
 // `rank` in a thread-block cluster of C CTAs that split the vocabulary pass and exchange
 // their slice totals through distributed shared memory (C = 1: one CTA, no exchange).
-template <typename T, bool GREEDY, bool TOPK, int NT>
+template <typename T, bool GREEDY, bool TOPK, bool RING, int NT>
 __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned C) {
   constexpr int VEC = Elem<T>::kVec;
   constexpr int NW = NT / 32;
@@ -760,10 +799,19 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
   __shared__ int s_wstar, s_tok, s_snear, s_rstar;
   __shared__ F2 s_base, s_t;
   __shared__ int8_t s_path[kMaxNodes];
+  // the ring of the final sample's pass (no top-k): stages in dynamic shared memory
+  extern __shared__ __align__(128) uint8_t sel_ring[];
+  __shared__ uint64_t ring_full[kRingStages];
+  __shared__ int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int N = p.tree.N, V = p.V;
   __syncthreads();  // the shared state may still be read for the previous sequence
+  if (RING && tid == 0) {
+    for (int i = 0; i < kRingStages; ++i) tc::mbar_init(&ring_full[i], 1);
+    tc::fence_barrier_init();
+    s_abort = 0;
+  }
   if (tid < kMaxNodes) {
     s_par[tid] = p.tree.parent[tid];
     s_dep[tid] = p.tree.depth[tid];
@@ -927,16 +975,23 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
     const float inv_sp = 1.f / sp.S;
     const float inv_sq = use_q && !q_probs ? 1.f / sq.S : 0.f;
     const int nvec = V / VEC;
-    // this CTA's slice of the vectors, each warp's segment of the slice, and the
-    // segment's chunks of 32 vectors (chunk k of warp w at s_chunk[w * cpw + k]).  Slices
-    // and segments start at multiples of 32 vectors, so that every chunk is the same 32
-    // vectors (and its float sum the same) however many CTAs share the pass.
+    // this CTA's slice of the vectors and its chunks of 32 vectors (chunk k = vectors
+    // [c0 + 32k, c0 + 32k + 32), its sum at s_chunk[k]).  Slices start at multiples of 32
+    // vectors, so that every chunk is the same 32 vectors (and its float sum the same)
+    // however many CTAs share the pass.  With top-k each warp takes a contiguous segment
+    // of the slice (whole chunks); without, the slice streams through the ring and warp w
+    // takes chunk w of every stage.
     const int per_cta = ((nvec + (int)C - 1) / (int)C + 31) / 32 * 32;
     const int c0 = min(nvec, (int)rank * per_cta), c1 = min(nvec, c0 + per_cta);
     const int seg = ((c1 - c0 + NW - 1) / NW + 31) / 32 * 32;
     const int s0 = min(c1, c0 + warp * seg), s1 = min(c1, s0 + seg);
-    const int cpw = (seg + 31) / 32;
-    const bool keep_chunks = cpw * NW <= kMaxChunks;  // same in every CTA and warp
+    const int nchs = (c1 - c0 + 31) / 32;         // chunks of the slice
+    const bool keep_chunks = nchs <= kMaxChunks;  // (only the owning CTA reads them)
+    const uint32_t stage_bytes = ring_stage_bytes<T>(q_probs);
+    const uint32_t nrs = RING ? (uint32_t)p.ring_stages : 1u;  // stages of the ring
+    uint32_t ring_seq = 0;   // ring stages consumed so far (all attempts)
+    uint32_t last_seq0 = 0;  // ring_seq at the start of the last attempt's pass
+    int ring_last = 0;       // stages of the last attempt's pass
 
     struct Raw {
       uint4 p, q[QV > 0 ? QV : 1];
@@ -1021,11 +1076,98 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
     verify_uniform_ints(p.seed, p.round, b, best, &k_acc, &k_smp);
 
     for (int attempt = 0; attempt < 2; ++attempt) {
-      // phase 1: chunk k of the warp's segment = its vectors [s0 + 32k, s0 + 32k + 32),
-      // lane i taking vector s0 + 32k + i; four chunks are loaded before any is used
-      constexpr int U = 4;
-      F2 wsum = f2(0.f);  // lane 0: the segment total
-      for (int k0 = 0; s0 + 32 * k0 < s1; k0 += U) {
+      F2 wsum = f2(0.f);  // lane 0: the sum of this warp's chunks
+      if constexpr (RING) {
+        // phase 1 through the ring: stage i holds vectors [c0 + i kRingVec, ...) of p and
+        // the matching q; thread 0 keeps nrs stages in flight
+        const int nstage = (c1 - c0 + kRingVec - 1) / kRingVec;
+        const uint32_t qmul = use_q ? (q_probs ? (uint32_t)QV : 1u) : 0u;
+        last_seq0 = ring_seq;
+        int issued = 0;
+        auto issue = [&](int i) {
+          const int sl = (int)((ring_seq + (uint32_t)i) % nrs);
+          const int v0 = c0 + i * kRingVec, nv = min(kRingVec, c1 - v0);
+          const uint32_t pb = (uint32_t)nv * 16u, qb = pb * qmul;
+          uint8_t *dst = sel_ring + (size_t)sl * stage_bytes;
+          tc::fence_proxy_async_smem();
+          tc::mbar_expect_tx(&ring_full[sl], pb + qb);
+          bulk_g2s(dst, pv + v0, pb, &ring_full[sl]);
+          if (qb) bulk_g2s(dst + kRingVec * 16, qv + (size_t)v0 * (q_probs ? QV : 1), qb, &ring_full[sl]);
+          issued = i + 1;
+        };
+        if (tid == 0)
+          for (int i = 0; i < min(nstage, (int)nrs); ++i) issue(i);
+        int waited_ok = 0;    // thread 0: stages whose copies are known to have landed
+        F2 lacc = f2(0.f);    // lane k < kChunksPerWarp: this warp's chunks k (float pairs)
+        for (int i = 0; i < nstage; ++i) {
+          const uint32_t gi = ring_seq + (uint32_t)i;
+          const int sl = (int)(gi % nrs);
+          const bool ok = tc::mbar_wait(&ring_full[sl], (gi / nrs) & 1u, &s_abort);
+          if (tid == 0 && ok && waited_ok == i) waited_ok = i + 1;
+          const uint8_t *st = sel_ring + (size_t)sl * stage_bytes;
+          const uint4 *sp4 = reinterpret_cast<const uint4 *>(st);
+          const uint4 *sq4 = reinterpret_cast<const uint4 *>(st + kRingVec * 16);
+          const int vs0 = c0 + i * kRingVec;  // first vector of the stage
+          // chunk j = warp + 8k of the stage: vectors vs0 + 32 j + lane
+          float cs[kChunksPerWarp];
+#pragma unroll
+          for (int k = 0; k < kChunksPerWarp; ++k) {
+            const int e = 32 * (warp + (kSelThreads / 32) * k) + lane;  // vector of the stage
+            const int v = vs0 + e;
+            cs[k] = 0.f;
+            if (v < c1) {
+              Raw r;
+              r.p = sp4[e];
+              if (use_q) {
+                if (q_probs) {
+#pragma unroll
+                  for (int h = 0; h < QV; ++h) r.q[h] = sq4[e * QV + h];
+                } else {
+                  r.q[0] = sq4[e];
+                }
+              }
+              cs[k] = vec_sum(v, r, use_q);
+            }
+          }
+          // the chunk sums, reduced together (every lane gets all of them)
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int k = 0; k < kChunksPerWarp; ++k) cs[k] += __shfl_xor_sync(0xFFFFFFFFu, cs[k], o);
+#pragma unroll
+          for (int k = 0; k < kChunksPerWarp; ++k) {
+            const int j = warp + (kSelThreads / 32) * k;  // chunk of the stage
+            if (lane == k && vs0 + 32 * j < c1) {
+              if (keep_chunks) s_chunk[i * kRingChunks + j] = cs[k];
+              lacc = f2_add(lacc, cs[k]);
+            }
+          }
+          __syncthreads();  // every warp is done with this stage
+          if (tid == 0 && i + (int)nrs < nstage && !s_abort) issue(i + (int)nrs);
+        }
+        // the warp's total: a butterfly of float-pair adds over lanes 0..kChunksPerWarp-1
+#pragma unroll 1
+        for (int o = 1; o < kChunksPerWarp; o <<= 1) lacc = f2_add(lacc, shfl_xor_f2(lacc, o));
+        if (lane == 0) wsum = lacc;
+        ring_last = nstage;
+        if (s_abort) {
+          // a wait gave up: let this CTA's copies in flight land before leaving
+          if (tid == 0) {
+            set_status(p.status, SV_DEV_TIMEOUT);
+            for (int i = waited_ok; i < issued; ++i) {
+              const uint32_t gi = ring_seq + (uint32_t)i;
+              mbar_wait_drain(&ring_full[gi % nrs], (gi / nrs) & 1u);
+            }
+          }
+          __syncthreads();
+        }
+        ring_seq += (uint32_t)nstage;
+      } else
+      // phase 1 from registers: chunk k of the warp's segment = its vectors [s0 + 32k, s0 +
+      // 32k + 32), lane i taking vector s0 + 32k + i; four chunks are loaded before any is
+      // used
+      for (int k0 = 0; s0 + 32 * k0 < s1; k0 += 4) {
+        constexpr int U = 4;
         Raw r[U];
         bool live[U];
         if constexpr (TOPK) {
@@ -1056,7 +1198,7 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
           if (v0 >= s1) break;
           const float cs = warp_sum_f(live[u] ? vec_sum(v0 + lane, r[u], use_q) : 0.f);
           if (lane == 0) {
-            if (keep_chunks) s_chunk[warp * cpw + k0 + u] = cs;
+            if (keep_chunks) s_chunk[(s0 - c0) / 32 + k0 + u] = cs;
             wsum = f2_add(wsum, cs);
           }
         }
@@ -1088,12 +1230,8 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
           t = f2_uniform_times(k_smp, total);
           rs = warp_find_cdf(tr, (int)C, f2(0.f), t, &base_r);
         }
-        if ((int)rank == rs) {
-          // the warp segment within this slice
-          F2 base_w;
-          const int ws = warp_find_cdf(lane < NW ? seg_sum[lane] : f2(0.f), NW, base_r, t, &base_w);
-          if (lane == 0) s_wstar = ws, s_base = base_w, s_t = t;
-        }
+        // in the CTA whose slice holds t, warp 0 finds the chunk and the token
+        if ((int)rank == rs && lane == 0) s_wstar = 0, s_base = base_r, s_t = t;
         if (lane == 0) s_rstar = rs;
       }
       __syncthreads();
@@ -1107,21 +1245,55 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
     const int rstar = s_rstar;
     writer = (int)rank == (rstar < 0 ? 0 : rstar);
 
-    // phase 2: the owning warp finds the chunk from the chunk sums, then the token in it
+    // phase 2: the owning warp finds the chunk from the chunk sums, then the token in it.
+    // A vector is re-read from the ring when its stage is still there (the last
+    // nrs stages of the last pass), else from global memory.
+    auto load_final = [&](int v) -> Raw {
+      if constexpr (RING) {
+        const int i = (v - c0) / kRingVec;
+        if (i < ring_last && ring_last - i <= (int)nrs) {
+          const uint8_t *st = sel_ring + (size_t)((last_seq0 + (uint32_t)i) % nrs) * stage_bytes;
+          const int e = v - c0 - i * kRingVec;
+          Raw r;
+          r.p = reinterpret_cast<const uint4 *>(st)[e];
+          if (use_q) {
+            const uint4 *sq4 = reinterpret_cast<const uint4 *>(st + kRingVec * 16);
+            if (q_probs) {
+#pragma unroll
+              for (int h = 0; h < QV; ++h) r.q[h] = sq4[e * QV + h];
+            } else {
+              r.q[0] = sq4[e];
+            }
+          }
+          return r;
+        }
+      }
+      return load_raw(v, use_q);
+    };
     if ((int)rank == rstar && warp == s_wstar) {
       __syncwarp();
       const F2 t = s_t;
       F2 base = s_base;
       int found = 0, tok = -1, near = 0, last_pos = -1;
-      const int nch = (s1 - s0 + 31) / 32;
+      const int nch = nchs;
       int k_first = 0;
       if (keep_chunks) {
-        // first chunk whose end passes t (else the last one with mass); the prefix over
-        // chunks is a float-pair sum, only the chunk sums themselves are float
-        int kstar = -1, klast = -1;
-        F2 base_k = base, base_last = base;
-        for (int k0 = 0; k0 < nch && kstar < 0; k0 += 32) {
-          const F2 x = f2(k0 + lane < nch ? s_chunk[warp * cpw + k0 + lane] : 0.f);
+        // first chunk whose end passes t (else the last one with mass), in two levels:
+        // groups of 32 chunks (lane g sums group g, float pairs), then the chunks of the
+        // group found; the prefixes are float-pair sums, only chunk sums are float
+        const int ngr = (nch + 31) / 32;
+        int gstar = ngr == 1 ? 0 : -1, glast = -1;  // one group: no group level
+        F2 base_g = base, base_glast = base;
+        for (int g0 = 0; g0 < ngr && gstar < 0; g0 += 32) {
+          const int g = g0 + lane;
+          F2 x = f2(0.f);
+          if (g < ngr) {
+            // lane g starts at chunk (g mod 32) of its group: no two lanes read one bank
+            for (int i = 0; i < 32; ++i) {
+              const int k = 32 * g + ((i + lane) & 31);
+              if (k < nch) x = f2_add(x, s_chunk[k]);
+            }
+          }
           F2 incl = x;
 #pragma unroll 1
           for (int o = 1; o < 32; o <<= 1) {
@@ -1129,31 +1301,52 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
             if (lane >= o) incl = f2_add(incl, y);
           }
           const F2 before = f2_add(base, f2_sub(incl, x));
-          const unsigned hit = __ballot_sync(0xFFFFFFFFu, k0 + lane < nch && f2_gt(f2_add(before, x), t));
-          const unsigned pos = __ballot_sync(0xFFFFFFFFu, k0 + lane < nch && x.hi > 0.f);
+          const unsigned hit = __ballot_sync(0xFFFFFFFFu, g < ngr && f2_gt(f2_add(before, x), t));
+          const unsigned pos = __ballot_sync(0xFFFFFFFFu, g < ngr && x.hi > 0.f);
           if (pos) {
             const int L = 31 - __clz(pos);
-            klast = k0 + L;
-            base_last = shfl_f2(before, L);
+            glast = g0 + L;
+            base_glast = shfl_f2(before, L);
           }
           if (hit) {
             const int L = __ffs(hit) - 1;
-            kstar = k0 + L;
-            base_k = shfl_f2(before, L);
+            gstar = g0 + L;
+            base_g = shfl_f2(before, L);
           }
           base = f2_add(base, shfl_f2(incl, 31));
         }
-        if (kstar < 0) kstar = klast, base_k = base_last;
+        if (gstar < 0) gstar = glast, base_g = base_glast;
+        int kstar = -1;
+        F2 base_k = s_base;
+        if (gstar >= 0) {
+          // the chunks of group gstar
+          const int k = 32 * gstar + lane;
+          const F2 x = f2(k < nch ? s_chunk[k] : 0.f);
+          F2 incl = x;
+#pragma unroll 1
+          for (int o = 1; o < 32; o <<= 1) {
+            const F2 y = shfl_up_f2(incl, o);
+            if (lane >= o) incl = f2_add(incl, y);
+          }
+          const F2 before = f2_add(base_g, f2_sub(incl, x));
+          const unsigned hit = __ballot_sync(0xFFFFFFFFu, k < nch && f2_gt(f2_add(before, x), t));
+          const unsigned pos = __ballot_sync(0xFFFFFFFFu, k < nch && x.hi > 0.f);
+          const int L = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+          if (L >= 0) {
+            kstar = 32 * gstar + L;
+            base_k = shfl_f2(before, L);
+          }
+        }
         if (kstar < 0) kstar = 0, base_k = s_base;
         k_first = kstar;
         base = base_k;
       }
       for (int k = k_first; k < nch && !found; ++k) {
-        const int v = s0 + 32 * k + lane;
+        const int v = c0 + 32 * k + lane;
         float w[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) w[e] = 0.f;
-        if (v < s1) weights(v, load_raw(v, use_q), w, use_q);
+        if (v < c1) weights(v, load_final(v), w, use_q);
         float lsum = 0.f;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
@@ -1233,41 +1426,63 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
   }
 }
 
-template <typename T, bool GREEDY, bool TOPK>
+template <typename T, bool GREEDY, bool TOPK, bool RING>
 __global__ void __launch_bounds__(kSelThreads) accept_select_kernel(const AcceptParams p) {
   const unsigned C = cluster_size(), rank = cluster_rank();
   // (select_seq waits for the statistics kernel once it has read its other inputs)
-  select_seq<T, GREEDY, TOPK, kSelThreads>(p, blockIdx.x / (int)C, rank, C);
+  select_seq<T, GREEDY, TOPK, RING, kSelThreads>(p, blockIdx.x / (int)C, rank, C);
 }
 
 
-// CTAs per sequence for the final sample: as many as keep the select grid within two CTAs
-// per SM (the pass over two rows per sequence is split among them), at most 16.
-int select_cluster(int B, int num_sms) {
+// CTAs per sequence for the final sample: the most (a power of two, at most 16) that keep
+// the select grid within one CTA per SM, so that its CTAs can start as the statistics
+// kernel's last CTAs leave (the pass over two rows per sequence is split among them).
+// With top-k, two per SM: its pass reads only the p row, at a few loads per vector.
+int select_cluster(int B, int num_sms, bool topk) {
+  const long long slots = (long long)num_sms * (topk ? 2 : 1);
   int C = 1;
-  while (C < kMaxCluster && (long long)B * C * 2 <= 2ll * num_sms) C *= 2;
+  while (C < kMaxCluster && (long long)B * C * 2 <= slots) C *= 2;
   return C;
 }
 
-template <typename T, bool GREEDY, bool TOPK>
-cudaError_t launch_select(const AcceptParams &p, int num_sms, cudaStream_t s) {
-  auto kern = accept_select_kernel<T, GREEDY, TOPK>;
-  int C = GREEDY ? 1 : select_cluster(p.B, num_sms);
+// Launch of one select kernel instantiation: C CTAs per sequence (clusters above 8 CTAs
+// need the non-portable size, else C = 8), dyn bytes of dynamic shared memory.
+template <typename T, bool GREEDY, bool TOPK, bool RING>
+cudaError_t launch_select_kernel(AcceptParams pl, int C, cudaStream_t s) {
+  auto kern = accept_select_kernel<T, GREEDY, TOPK, RING>;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const bool dev_ok = dev >= 0 && dev < 64;
   if (C > 8) {
     static bool big_ok[64] = {false}, tried[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !tried[dev]) {
+    if (dev_ok && !tried[dev]) {
       tried[dev] = true;
       big_ok[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
                     cudaSuccess;
       cudaGetLastError();
     }
-    if (dev < 0 || dev >= 64 || !big_ok[dev]) C = 8;
+    if (!dev_ok || !big_ok[dev]) C = 8;
+  }
+  size_t dyn = 0;
+  if constexpr (RING) {
+    // as many stages as one CTA's slice fills, at most kRingStages
+    const int nvec = pl.V / Elem<T>::kVec;
+    const int per_cta = ((nvec + C - 1) / C + 31) / 32 * 32;
+    pl.ring_stages = std::max(1, std::min(kRingStages, (per_cta + kRingVec - 1) / kRingVec));
+    dyn = (size_t)pl.ring_stages * ring_stage_bytes<T>(pl.q_kind == SV_Q_PROBS_F32);
+    static bool attr_ok[64] = {false};
+    if (!dev_ok || !attr_ok[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          (int)((size_t)kRingStages * ring_stage_bytes<T>(true)));
+      if (e != cudaSuccess) return e;
+      if (dev_ok) attr_ok[dev] = true;
+    }
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.B * C));
+  cfg.gridDim = dim3((unsigned)(pl.B * C));
   cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = dyn;
   cfg.stream = s;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1279,7 +1494,24 @@ cudaError_t launch_select(const AcceptParams &p, int num_sms, cudaStream_t s) {
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return cudaLaunchKernelEx(&cfg, kern, pl);
+}
+
+// Select kernel of a call: the ring variant (final sample streamed through shared
+// memory) when each CTA's slice of the vocabulary is long, else the register variant
+// (short slices are latency-bound; it keeps the dynamic shared memory at zero, so that its
+// CTAs can start beside the statistics kernel's last CTAs).
+template <typename T, bool GREEDY, bool TOPK>
+cudaError_t launch_select(const AcceptParams &p, int num_sms, cudaStream_t s) {
+  const int C = GREEDY ? 1 : select_cluster(p.B, num_sms, TOPK);
+  AcceptParams pl = p;
+  pl.ring_stages = 0;
+  if constexpr (!GREEDY && !TOPK) {
+    const int nvec = p.V / Elem<T>::kVec;
+    const int per_cta = ((nvec + C - 1) / C + 31) / 32 * 32;
+    if (per_cta >= kRingMinVec) return launch_select_kernel<T, GREEDY, TOPK, true>(pl, C, s);
+  }
+  return launch_select_kernel<T, GREEDY, TOPK, false>(pl, C, s);
 }
 
 template <typename T>

@@ -118,6 +118,7 @@ struct AcceptParams {
   float temperature;
   float c_log2;              // log2(e) / T
   int top_k;                 // 0 = off
+  int ring_stages;           // stages of the select kernel's ring (set at its launch)
   uint64_t seed, round;
   RowStat *stats;            // [B*N + B*Dq]
   int32_t *out_path_nodes;   // [B,Dmax+1] or NULL
