@@ -429,41 +429,62 @@ def run_e2e(args, dist, w, step, prepare, stream, toks, cand):
 
 # ------------------------------------------------------------ CPU oracle
 
+def _seq_on_host(w, b):
+    """Sequence b's inputs on the host, with a cache of its own rows only: a contiguous
+    cache row, or its blocks of a paged pool (in order, with a block table 0, 1, ...) with
+    room for the commit."""
+    sel = slice(b, b + 1)
+    d = {k: w[k][sel].cpu() for k in ("q", "k_tree", "v_tree", "target_logits", "draft_logits",
+                                      "prefix_len")}
+    d["toks"] = (w["draft_tokens"] if "draft_tokens" in w and w["cfg"]["kind"] == "chain"
+                 else w["node_tokens"])[sel].cpu()
+    if w["block_table"] is None:
+        d["cache_k"], d["cache_v"], d["bt"] = w["cache_k"][sel].cpu(), w["cache_v"][sel].cpu(), None
+    else:
+        bs = w.get("block_size", 16)
+        nblk = min(w["block_table"].shape[1], (int(w["prefix_len"][b]) + w["N"] + bs - 1) // bs)
+        ids = w["block_table"][b, :nblk].long()
+        d["cache_k"], d["cache_v"] = w["cache_k"][ids].cpu(), w["cache_v"][ids].cpu()
+        d["bt"] = torch.arange(nblk, dtype=torch.int32).unsqueeze(0)
+    return d
+
+
 def oracle_sample(w, budget_s: float, mode: int, b_limit=None):
     """Time the oracle on whole sequences (attention of every node and head, acceptance,
     commit) until the budget is spent, cycling over the workload's sequences (at most 64
-    passes) when they take less; returns (candidates, seconds, sequence evaluations)."""
+    passes) when they take less; returns (candidates, seconds, sequence evaluations).
+    Only the evaluated sequence's inputs are brought to the host, outside the timing."""
     import oracle
     c = w["cfg"]
     chain = c["kind"] == "chain"
     limit = 64 * c["B"] if b_limit is None else min(b_limit, c["B"])
-    cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in w.items()}
     done, spent = 0, 0.0
+    seqs = {}
     while done < limit and (done == 0 or spent < budget_s):
         b = done % c["B"]
-        sel = slice(b, b + 1)
-        if cpu["block_table"] is None:
-            ck, cv, bt = cpu["cache_k"][sel], cpu["cache_v"][sel], None
-        else:
-            ck, cv, bt = cpu["cache_k"], cpu["cache_v"], cpu["block_table"][sel]
+        if b not in seqs:
+            if len(seqs) >= 16:
+                seqs.pop(next(iter(seqs)))
+            seqs[b] = _seq_on_host(w, b)
+        d = seqs[b]
         t0 = time.perf_counter()
-        oracle.tree_attention(cpu["q"][sel], cpu["k_tree"][sel], cpu["v_tree"][sel], ck, cv,
-                              cpu["prefix_len"][sel], cpu["parent"], cpu["scale"], block_table=bt,
+        oracle.tree_attention(d["q"], d["k_tree"], d["v_tree"], d["cache_k"], d["cache_v"],
+                              d["prefix_len"], w["parent"], w["scale"], block_table=d["bt"],
                               block_size=w.get("block_size", 16))
         if chain:
-            r = oracle.accept_chain(mode, cpu["target_logits"][sel], cpu["draft_logits"][sel],
-                                    oracle.Q_LOGITS, cpu["draft_tokens"][sel],
-                                    temperature=c["temperature"], top_k=c["top_k"],
+            r = oracle.accept_chain(mode, d["target_logits"], d["draft_logits"], oracle.Q_LOGITS,
+                                    d["toks"], temperature=c["temperature"], top_k=c["top_k"],
                                     seed=w["seed"])
-            W = cpu["draft_tokens"].shape[1] + 1
+            W = d["toks"].shape[1] + 1
             path = torch.arange(W, dtype=torch.int32).unsqueeze(0)
         else:
-            r = oracle.accept_tree(mode, cpu["target_logits"][sel], cpu["draft_logits"][sel],
-                                   oracle.Q_LOGITS, cpu["parent"], cpu["node_tokens"][sel],
-                                   temperature=c["temperature"], top_k=c["top_k"], seed=w["seed"])
+            r = oracle.accept_tree(mode, d["target_logits"], d["draft_logits"], oracle.Q_LOGITS,
+                                   w["parent"], d["toks"], temperature=c["temperature"],
+                                   top_k=c["top_k"], seed=w["seed"])
             path = r["path_nodes"]
-        oracle.commit_kv(cpu["k_tree"][sel], cpu["v_tree"][sel], path, r["num_accepted"], ck, cv,
-                         cpu["prefix_len"][sel], block_table=bt, block_size=w.get("block_size", 16))
+        oracle.commit_kv(d["k_tree"], d["v_tree"], path, r["num_accepted"], d["cache_k"],
+                         d["cache_v"], d["prefix_len"], block_table=d["bt"],
+                         block_size=w.get("block_size", 16))
         spent += time.perf_counter() - t0
         done += 1
     return done * (w["N"] - 1), spent, done

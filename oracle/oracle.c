@@ -42,6 +42,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
@@ -55,6 +56,16 @@
 #define ORC_Q_PROBS_F32 0
 #define ORC_Q_LOGITS 1
 #define ORC_NEAR_TIE 1e-6
+
+/* Host memory for scratch; a failed allocation stops the process with a message. */
+static void *orc_alloc(size_t n) {
+  void *p = malloc(n > 0 ? n : 1);
+  if (!p) {
+    fprintf(stderr, "oracle: out of host memory (%zu bytes)\n", n);
+    abort();
+  }
+  return p;
+}
 
 /* ------------------------------------------------------------------ threads */
 
@@ -192,7 +203,7 @@ void orc_tree_attention(int dtype, int B, int N, int Hq, int Hkv, int D, const v
     int g = h / G;
     int L = prefix_len[b];
     int nk = L + N;
-    double *s = (double *)malloc(sizeof(double) * (size_t)nk);
+    double *s = (double *)orc_alloc(sizeof(double) * (size_t)nk);
     size_t qoff = (((size_t)b * N + n) * Hq + h) * D;
     double smax = -INFINITY;
     for (int j = 0; j < nk; ++j) {
@@ -264,14 +275,14 @@ static int orc_argmax(const double *z, int V) {
 /* Effective sampling distribution of one logit row: y = z / T, keep the top_k
  * largest y (if 0 < top_k < V; ties keep lower ids), p = softmax over the kept set. */
 static void orc_effective_dist(const double *z, int V, double T, int top_k, double *p) {
-  double *y = (double *)malloc(sizeof(double) * (size_t)V);
-  unsigned char *keep = (unsigned char *)malloc((size_t)V);
+  double *y = (double *)orc_alloc(sizeof(double) * (size_t)V);
+  unsigned char *keep = (unsigned char *)orc_alloc((size_t)V);
   for (int j = 0; j < V; ++j) {
     y[j] = z[j] / T;
     keep[j] = 1;
   }
   if (top_k > 0 && top_k < V) {
-    orc_ranked *r = (orc_ranked *)malloc(sizeof(orc_ranked) * (size_t)V);
+    orc_ranked *r = (orc_ranked *)orc_alloc(sizeof(orc_ranked) * (size_t)V);
     for (int j = 0; j < V; ++j) {
       r[j].value = y[j];
       r[j].index = j;
@@ -323,7 +334,7 @@ static int orc_inverse_cdf(const double *w, int V, double u, int *near) {
 /* Sample from norm([p - q]+), or from p if q is NULL; falls back to p (and reports
  * a near tie) when the residual has no mass. */
 static int orc_sample_residual(const double *p, const double *q, int V, double u, int *near) {
-  double *w = (double *)malloc(sizeof(double) * (size_t)V);
+  double *w = (double *)orc_alloc(sizeof(double) * (size_t)V);
   double total = 0.0;
   for (int j = 0; j < V; ++j) {
     w[j] = q ? (p[j] - q[j] > 0.0 ? p[j] - q[j] : 0.0) : p[j];
@@ -366,7 +377,7 @@ int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *par
                     double *out_ratio, uint32_t *out_flags) {
   if (orc_check_tree(N, parent)) return 1;
   int Dmax = 0;
-  int *depth = (int *)malloc(sizeof(int) * (size_t)N);
+  int *depth = (int *)orc_alloc(sizeof(int) * (size_t)N);
   for (int n = 0; n < N; ++n) {
     depth[n] = orc_depth(parent, n);
     if (depth[n] > Dmax) Dmax = depth[n];
@@ -379,12 +390,12 @@ int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *par
   int W = Dmax + 1;
 #pragma omp parallel for schedule(dynamic)
   for (int b = 0; b < B; ++b) {
-    double *z = (double *)malloc(sizeof(double) * (size_t)V);
-    double *pa = (double *)malloc(sizeof(double) * (size_t)V);
-    double *qd = (double *)malloc(sizeof(double) * (size_t)V);
+    double *z = (double *)orc_alloc(sizeof(double) * (size_t)V);
+    double *pa = (double *)orc_alloc(sizeof(double) * (size_t)V);
+    double *qd = (double *)orc_alloc(sizeof(double) * (size_t)V);
     unsigned char *acc = (unsigned char *)calloc((size_t)N, 1);
     unsigned char *ok = (unsigned char *)calloc((size_t)N, 1);
-    double *ratio = (double *)malloc(sizeof(double) * (size_t)N);
+    double *ratio = (double *)orc_alloc(sizeof(double) * (size_t)N);
     unsigned char *dec_near = (unsigned char *)calloc((size_t)N, 1);
     uint32_t flags = 0;
     for (int c = 0; c < N; ++c) ratio[c] = NAN;
@@ -504,9 +515,9 @@ int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *t
   int W = gamma + 1;
 #pragma omp parallel for schedule(dynamic)
   for (int b = 0; b < B; ++b) {
-    double *z = (double *)malloc(sizeof(double) * (size_t)V);
-    double *p = (double *)malloc(sizeof(double) * (size_t)V);
-    double *qi = (double *)malloc(sizeof(double) * (size_t)V);
+    double *z = (double *)orc_alloc(sizeof(double) * (size_t)V);
+    double *p = (double *)orc_alloc(sizeof(double) * (size_t)V);
+    double *qi = (double *)orc_alloc(sizeof(double) * (size_t)V);
     int32_t *tk = out_tokens + (size_t)b * W;
     uint32_t near = 0, flags = 0;
     for (int i = 0; i < W; ++i) tk[i] = -1;

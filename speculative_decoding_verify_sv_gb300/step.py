@@ -18,6 +18,10 @@ from . import (EXACT, GREEDY, Q_LOGITS, KVCache, sv_accept_chain, sv_accept_chai
                sv_tree_attention, sv_tree_attention_workspace_size)
 
 
+# inputs of the attention call (the rest feed the acceptance)
+_ATTN_INPUTS = ("q", "k_tree", "v_tree")
+
+
 def _depths(parent):
     d = []
     for p in parent:
@@ -116,6 +120,7 @@ class VerifyStep:
     def alloc_inputs(self, like: dict):
         """Device input buffers shaped like the host tensors in ``like``."""
         self.dev_in = {k: torch.empty_like(v, device=self.device) for k, v in like.items()}
+        self._copy_stream = None
         W = self.Dmax + 1
         pin = dict(dtype=torch.int32, pin_memory=True)
         self.host_out = dict(tokens=torch.empty((self.B, W), **pin),
@@ -126,14 +131,34 @@ class VerifyStep:
 
     def run_host(self, host_in: dict, seed=0, round_=0, stream=None):
         """H2D copies of the step inputs (pinned host tensors), the step, and the D2H
-        copy of the emitted tokens and counts; returns the pinned host outputs."""
+        copy of the emitted tokens and counts; returns the pinned host outputs.
+
+        The attention's inputs are copied on the step's stream and the acceptance's (the
+        logits, the node tokens) on a second stream at the same time, so that the logits'
+        copy overlaps the attention; the acceptance waits for it.  The second stream first
+        waits for everything already queued on the step's stream, which may still read
+        these device buffers."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
         d = self.dev_in
-        for k, v in host_in.items():
-            d[k].copy_(v, non_blocking=True)
-        self.run(d["q"], d["k_tree"], d["v_tree"], d["target_logits"], d["draft_logits"],
-                 d["node_tokens"], seed, round_, stream)
-        for k, v in self.host_out.items():
-            v.copy_(self.outs[k], non_blocking=True)
+        if self._copy_stream is None:
+            self._copy_stream = torch.cuda.Stream(self.device)
+            self._copied = torch.cuda.Event()
+        cs = self._copy_stream
+        cs.wait_stream(s)
+        with torch.cuda.stream(cs):
+            for k, v in host_in.items():
+                if k not in _ATTN_INPUTS:
+                    d[k].copy_(v, non_blocking=True)
+            self._copied.record(cs)
+        with torch.cuda.stream(s):
+            for k in _ATTN_INPUTS:
+                d[k].copy_(host_in[k], non_blocking=True)
+            self.attention(d["q"], d["k_tree"], d["v_tree"], s)
+            s.wait_event(self._copied)
+            self.accept_commit(d["target_logits"], d["draft_logits"], d["node_tokens"],
+                               d["k_tree"], d["v_tree"], seed, round_, s)
+            for k, v in self.host_out.items():
+                v.copy_(self.outs[k], non_blocking=True)
         return self.host_out
 
     def h2d_bytes(self, host_in: dict) -> int:
