@@ -56,10 +56,15 @@ class VerifyStep:
                                   device=self.device)
         self.out = torch.empty((B, self.N, Hq, D), dtype=dtype, device=self.device)
         W = self.Dmax + 1
-        i32 = dict(dtype=torch.int32, device=self.device)
-        self.outs = dict(tokens=torch.empty((B, W), **i32), num_emitted=torch.empty(B, **i32),
-                         num_accepted=torch.empty(B, **i32), near_ties=torch.empty(B, **i32),
-                         path_nodes=torch.empty((B, W), **i32))
+        # the outputs are views of one int32 buffer, tokens and counts first, so that the
+        # end-to-end step reads them back with a single copy
+        self._out_buf = torch.empty(2 * B * W + 3 * B, dtype=torch.int32, device=self.device)
+        self._out_head = B * W + 3 * B  # tokens, num_emitted, num_accepted, near_ties
+        o = self._out_buf
+        self.outs = dict(tokens=o[:B * W].view(B, W), num_emitted=o[B * W:B * W + B],
+                         num_accepted=o[B * W + B:B * W + 2 * B],
+                         near_ties=o[B * W + 2 * B:B * W + 3 * B],
+                         path_nodes=o[B * W + 3 * B:].view(B, W))
         if chain:
             pn = torch.arange(W, dtype=torch.int32, device=self.device)
             self.chain_path = pn.unsqueeze(0).expand(B, W).contiguous()
@@ -121,12 +126,12 @@ class VerifyStep:
         """Device input buffers shaped like the host tensors in ``like``."""
         self.dev_in = {k: torch.empty_like(v, device=self.device) for k, v in like.items()}
         self._copy_stream = None
-        W = self.Dmax + 1
-        pin = dict(dtype=torch.int32, pin_memory=True)
-        self.host_out = dict(tokens=torch.empty((self.B, W), **pin),
-                             num_emitted=torch.empty(self.B, **pin),
-                             num_accepted=torch.empty(self.B, **pin),
-                             near_ties=torch.empty(self.B, **pin))
+        B, W = self.B, self.Dmax + 1
+        self._host_buf = torch.empty(self._out_head, dtype=torch.int32, pin_memory=True)
+        h = self._host_buf
+        self.host_out = dict(tokens=h[:B * W].view(B, W), num_emitted=h[B * W:B * W + B],
+                             num_accepted=h[B * W + B:B * W + 2 * B],
+                             near_ties=h[B * W + 2 * B:B * W + 3 * B])
         return self.dev_in
 
     def run_host(self, host_in: dict, seed=0, round_=0, stream=None):
@@ -157,8 +162,7 @@ class VerifyStep:
             s.wait_event(self._copied)
             self.accept_commit(d["target_logits"], d["draft_logits"], d["node_tokens"],
                                d["k_tree"], d["v_tree"], seed, round_, s)
-            for k, v in self.host_out.items():
-                v.copy_(self.outs[k], non_blocking=True)
+            self._host_buf.copy_(self._out_buf[:self._out_head], non_blocking=True)
         return self.host_out
 
     def h2d_bytes(self, host_in: dict) -> int:
