@@ -108,6 +108,24 @@ def test_chain_large_vocab_top_k(cuda_ok, V, B):
     assert sv.sv_read_device_status() == 0
 
 
+@pytest.mark.parametrize("dtype,V,B,q_probs", [
+    (torch.bfloat16, 152064, 16, True),   # bf16 rows, f32 q probabilities (two q vectors per p vector)
+    (torch.float32, 131072, 8, False),    # fp32 rows, q as logits
+    (torch.float32, 131072, 8, True),
+])
+def test_select_ring_layouts(cuda_ok, dtype, V, B, q_probs):
+    """Rows long enough that each select CTA's slice of the vocabulary streams through its
+    shared-memory ring, for each stage layout the ring has."""
+    lg = wl.chain_logits(B, 4, V, sigma=3.0, draft_sigma=1.0, dtype=dtype, seed=17)
+    if q_probs:
+        qp = wl.draft_probs(lg["draft_logits"])
+        out, ref = _chain(sv.EXACT, lg, q_kind=sv.Q_PROBS_F32, q=qp, seed=8, rnd=5)
+    else:
+        out, ref = _chain(sv.EXACT, lg, seed=8, rnd=5)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"], max_exempt_frac=0.15)
+    assert sv.sv_read_device_status() == 0
+
+
 def test_top_k_tie_fallback(cuda_ok):
     """Every logit equal: more than 3072 entries tie at the threshold, so the kernel
     takes its counting path; the kept set is the k lowest ids."""
