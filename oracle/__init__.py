@@ -58,10 +58,10 @@ def _load():
             lib.orc_tree_mask.argtypes = [I, P, P]
             lib.orc_tree_attention.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, I, I, I,
                                                P, Dbl, I, I, P]
-            lib.orc_accept_tree.argtypes = [I, I, I, I, I, P, P, P, P, I, I, Dbl, I, U64, U64,
+            lib.orc_accept_tree.argtypes = [I, I, I, I, I, P, P, P, P, I, I, Dbl, I, Dbl, U64, U64,
                                             P, P, P, P, P, P, P, P]
             lib.orc_accept_tree.restype = I
-            lib.orc_accept_chain.argtypes = [I, I, I, I, I, P, P, I, P, Dbl, I, U64, U64,
+            lib.orc_accept_chain.argtypes = [I, I, I, I, I, P, P, I, P, Dbl, I, Dbl, U64, U64,
                                              P, P, P, P, P]
             lib.orc_accept_chain.restype = I
             lib.orc_commit_kv.argtypes = [I, I, I, I, I, P, P, P, I, P, P, P, P, P, I, I, I]
@@ -183,8 +183,9 @@ def _q_args(q, q_kind):
 
 
 def accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperature=1.0,
-                top_k=0, seed=0, round_=0):
-    """Tree acceptance; returns a dict of CPU tensors (see oracle.c)."""
+                top_k=0, seed=0, round_=0, top_p=1.0):
+    """Tree acceptance; returns a dict of CPU tensors (see oracle.c).  top_p < 1 keeps
+    the nucleus of the top-k distribution (needs 0 < top_k < V)."""
     tl = _cpu(target_logits)
     dt = _dtype_code(tl)
     B, N, V = tl.shape
@@ -205,7 +206,7 @@ def accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperature
     }
     rc = _load().orc_accept_tree(
         mode, dt, B, N, V, _ptr(par), _ptr(toks), _ptr(tl), _ptr(qq), q_kind, Dq,
-        float(temperature), int(top_k), int(seed), int(round_), _ptr(out["path_nodes"]),
+        float(temperature), int(top_k), float(top_p), int(seed), int(round_), _ptr(out["path_nodes"]),
         _ptr(out["tokens"]), _ptr(out["num_emitted"]), _ptr(out["num_accepted"]),
         _ptr(out["near_ties"]), _ptr(out["acc"]), _ptr(out["ratio"]), _ptr(out["flags"]))
     if rc != 0:
@@ -214,8 +215,9 @@ def accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperature
 
 
 def accept_chain(mode, target_logits, q, q_kind, draft_tokens, temperature=1.0, top_k=0,
-                 seed=0, round_=0):
-    """Chain acceptance as the left-to-right procedure; returns a dict of CPU tensors."""
+                 seed=0, round_=0, top_p=1.0):
+    """Chain acceptance as the left-to-right procedure; returns a dict of CPU tensors.
+    top_p < 1 keeps the nucleus of the top-k distribution (needs 0 < top_k < V)."""
     tl = _cpu(target_logits)
     dt = _dtype_code(tl)
     B, W, V = tl.shape
@@ -230,8 +232,8 @@ def accept_chain(mode, target_logits, q, q_kind, draft_tokens, temperature=1.0, 
         "flags": torch.zeros(B, dtype=torch.int32),
     }
     rc = _load().orc_accept_chain(mode, dt, B, gamma, V, _ptr(tl), _ptr(qq), q_kind, _ptr(toks),
-                                  float(temperature), int(top_k), int(seed), int(round_),
-                                  _ptr(out["tokens"]), _ptr(out["num_emitted"]),
+                                  float(temperature), int(top_k), float(top_p), int(seed),
+                                  int(round_), _ptr(out["tokens"]), _ptr(out["num_emitted"]),
                                   _ptr(out["num_accepted"]), _ptr(out["near_ties"]),
                                   _ptr(out["flags"]))
     if rc != 0:

@@ -30,6 +30,12 @@
  *    from norm([p_a - q_{d+1}]+) if that node has children, else the bonus from p_a.
  *  - top-k ties at the k-th value keep the lower token ids; argmax ties pick the
  *    lowest token id; temperature T == 0 means greedy.
+ *  - top-p (nucleus; named as a sampling knob by the jennyma11 blog, section
+ *    "先弄清无损验证", and the lpnh.cn walkthrough, section 4.2): applied within the
+ *    top-k distribution (top-k first, then top-p; top_p < 1 needs 0 < top_k < V).  In
+ *    the top-k ranking an entry stays while the mass ranked above it is below top_p,
+ *    then p is renormalised over the kept entries; a cut within 1e-6 of top_p counts as
+ *    one near tie of the sequence.
  *  - uniforms: counter (node, seq, round_lo, round_hi ^ domain), key (seed_lo, seed_hi);
  *    u_acc from word 0 and u_smp from word 1, u = ((w >> 8) + 0.5) * 2^-24.
  *  - inverse CDF in ascending token order: smallest j with C_j > u * sum(w).
@@ -273,16 +279,23 @@ static int orc_argmax(const double *z, int V) {
 }
 
 /* Effective sampling distribution of one logit row: y = z / T, keep the top_k
- * largest y (if 0 < top_k < V; ties keep lower ids), p = softmax over the kept set. */
-static void orc_effective_dist(const double *z, int V, double T, int top_k, double *p) {
+ * largest y (if 0 < top_k < V; ties keep lower ids), p = softmax over the kept set.
+ * With top_p < 1 (only together with top-k), the nucleus of that distribution is kept
+ * instead: in the same ranking, an entry stays while the mass ranked above it is below
+ * top_p (the smallest set with mass >= top_p; the first entry always stays), and p is
+ * renormalised over it.  A cut whose mass lies within 1e-6 of top_p on either side sets
+ * *near (if near is not NULL). */
+static void orc_effective_dist(const double *z, int V, double T, int top_k, double top_p,
+                               double *p, int *near) {
   double *y = (double *)orc_alloc(sizeof(double) * (size_t)V);
   unsigned char *keep = (unsigned char *)orc_alloc((size_t)V);
+  orc_ranked *r = NULL;
   for (int j = 0; j < V; ++j) {
     y[j] = z[j] / T;
     keep[j] = 1;
   }
   if (top_k > 0 && top_k < V) {
-    orc_ranked *r = (orc_ranked *)orc_alloc(sizeof(orc_ranked) * (size_t)V);
+    r = (orc_ranked *)orc_alloc(sizeof(orc_ranked) * (size_t)V);
     for (int j = 0; j < V; ++j) {
       r[j].value = y[j];
       r[j].index = j;
@@ -290,7 +303,6 @@ static void orc_effective_dist(const double *z, int V, double T, int top_k, doub
     qsort(r, (size_t)V, sizeof(orc_ranked), orc_cmp_desc_value_asc_index);
     memset(keep, 0, (size_t)V);
     for (int i = 0; i < top_k; ++i) keep[r[i].index] = 1;
-    free(r);
   }
   double ymax = -INFINITY;
   for (int j = 0; j < V; ++j)
@@ -301,6 +313,25 @@ static void orc_effective_dist(const double *z, int V, double T, int top_k, doub
     sum += p[j];
   }
   for (int j = 0; j < V; ++j) p[j] /= sum;
+  if (r != NULL && top_p < 1.0) {
+    double c = 0.0;
+    int m = top_k - 1;
+    for (int i = 0; i < top_k; ++i) {
+      double before = c;
+      c += p[r[i].index];
+      if (c >= top_p) {
+        m = i;
+        if (near && (c - top_p < ORC_NEAR_TIE || (i > 0 && top_p - before < ORC_NEAR_TIE)))
+          *near = 1;
+        break;
+      }
+    }
+    double kept = 0.0;
+    for (int i = 0; i <= m; ++i) kept += p[r[i].index];
+    for (int i = m + 1; i < top_k; ++i) p[r[i].index] = 0.0;
+    for (int i = 0; i <= m; ++i) p[r[i].index] /= kept;
+  }
+  free(r);
   free(y);
   free(keep);
 }
@@ -352,13 +383,13 @@ static int orc_sample_residual(const double *p, const double *q, int V, double u
 /* Effective q row for depth d (1-based): from draft logits (T, top-k applied) or given
  * directly as probabilities (f32). */
 static void orc_q_row(const void *q, int q_kind, int dtype, int b, int Dq, int d, int V,
-                      double T, int top_k, double *zbuf, double *out) {
+                      double T, int top_k, double top_p, double *zbuf, double *out, int *near) {
   size_t row = (size_t)b * Dq + (d - 1);
   if (q_kind == ORC_Q_PROBS_F32) {
     orc_load_row(q, ORC_F32, row, V, out);
   } else {
     orc_load_row(q, dtype, row, V, zbuf);
-    orc_effective_dist(zbuf, V, T, top_k, out);
+    orc_effective_dist(zbuf, V, T, top_k, top_p, out, near);
   }
 }
 
@@ -371,8 +402,8 @@ static void orc_q_row(const void *q, int q_kind, int dtype, int b, int Dq, int d
  * out_flags [B] optional: bit0 = a draft had q(x)=0, bit1 = token id out of range. */
 int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *parent,
                     const int32_t *node_tokens, const void *target_logits, const void *q,
-                    int q_kind, int Dq, double T, int top_k, uint64_t seed, uint64_t round,
-                    int32_t *out_path_nodes, int32_t *out_tokens, int32_t *out_num_emitted,
+                    int q_kind, int Dq, double T, int top_k, double top_p, uint64_t seed,
+                    uint64_t round, int32_t *out_path_nodes, int32_t *out_tokens, int32_t *out_num_emitted,
                     int32_t *out_num_accepted, uint32_t *out_near_ties, uint8_t *out_acc,
                     double *out_ratio, uint32_t *out_flags) {
   if (orc_check_tree(N, parent)) return 1;
@@ -398,6 +429,7 @@ int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *par
     double *ratio = (double *)orc_alloc(sizeof(double) * (size_t)N);
     unsigned char *dec_near = (unsigned char *)calloc((size_t)N, 1);
     uint32_t flags = 0;
+    int nuc_near = 0;  /* a nucleus cut of one of the rows used was a near tie */
     for (int c = 0; c < N; ++c) ratio[c] = NAN;
 
     /* decisions: node c against its parent's p and the q of its depth */
@@ -409,8 +441,8 @@ int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *par
       orc_load_row(target_logits, dtype, (size_t)b * N + a, V, z);
       int amax = orc_argmax(z, V);
       if (!greedy) {
-        orc_effective_dist(z, V, T, top_k, pa);
-        orc_q_row(q, q_kind, dtype, b, Dq, depth[a] + 1, V, T, top_k, z, qd);
+        orc_effective_dist(z, V, T, top_k, top_p, pa, &nuc_near);
+        orc_q_row(q, q_kind, dtype, b, Dq, depth[a] + 1, V, T, top_k, top_p, z, qd, &nuc_near);
       }
       for (int c = a + 1; c < N; ++c) {
         if (parent[c] != a) continue;
@@ -460,15 +492,15 @@ int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *par
     } else {
       double u_acc, u_smp;
       orc_uniforms(seed, round, 0u, b, best, &u_acc, &u_smp);
-      orc_effective_dist(z, V, T, top_k, pa);
+      orc_effective_dist(z, V, T, top_k, top_p, pa, &nuc_near);
       int near_s = 0;
       if (has_child) {
-        orc_q_row(q, q_kind, dtype, b, Dq, depth[best] + 1, V, T, top_k, z, qd);
+        orc_q_row(q, q_kind, dtype, b, Dq, depth[best] + 1, V, T, top_k, top_p, z, qd, &nuc_near);
         tok = orc_sample_residual(pa, qd, V, u_smp, &near_s);
       } else {
         tok = orc_sample_residual(pa, NULL, V, u_smp, &near_s);
       }
-      near += (uint32_t)near_s;
+      near += (uint32_t)near_s + (uint32_t)nuc_near;
     }
 
     /* outputs: path nodes root..best in depth order, their tokens, then the sample */
@@ -508,7 +540,7 @@ int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *par
  * out_tokens [B,gamma+1] (unused -1).  Node ids for the uniforms: draft i is node i. */
 int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *target_logits,
                      const void *q, int q_kind, const int32_t *draft_tokens, double T,
-                     int top_k, uint64_t seed, uint64_t round, int32_t *out_tokens,
+                     int top_k, double top_p, uint64_t seed, uint64_t round, int32_t *out_tokens,
                      int32_t *out_num_emitted, int32_t *out_num_accepted,
                      uint32_t *out_near_ties, uint32_t *out_flags) {
   int greedy = (mode == ORC_GREEDY) || (T == 0.0);
@@ -520,6 +552,7 @@ int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *t
     double *qi = (double *)orc_alloc(sizeof(double) * (size_t)V);
     int32_t *tk = out_tokens + (size_t)b * W;
     uint32_t near = 0, flags = 0;
+    int nuc_near = 0;  /* a nucleus cut of one of the rows used was a near tie */
     for (int i = 0; i < W; ++i) tk[i] = -1;
     int i = 1, tok = -1;
     for (; i <= gamma; ++i) {
@@ -535,8 +568,8 @@ int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *t
         tok = amax;
         break;
       }
-      orc_effective_dist(z, V, T, top_k, p);
-      orc_q_row(q, q_kind, dtype, b, gamma, i, V, T, top_k, z, qi);
+      orc_effective_dist(z, V, T, top_k, top_p, p, &nuc_near);
+      orc_q_row(q, q_kind, dtype, b, gamma, i, V, T, top_k, top_p, z, qi, &nuc_near);
       double u_acc, u_smp;
       orc_uniforms(seed, round, 0u, b, i, &u_acc, &u_smp);
       int accepted = 0;
@@ -570,7 +603,7 @@ int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *t
       if (greedy) {
         tok = orc_argmax(z, V);
       } else {
-        orc_effective_dist(z, V, T, top_k, p);
+        orc_effective_dist(z, V, T, top_k, top_p, p, &nuc_near);
         double ua, us;
         orc_uniforms(seed, round, 0u, b, gamma, &ua, &us);
         int near_s = 0;
@@ -578,6 +611,7 @@ int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *t
         near += (uint32_t)near_s;
       }
     }
+    near += (uint32_t)nuc_near;
     int acc_n = i - 1;
     tk[acc_n] = tok;
     out_num_emitted[b] = acc_n + 1;

@@ -145,13 +145,19 @@ def _ranked_tokens(logits_row: torch.Tensor, k: int) -> torch.Tensor:
     return order[:k]
 
 
-def _draft_sample(logits_row: torch.Tensor, T: float, top_k: int, g) -> int:
+def _draft_sample(logits_row: torch.Tensor, T: float, top_k: int, g, top_p: float = 1.0) -> int:
     """The drafter's own sample from its row: Gumbel-max over the top_k highest logits
-    (all tokens if top_k == 0).  Sits upstream of verification."""
+    (all tokens if top_k == 0), narrowed to their nucleus when top_p < 1 (the drafter
+    samples only tokens its own distribution gives mass).  Sits upstream of
+    verification."""
     z = logits_row.float().cpu()
     V = z.numel()
     if 0 < top_k < V:
         cand = _ranked_tokens(z, top_k)
+        if top_p < 1.0 and T > 0:
+            w = torch.softmax(z[cand].double() / T, dim=0)
+            before = torch.cumsum(w, 0) - w
+            cand = cand[before < top_p]
     else:
         cand = torch.arange(V)
     if T == 0:
@@ -162,7 +168,7 @@ def _draft_sample(logits_row: torch.Tensor, T: float, top_k: int, g) -> int:
 
 
 def chain_logits(B, gamma, V, sigma=3.0, draft_sigma=1.0, dtype=torch.bfloat16,
-                 temperature=1.0, top_k=0, seed=0, device="cpu"):
+                 temperature=1.0, top_k=0, seed=0, device="cpu", top_p=1.0):
     """Target logits [B,gamma+1,V] ~N(0,sigma); draft logits [B,gamma,V] with row i =
     target row i + N(0,draft_sigma) (the draft of token i+1 sees the same context as
     target row i); draft tokens [B,gamma] sampled by the drafter from its rows."""
@@ -176,7 +182,7 @@ def chain_logits(B, gamma, V, sigma=3.0, draft_sigma=1.0, dtype=torch.bfloat16,
     dl_cpu = dl.float().cpu()
     for b in range(B):
         for i in range(gamma):
-            toks[b, i] = _draft_sample(dl_cpu[b, i], temperature, top_k, gc)
+            toks[b, i] = _draft_sample(dl_cpu[b, i], temperature, top_k, gc, top_p)
     return dict(target_logits=tl, draft_logits=dl, draft_tokens=toks.to(device))
 
 

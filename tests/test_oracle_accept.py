@@ -348,6 +348,63 @@ def test_temperature_and_top_k_ratio_closed_form():
             assert int(out["flags"][0]) & 1
 
 
+def test_top_p_nucleus_closed_form():
+    """Top-p within top-k, on masses chosen so the nucleus is plain to see: the top-4
+    distribution of the target row is (0.5, 0.25, 0.15, 0.10) (two entries outside the
+    top 4); at top_p = 0.7 the first two stay (0.5 < 0.7 before the second, 0.75 >= 0.7
+    before the third), so p' = (2/3, 1/3).  The q row's top-4 distribution is
+    (0.45, 0.3, 0.15, 0.1): 0.45 and 0.3 stay (0.75 >= 0.7 before the third),
+    q' = (0.6, 0.4).  The ratio p'(x)/q'(x) follows for every x (T = 1)."""
+    V, k, top_p = 6, 4, 0.7
+    pt = np.array([0.25, 0.001, 0.5, 0.15, 0.10, 0.002])   # top-4: 2, 0, 3, 4
+    pq = np.array([0.3, 0.15, 0.45, 0.001, 0.002, 0.1])    # top-4: 2, 0, 1, 5
+    zt, zq = np.log(pt), np.log(pq)
+    tl = torch.from_numpy(np.stack([zt, zt])).unsqueeze(0)          # float64 rows
+    ql = torch.from_numpy(zq).view(1, 1, V)
+    p_eff = {2: 2 / 3, 0: 1 / 3}
+    q_eff = {2: 0.6, 0: 0.4}
+    for x in range(V):
+        out = oracle.accept_tree(oracle.EXACT, tl.float(), ql.float(), oracle.Q_LOGITS,
+                                 [-1, 0], torch.tensor([[0, x]], dtype=torch.int32),
+                                 temperature=1.0, top_k=k, top_p=top_p, seed=3)
+        r = out["ratio"][0, 1].item()
+        px, qx = p_eff.get(x, 0.0), q_eff.get(x, 0.0)
+        if qx > 0:
+            assert abs(r - px / qx) < 1e-6, (x, r, px / qx)   # float32 logits of these masses
+        else:
+            assert r == (math.inf if px > 0 else 0.0)
+    # top_p = 1 keeps the whole top-k set: the same as top-k alone
+    toks = torch.tensor([[0, 3]], dtype=torch.int32)
+    a1 = oracle.accept_tree(oracle.EXACT, tl.float(), ql.float(), oracle.Q_LOGITS, [-1, 0], toks,
+                            top_k=k, top_p=1.0, seed=3)
+    a2 = oracle.accept_tree(oracle.EXACT, tl.float(), ql.float(), oracle.Q_LOGITS, [-1, 0], toks,
+                            top_k=k, seed=3)
+    assert a1["ratio"][0, 1].item() == a2["ratio"][0, 1].item()
+
+
+def test_chi_square_first_token_top_p():
+    """(P5) with top-k 10 and top-p 0.8 on the target rows (q given as probabilities):
+    the first emitted token follows the nucleus of p_0's top-10 distribution."""
+    gamma, V, B, k, top_p = 4, 16, 400_000, 10, 0.8
+    p, q = _random_pq(gamma, V, 31)
+    tl, qq, toks = _chain_inputs(B, p, q, seed=13)
+    out = oracle.accept_chain(oracle.EXACT, tl, qq, oracle.Q_PROBS_F32, toks, top_k=k,
+                              top_p=top_p, seed=6, round_=2)
+    first = out["tokens"][:, 0].numpy()
+    counts = np.bincount(first, minlength=V)
+    p0 = np.exp(_log(p[0]).astype(np.float32).astype(np.float64))
+    order = np.argsort(-p0, kind="stable")[:k]
+    w = p0[order] / p0[order].sum()
+    before = np.cumsum(w) - w
+    nucleus = order[before < top_p]
+    expected = np.zeros(V)
+    expected[nucleus] = p0[nucleus] / p0[nucleus].sum()
+    assert counts[expected == 0].sum() == 0          # nothing outside the nucleus
+    keep = expected > 0
+    chi2, pval = stats.chisquare(counts[keep], B * expected[keep])
+    assert pval > 1e-4, (chi2, pval)
+
+
 def test_bonus_inverse_cdf_matches_searchsorted():
     """The bonus token is the smallest j with cumsum(p)_j > u * sum(p) (numpy search)."""
     V, B = 10, 300
