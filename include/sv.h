@@ -134,10 +134,17 @@ size_t sv_tree_attention_workspace_size(sv_dtype dt, int B, int N, int Hq, int H
  * of decisions with |u_acc - ratio| < 1e-6 and samples within 1e-6 of a CDF
  * boundary: reported, not hidden; may be NULL).
  * logit_dt: SV_BF16 or SV_F32.  V % 8 == 0, 1 <= gamma <= 63, 0 <= top_k <= 1024
- * (0 = off).  Workspace: sv_accept_workspace_size(B, gamma+1, V, gamma). */
+ * (0 = off).  top_p in (0, 1], 1 = off: below 1 the nucleus of the top-k distribution
+ * is kept (top-k first, then top-p; needs 0 < top_k < V, else SV_ERR_UNSUPPORTED): in the
+ * top-k ranking an entry stays while the mass ranked above it is below top_p, and p is
+ * renormalised over the kept entries; a cut whose mass lies within 1e-6 of top_p counts
+ * as one near tie of the sequence (the lpnh.cn walkthrough, section 4.2, and the
+ * jennyma11 blog name top-p among the sampling settings the effective distributions
+ * carry).  Ignored in greedy mode.
+ * Workspace: sv_accept_workspace_size(B, gamma+1, V, gamma). */
 sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
                           const void *target_logits, const void *q, sv_q_kind q_kind,
-                          const int32_t *draft_tokens, float temperature, int top_k,
+                          const int32_t *draft_tokens, float temperature, int top_k, float top_p,
                           uint64_t seed, uint64_t round, int32_t *out_tokens,
                           int32_t *out_num_emitted, int32_t *out_num_accepted,
                           uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
@@ -158,7 +165,7 @@ sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int
 sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
                          const int32_t *parent, const int32_t *node_tokens,
                          const void *target_logits, const void *q, sv_q_kind q_kind, int Dq,
-                         float temperature, int top_k, uint64_t seed, uint64_t round,
+                         float temperature, int top_k, float top_p, uint64_t seed, uint64_t round,
                          int32_t *out_path_nodes, int32_t *out_tokens,
                          int32_t *out_num_emitted, int32_t *out_num_accepted,
                          uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
@@ -184,7 +191,7 @@ size_t sv_accept_workspace_size(int B, int N, int V, int Dq);
 sv_status sv_accept_tree_noalloc(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
                                  const int32_t *parent, const int32_t *node_tokens,
                                  const void *target_logits, const void *q, sv_q_kind q_kind,
-                                 int Dq, float temperature, int top_k, uint64_t seed,
+                                 int Dq, float temperature, int top_k, float top_p, uint64_t seed,
                                  uint64_t round, int32_t *out_path_nodes, int32_t *out_tokens,
                                  int32_t *out_num_emitted, int32_t *out_num_accepted,
                                  uint32_t *out_near_ties, void *stream);
@@ -215,7 +222,7 @@ sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_
 sv_status sv_accept_tree_commit(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
                                 const int32_t *parent, const int32_t *node_tokens,
                                 const void *target_logits, const void *q, sv_q_kind q_kind,
-                                int Dq, float temperature, int top_k, uint64_t seed,
+                                int Dq, float temperature, int top_k, float top_p, uint64_t seed,
                                 uint64_t round, sv_dtype kv_dt, int Hkv, int D,
                                 const void *k_tree, const void *v_tree, sv_kv_cache cache,
                                 int32_t *out_path_nodes, int32_t *out_tokens,
@@ -224,7 +231,7 @@ sv_status sv_accept_tree_commit(sv_mode mode, sv_dtype logit_dt, int B, int N, i
                                 void *stream);
 sv_status sv_accept_chain_commit(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
                                  const void *target_logits, const void *q, sv_q_kind q_kind,
-                                 const int32_t *draft_tokens, float temperature, int top_k,
+                                 const int32_t *draft_tokens, float temperature, int top_k, float top_p,
                                  uint64_t seed, uint64_t round, sv_dtype kv_dt, int Hkv, int D,
                                  const void *k_tree, const void *v_tree, sv_kv_cache cache,
                                  int32_t *out_tokens, int32_t *out_num_emitted,

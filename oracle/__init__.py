@@ -185,7 +185,9 @@ def _q_args(q, q_kind):
 def accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperature=1.0,
                 top_k=0, seed=0, round_=0, top_p=1.0):
     """Tree acceptance; returns a dict of CPU tensors (see oracle.c).  top_p < 1 keeps
-    the nucleus of the top-k distribution (needs 0 < top_k < V)."""
+    the nucleus of the top-k distribution (needs 0 < top_k < V); top_p is taken as the
+    float32 value the library's interface carries, so that both sides cut at the same
+    threshold."""
     tl = _cpu(target_logits)
     dt = _dtype_code(tl)
     B, N, V = tl.shape
@@ -206,7 +208,7 @@ def accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperature
     }
     rc = _load().orc_accept_tree(
         mode, dt, B, N, V, _ptr(par), _ptr(toks), _ptr(tl), _ptr(qq), q_kind, Dq,
-        float(temperature), int(top_k), float(top_p), int(seed), int(round_), _ptr(out["path_nodes"]),
+        float(temperature), int(top_k), float(np.float32(top_p)), int(seed), int(round_), _ptr(out["path_nodes"]),
         _ptr(out["tokens"]), _ptr(out["num_emitted"]), _ptr(out["num_accepted"]),
         _ptr(out["near_ties"]), _ptr(out["acc"]), _ptr(out["ratio"]), _ptr(out["flags"]))
     if rc != 0:
@@ -232,7 +234,7 @@ def accept_chain(mode, target_logits, q, q_kind, draft_tokens, temperature=1.0, 
         "flags": torch.zeros(B, dtype=torch.int32),
     }
     rc = _load().orc_accept_chain(mode, dt, B, gamma, V, _ptr(tl), _ptr(qq), q_kind, _ptr(toks),
-                                  float(temperature), int(top_k), float(top_p), int(seed),
+                                  float(temperature), int(top_k), float(np.float32(top_p)), int(seed),
                                   int(round_), _ptr(out["tokens"]), _ptr(out["num_emitted"]),
                                   _ptr(out["num_accepted"]), _ptr(out["near_ties"]),
                                   _ptr(out["flags"]))

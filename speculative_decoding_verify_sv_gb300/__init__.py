@@ -76,18 +76,18 @@ def load_library():
         lib.sv_tree_attention_path.argtypes = [I, I, I, I, I, I]
         lib.sv_tree_attention_path.restype = I
         lib.sv_tree_attention_workspace_size.restype = SZ
-        lib.sv_accept_chain.argtypes = [I, I, I, I, I, P, P, I, P, F, I, U64, U64, P, P, P, P, P,
+        lib.sv_accept_chain.argtypes = [I, I, I, I, I, P, P, I, P, F, I, F, U64, U64, P, P, P, P, P,
                                         SZ, P]
-        lib.sv_accept_tree.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, U64, U64, P, P, P, P,
+        lib.sv_accept_tree.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, F, U64, U64, P, P, P, P,
                                        P, P, SZ, P]
-        lib.sv_accept_tree_noalloc.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, U64, U64, P,
+        lib.sv_accept_tree_noalloc.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, F, U64, U64, P,
                                                P, P, P, P, P]
         lib.sv_accept_workspace_size.argtypes = [I, I, I, I]
         lib.sv_accept_workspace_size.restype = SZ
         lib.sv_commit_kv.argtypes = [I, I, I, I, I, P, P, P, I, P, _KVCacheC, P]
-        lib.sv_accept_tree_commit.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, U64, U64,
+        lib.sv_accept_tree_commit.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, F, U64, U64,
                                               I, I, I, P, P, _KVCacheC, P, P, P, P, P, P, SZ, P]
-        lib.sv_accept_chain_commit.argtypes = [I, I, I, I, I, P, P, I, P, F, I, U64, U64,
+        lib.sv_accept_chain_commit.argtypes = [I, I, I, I, I, P, P, I, P, F, I, F, U64, U64,
                                                I, I, I, P, P, _KVCacheC, P, P, P, P, P, SZ, P]
         lib.sv_tree_prepare.argtypes = [I, P, P, P]
         lib.sv_read_device_status.argtypes = [P, P]
@@ -257,7 +257,7 @@ def _accept_outputs(B, W, device, outs):
 
 
 def sv_accept_chain(mode, target_logits, q, q_kind, draft_tokens, temperature=1.0, top_k=0,
-                    seed=0, round_=0, outs=None, workspace=None, stream=None) -> dict:
+                    seed=0, round_=0, outs=None, workspace=None, stream=None, top_p=1.0) -> dict:
     """Chain acceptance; target_logits [B,gamma+1,V], q [B,gamma,V] (or None in greedy
     mode), draft_tokens [B,gamma] int32.  Returns dict of device tensors."""
     lib = load_library()
@@ -275,7 +275,7 @@ def sv_accept_chain(mode, target_logits, q, q_kind, draft_tokens, temperature=1.
                                      workspace)
     _check(lib.sv_accept_chain(mode, _dt(target_logits), B, gamma, V, _ptr(target_logits), _ptr(q),
                                q_kind, _ptr(draft_tokens), float(temperature), int(top_k),
-                               int(seed), int(round_), _ptr(outs["tokens"]),
+                               float(top_p), int(seed), int(round_), _ptr(outs["tokens"]),
                                _ptr(outs["num_emitted"]), _ptr(outs["num_accepted"]),
                                _ptr(outs["near_ties"]), _ptr(workspace), ws_bytes,
                                _stream(stream)))
@@ -290,7 +290,7 @@ def _tree_depth(parent) -> int:
 
 
 def sv_accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperature=1.0,
-                   top_k=0, seed=0, round_=0, outs=None, workspace=None, stream=None) -> dict:
+                   top_k=0, seed=0, round_=0, outs=None, workspace=None, stream=None, top_p=1.0) -> dict:
     """Tree acceptance; target_logits [B,N,V], q [B,Dq,V] (row d-1 = depth d),
     node_tokens [B,N] int32, parent (host sequence, BFS order).  Returns dict."""
     lib = load_library()
@@ -314,7 +314,7 @@ def sv_accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperat
         raise ValueError(f"parent has {n} entries, logits have {N} rows")
     _check(lib.sv_accept_tree(mode, _dt(target_logits), B, N, V, par, _ptr(node_tokens),
                               _ptr(target_logits), _ptr(q), q_kind, Dq, float(temperature),
-                              int(top_k), int(seed), int(round_), _ptr(outs["path_nodes"]),
+                              int(top_k), float(top_p), int(seed), int(round_), _ptr(outs["path_nodes"]),
                               _ptr(outs["tokens"]), _ptr(outs["num_emitted"]),
                               _ptr(outs["num_accepted"]), _ptr(outs["near_ties"]),
                               _ptr(workspace), ws_bytes, _stream(stream)))
@@ -323,7 +323,7 @@ def sv_accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperat
 
 def sv_accept_tree_noalloc(mode, target_logits, q, q_kind, parent, node_tokens,
                            temperature=1.0, top_k=0, seed=0, round_=0, outs=None,
-                           stream=None) -> dict:
+                           stream=None, top_p=1.0) -> dict:
     """sv_accept_tree without a workspace, for callers that cannot allocate device
     memory: the library keeps the per-row statistics in a fixed device array.  Calls
     that overlap on the GPU share that array and race; order them on one stream.  The
@@ -344,7 +344,7 @@ def sv_accept_tree_noalloc(mode, target_logits, q, q_kind, parent, node_tokens,
         raise ValueError(f"parent has {n} entries, logits have {N} rows")
     _check(lib.sv_accept_tree_noalloc(mode, _dt(target_logits), B, N, V, par, _ptr(node_tokens),
                                       _ptr(target_logits), _ptr(q), q_kind, Dq, float(temperature),
-                                      int(top_k), int(seed), int(round_), _ptr(outs["path_nodes"]),
+                                      int(top_k), float(top_p), int(seed), int(round_), _ptr(outs["path_nodes"]),
                                       _ptr(outs["tokens"]), _ptr(outs["num_emitted"]),
                                       _ptr(outs["num_accepted"]), _ptr(outs["near_ties"]),
                                       _stream(stream)))
@@ -376,7 +376,7 @@ def _kv_args(k_tree, v_tree, cache: KVCache):
 
 def sv_accept_chain_commit(mode, target_logits, q, q_kind, draft_tokens, k_tree, v_tree,
                            cache: KVCache, temperature=1.0, top_k=0, seed=0, round_=0,
-                           outs=None, workspace=None, stream=None) -> dict:
+                           outs=None, workspace=None, stream=None, top_p=1.0) -> dict:
     """sv_accept_chain, then the commit of nodes 0..accepted of k_tree/v_tree
     [B,gamma+1,Hkv,D] into the cache, in the same launches."""
     lib = load_library()
@@ -394,7 +394,7 @@ def sv_accept_chain_commit(mode, target_logits, q, q_kind, draft_tokens, k_tree,
                                      workspace)
     _check(lib.sv_accept_chain_commit(mode, _dt(target_logits), B, gamma, V, _ptr(target_logits),
                                       _ptr(q), q_kind, _ptr(draft_tokens), float(temperature),
-                                      int(top_k), int(seed), int(round_), kv_dt, Hkv, D,
+                                      int(top_k), float(top_p), int(seed), int(round_), kv_dt, Hkv, D,
                                       _ptr(k_tree), _ptr(v_tree), cs, _ptr(outs["tokens"]),
                                       _ptr(outs["num_emitted"]), _ptr(outs["num_accepted"]),
                                       _ptr(outs["near_ties"]), _ptr(workspace), ws_bytes,
@@ -404,7 +404,7 @@ def sv_accept_chain_commit(mode, target_logits, q, q_kind, draft_tokens, k_tree,
 
 def sv_accept_tree_commit(mode, target_logits, q, q_kind, parent, node_tokens, k_tree, v_tree,
                           cache: KVCache, temperature=1.0, top_k=0, seed=0, round_=0, outs=None,
-                          workspace=None, stream=None) -> dict:
+                          workspace=None, stream=None, top_p=1.0) -> dict:
     """sv_accept_tree, then the commit of the kept path of k_tree/v_tree [B,N,Hkv,D] into
     the cache, in the same launches."""
     lib = load_library()
@@ -428,7 +428,7 @@ def sv_accept_tree_commit(mode, target_logits, q, q_kind, parent, node_tokens, k
         raise ValueError(f"parent has {n} entries, logits have {N} rows")
     _check(lib.sv_accept_tree_commit(mode, _dt(target_logits), B, N, V, par, _ptr(node_tokens),
                                      _ptr(target_logits), _ptr(q), q_kind, Dq, float(temperature),
-                                     int(top_k), int(seed), int(round_), kv_dt, Hkv, D,
+                                     int(top_k), float(top_p), int(seed), int(round_), kv_dt, Hkv, D,
                                      _ptr(k_tree), _ptr(v_tree), cs, _ptr(outs["path_nodes"]),
                                      _ptr(outs["tokens"]), _ptr(outs["num_emitted"]),
                                      _ptr(outs["num_accepted"]), _ptr(outs["near_ties"]),

@@ -218,6 +218,7 @@ __device__ __forceinline__ RowStat load_stat(const RowStat *s) {
   r.key_k = __ldcg(&s->key_k);
   r.idx_k = __ldcg(&s->idx_k);
   r.S = __ldcg(&s->S);
+  r.flags = __ldcg(&s->flags);
   return r;
 }
 
@@ -359,6 +360,7 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
   st.key_k = 0u;
   st.idx_k = INT_MAX;
   st.S = 0.f;
+  st.flags = 0u;
 
   if constexpr (!GREEDY && !TOPK) {
     const float part = m == -INFINITY ? 0.f : acc.value() * exp2f((m - zmax) * c);
@@ -446,49 +448,11 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
       }
     }
     __syncthreads();
-    const unsigned nc = n_cand;
-    if (nc <= kMaxCand) {
-      // rank every candidate: entries beating it (larger value, or equal and lower id);
-      // each candidate's comparisons are split over tpc adjacent threads (a power of two,
-      // the same in every thread), whose counts are summed by shuffles
-      __shared__ uint32_t thr_key;
-      __shared__ int thr_idx;
-      int tpc = 1;
-      while (tpc < 32 && nc * (unsigned)tpc * 2u <= (unsigned)NT) tpc *= 2;
-      const int per_round = NT / tpc, sub = tid & (tpc - 1);
-      float part = 0.f;
-      for (unsigned base = 0; base < nc; base += (unsigned)per_round) {
-        const unsigned i = base + (unsigned)(tid / tpc);
-        unsigned rank = 0;
-        Cand ci{0.f, 0};
-        if (i < nc) {
-          ci = cand[i];
-          unsigned j = (unsigned)sub;
-          for (; j + 3u * tpc < nc; j += 4u * tpc) {
-            const Cand c0 = cand[j], c1 = cand[j + tpc], c2 = cand[j + 2 * tpc], c3 = cand[j + 3 * tpc];
-            rank += (c0.z > ci.z || (c0.z == ci.z && c0.idx < ci.idx)) ? 1u : 0u;
-            rank += (c1.z > ci.z || (c1.z == ci.z && c1.idx < ci.idx)) ? 1u : 0u;
-            rank += (c2.z > ci.z || (c2.z == ci.z && c2.idx < ci.idx)) ? 1u : 0u;
-            rank += (c3.z > ci.z || (c3.z == ci.z && c3.idx < ci.idx)) ? 1u : 0u;
-          }
-          for (; j < nc; j += tpc) {
-            const Cand cj = cand[j];
-            rank += (cj.z > ci.z || (cj.z == ci.z && cj.idx < ci.idx)) ? 1u : 0u;
-          }
-        }
-        for (int o = 1; o < tpc; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
-        if (i < nc && sub == 0) {
-          if (rank < (unsigned)k) part += exp2f((ci.z - zmax) * c);
-          if (rank == (unsigned)k - 1u) thr_key = Elem<T>::key(ci.z), thr_idx = ci.idx;
-        }
-      }
-      __syncthreads();
-      st.key_k = thr_key;
-      st.idx_k = thr_idx;
-      st.S = block_sum_f<NT>(part, sh_d);
-    } else {
+    unsigned nc = n_cand;
+    if (nc > (unsigned)kMaxCand) {
       // many equal values near the top: find the threshold key bit by bit with counting
-      // passes, then the index cut among entries equal to it, then the kept sum
+      // passes and the index cut among the entries equal to it; then the kept set
+      // (exactly k entries) becomes the candidate list
       uint32_t K = 0u;
       for (int bit = Elem<T>::kKeyBits - 1; bit >= 0; --bit) {
         const uint32_t cand_key = K | (1u << bit);
@@ -532,6 +496,7 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
           scan[t] = run;
           run += cnt;
         }
+        n_cand = 0u;
       }
       __syncthreads();
       const unsigned before = scan[tid];
@@ -552,19 +517,130 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
         }
       }
       __syncthreads();
-      st.key_k = K;
-      st.idx_k = idx_sh;
-      KahanF s2;
+      RowStat cut{};
+      cut.key_k = K;
+      cut.idx_k = idx_sh;
       for (int v = tid; v < nvec; v += NT) {
         float f[VEC];
         Elem<T>::unpack(__ldg(xv + v), f);
-        float vs = 0.f;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e)
-          vs += kept<T>(f[e], v * VEC + e, st) ? exp2f((f[e] - zmax) * c) : 0.f;
-        s2.add(vs);
+        for (int e = 0; e < VEC; ++e) {
+          if (kept<T>(f[e], v * VEC + e, cut)) {
+            const unsigned slot = atomicAdd(&n_cand, 1u);
+            if (slot < kMaxCand) cand[slot] = Cand{f[e], v * VEC + e};
+          }
+        }
       }
-      st.S = block_sum_f<NT>(s2.value(), sh_d);
+      __syncthreads();
+      nc = min(n_cand, (unsigned)kMaxCand);
+    }
+    {
+      // rank every candidate: entries beating it (larger value, or equal and lower id);
+      // each candidate's comparisons are split over tpc adjacent threads (a power of two,
+      // the same in every thread), whose counts are summed by shuffles.  With top-p the
+      // kept entries are also laid out by rank (in the gather list's memory).
+      __shared__ uint32_t thr_key;
+      __shared__ int thr_idx;
+      const bool nucleus = p.top_p < 1.f;
+      float *srt_z = reinterpret_cast<float *>(s_glist);
+      int *srt_i = reinterpret_cast<int *>(s_glist) + SV_MAX_TOP_K;
+      static_assert(2 * SV_MAX_TOP_K <= kMaxGatherList, "ranked entries fit the gather list");
+      int tpc = 1;
+      while (tpc < 32 && nc * (unsigned)tpc * 2u <= (unsigned)NT) tpc *= 2;
+      const int per_round = NT / tpc, sub = tid & (tpc - 1);
+      float part = 0.f;
+      for (unsigned base = 0; base < nc; base += (unsigned)per_round) {
+        const unsigned i = base + (unsigned)(tid / tpc);
+        unsigned rank = 0;
+        Cand ci{0.f, 0};
+        if (i < nc) {
+          ci = cand[i];
+          unsigned j = (unsigned)sub;
+          for (; j + 3u * tpc < nc; j += 4u * tpc) {
+            const Cand c0 = cand[j], c1 = cand[j + tpc], c2 = cand[j + 2 * tpc], c3 = cand[j + 3 * tpc];
+            rank += (c0.z > ci.z || (c0.z == ci.z && c0.idx < ci.idx)) ? 1u : 0u;
+            rank += (c1.z > ci.z || (c1.z == ci.z && c1.idx < ci.idx)) ? 1u : 0u;
+            rank += (c2.z > ci.z || (c2.z == ci.z && c2.idx < ci.idx)) ? 1u : 0u;
+            rank += (c3.z > ci.z || (c3.z == ci.z && c3.idx < ci.idx)) ? 1u : 0u;
+          }
+          for (; j < nc; j += tpc) {
+            const Cand cj = cand[j];
+            rank += (cj.z > ci.z || (cj.z == ci.z && cj.idx < ci.idx)) ? 1u : 0u;
+          }
+        }
+        for (int o = 1; o < tpc; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+        if (i < nc && sub == 0) {
+          if (rank < (unsigned)k) {
+            part += exp2f((ci.z - zmax) * c);
+            if (nucleus) {
+              srt_z[rank] = ci.z;
+              srt_i[rank] = ci.idx;
+            }
+          }
+          if (rank == (unsigned)k - 1u) thr_key = Elem<T>::key(ci.z), thr_idx = ci.idx;
+        }
+      }
+      __syncthreads();
+      st.key_k = thr_key;
+      st.idx_k = thr_idx;
+      st.S = block_sum_f<NT>(part, sh_d);
+      if (nucleus) {
+        // top-p within the top-k distribution: the first rank whose cumulative mass (rank
+        // order, float pairs) reaches top_p of the total becomes the cut (its key and
+        // index; its cumulative mass the kept sum).  A cut within 1e-6 of top_p, in
+        // probability units, is reported as a near tie of the row.
+        __shared__ F2 s_wtot[NT / 32];
+        __shared__ int s_cut;
+        __shared__ float s_cut_S;
+        __shared__ unsigned s_cut_near;
+        const int lane = tid & 31, warp = tid >> 5;
+        const int r0 = 4 * tid;
+        F2 loc[4];
+        F2 tsum = f2(0.f);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = r0 + q;
+          tsum = f2_add(tsum, r < k ? exp2f((srt_z[r] - zmax) * c) : 0.f);
+          loc[q] = tsum;
+        }
+        F2 incl = tsum;
+#pragma unroll 1
+        for (int o = 1; o < 32; o <<= 1) {
+          const F2 y = shfl_up_f2(incl, o);
+          if (lane >= o) incl = f2_add(incl, y);
+        }
+        if (lane == 31) s_wtot[warp] = incl;
+        if (tid == 0) s_cut = k - 1, s_cut_S = st.S, s_cut_near = 0u;
+        __syncthreads();
+        F2 wbase = f2(0.f), tot = f2(0.f);
+        for (int w2 = 0; w2 < NT / 32; ++w2) {
+          if (w2 < warp) wbase = f2_add(wbase, s_wtot[w2]);
+          tot = f2_add(tot, s_wtot[w2]);
+        }
+        const F2 tbase = f2_add(wbase, f2_sub(incl, tsum));
+        const double Sk = (double)tot.hi + (double)tot.lo;
+        const double target = (double)p.top_p * Sk, tol = 1e-6 * Sk;
+        double prev = (double)tbase.hi + (double)tbase.lo;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = r0 + q;
+          if (r >= k) break;
+          const F2 cf = f2_add(tbase, loc[q]);
+          const double cur = (double)cf.hi + (double)cf.lo;
+          if (cur >= target && prev < target) {
+            s_cut = r;
+            s_cut_S = (float)cur;
+            s_cut_near = (cur - target < tol || (r > 0 && target - prev < tol)) ? 1u : 0u;
+          }
+          prev = cur;
+        }
+        __syncthreads();
+        const int m = s_cut;
+        st.key_k = Elem<T>::key(srt_z[m]);
+        st.idx_k = srt_i[m];
+        st.S = s_cut_S;
+        st.flags |= s_cut_near;
+      }
     }
   }
 
@@ -851,6 +927,13 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
   // them here, before the warp-wide work that follows.  (Left diverged, later full-warp
   // shuffles were measured to cost several hundred cycles each.)
   __syncwarp();
+  // a row of this sequence whose top-p cut was a near tie counts as one near tie
+  int nuc = 0;
+  if (!GREEDY && p.top_p < 1.f) {
+    if (tid < N) nuc = (int)(__ldcg(&tstat[tid].flags) & 1u);
+    else if (logits && tid < N + p.Dq) nuc = (int)(__ldcg(&qstat[tid - N].flags) & 1u);
+  }
+  const int nuc_near = __syncthreads_or(nuc) ? 1 : 0;
 
   // decisions, one thread per non-root node: accept iff u_acc < p(x)/q(x).  The ratio
   // and u are formed in float; when the ratio falls within kDecideMargin (relative) of u
@@ -1421,7 +1504,7 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
     tk[depth] = s_tok;
     p.out_num_emitted[b] = depth + 1;
     p.out_num_accepted[b] = depth;
-    if (p.out_near_ties) p.out_near_ties[b] = (uint32_t)(s_nd + s_snear);
+    if (p.out_near_ties) p.out_near_ties[b] = (uint32_t)(s_nd + s_snear + nuc_near);
     if (p.commit && commit_L >= 0) p.cm.prefix_len[b] = commit_L + commit_count;
   }
 }

@@ -259,7 +259,7 @@ namespace {
 
 sv_status accept_common(sv_mode mode, sv_dtype dt, int B, int V, const void *target,
                         const void *q, sv_q_kind q_kind, float temperature, int top_k,
-                        int32_t *out_tokens, int32_t *out_num_emitted,
+                        float top_p, int32_t *out_tokens, int32_t *out_num_emitted,
                         int32_t *out_num_accepted, bool *greedy) {
   if (mode != SV_GREEDY && mode != SV_EXACT) return fail(SV_ERR_INVALID_ARG, "mode %d", (int)mode);
   if (dt != SV_F32 && dt != SV_BF16) return fail(SV_ERR_UNSUPPORTED, "logit dtype %d", (int)dt);
@@ -269,7 +269,11 @@ sv_status accept_common(sv_mode mode, sv_dtype dt, int B, int V, const void *tar
     return fail(SV_ERR_INVALID_ARG, "temperature must be finite and >= 0");
   if (top_k < 0 || top_k > SV_MAX_TOP_K)
     return fail(SV_ERR_INVALID_ARG, "top_k = %d (0..%d)", top_k, SV_MAX_TOP_K);
+  if (!(top_p > 0.f && top_p <= 1.f))
+    return fail(SV_ERR_INVALID_ARG, "top_p must lie in (0, 1]");
   *greedy = mode == SV_GREEDY || temperature == 0.f;
+  if (!*greedy && top_p < 1.f && !(top_k > 0 && top_k < V))
+    return fail(SV_ERR_UNSUPPORTED, "top_p < 1 is applied within top-k: needs 0 < top_k < V");
   if (!target) return fail(SV_ERR_INVALID_ARG, "target_logits is NULL");
   if (!aligned16(target)) return fail(SV_ERR_INVALID_ARG, "target_logits not 16-byte aligned");
   if (!*greedy) {
@@ -294,6 +298,7 @@ sv_status accept_launch(sv_dtype dt, sv::AcceptParams &p, bool greedy, void *wor
   p.mode = greedy ? SV_GREEDY : SV_EXACT;
   p.c_log2 = greedy ? 0.f : (float)(1.4426950408889634 / (double)p.temperature);
   if (p.top_k >= p.V) p.top_k = 0;
+  if (greedy) p.top_p = 1.f;
   p.stats = static_cast<sv::RowStat *>(workspace);
   if (p.B == 0) return SV_OK;
   cudaError_t e = sv::launch_accept(dt, p, num_sms(), static_cast<cudaStream_t>(stream));
@@ -308,12 +313,12 @@ namespace {
 
 sv_status chain_params(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
                        const void *target_logits, const void *q, sv_q_kind q_kind,
-                       const int32_t *draft_tokens, float temperature, int top_k, uint64_t seed,
+                       const int32_t *draft_tokens, float temperature, int top_k, float top_p, uint64_t seed,
                        uint64_t round, int32_t *out_tokens, int32_t *out_num_emitted,
                        int32_t *out_num_accepted, uint32_t *out_near_ties, sv::AcceptParams &p,
                        bool *greedy) {
   sv_status st = accept_common(mode, logit_dt, B, V, target_logits, q, q_kind, temperature, top_k,
-                               out_tokens, out_num_emitted, out_num_accepted, greedy);
+                               top_p, out_tokens, out_num_emitted, out_num_accepted, greedy);
   if (st != SV_OK) return st;
   if (gamma < 1 || gamma >= SV_MAX_TREE_NODES)
     return fail(SV_ERR_UNSUPPORTED, "gamma = %d (supported 1..%d)", gamma, SV_MAX_TREE_NODES - 1);
@@ -334,6 +339,7 @@ sv_status chain_params(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
   p.tok_offset = 1;
   p.temperature = temperature;
   p.top_k = top_k;
+  p.top_p = top_p;
   p.seed = seed;
   p.round = round;
   p.out_path_nodes = nullptr;
@@ -346,12 +352,12 @@ sv_status chain_params(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
 
 sv_status tree_params(sv_mode mode, sv_dtype logit_dt, int B, int N, int V, const int32_t *parent,
                       const int32_t *node_tokens, const void *target_logits, const void *q,
-                      sv_q_kind q_kind, int Dq, float temperature, int top_k, uint64_t seed,
+                      sv_q_kind q_kind, int Dq, float temperature, int top_k, float top_p, uint64_t seed,
                       uint64_t round, int32_t *out_path_nodes, int32_t *out_tokens,
                       int32_t *out_num_emitted, int32_t *out_num_accepted,
                       uint32_t *out_near_ties, sv::AcceptParams &p, bool *greedy) {
   sv_status st = accept_common(mode, logit_dt, B, V, target_logits, q, q_kind, temperature, top_k,
-                               out_tokens, out_num_emitted, out_num_accepted, greedy);
+                               top_p, out_tokens, out_num_emitted, out_num_accepted, greedy);
   if (st != SV_OK) return st;
   p = sv::AcceptParams{};
   if ((st = make_tree(N, parent, &p.tree)) != SV_OK) return st;
@@ -372,6 +378,7 @@ sv_status tree_params(sv_mode mode, sv_dtype logit_dt, int B, int N, int V, cons
   p.tok_offset = 0;
   p.temperature = temperature;
   p.top_k = top_k;
+  p.top_p = top_p;
   p.seed = seed;
   p.round = round;
   p.out_path_nodes = out_path_nodes;
@@ -421,7 +428,7 @@ sv_status commit_params(sv_dtype dt, int B, int N, int Hkv, int D, const void *k
 
 sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
                           const void *target_logits, const void *q, sv_q_kind q_kind,
-                          const int32_t *draft_tokens, float temperature, int top_k,
+                          const int32_t *draft_tokens, float temperature, int top_k, float top_p,
                           uint64_t seed, uint64_t round, int32_t *out_tokens,
                           int32_t *out_num_emitted, int32_t *out_num_accepted,
                           uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
@@ -429,7 +436,7 @@ sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int
   sv::AcceptParams p;
   bool greedy = false;
   sv_status st = chain_params(mode, logit_dt, B, gamma, V, target_logits, q, q_kind, draft_tokens,
-                              temperature, top_k, seed, round, out_tokens, out_num_emitted,
+                              temperature, top_k, top_p, seed, round, out_tokens, out_num_emitted,
                               out_num_accepted, out_near_ties, p, &greedy);
   if (st != SV_OK) return st;
   return accept_launch(logit_dt, p, greedy, workspace, workspace_bytes, stream);
@@ -438,7 +445,7 @@ sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int
 sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
                          const int32_t *parent, const int32_t *node_tokens,
                          const void *target_logits, const void *q, sv_q_kind q_kind, int Dq,
-                         float temperature, int top_k, uint64_t seed, uint64_t round,
+                         float temperature, int top_k, float top_p, uint64_t seed, uint64_t round,
                          int32_t *out_path_nodes, int32_t *out_tokens,
                          int32_t *out_num_emitted, int32_t *out_num_accepted,
                          uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
@@ -446,7 +453,7 @@ sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
   sv::AcceptParams p;
   bool greedy = false;
   sv_status st = tree_params(mode, logit_dt, B, N, V, parent, node_tokens, target_logits, q,
-                             q_kind, Dq, temperature, top_k, seed, round, out_path_nodes,
+                             q_kind, Dq, temperature, top_k, top_p, seed, round, out_path_nodes,
                              out_tokens, out_num_emitted, out_num_accepted, out_near_ties, p,
                              &greedy);
   if (st != SV_OK) return st;
@@ -455,7 +462,7 @@ sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
 
 sv_status sv_accept_chain_commit(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
                                  const void *target_logits, const void *q, sv_q_kind q_kind,
-                                 const int32_t *draft_tokens, float temperature, int top_k,
+                                 const int32_t *draft_tokens, float temperature, int top_k, float top_p,
                                  uint64_t seed, uint64_t round, sv_dtype kv_dt, int Hkv, int D,
                                  const void *k_tree, const void *v_tree, sv_kv_cache cache,
                                  int32_t *out_tokens, int32_t *out_num_emitted,
@@ -464,7 +471,7 @@ sv_status sv_accept_chain_commit(sv_mode mode, sv_dtype logit_dt, int B, int gam
   sv::AcceptParams p;
   bool greedy = false;
   sv_status st = chain_params(mode, logit_dt, B, gamma, V, target_logits, q, q_kind, draft_tokens,
-                              temperature, top_k, seed, round, out_tokens, out_num_emitted,
+                              temperature, top_k, top_p, seed, round, out_tokens, out_num_emitted,
                               out_num_accepted, out_near_ties, p, &greedy);
   if (st != SV_OK) return st;
   if ((st = commit_params(kv_dt, B, gamma + 1, Hkv, D, k_tree, v_tree, cache, p.cm)) != SV_OK)
@@ -476,7 +483,7 @@ sv_status sv_accept_chain_commit(sv_mode mode, sv_dtype logit_dt, int B, int gam
 sv_status sv_accept_tree_commit(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
                                 const int32_t *parent, const int32_t *node_tokens,
                                 const void *target_logits, const void *q, sv_q_kind q_kind,
-                                int Dq, float temperature, int top_k, uint64_t seed,
+                                int Dq, float temperature, int top_k, float top_p, uint64_t seed,
                                 uint64_t round, sv_dtype kv_dt, int Hkv, int D,
                                 const void *k_tree, const void *v_tree, sv_kv_cache cache,
                                 int32_t *out_path_nodes, int32_t *out_tokens,
@@ -486,7 +493,7 @@ sv_status sv_accept_tree_commit(sv_mode mode, sv_dtype logit_dt, int B, int N, i
   sv::AcceptParams p;
   bool greedy = false;
   sv_status st = tree_params(mode, logit_dt, B, N, V, parent, node_tokens, target_logits, q,
-                             q_kind, Dq, temperature, top_k, seed, round, out_path_nodes,
+                             q_kind, Dq, temperature, top_k, top_p, seed, round, out_path_nodes,
                              out_tokens, out_num_emitted, out_num_accepted, out_near_ties, p,
                              &greedy);
   if (st != SV_OK) return st;
@@ -558,7 +565,7 @@ extern "C" {
 sv_status sv_accept_tree_noalloc(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
                                  const int32_t *parent, const int32_t *node_tokens,
                                  const void *target_logits, const void *q, sv_q_kind q_kind,
-                                 int Dq, float temperature, int top_k, uint64_t seed,
+                                 int Dq, float temperature, int top_k, float top_p, uint64_t seed,
                                  uint64_t round, int32_t *out_path_nodes, int32_t *out_tokens,
                                  int32_t *out_num_emitted, int32_t *out_num_accepted,
                                  uint32_t *out_near_ties, void *stream) {
@@ -573,7 +580,7 @@ sv_status sv_accept_tree_noalloc(sv_mode mode, sv_dtype logit_dt, int B, int N, 
   void *scratch = noalloc_rows_address(&st);
   if (!scratch) return st;
   return sv_accept_tree(mode, logit_dt, B, N, V, parent, node_tokens, target_logits, q, q_kind,
-                        Dq, temperature, top_k, seed, round, out_path_nodes, out_tokens,
+                        Dq, temperature, top_k, top_p, seed, round, out_path_nodes, out_tokens,
                         out_num_emitted, out_num_accepted, out_near_ties, scratch,
                         sizeof(g_sv_noalloc_rows), stream);
 }

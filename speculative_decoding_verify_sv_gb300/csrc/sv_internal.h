@@ -90,6 +90,7 @@ struct RowStat {
   uint32_t key_k; // top-k threshold key (kept: key > key_k, or == key_k and idx <= idx_k)
   int32_t idx_k;
   float S;        // sum over kept entries of exp((z - zmax) / T)
+  uint32_t flags; // bit 0: the top-p cut lies within 1e-6 of top_p (a near tie)
 };
 
 // ------------------------------------------------------------------- commit
@@ -118,6 +119,7 @@ struct AcceptParams {
   float temperature;
   float c_log2;              // log2(e) / T
   int top_k;                 // 0 = off
+  float top_p;               // 1 = off; < 1 only with top-k (the nucleus of its distribution)
   int ring_stages;           // stages of the select kernel's ring (set at its launch)
   uint64_t seed, round;
   RowStat *stats;            // [B*N + B*Dq]

@@ -38,13 +38,14 @@ class VerifyStep:
     def __init__(self, parent: Sequence[int], B: int, Hq: int, Hkv: int, D: int, V: int,
                  cache: KVCache, dtype=torch.bfloat16, mode=EXACT, q_kind=Q_LOGITS,
                  temperature: float = 1.0, top_k: int = 0, chain: bool = False,
-                 device: Optional[torch.device] = None):
+                 device: Optional[torch.device] = None, top_p: float = 1.0):
         self.parent = list(parent)
         self.N = len(self.parent)
         self.Dmax = max(_depths(self.parent))
         self.B, self.Hq, self.Hkv, self.D, self.V = B, Hq, Hkv, D, V
         self.cache, self.dtype, self.mode, self.q_kind = cache, dtype, mode, q_kind
         self.temperature, self.top_k, self.chain = temperature, top_k, chain
+        self.top_p = top_p
         self.device = device or cache.k.device
         self.scale = D ** -0.5
         ws = sv_tree_attention_workspace_size(dtype, B, self.N, Hq, Hkv, D, cache.max_prefix)
@@ -83,13 +84,13 @@ class VerifyStep:
             toks = node_tokens[:, 1:] if node_tokens.shape[1] == self.N else node_tokens
             r = sv_accept_chain(self.mode, target_logits, q_draft, self.q_kind,
                                 toks.contiguous() if not toks.is_contiguous() else toks,
-                                temperature=self.temperature, top_k=self.top_k, seed=seed,
+                                temperature=self.temperature, top_k=self.top_k, top_p=self.top_p, seed=seed,
                                 round_=round_, outs=self.outs, workspace=self.acc_ws,
                                 stream=stream)
             # a chain's accepted path is nodes 0..num_accepted
             return r
         return sv_accept_tree(self.mode, target_logits, q_draft, self.q_kind, self.parent,
-                              node_tokens, temperature=self.temperature, top_k=self.top_k,
+                              node_tokens, temperature=self.temperature, top_k=self.top_k, top_p=self.top_p,
                               seed=seed, round_=round_, outs=self.outs, workspace=self.acc_ws,
                               stream=stream)
 
@@ -105,11 +106,11 @@ class VerifyStep:
             return sv_accept_chain_commit(
                 self.mode, target_logits, q_draft, self.q_kind,
                 toks.contiguous() if not toks.is_contiguous() else toks, k_tree, v_tree,
-                self.cache, temperature=self.temperature, top_k=self.top_k, seed=seed,
+                self.cache, temperature=self.temperature, top_k=self.top_k, top_p=self.top_p, seed=seed,
                 round_=round_, outs=self.outs, workspace=self.acc_ws, stream=stream)
         return sv_accept_tree_commit(self.mode, target_logits, q_draft, self.q_kind, self.parent,
                                      node_tokens, k_tree, v_tree, self.cache,
-                                     temperature=self.temperature, top_k=self.top_k, seed=seed,
+                                     temperature=self.temperature, top_k=self.top_k, top_p=self.top_p, seed=seed,
                                      round_=round_, outs=self.outs, workspace=self.acc_ws,
                                      stream=stream)
 

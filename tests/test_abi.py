@@ -94,23 +94,30 @@ def test_accept_rejects_before_launch(lib):
     par = (ctypes.c_int32 * 3)(-1, 0, 0)
     common = dict(seed=0, round=0)
     # V not a multiple of 8
-    assert lib.sv_accept_chain(1, 1, 1, 4, 1001, P, P, 1, P, 1.0, 0, 0, 0, P, P, P, P, P, 1 << 20,
+    assert lib.sv_accept_chain(1, 1, 1, 4, 1001, P, P, 1, P, 1.0, 0, 1.0, 0, 0, P, P, P, P, P, 1 << 20,
                                None) == sv.SV_ERR_UNSUPPORTED
     # negative temperature, top_k too large
-    assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, P, 1, P, -1.0, 0, 0, 0, P, P, P, P, P, 1 << 20,
+    assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, P, 1, P, -1.0, 0, 1.0, 0, 0, P, P, P, P, P, 1 << 20,
                                None) == sv.SV_ERR_INVALID_ARG
-    assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, P, 1, P, 1.0, 5000, 0, 0, P, P, P, P, P,
+    assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, P, 1, P, 1.0, 5000, 1.0, 0, 0, P, P, P, P, P,
                                1 << 20, None) == sv.SV_ERR_INVALID_ARG
     # exact mode needs q
-    assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, None, 1, P, 1.0, 0, 0, 0, P, P, P, P, P,
+    assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, None, 1, P, 1.0, 0, 1.0, 0, 0, P, P, P, P, P,
                                1 << 20, None) == sv.SV_ERR_INVALID_ARG
     # q rows must cover the tree depth
-    assert lib.sv_accept_tree(1, 1, 1, 3, 1000, par, P, P, P, 1, 0, 1.0, 0, 0, 0, P, P, P, P, P,
+    assert lib.sv_accept_tree(1, 1, 1, 3, 1000, par, P, P, P, 1, 0, 1.0, 0, 1.0, 0, 0, P, P, P, P, P,
                               P, 1 << 20, None) == sv.SV_ERR_INVALID_ARG
+    # top_p outside (0, 1]; top_p < 1 without top-k in exact mode
+    assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, P, 1, P, 1.0, 5, 0.0, 0, 0, P, P, P, P, P,
+                               1 << 20, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, P, 1, P, 1.0, 5, 1.5, 0, 0, P, P, P, P, P,
+                               1 << 20, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, P, 1, P, 1.0, 0, 0.9, 0, 0, P, P, P, P, P,
+                               1 << 20, None) == sv.SV_ERR_UNSUPPORTED
     # workspace too small
     need = lib.sv_accept_workspace_size(2, 3, 1000, 1)
     assert need > 0
-    assert lib.sv_accept_tree(1, 1, 2, 3, 1000, par, P, P, P, 1, 1, 1.0, 0, 0, 0, P, P, P, P, P,
+    assert lib.sv_accept_tree(1, 1, 2, 3, 1000, par, P, P, P, 1, 1, 1.0, 0, 1.0, 0, 0, P, P, P, P, P,
                               P, 16, None) == sv.SV_ERR_WORKSPACE
     del common
 
@@ -126,16 +133,16 @@ def test_fused_accept_commit_rejects_before_launch(lib):
     P = ctypes.c_void_p(16)
     par = (ctypes.c_int32 * 3)(-1, 0, 0)
     # a bad acceptance argument (V not a multiple of 8) is reported as by sv_accept_tree
-    assert lib.sv_accept_tree_commit(1, 1, 1, 3, 1001, par, P, P, P, 1, 2, 1.0, 0, 0, 0,
+    assert lib.sv_accept_tree_commit(1, 1, 1, 3, 1001, par, P, P, P, 1, 2, 1.0, 0, 1.0, 0, 0,
                                      1, 4, 128, P, P, _cache(), P, P, P, P, P, P, 1 << 20,
                                      None) == sv.SV_ERR_UNSUPPORTED
     # a bad commit argument (missing tree V) is reported as by sv_commit_kv
-    assert lib.sv_accept_tree_commit(1, 1, 1, 3, 1000, par, P, P, P, 1, 2, 1.0, 0, 0, 0,
+    assert lib.sv_accept_tree_commit(1, 1, 1, 3, 1000, par, P, P, P, 1, 2, 1.0, 0, 1.0, 0, 0,
                                      1, 4, 128, P, None, _cache(), P, P, P, P, P, P, 1 << 20,
                                      None) == sv.SV_ERR_INVALID_ARG
     assert "v_tree" in lib.sv_last_error().decode()
     # rows must be whole 16-byte vectors
-    assert lib.sv_accept_chain_commit(1, 1, 1, 2, 1000, P, P, 1, P, 1.0, 0, 0, 0,
+    assert lib.sv_accept_chain_commit(1, 1, 1, 2, 1000, P, P, 1, P, 1.0, 0, 1.0, 0, 0,
                                       1, 1, 3, P, P, _cache(), P, P, P, P, P, 1 << 20,
                                       None) == sv.SV_ERR_UNSUPPORTED
 

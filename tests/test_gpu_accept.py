@@ -39,16 +39,17 @@ def _compare(gpu, ref, keys, max_exempt_frac=0.01):
     return n_ex
 
 
-def _chain(mode, lg, q_kind=sv.Q_LOGITS, T=1.0, top_k=0, seed=3, rnd=1, q=None):
+def _chain(mode, lg, q_kind=sv.Q_LOGITS, T=1.0, top_k=0, seed=3, rnd=1, q=None, top_p=1.0):
     dev = torch.device("cuda")
     tl = lg["target_logits"].to(dev)
     qq = (lg["draft_logits"] if q is None else q)
     qq = None if mode == sv.GREEDY and q is None else qq.to(dev)
     out = sv.sv_accept_chain(mode, tl, qq, q_kind, lg["draft_tokens"].to(dev), temperature=T,
-                             top_k=top_k, seed=seed, round_=rnd)
+                             top_k=top_k, seed=seed, round_=rnd, top_p=top_p)
     torch.cuda.synchronize()
     ref = oracle.accept_chain(mode, lg["target_logits"], None if qq is None else qq.cpu(), q_kind,
-                              lg["draft_tokens"], temperature=T, top_k=top_k, seed=seed, round_=rnd)
+                              lg["draft_tokens"], temperature=T, top_k=top_k, seed=seed, round_=rnd,
+                              top_p=top_p)
     return out, ref
 
 
@@ -123,6 +124,50 @@ def test_select_ring_layouts(cuda_ok, dtype, V, B, q_probs):
     else:
         out, ref = _chain(sv.EXACT, lg, seed=8, rnd=5)
     _compare(out, ref, ["tokens", "num_emitted", "num_accepted"], max_exempt_frac=0.15)
+    assert sv.sv_read_device_status() == 0
+
+
+@pytest.mark.parametrize("V,B", [(4000, 96), (128256, 24)])
+def test_chain_top_p(cuda_ok, V, B):
+    """Top-k 50 then top-p 0.9 at T = 0.7 on p and q (the drafter samples within its own
+    nucleus): tokens and counts equal the oracle's."""
+    lg = wl.chain_logits(B, 5, V, sigma=3.0, draft_sigma=1.0, dtype=torch.bfloat16,
+                         temperature=0.7, top_k=50, top_p=0.9, seed=18)
+    out, ref = _chain(sv.EXACT, lg, T=0.7, top_k=50, seed=6, rnd=3, top_p=0.9)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"])
+    assert sv.sv_read_device_status() == 0
+
+
+def test_tree_top_p(cuda_ok):
+    B = 64
+    par = wl.TREE_T26
+    lg = wl.medusa_logits(B, par, 2000, sigma=3.0, seed=19, coverage=True, coverage_sigma=0.7)
+    dev = torch.device("cuda")
+    out = sv.sv_accept_tree(sv.EXACT, lg["target_logits"].to(dev), lg["draft_logits"].to(dev),
+                            sv.Q_LOGITS, par, lg["node_tokens"].to(dev), top_k=20, top_p=0.8,
+                            seed=23, round_=1)
+    torch.cuda.synchronize()
+    ref = oracle.accept_tree(oracle.EXACT, lg["target_logits"], lg["draft_logits"], oracle.Q_LOGITS,
+                             par, lg["node_tokens"], top_k=20, top_p=0.8, seed=23, round_=1)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted", "path_nodes"], max_exempt_frac=0.05)
+    # node tokens are the heads' ranked tokens: a nucleus narrower than the tree's caps
+    # leaves some with q(x) = 0, which is reported (and read, which clears the word)
+    assert sv.sv_read_device_status() & ~sv.SV_DEV_ZERO_DRAFT_PROB == 0
+
+
+def test_top_p_after_tie_fallback(cuda_ok):
+    """Every logit equal: the top-7 set is the 7 lowest ids (the counting path), and its
+    nucleus at top_p = 0.5 is the 4 lowest (3/7 < 0.5 <= 4/7)."""
+    B, gamma, V, k = 4, 3, 8192, 7
+    tl = torch.zeros((B, gamma + 1, V), dtype=torch.bfloat16)
+    ql = torch.zeros((B, gamma, V), dtype=torch.bfloat16)
+    toks = torch.tensor([[0, 3, 2], [1, 2, 0], [3, 1, 1], [2, 0, 3]], dtype=torch.int32)
+    lg = dict(target_logits=tl, draft_logits=ql, draft_tokens=toks)
+    sv.sv_read_device_status()  # start from a clear status word
+    out, ref = _chain(sv.EXACT, lg, T=1.0, top_k=k, seed=2, top_p=0.5)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"], max_exempt_frac=1.0)
+    t = out["tokens"].cpu()
+    assert torch.all(t[t >= 0] < 4)
     assert sv.sv_read_device_status() == 0
 
 
