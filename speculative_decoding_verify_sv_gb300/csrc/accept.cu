@@ -4,22 +4,24 @@
 // qwbw.cn section 2.3): a draft x checked against target row p and draft row q is
 // accepted iff u_acc < p(x)/q(x); at the first rejection the next token is drawn from
 // norm([p - q]+); if every draft passes, a bonus token is drawn from the target's next
-// row; p and q are the effective distributions (temperature, top-k).  Greedy accepts
-// while the draft is the target's argmax.  For a tree every node is decided against
-// its parent's row and the q row of its depth; the deepest node whose root path is all
-// accepted is kept.
+// row; p and q are the effective distributions (temperature, top-k, then top-p within
+// the top k).  Greedy accepts while the draft is the target's argmax.  For a tree every
+// node is decided against its parent's row and the q row of its depth; the deepest node
+// whose root path is all accepted is kept.
 //
 // Kernel 1 (one CTA per logit row, target rows then q rows): one coalesced pass of
 // 16-byte loads gives the row max / argmax and, without top-k, the softmax sum by a
-// per-thread online accumulation.  With top-k, a second pass gathers the few entries
-// that can be in the top k (those at or above the smallest of k disjoint group
-// maxima) into shared memory, ranks them, and sums the kept ones.
-// Kernel 2 (one cluster of CTAs per sequence): per-node ratios in double from the row
-// statistics and the two logits of the candidate, the longest accepted path, and the
-// final sample: a coalesced pass summing w = [p - q]+ (or p) per warp segment of each
-// CTA's slice of the vocabulary, slice totals exchanged through distributed shared
-// memory, then the owning warp re-walks its segment with a warp scan to find the
-// inverse-CDF token.
+// per-thread online accumulation.  With top-k, the pass also keeps packed unit maxima
+// and one key per batch of loads; the batches that can hold an entry of the top k (a
+// maximum at or above the smallest of k group maxima) are re-read as one list, their
+// candidates ranked and the kept ones summed; top-p cuts the ranked list by cumulative
+// mass.
+// Kernel 2 (one cluster of CTAs per sequence): per-node ratios from the row statistics
+// and the two logits of the candidate, the longest accepted path, and the final sample:
+// a pass summing w = [p - q]+ (or p) per chunk of 32 vectors over each CTA's slice of
+// the vocabulary (long slices streamed through a shared-memory ring of bulk copies),
+// slice totals exchanged through distributed shared memory, then one warp of the CTA
+// whose slice holds the target finds the chunk and, in it, the inverse-CDF token.
 #include <algorithm>
 #include <cfloat>
 #include <climits>
