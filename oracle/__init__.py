@@ -65,6 +65,7 @@ def _load():
                                              P, P, P, P, P]
             lib.orc_accept_chain.restype = I
             lib.orc_commit_kv.argtypes = [I, I, I, I, I, P, P, P, I, P, P, P, P, P, I, I, I]
+            lib.orc_ngram_draft.argtypes = [I, I, P, P, I, I, I, P, P]
             lib.orc_set_threads.argtypes = [I]
             lib.orc_get_threads.restype = I
             _lib = lib
@@ -271,3 +272,17 @@ def commit_kv(k_tree, v_tree, path_nodes, num_accepted, cache_k, cache_v, prefix
                           _ptr(na), _ptr(ck), _ptr(cv), _ptr(pl), _ptr(bt), max_blocks,
                           block_size, Lmax)
     return ck, cv, pl
+
+
+# ------------------------------------------------------------ n-gram drafts
+
+def ngram_draft(history, length, max_n=3, min_n=1, gamma=4):
+    """Prompt-lookup drafts (see oracle.c): returns (drafts [B,gamma] int32, num [B])."""
+    h = _i32(history)
+    ln = _i32(length)
+    B, Lmax = h.shape
+    drafts = torch.full((B, gamma), -1, dtype=torch.int32)
+    num = torch.zeros(B, dtype=torch.int32)
+    _load().orc_ngram_draft(B, Lmax, _ptr(h), _ptr(ln), int(max_n), int(min_n), int(gamma),
+                            _ptr(drafts), _ptr(num))
+    return drafts, num

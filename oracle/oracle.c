@@ -647,3 +647,45 @@ void orc_commit_kv(int dtype, int B, int N, int Hkv, int D, const void *k_tree,
     prefix_len[b] = L + num_accepted[b] + 1;
   }
 }
+
+/* ------------------------------------------------------ n-gram (prompt lookup) drafts */
+
+/* Prompt-lookup drafting ("投机解码的五条路线" (jennyma11 blog), section "Prompt Lookup /
+ * N-gram"): take the last n tokens of the history, find the same n tokens earlier in
+ * it, and propose the tokens that follow that earlier occurrence.  Readings: n runs
+ * from max_n down to min_n and the first n with a match wins; among matches the most
+ * recent one (largest start j) is taken; a match must end before the last token so that
+ * at least one token follows it; the drafts are the up to gamma tokens after the match
+ * (fewer when the history ends), unused slots -1.  history [B,Lmax]; length [B] (clamped
+ * to [0, Lmax]); out_drafts [B,gamma]; out_num [B] (0 when nothing matches). */
+void orc_ngram_draft(int B, int Lmax, const int32_t *history, const int32_t *length, int max_n,
+                     int min_n, int gamma, int32_t *out_drafts, int32_t *out_num) {
+  for (int b = 0; b < B; ++b) {
+    const int32_t *h = history + (size_t)b * Lmax;
+    int L = length[b];
+    if (L < 0) L = 0;
+    if (L > Lmax) L = Lmax;
+    int32_t *d = out_drafts + (size_t)b * gamma;
+    for (int i = 0; i < gamma; ++i) d[i] = -1;
+    out_num[b] = 0;
+    for (int n = max_n; n >= min_n; --n) {
+      if (n < 1 || L < n + 1) continue;
+      int found = -1;
+      for (int j = L - n - 1; j >= 0 && found < 0; --j) {
+        int same = 1;
+        for (int t = 0; t < n; ++t)
+          if (h[j + t] != h[L - n + t]) {
+            same = 0;
+            break;
+          }
+        if (same) found = j;
+      }
+      if (found >= 0) {
+        int cnt = 0;
+        for (int i = 0; i < gamma && found + n + i < L; ++i) d[cnt++] = h[found + n + i];
+        out_num[b] = cnt;
+        break;
+      }
+    }
+  }
+}
