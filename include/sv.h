@@ -196,6 +196,24 @@ sv_status sv_accept_tree_noalloc(sv_mode mode, sv_dtype logit_dt, int B, int N, 
                                  int32_t *out_num_emitted, int32_t *out_num_accepted,
                                  uint32_t *out_near_ties, void *stream);
 
+/* --------------------------------------------------------------- n-gram drafts */
+
+/* Prompt-lookup (n-gram) drafting ("投机解码的五条路线" (jennyma11 blog), section "Prompt
+ * Lookup / N-gram"): take the last n tokens of a sequence's history, find the same n
+ * tokens earlier in it, and propose the tokens that follow that occurrence; the drafts
+ * still go to the target's verification (sv_accept_chain) like any other.  For n from
+ * max_ngram down to min_ngram the first n with a match wins; among its matches the most
+ * recent (largest start) is taken; a match must end before the last token; up to gamma
+ * tokens follow it (fewer when the history ends).
+ * history [B,Lmax] int32 (device); length [B] int32 (device; a value outside [0, Lmax]
+ * is clamped and sets SV_DEV_BAD_PREFIX).  1 <= min_ngram <= max_ngram <= SV_MAX_NGRAM,
+ * 1 <= gamma <= 63.  Outputs: out_drafts [B,gamma] (-1 after the proposed tokens) and
+ * out_num_drafts [B] (0 when nothing matches).  No workspace. */
+#define SV_MAX_NGRAM 32
+sv_status sv_ngram_draft(int B, int Lmax, const int32_t *history, const int32_t *length,
+                         int max_ngram, int min_ngram, int gamma, int32_t *out_drafts,
+                         int32_t *out_num_drafts, void *stream);
+
 /* --------------------------------------------------------------------- commit */
 
 /* KV commit (qwbw.cn sections 3.1.4 and 6.3; hncyxsy.com section 4.3: keep the KV of

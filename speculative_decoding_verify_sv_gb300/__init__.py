@@ -20,7 +20,7 @@ __all__ = [
     "SVError", "KVCache", "library_path", "load_library", "sv_tree_attention",
     "sv_tree_attention_workspace_size", "sv_tree_attention_path", "sv_accept_chain", "sv_accept_tree",
     "sv_accept_workspace_size", "sv_accept_tree_noalloc", "sv_commit_kv", "sv_accept_tree_commit",
-    "sv_accept_chain_commit", "sv_tree_prepare", "sv_read_device_status",
+    "sv_accept_chain_commit", "sv_ngram_draft", "sv_tree_prepare", "sv_read_device_status",
     "sv_version", "sv_kernel_launches", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "SV_MAX_TREE_NODES",
 ]
 
@@ -91,12 +91,13 @@ def load_library():
                                                I, I, I, P, P, _KVCacheC, P, P, P, P, P, SZ, P]
         lib.sv_tree_prepare.argtypes = [I, P, P, P]
         lib.sv_read_device_status.argtypes = [P, P]
+        lib.sv_ngram_draft.argtypes = [I, I, P, P, I, I, I, P, P, P]
         lib.sv_last_error.restype = ctypes.c_char_p
         lib.sv_version.restype = ctypes.c_char_p
         lib.sv_kernel_launches.restype = ctypes.c_uint64
         for fn in ("sv_tree_attention", "sv_accept_chain", "sv_accept_tree", "sv_commit_kv",
                    "sv_tree_prepare", "sv_read_device_status", "sv_accept_tree_noalloc",
-                   "sv_accept_tree_commit", "sv_accept_chain_commit"):
+                   "sv_accept_tree_commit", "sv_accept_chain_commit", "sv_ngram_draft"):
             getattr(lib, fn).restype = ctypes.c_int32
         _lib = lib
         return lib
@@ -454,3 +455,26 @@ def sv_read_device_status(stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check(lib.sv_read_device_status(ctypes.byref(v), _stream(stream)))
     return int(v.value)
+
+
+def sv_ngram_draft(history, length, max_ngram=3, min_ngram=1, gamma=4, out=None,
+                   stream=None):
+    """Prompt-lookup drafts: history [B,Lmax] int32 and length [B] int32 (CUDA tensors).
+    Returns (drafts [B,gamma] int32, -1 after the proposed tokens; num_drafts [B])."""
+    lib = load_library()
+    _dev(history, "history", torch.int32)
+    if history.dim() != 2:
+        raise ValueError("history must be [B, Lmax]")
+    B, Lmax = history.shape
+    _dev(length, "length", torch.int32, (B,))
+    if out is None:
+        drafts = torch.empty((B, gamma), dtype=torch.int32, device=history.device)
+        num = torch.empty(B, dtype=torch.int32, device=history.device)
+    else:
+        drafts, num = out
+        _dev(drafts, "drafts", torch.int32, (B, gamma))
+        _dev(num, "num_drafts", torch.int32, (B,))
+    _check(lib.sv_ngram_draft(B, Lmax, _ptr(history), _ptr(length), int(max_ngram),
+                              int(min_ngram), int(gamma), _ptr(drafts), _ptr(num),
+                              _stream(stream)))
+    return drafts, num

@@ -502,6 +502,29 @@ sv_status sv_accept_tree_commit(sv_mode mode, sv_dtype logit_dt, int B, int N, i
   return accept_launch(logit_dt, p, greedy, workspace, workspace_bytes, stream);
 }
 
+// --------------------------------------------------------------- n-gram drafts
+
+sv_status sv_ngram_draft(int B, int Lmax, const int32_t *history, const int32_t *length,
+                         int max_ngram, int min_ngram, int gamma, int32_t *out_drafts,
+                         int32_t *out_num_drafts, void *stream) {
+  if (B < 0 || Lmax < 1) return fail(SV_ERR_INVALID_ARG, "B = %d, Lmax = %d", B, Lmax);
+  if (min_ngram < 1 || max_ngram < min_ngram || max_ngram > SV_MAX_NGRAM)
+    return fail(SV_ERR_INVALID_ARG, "n-gram sizes %d..%d (1 <= min <= max <= %d)", min_ngram,
+                max_ngram, SV_MAX_NGRAM);
+  if (gamma < 1 || gamma >= SV_MAX_TREE_NODES)
+    return fail(SV_ERR_UNSUPPORTED, "gamma = %d (supported 1..%d)", gamma, SV_MAX_TREE_NODES - 1);
+  if (!history || !length || !out_drafts || !out_num_drafts)
+    return fail(SV_ERR_INVALID_ARG, "a pointer argument is NULL");
+  sv::NgramParams p{history, length, B, Lmax, max_ngram, min_ngram, gamma, out_drafts,
+                    out_num_drafts, status_word()};
+  if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
+  if (B == 0) return SV_OK;
+  const cudaError_t e = sv::launch_ngram(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "n-gram draft launch");
+  sv::count_launches(1);
+  return SV_OK;
+}
+
 // --------------------------------------------------------------------- commit
 
 sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_tree,

@@ -136,6 +136,18 @@ struct AcceptParams {
 };
 
 size_t accept_ws_bytes(int B, int N, int Dq);
+
+// ------------------------------------------------------------ n-gram drafts
+
+struct NgramParams {
+  const int32_t *history;  // [B,Lmax]
+  const int32_t *length;   // [B]
+  int B, Lmax, max_n, min_n, gamma;
+  int32_t *out_drafts;     // [B,gamma]
+  int32_t *out_num;        // [B]
+  unsigned int *status;
+};
+cudaError_t launch_ngram(const NgramParams &p, cudaStream_t s);
 cudaError_t launch_accept(sv_dtype dt, const AcceptParams &p, int num_sms, cudaStream_t s);
 
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);

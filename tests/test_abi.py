@@ -147,6 +147,17 @@ def test_fused_accept_commit_rejects_before_launch(lib):
                                       None) == sv.SV_ERR_UNSUPPORTED
 
 
+def test_ngram_draft_rejects_before_launch(lib):
+    P = ctypes.c_void_p(16)
+    # n-gram sizes out of order or past the maximum, gamma out of range, null pointers
+    assert lib.sv_ngram_draft(2, 64, P, P, 1, 2, 4, P, P, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.sv_ngram_draft(2, 64, P, P, 33, 1, 4, P, P, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.sv_ngram_draft(2, 64, P, P, 3, 0, 4, P, P, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.sv_ngram_draft(2, 64, P, P, 3, 1, 64, P, P, None) == sv.SV_ERR_UNSUPPORTED
+    assert lib.sv_ngram_draft(2, 64, None, P, 3, 1, 4, P, P, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.sv_ngram_draft(2, 0, P, P, 3, 1, 4, P, P, None) == sv.SV_ERR_INVALID_ARG
+
+
 def test_binding_requires_cuda_tensors(lib):
     import torch
     with pytest.raises(TypeError):
