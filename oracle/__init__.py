@@ -66,6 +66,9 @@ def _load():
             lib.orc_accept_chain.restype = I
             lib.orc_commit_kv.argtypes = [I, I, I, I, I, P, P, P, I, P, P, P, P, P, I, I, I]
             lib.orc_ngram_draft.argtypes = [I, I, P, P, I, I, I, P, P]
+            lib.orc_accept_tree_recursive.argtypes = [I, I, I, I, P, P, P, P, I, I, Dbl, I, Dbl,
+                                                      U64, U64, P, P, P, P, P, P]
+            lib.orc_accept_tree_recursive.restype = I
             lib.orc_set_threads.argtypes = [I]
             lib.orc_get_threads.restype = I
             _lib = lib
@@ -286,3 +289,32 @@ def ngram_draft(history, length, max_n=3, min_n=1, gamma=4):
     _load().orc_ngram_draft(B, Lmax, _ptr(h), _ptr(ln), int(max_n), int(min_n), int(gamma),
                             _ptr(drafts), _ptr(num))
     return drafts, num
+
+
+def accept_tree_recursive(target_logits, q, q_kind, parent, node_tokens, temperature=1.0,
+                          top_k=0, seed=0, round_=0, top_p=1.0):
+    """Exact tree acceptance with siblings tried in rank order (see oracle.c); returns a
+    dict of CPU tensors like accept_tree (no per-node decision outputs)."""
+    tl = _cpu(target_logits)
+    dt = _dtype_code(tl)
+    B, N, V = tl.shape
+    par = _i32(parent)
+    toks = _i32(node_tokens)
+    qq, Dq = _q_args(q, q_kind)
+    W = max(_depths(par.tolist())) + 1
+    out = {
+        "path_nodes": torch.full((B, W), -1, dtype=torch.int32),
+        "tokens": torch.full((B, W), -1, dtype=torch.int32),
+        "num_emitted": torch.zeros(B, dtype=torch.int32),
+        "num_accepted": torch.zeros(B, dtype=torch.int32),
+        "near_ties": torch.zeros(B, dtype=torch.int32),
+        "flags": torch.zeros(B, dtype=torch.int32),
+    }
+    rc = _load().orc_accept_tree_recursive(
+        dt, B, N, V, _ptr(par), _ptr(toks), _ptr(tl), _ptr(qq), q_kind, Dq, float(temperature),
+        int(top_k), float(np.float32(top_p)), int(seed), int(round_), _ptr(out["path_nodes"]),
+        _ptr(out["tokens"]), _ptr(out["num_emitted"]), _ptr(out["num_accepted"]),
+        _ptr(out["near_ties"]), _ptr(out["flags"]))
+    if rc != 0:
+        raise ValueError(f"oracle accept_tree_recursive rejected its arguments (code {rc})")
+    return out

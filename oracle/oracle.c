@@ -689,3 +689,129 @@ void orc_ngram_draft(int B, int Lmax, const int32_t *history, const int32_t *len
     }
   }
 }
+
+/* ------------------------------------ acceptance: tree, siblings tried in rank order */
+
+/* Exact tree acceptance with the siblings of a node tried in turn (the multi-candidate
+ * form of the acceptance rule of hncyxsy.com sections 2.1-2.2: after a rejected
+ * candidate the target distribution becomes the residual norm([p - q]+) for the next
+ * one; the jennyma11 blog, section "Medusa", separates this lossless tree verification
+ * from typical acceptance).  From the root: the children of the current node are tried
+ * in row (rank) order, child c accepted iff u_acc(b, c) < p_cur(x_c) / q_{d+1}(x_c), where
+ * p_cur starts as the node's effective target distribution and after each rejection is
+ * replaced by norm([p_cur - q_{d+1}]+) (kept unchanged, and reported as a near tie, when
+ * that residual has no mass).  An accepted child becomes the current node; when the last
+ * child is rejected the next token is sampled with u_smp(b, node) from the residual of the
+ * last p_cur; a leaf reached draws the bonus from its p.  For drafts sampled independently
+ * from q this keeps the output distributed as p; with one child per node it is the chain
+ * procedure.  Exact mode only (greedy: orc_accept_tree).  Arguments and outputs as
+ * orc_accept_tree (no per-node decision outputs). */
+int orc_accept_tree_recursive(int dtype, int B, int N, int V, const int32_t *parent,
+                              const int32_t *node_tokens, const void *target_logits,
+                              const void *q, int q_kind, int Dq, double T, int top_k,
+                              double top_p, uint64_t seed, uint64_t round,
+                              int32_t *out_path_nodes, int32_t *out_tokens,
+                              int32_t *out_num_emitted, int32_t *out_num_accepted,
+                              uint32_t *out_near_ties, uint32_t *out_flags) {
+  if (orc_check_tree(N, parent)) return 1;
+  if (T == 0.0) return 3;
+  int Dmax = 0;
+  int *depth = (int *)orc_alloc(sizeof(int) * (size_t)N);
+  for (int n = 0; n < N; ++n) {
+    depth[n] = orc_depth(parent, n);
+    if (depth[n] > Dmax) Dmax = depth[n];
+  }
+  if (Dq < Dmax) {
+    free(depth);
+    return 2;
+  }
+  int W = Dmax + 1;
+#pragma omp parallel for schedule(dynamic)
+  for (int b = 0; b < B; ++b) {
+    double *z = (double *)orc_alloc(sizeof(double) * (size_t)V);
+    double *pc = (double *)orc_alloc(sizeof(double) * (size_t)V);
+    double *qd = (double *)orc_alloc(sizeof(double) * (size_t)V);
+    uint32_t near = 0, flags = 0;
+    int nuc_near = 0;
+    int node = 0, tok = -1;
+    for (;;) {
+      int first = -1, last = -1;
+      for (int c = node + 1; c < N; ++c)
+        if (parent[c] == node) {
+          if (first < 0) first = c;
+          last = c;
+        }
+      orc_load_row(target_logits, dtype, (size_t)b * N + node, V, z);
+      orc_effective_dist(z, V, T, top_k, top_p, pc, &nuc_near);
+      double ua, us;
+      orc_uniforms(seed, round, 0u, b, node, &ua, &us);
+      int near_s = 0;
+      if (first < 0) { /* a leaf: the bonus from its p */
+        tok = orc_sample_residual(pc, NULL, V, us, &near_s);
+        near += (uint32_t)near_s;
+        break;
+      }
+      orc_q_row(q, q_kind, dtype, b, Dq, depth[node] + 1, V, T, top_k, top_p, z, qd, &nuc_near);
+      int next = -1;
+      for (int c = first; c <= last; ++c) {
+        if (parent[c] != node) continue;
+        int x = node_tokens[(size_t)b * N + c];
+        int accepted = 0;
+        if (x >= 0 && x < V) {
+          double u_acc, u_smp, r;
+          orc_uniforms(seed, round, 0u, b, c, &u_acc, &u_smp);
+          if (qd[x] > 0.0) {
+            r = pc[x] / qd[x];
+          } else {
+            flags |= 1u;
+            r = pc[x] > 0.0 ? INFINITY : 0.0;
+          }
+          if (fabs(u_acc - r) < ORC_NEAR_TIE) ++near;
+          accepted = (u_acc < r);
+        } else {
+          flags |= 2u;
+        }
+        if (accepted) {
+          next = c;
+          break;
+        }
+        if (c == last) break; /* the residual of this p_cur is sampled below */
+        /* the next sibling sees the residual */
+        double total = 0.0;
+        for (int j = 0; j < V; ++j) total += pc[j] - qd[j] > 0.0 ? pc[j] - qd[j] : 0.0;
+        if (total > 0.0) {
+          for (int j = 0; j < V; ++j) pc[j] = pc[j] - qd[j] > 0.0 ? (pc[j] - qd[j]) / total : 0.0;
+        } else {
+          ++near;
+        }
+      }
+      if (next >= 0) {
+        node = next;
+        continue;
+      }
+      tok = orc_sample_residual(pc, qd, V, us, &near_s);
+      near += (uint32_t)near_s;
+      break;
+    }
+    near += (uint32_t)nuc_near;
+    int D = depth[node];
+    int32_t *pn = out_path_nodes ? out_path_nodes + (size_t)b * W : NULL;
+    int32_t *tk = out_tokens + (size_t)b * W;
+    for (int i = 0; i < W; ++i) {
+      if (pn) pn[i] = -1;
+      tk[i] = -1;
+    }
+    for (int a = node, i = D; a >= 0; a = parent[a], --i) {
+      if (pn) pn[i] = a;
+      if (i >= 1) tk[i - 1] = node_tokens[(size_t)b * N + a];
+    }
+    tk[D] = tok;
+    out_num_emitted[b] = D + 1;
+    out_num_accepted[b] = D;
+    if (out_near_ties) out_near_ties[b] = near;
+    if (out_flags) out_flags[b] = flags;
+    free(z); free(pc); free(qd);
+  }
+  free(depth);
+  return 0;
+}
