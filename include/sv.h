@@ -159,6 +159,7 @@ sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int
  * u_smp(b, a*) from norm([p_{a*} - q_{d(a*)+1}]+) if a* has children, else from p_{a*}.
  * parent [N] host; node_tokens [B,N] (column 0, the root, is not read);
  * target_logits [B,N,V]; q [B,Dq,V] with row d-1 = depth d (Dq >= tree depth).
+ * temperature, top_k, top_p, the uniforms and the near-tie reports as sv_accept_chain.
  * Outputs (Dmax = tree depth): out_path_nodes [B,Dmax+1] (root..a*, -1 after),
  * out_tokens [B,Dmax+1], out_num_emitted [B], out_num_accepted [B], out_near_ties [B].
  * Workspace: sv_accept_workspace_size(B, N, V, Dq). */
