@@ -172,6 +172,32 @@ sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
                          uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
                          void *stream);
 
+/* Exact tree acceptance with the siblings of a node tried in turn (hncyxsy.com sections
+ * 2.1-2.2: after a rejected candidate the target becomes the residual norm([p - q]+);
+ * jennyma11 blog, section "Medusa": lossless tree verification).  From the root, the
+ * children of the current node are tried in row order: child c (token x_c) is accepted iff
+ * u_acc(b, c) < r(x_c) / q_{d+1}(x_c), where r starts as the node's effective target p and
+ * after each rejected child becomes norm([r - q_{d+1}]+) (kept unchanged, and counted as a
+ * near tie, when that has no mass); an accepted child becomes the current node.  When all
+ * children are rejected the token is drawn with u_smp(b, node) from norm([r - q_{d+1}]+)
+ * of the last r (r itself when that has no mass); a leaf draws the bonus from its p.  With
+ * drafts drawn independently from q this keeps the emitted tokens distributed as the
+ * target's; with one child per node it equals sv_accept_chain.
+ * Exact mode only: temperature must be > 0 (else SV_ERR_UNSUPPORTED; greedy trees use
+ * sv_accept_tree).  Every other argument, the outputs, the uniforms, the workspace
+ * (sv_accept_workspace_size(B, N, V, Dq)) and the errors as sv_accept_tree; near ties
+ * count decisions with |u_acc - ratio| < 1e-6, empty residuals, a sample within 1e-6 of a
+ * CDF boundary (in units of the normalised residual) and one for a near top-p cut on a
+ * visited row.  Launches: the statistics kernel, then one CTA per sequence. */
+sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const int32_t *parent,
+                                   const int32_t *node_tokens, const void *target_logits,
+                                   const void *q, sv_q_kind q_kind, int Dq, float temperature,
+                                   int top_k, float top_p, uint64_t seed, uint64_t round,
+                                   int32_t *out_path_nodes, int32_t *out_tokens,
+                                   int32_t *out_num_emitted, int32_t *out_num_accepted,
+                                   uint32_t *out_near_ties, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
 /* Workspace bytes for sv_accept_chain (N = gamma+1, Dq = gamma) / sv_accept_tree. */
 size_t sv_accept_workspace_size(int B, int N, int V, int Dq);
 

@@ -20,7 +20,7 @@ __all__ = [
     "SVError", "KVCache", "library_path", "load_library", "sv_tree_attention",
     "sv_tree_attention_workspace_size", "sv_tree_attention_path", "sv_accept_chain", "sv_accept_tree",
     "sv_accept_workspace_size", "sv_accept_tree_noalloc", "sv_commit_kv", "sv_accept_tree_commit",
-    "sv_accept_chain_commit", "sv_ngram_draft", "sv_tree_prepare", "sv_read_device_status",
+    "sv_accept_chain_commit", "sv_accept_tree_recursive", "sv_ngram_draft", "sv_tree_prepare", "sv_read_device_status",
     "sv_version", "sv_kernel_launches", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "SV_MAX_TREE_NODES",
 ]
 
@@ -80,6 +80,8 @@ def load_library():
                                         SZ, P]
         lib.sv_accept_tree.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, F, U64, U64, P, P, P, P,
                                        P, P, SZ, P]
+        lib.sv_accept_tree_recursive.argtypes = [I, I, I, I, P, P, P, P, I, I, F, I, F, U64, U64,
+                                                 P, P, P, P, P, P, SZ, P]
         lib.sv_accept_tree_noalloc.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, F, U64, U64, P,
                                                P, P, P, P, P]
         lib.sv_accept_workspace_size.argtypes = [I, I, I, I]
@@ -97,7 +99,8 @@ def load_library():
         lib.sv_kernel_launches.restype = ctypes.c_uint64
         for fn in ("sv_tree_attention", "sv_accept_chain", "sv_accept_tree", "sv_commit_kv",
                    "sv_tree_prepare", "sv_read_device_status", "sv_accept_tree_noalloc",
-                   "sv_accept_tree_commit", "sv_accept_chain_commit", "sv_ngram_draft"):
+                   "sv_accept_tree_commit", "sv_accept_chain_commit", "sv_ngram_draft",
+                   "sv_accept_tree_recursive"):
             getattr(lib, fn).restype = ctypes.c_int32
         _lib = lib
         return lib
@@ -319,6 +322,38 @@ def sv_accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperat
                               _ptr(outs["tokens"]), _ptr(outs["num_emitted"]),
                               _ptr(outs["num_accepted"]), _ptr(outs["near_ties"]),
                               _ptr(workspace), ws_bytes, _stream(stream)))
+    return outs
+
+
+def sv_accept_tree_recursive(target_logits, q, q_kind, parent, node_tokens, temperature=1.0,
+                             top_k=0, top_p=1.0, seed=0, round_=0, outs=None, workspace=None,
+                             stream=None) -> dict:
+    """Exact tree acceptance with the siblings of a node tried in turn (the residual of a
+    rejected child goes to the next); arguments and outputs as sv_accept_tree, exact mode
+    only (temperature > 0)."""
+    lib = load_library()
+    _dev(target_logits, "target_logits", (torch.bfloat16, torch.float32))
+    B, N, V = target_logits.shape
+    _dev(node_tokens, "node_tokens", torch.int32, (B, N))
+    if q is None:
+        raise ValueError("q is required (exact mode)")
+    Dq = q.shape[1]
+    _dev(q, "q", target_logits.dtype if q_kind == Q_LOGITS else torch.float32, (B, Dq, V))
+    W = _tree_depth(parent) + 1
+    outs = _accept_outputs(B, W, target_logits.device, outs)
+    outs.setdefault("path_nodes", torch.empty((B, W), dtype=torch.int32, device=target_logits.device))
+    workspace, ws_bytes = _workspace(sv_accept_workspace_size(B, N, V, Dq), target_logits.device,
+                                     workspace)
+    par, n = _parent_arr(parent)
+    if n != N:
+        raise ValueError(f"parent has {n} entries, logits have {N} rows")
+    _check(lib.sv_accept_tree_recursive(_dt(target_logits), B, N, V, par, _ptr(node_tokens),
+                                        _ptr(target_logits), _ptr(q), q_kind, Dq,
+                                        float(temperature), int(top_k), float(top_p), int(seed),
+                                        int(round_), _ptr(outs["path_nodes"]), _ptr(outs["tokens"]),
+                                        _ptr(outs["num_emitted"]), _ptr(outs["num_accepted"]),
+                                        _ptr(outs["near_ties"]), _ptr(workspace), ws_bytes,
+                                        _stream(stream)))
     return outs
 
 

@@ -27,6 +27,7 @@
 #include <climits>
 
 #include "sv_common.cuh"
+#include "row_stat.cuh"
 #include "sv_internal.h"
 #include "tc_primitives.cuh"
 
@@ -209,25 +210,6 @@ __device__ __forceinline__ float vec_max(const uint4 &r) {
     return fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
                  fmaxf(__uint_as_float(r.z), __uint_as_float(r.w)));
   }
-}
-
-// Is entry (value z, index j) inside the row's top-k set?
-// Row statistics written by other CTAs of the same launch: read from L2, not L1.
-__device__ __forceinline__ RowStat load_stat(const RowStat *s) {
-  RowStat r;
-  r.zmax = __ldcg(&s->zmax);
-  r.argmax = __ldcg(&s->argmax);
-  r.key_k = __ldcg(&s->key_k);
-  r.idx_k = __ldcg(&s->idx_k);
-  r.S = __ldcg(&s->S);
-  r.flags = __ldcg(&s->flags);
-  return r;
-}
-
-template <typename T>
-__device__ __forceinline__ bool kept(float z, int j, const RowStat &st) {
-  const uint32_t k = Elem<T>::key(z);
-  return k > st.key_k || (k == st.key_k && j <= st.idx_k);
 }
 
 // ------------------------------------------------------------ kernel 1
@@ -1599,8 +1581,9 @@ cudaError_t launch_select(const AcceptParams &p, int num_sms, cudaStream_t s) {
   return launch_select_kernel<T, GREEDY, TOPK, false>(pl, C, s);
 }
 
+// Kernel 1 alone: the statistics of every target row, then of every q row (q logits).
 template <typename T>
-cudaError_t launch_typed(const AcceptParams &p, int num_sms, cudaStream_t s) {
+cudaError_t launch_stats_typed(const AcceptParams &p, cudaStream_t s) {
   const bool greedy = p.mode == SV_GREEDY;
   const bool topk = !greedy && p.top_k > 0 && p.top_k < p.V;
   const int rows = p.B * p.N + ((!greedy && p.q_kind == SV_Q_LOGITS) ? p.B * p.Dq : 0);
@@ -1610,7 +1593,14 @@ cudaError_t launch_typed(const AcceptParams &p, int num_sms, cudaStream_t s) {
     accept_stats_kernel<T, false, true><<<rows, stat_threads<true>(), 0, s>>>(p);
   else
     accept_stats_kernel<T, false, false><<<rows, stat_threads<false>(), 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_typed(const AcceptParams &p, int num_sms, cudaStream_t s) {
+  const bool greedy = p.mode == SV_GREEDY;
+  const bool topk = !greedy && p.top_k > 0 && p.top_k < p.V;
+  cudaError_t e = launch_stats_typed<T>(p, s);
   if (e != cudaSuccess) return e;
   if (greedy) return launch_select<T, true, false>(p, num_sms, s);
   return topk ? launch_select<T, false, true>(p, num_sms, s)
@@ -1625,6 +1615,10 @@ size_t accept_ws_bytes(int B, int N, int Dq) {
 
 cudaError_t launch_accept(sv_dtype dt, const AcceptParams &p, int num_sms, cudaStream_t s) {
   return dt == SV_F32 ? launch_typed<float>(p, num_sms, s) : launch_typed<bf16>(p, num_sms, s);
+}
+
+cudaError_t launch_accept_stats(sv_dtype dt, const AcceptParams &p, cudaStream_t s) {
+  return dt == SV_F32 ? launch_stats_typed<float>(p, s) : launch_stats_typed<bf16>(p, s);
 }
 
 }  // namespace sv

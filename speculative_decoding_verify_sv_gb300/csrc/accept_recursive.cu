@@ -1,0 +1,345 @@
+// Exact tree acceptance with the siblings of a node tried in turn (sm_103a).
+//
+// Method (hncyxsy.com sections 2.1-2.2: after a rejected candidate the target becomes the
+// residual norm([p - q]+); the jennyma11 blog, section "Medusa", separates this lossless
+// tree verification from typical acceptance).  From the root, the children of the current
+// node are tried in row (rank) order: child c is accepted iff u_acc(b, c) < r(x_c) / q(x_c),
+// where r starts as the node's effective target distribution p and, after each rejected
+// sibling, becomes the residual norm([r - q]+) (kept as it was, and counted as a near tie,
+// when that residual has no mass); q is the effective draft distribution of the children's
+// depth.  An accepted child becomes the current node.  When every child is rejected the
+// next token is drawn with u_smp(b, node) from norm([r - q]+) of the last r; a leaf draws
+// the bonus token from its p.  With one child per node this is the chain procedure.
+//
+// The residual after k rejections has a closed form: r_k = [p - c_k q]+ / N_k with
+// c_0 = 0, N_0 = 1, c_k = c_{k-1} + N_{k-1} and N_k = sum_j [p_j - c_k q_j]+ (because
+// [p - c q]+ / N - q is positive only where p - c q > N q >= 0, and there equals
+// (p - (c + N) q) / N).  So each rejection costs one reduction pass over the vocabulary
+// of the current node's target row and the depth's q row, and the final sample is one
+// inverse-CDF pass over w = [p - c q]+.
+//
+// One CTA per sequence walks the tree; thread 0 takes each decision in double from the
+// two logits at the candidate and the rows' statistics (kernel 1 of the acceptance);
+// the block sums the residual masses (each entry formed in float, summed in double).
+// The final sample: per-chunk sums of w by the warps, the chunk holding u * sum(w) found
+// by warp 0 from a scan of the chunk sums, then the token inside it by warp-wide
+// inclusive scans in token order.  No waits on other CTAs or on memory barriers: every
+// loop is bounded by the vocabulary or the tree size.
+#include <climits>
+
+#include "row_stat.cuh"
+#include "sv_common.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+
+namespace {
+
+constexpr int kRecThreads = 512;
+constexpr int kRecWarps = kRecThreads / 32;
+constexpr int kRecMaxChunks = 1024;  // chunk sums kept by a CTA (chunks >= 1024 entries)
+constexpr double kRecNearTie = 1e-6;
+
+// One sequence's view of the current node's target row and the depth's q row.
+template <typename T>
+struct RowPair {
+  const T *zt;        // target logits of the current node
+  const T *zq;        // q logits of the children's depth (q logits), else NULL
+  const float *qp;    // q probabilities of that depth (q probabilities), else NULL
+  RowStat sa, sq;     // statistics of the two rows (sq: q logits only)
+  float c_log2;       // log2(e) / T
+  float inv_sa, inv_sq;
+};
+
+// w_j = [p_j - c q_j]+ of entry j, in float (c == 0: p_j, the q row is not read).
+template <typename T>
+__device__ __forceinline__ float w_at(const RowPair<T> &r, int j, float c) {
+  const float z = Elem<T>::load(r.zt + j);
+  const float pj = kept<T>(z, j, r.sa) ? exp2f((z - r.sa.zmax) * r.c_log2) * r.inv_sa : 0.f;
+  if (c == 0.f) return pj;
+  float qj;
+  if (r.zq != nullptr) {
+    const float zq = Elem<T>::load(r.zq + j);
+    qj = kept<T>(zq, j, r.sq) ? exp2f((zq - r.sq.zmax) * r.c_log2) * r.inv_sq : 0.f;
+  } else {
+    qj = r.qp[j];
+  }
+  return fmaxf(pj - c * qj, 0.f);
+}
+
+// Sum over the CTA of one double per thread; every thread returns the same value (the
+// warp sums are added in warp order by each thread).
+__device__ __forceinline__ double block_sum_d(double v, double *sh) {
+  v = warp_sum_d(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  double t = 0.0;
+#pragma unroll
+  for (int i = 0; i < kRecWarps; ++i) t += sh[i];
+  __syncthreads();  // sh may be rewritten by the next call
+  return t;
+}
+
+__device__ __forceinline__ double warp_incl_scan_d(double v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+// The decision on candidate child ch of the current node (thread 0 only), in double:
+// ratio = [p(x) - c q(x)]+ / (n q(x)).  Returns bit 0: accepted, bit 1: near tie.
+template <typename T>
+__device__ int decide_child(const AcceptParams &p, const RowPair<T> &r, int b, int ch, double c,
+                            double n, bool logits) {
+  const int x = p.tokens[(size_t)b * p.tok_stride + ch - p.tok_offset];
+  if (x < 0 || x >= p.V) {
+    set_status(p.status, SV_DEV_BAD_TOKEN);
+    return 0;
+  }
+  const double temp = (double)p.temperature;
+  const float zp = Elem<T>::load(r.zt + x);
+  const double px =
+      kept<T>(zp, x, r.sa) ? exp(((double)zp - (double)r.sa.zmax) / temp) / (double)r.sa.S : 0.0;
+  double qx;
+  if (logits) {
+    const float zq = Elem<T>::load(r.zq + x);
+    qx = kept<T>(zq, x, r.sq) ? exp(((double)zq - (double)r.sq.zmax) / temp) / (double)r.sq.S : 0.0;
+  } else {
+    qx = (double)r.qp[x];
+  }
+  const double rx = fmax(px - c * qx, 0.0) / n;
+  uint32_t k_acc = 0u, k_smp = 0u;
+  verify_uniform_ints(p.seed, p.round, b, ch, &k_acc, &k_smp);
+  const double u = ((double)k_acc + 0.5) * (1.0 / 16777216.0);
+  double ratio;
+  if (qx > 0.0) {
+    ratio = rx / qx;
+  } else {
+    set_status(p.status, SV_DEV_ZERO_DRAFT_PROB);
+    ratio = rx > 0.0 ? INFINITY : 0.0;
+  }
+  return (u < ratio ? 1 : 0) | (fabs(u - ratio) < kRecNearTie ? 2 : 0);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const AcceptParams p) {
+  __shared__ double s_red[kRecWarps];
+  __shared__ double s_chunk[kRecMaxChunks];
+  __shared__ double s_total;
+  __shared__ int s_dec, s_tok, s_near;
+
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int N = p.tree.N, V = p.V;
+  const bool logits = p.q_kind == SV_Q_LOGITS;
+  const RowStat *tstat = p.stats + (size_t)b * N;
+  const RowStat *qstat = p.stats + (size_t)p.B * N + (size_t)b * p.Dq;
+
+  // thread 0's running counts (near ties of decisions and empty residuals; nucleus cuts)
+  unsigned near = 0u;
+  bool nuc = false;
+
+  RowPair<T> r;
+  r.c_log2 = p.c_log2;
+  r.zq = nullptr;
+  r.qp = nullptr;
+  r.inv_sq = 0.f;
+  int node = 0;
+  double c = 0.0, n = 1.0;    // the current residual: [p - c q]+ / n
+  double c_fin = 0.0;         // the final sample's w = [p - c_fin q]+
+  for (int steps = 0; steps < N; ++steps) {
+    // the children of the node: rows after it whose parent it is (the same in every thread)
+    int first = -1, last = -1;
+    for (int ch = node + 1; ch < N; ++ch)
+      if (p.tree.parent[ch] == node) {
+        if (first < 0) first = ch;
+        last = ch;
+      }
+    r.zt = reinterpret_cast<const T *>(p.target) + ((size_t)b * N + node) * V;
+    r.sa = load_stat(tstat + node);
+    r.inv_sa = 1.f / r.sa.S;
+    if (tid == 0) nuc |= (r.sa.flags & 1u) != 0u;
+    c = 0.0;
+    n = 1.0;
+    if (first < 0) {  // a leaf: the bonus token from its p
+      c_fin = 0.0;
+      break;
+    }
+    const int drow = p.tree.depth[node];  // q row of the children's depth (depth - 1)
+    if (logits) {
+      r.zq = reinterpret_cast<const T *>(p.q) + ((size_t)b * p.Dq + drow) * V;
+      r.sq = load_stat(qstat + drow);
+      r.inv_sq = 1.f / r.sq.S;
+      if (tid == 0) nuc |= (r.sq.flags & 1u) != 0u;
+    } else {
+      r.qp = static_cast<const float *>(p.q) + ((size_t)b * p.Dq + drow) * V;
+    }
+    int next = -1;
+    for (int ch = first; ch <= last; ++ch) {
+      if (p.tree.parent[ch] != node) continue;
+      if (tid == 0) {
+        const int d = decide_child<T>(p, r, b, ch, c, n, logits);
+        near += (unsigned)(d >> 1);
+        s_dec = d & 1;
+      }
+      __syncthreads();
+      const int acc = s_dec;
+      __syncthreads();  // s_dec is rewritten only after every thread has read it
+      if (acc) {
+        next = ch;
+        break;
+      }
+      if (ch == last) break;
+      // the next sibling sees the residual [p - (c + n) q]+ / its mass
+      const double c1 = c + n;
+      const float c1f = (float)c1;
+      double part = 0.0;
+      for (int j = tid; j < V; j += kRecThreads) part += (double)w_at<T>(r, j, c1f);
+      const double tot = block_sum_d(part, s_red);
+      if (tot > 0.0) {
+        c = c1;
+        n = tot;
+      } else if (tid == 0) {
+        ++near;  // no mass left: the residual stays as it was
+      }
+    }
+    if (next >= 0) {
+      node = next;
+      continue;
+    }
+    c_fin = c + n;  // every child rejected: sample from the last residual's residual
+    break;
+  }
+
+  // ---- final sample: inverse CDF of w = [p - c_fin q]+ in token order, with u_smp(b, node)
+  const int CH = max(1024, ((V + kRecMaxChunks - 1) / kRecMaxChunks + 31) / 32 * 32);
+  const int nch = (V + CH - 1) / CH;
+  float cf = (float)c_fin;
+  double tol = kRecNearTie * n;  // the page's 1e-6 window, in units of the normalised w
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    for (int k = warp; k < nch; k += kRecWarps) {
+      double s = 0.0;
+      const int j_end = min(V, (k + 1) * CH);
+      for (int j = k * CH + lane; j < j_end; j += 32) s += (double)w_at<T>(r, j, cf);
+      s = warp_sum_d(s);
+      if (lane == 0) s_chunk[k] = s;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      double s = 0.0;
+      for (int k = lane; k < nch; k += 32) s += s_chunk[k];
+      s = warp_sum_d(s);
+      if (lane == 0) s_total = s;
+    }
+    __syncthreads();
+    if (s_total > 0.0 || attempt == 1) break;
+    // the residual has no mass: sample from the last residual itself
+    if (tid == 0) ++near;
+    cf = (float)c;
+    __syncthreads();  // s_total and s_chunk are rewritten by the second attempt
+  }
+
+  if (warp == 0) {
+    uint32_t k_acc = 0u, k_smp = 0u;
+    verify_uniform_ints(p.seed, p.round, b, node, &k_acc, &k_smp);
+    const double u = ((double)k_smp + 0.5) * (1.0 / 16777216.0);
+    // lane l owns chunks [l * per, (l + 1) * per): its sum, then a scan over the lanes
+    const int per = (nch + 31) / 32;
+    const int k0 = min(nch, lane * per), k1 = min(nch, k0 + per);
+    double ls = 0.0;
+    for (int k = k0; k < k1; ++k) ls += s_chunk[k];
+    const double incl = warp_incl_scan_d(ls);
+    const double total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const double t = u * total;
+    unsigned hit = __ballot_sync(0xFFFFFFFFu, k1 > k0 && incl > t);
+    if (hit == 0u) {  // t at or past the end (rounding): start at the last lane with mass
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, ls > 0.0);
+      hit = m != 0u ? 1u << (31 - __clz(m)) : 1u;
+    }
+    const int L = __ffs(hit) - 1;
+    // lane L finds its first chunk whose end passes t (else its last chunk)
+    int my_start = k1 - 1;
+    double my_base = incl - ls;
+    if (lane == L) {
+      for (int k = k0; k < k1; ++k) {
+        if (my_base + s_chunk[k] > t) {
+          my_start = k;
+          break;
+        }
+        if (k + 1 < k1) my_base += s_chunk[k];
+      }
+    }
+    const int start = max(0, __shfl_sync(0xFFFFFFFFu, my_start, L));
+    const double base = __shfl_sync(0xFFFFFFFFu, my_base, L);
+    // the token: warp-wide scans in token order from the start chunk onwards
+    int tok = -1, last_pos = -1, nearf = 0;
+    double run = base;
+    for (int j0 = start * CH; j0 < V; j0 += 32) {
+      const int j = j0 + lane;
+      const double w = j < V ? (double)w_at<T>(r, j, cf) : 0.0;
+      const double ci = warp_incl_scan_d(w);
+      const double cum = run + ci, prev = cum - w;
+      const unsigned h = __ballot_sync(0xFFFFFFFFu, w > 0.0 && cum > t);
+      const unsigned pos = __ballot_sync(0xFFFFFFFFu, w > 0.0);
+      if (h != 0u) {
+        const int lh = __ffs(h) - 1;
+        const int nr = (t - prev < tol || cum - t < tol) ? 1 : 0;
+        nearf = __shfl_sync(0xFFFFFFFFu, nr, lh);
+        tok = j0 + lh;
+        break;
+      }
+      if (pos != 0u) last_pos = j0 + 31 - __clz(pos);
+      run += __shfl_sync(0xFFFFFFFFu, ci, 31);
+    }
+    if (tok < 0) {  // rounding put u * sum(w) at or past the end: the last token with mass
+      tok = last_pos >= 0 ? last_pos : 0;
+      nearf = 1;
+    }
+    if (lane == 0) {
+      s_tok = tok;
+      s_near = nearf;
+    }
+  }
+  __syncthreads();
+
+  if (tid == 0) {
+    near += (unsigned)s_near + (nuc ? 1u : 0u);
+    const int W = p.tree.Dmax + 1;
+    const int D = p.tree.depth[node];
+    int32_t *pn = p.out_path_nodes ? p.out_path_nodes + (size_t)b * W : nullptr;
+    int32_t *tk = p.out_tokens + (size_t)b * W;
+    for (int i = 0; i < W; ++i) {
+      if (pn) pn[i] = -1;
+      tk[i] = -1;
+    }
+    int i = D;
+    for (int a = node; a >= 0 && i >= 0; a = p.tree.parent[a], --i) {
+      if (pn) pn[i] = a;
+      if (i >= 1) tk[i - 1] = p.tokens[(size_t)b * p.tok_stride + a - p.tok_offset];
+    }
+    tk[D] = s_tok;
+    p.out_num_emitted[b] = D + 1;
+    p.out_num_accepted[b] = D;
+    if (p.out_near_ties) p.out_near_ties[b] = near;
+  }
+}
+
+template <typename T>
+cudaError_t launch_recursive_typed(const AcceptParams &p, cudaStream_t s) {
+  accept_recursive_kernel<T><<<p.B, kRecThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_accept_recursive(sv_dtype dt, const AcceptParams &p, cudaStream_t s) {
+  cudaError_t e = launch_accept_stats(dt, p, s);
+  if (e != cudaSuccess) return e;
+  return dt == SV_F32 ? launch_recursive_typed<float>(p, s) : launch_recursive_typed<bf16>(p, s);
+}
+
+}  // namespace sv

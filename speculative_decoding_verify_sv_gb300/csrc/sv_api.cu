@@ -460,6 +460,41 @@ sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
   return accept_launch(logit_dt, p, greedy, workspace, workspace_bytes, stream);
 }
 
+sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const int32_t *parent,
+                                   const int32_t *node_tokens, const void *target_logits,
+                                   const void *q, sv_q_kind q_kind, int Dq, float temperature,
+                                   int top_k, float top_p, uint64_t seed, uint64_t round,
+                                   int32_t *out_path_nodes, int32_t *out_tokens,
+                                   int32_t *out_num_emitted, int32_t *out_num_accepted,
+                                   uint32_t *out_near_ties, void *workspace,
+                                   size_t workspace_bytes, void *stream) {
+  sv::AcceptParams p;
+  bool greedy = false;
+  sv_status st = tree_params(SV_EXACT, logit_dt, B, N, V, parent, node_tokens, target_logits, q,
+                             q_kind, Dq, temperature, top_k, top_p, seed, round, out_path_nodes,
+                             out_tokens, out_num_emitted, out_num_accepted, out_near_ties, p,
+                             &greedy);
+  if (st != SV_OK) return st;
+  if (greedy)
+    return fail(SV_ERR_UNSUPPORTED,
+                "siblings tried in turn need temperature > 0 (greedy: sv_accept_tree)");
+  const size_t need = sv::accept_ws_bytes(p.B, p.N, p.Dq);
+  if (!workspace || workspace_bytes < need)
+    return fail(SV_ERR_WORKSPACE, "acceptance workspace %zu bytes, need %zu", workspace_bytes, need);
+  if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  p.status = status_word();
+  if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
+  p.mode = SV_EXACT;
+  p.c_log2 = (float)(1.4426950408889634 / (double)p.temperature);
+  if (p.top_k >= p.V) p.top_k = 0;
+  p.stats = static_cast<sv::RowStat *>(workspace);
+  if (p.B == 0) return SV_OK;
+  cudaError_t e = sv::launch_accept_recursive(logit_dt, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "recursive tree acceptance launch");
+  sv::count_launches(2);
+  return SV_OK;
+}
+
 sv_status sv_accept_chain_commit(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
                                  const void *target_logits, const void *q, sv_q_kind q_kind,
                                  const int32_t *draft_tokens, float temperature, int top_k, float top_p,

@@ -149,6 +149,11 @@ struct NgramParams {
 };
 cudaError_t launch_ngram(const NgramParams &p, cudaStream_t s);
 cudaError_t launch_accept(sv_dtype dt, const AcceptParams &p, int num_sms, cudaStream_t s);
+// The statistics kernel alone (every target row, then every q row for q logits).
+cudaError_t launch_accept_stats(sv_dtype dt, const AcceptParams &p, cudaStream_t s);
+// Exact tree acceptance with siblings tried in rank order: the statistics kernel, then one
+// CTA per sequence walking the tree (exact mode only; no commit).
+cudaError_t launch_accept_recursive(sv_dtype dt, const AcceptParams &p, cudaStream_t s);
 
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
 

@@ -147,6 +147,25 @@ def test_fused_accept_commit_rejects_before_launch(lib):
                                       None) == sv.SV_ERR_UNSUPPORTED
 
 
+def test_tree_recursive_rejects_before_launch(lib):
+    P = ctypes.c_void_p(16)
+    par = (ctypes.c_int32 * 3)(-1, 0, 0)
+    bad = (ctypes.c_int32 * 3)(-1, 2, 0)  # a parent after its child
+
+    def call(parent=par, V=1000, q=P, Dq=1, T=1.0, top_k=0, top_p=1.0, ws=1 << 20):
+        return lib.sv_accept_tree_recursive(1, 2, 3, V, parent, P, P, q, 1, Dq, T, top_k, top_p,
+                                            0, 0, P, P, P, P, P, P, ws, None)
+    # greedy (temperature 0) has no sibling residuals: unsupported here
+    assert call(T=0.0) == sv.SV_ERR_UNSUPPORTED
+    assert "temperature" in lib.sv_last_error().decode()
+    assert call(parent=bad) == sv.SV_ERR_INVALID_ARG
+    assert call(V=1001) == sv.SV_ERR_UNSUPPORTED
+    assert call(q=None) == sv.SV_ERR_INVALID_ARG
+    assert call(Dq=0) == sv.SV_ERR_INVALID_ARG      # q rows must cover the tree depth
+    assert call(top_p=0.9) == sv.SV_ERR_UNSUPPORTED  # top-p needs top-k
+    assert call(ws=16) == sv.SV_ERR_WORKSPACE
+
+
 def test_ngram_draft_rejects_before_launch(lib):
     P = ctypes.c_void_p(16)
     # n-gram sizes out of order or past the maximum, gamma out of range, null pointers
