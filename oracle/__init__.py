@@ -25,7 +25,7 @@ _LIB = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, BF16 = 0, 1
+F32, BF16, F64 = 0, 1, 2
 GREEDY, EXACT = 0, 1
 Q_PROBS_F32, Q_LOGITS = 0, 1
 
@@ -69,6 +69,7 @@ def _load():
             lib.orc_accept_tree_recursive.argtypes = [I, I, I, I, P, P, P, P, I, I, Dbl, I, Dbl,
                                                       U64, U64, P, P, P, P, P, P]
             lib.orc_accept_tree_recursive.restype = I
+            lib.orc_lm_head.argtypes = [I, I, I, P, I, P, I, P]
             lib.orc_set_threads.argtypes = [I]
             lib.orc_get_threads.restype = I
             _lib = lib
@@ -103,7 +104,9 @@ def _dtype_code(t) -> int:
         return F32
     if t.dtype == torch.bfloat16:
         return BF16
-    raise TypeError(f"oracle supports float32 and bfloat16, got {t.dtype}")
+    if t.dtype == torch.float64:
+        return F64  # logits computed by lm_head
+    raise TypeError(f"oracle supports float32, bfloat16 and float64, got {t.dtype}")
 
 
 def _i32(x):
@@ -317,4 +320,23 @@ def accept_tree_recursive(target_logits, q, q_kind, parent, node_tokens, tempera
         _ptr(out["near_ties"]), _ptr(out["flags"]))
     if rc != 0:
         raise ValueError(f"oracle accept_tree_recursive rejected its arguments (code {rc})")
+    return out
+
+
+def lm_head(hidden, weight):
+    """Target logits from hidden states: z[..., v] = sum_k hidden[..., k] * weight[v, k] in
+    double (see oracle.c, orc_lm_head).  hidden [..., Dm], weight [V, Dm], float32 or
+    bfloat16; returns float64 [..., V], which accept_chain / accept_tree /
+    accept_tree_recursive take as target logits."""
+    h = _cpu(hidden)
+    w = _cpu(weight)
+    if h.dtype == torch.float64 or w.dtype == torch.float64:
+        raise TypeError("hidden and weight are float32 or bfloat16")
+    Dm = h.shape[-1]
+    V = w.shape[0]
+    if w.dim() != 2 or w.shape[1] != Dm:
+        raise ValueError(f"weight must be [V, {Dm}], got {tuple(w.shape)}")
+    rows = h.numel() // Dm if Dm > 0 else 0
+    out = torch.zeros(tuple(h.shape[:-1]) + (V,), dtype=torch.float64)
+    _load().orc_lm_head(rows, Dm, V, _ptr(h), _dtype_code(h), _ptr(w), _dtype_code(w), _ptr(out))
     return out

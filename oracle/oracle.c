@@ -57,6 +57,7 @@
 
 #define ORC_F32 0
 #define ORC_BF16 1
+#define ORC_F64 2
 #define ORC_GREEDY 0
 #define ORC_EXACT 1
 #define ORC_Q_PROBS_F32 0
@@ -96,6 +97,7 @@ int orc_get_threads(void) {
 /* Widen one stored element to double.  bf16 is the upper half of an IEEE binary32
  * word, so shifting its 16 bits up gives the same value exactly. */
 static double orc_elem(const void *base, int dtype, size_t i) {
+  if (dtype == ORC_F64) return ((const double *)base)[i];
   if (dtype == ORC_F32) return (double)((const float *)base)[i];
   uint32_t w = ((uint32_t)((const uint16_t *)base)[i]) << 16;
   float f;
@@ -103,7 +105,7 @@ static double orc_elem(const void *base, int dtype, size_t i) {
   return (double)f;
 }
 
-static size_t orc_esize(int dtype) { return dtype == ORC_F32 ? 4 : 2; }
+static size_t orc_esize(int dtype) { return dtype == ORC_F64 ? 8 : dtype == ORC_F32 ? 4 : 2; }
 
 /* --------------------------------------------------------- Philox4x32-10 */
 
@@ -645,6 +647,29 @@ void orc_commit_kv(int dtype, int B, int N, int Hkv, int D, const void *k_tree,
       memcpy((char *)cache_v + dst, (const char *)v_tree + src, row_bytes);
     }
     prefix_len[b] = L + num_accepted[b] + 1;
+  }
+}
+
+/* ------------------------------------------------------------------- LM head */
+
+/* Logits from hidden states: z[r, v] = sum_k h[r, k] * W[v, k].  "推测解码技术详解：加速LLM
+ * 推理的关键", section "Medusa Heads", architecture figure: the original LM head and the
+ * Medusa heads all read the backbone's hidden states; lpnh.cn section 3.1: a head is a
+ * Linear(H, V) from the hidden state h_t to V logits.  hidden [rows, Dm] and weight
+ * [V, Dm] (row v = token v's output embedding) in f32 or bf16; out [rows, V] in double,
+ * each sum taken in ascending k.  Readings: no bias term; the hidden state arrives
+ * already normalised (the final norm is the model's, outside the verify step).  The
+ * acceptance functions read the result with dtype ORC_F64. */
+void orc_lm_head(int rows, int Dm, int V, const void *hidden, int h_dtype, const void *weight,
+                 int w_dtype, double *out) {
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    for (int v = 0; v < V; ++v) {
+      double acc = 0.0;
+      for (int k = 0; k < Dm; ++k)
+        acc += orc_elem(hidden, h_dtype, (size_t)r * Dm + k) * orc_elem(weight, w_dtype, (size_t)v * Dm + k);
+      out[(size_t)r * V + v] = acc;
+    }
   }
 }
 
