@@ -205,9 +205,13 @@ def accept_bytes(w) -> int:
 
 
 def attention_flops(w) -> int:
+    """Algorithmic flops of one tree-attention launch: 4*D per (query row, attended key);
+    a node attends to the prefix and to its root path (depth + 1 tree keys)."""
+    from speculative_decoding_verify_sv_gb300 import workloads as wl
     c = w["cfg"]
     B, N, Hq, D = c["B"], w["N"], c["Hq"], c["D"]
-    keys = int(w["prefix_len"].sum().item()) * N * Hq + B * N * N * Hq
+    path_keys = sum(d + 1 for d in wl.depths(w["parent"]))
+    keys = int(w["prefix_len"].sum().item()) * N * Hq + B * Hq * path_keys
     return 4 * keys * D
 
 
