@@ -95,3 +95,45 @@ def test_peak_falls_back_without_the_measured_file(tmp_path, monkeypatch):
     assert kind == "fallback" and peak == bench.FALLBACK_HBM_GBS
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6765.3}))
     assert bench.measured_peaks() == (6765.3, "measured")
+
+
+class _FakeSmi:
+    """Stands in for the nvidia-smi sampling process: returns fixed CSV rows."""
+
+    def __init__(self, out):
+        self.out = out
+
+    def terminate(self):
+        pass
+
+    def kill(self):
+        pass
+
+    def communicate(self, timeout=None):
+        return self.out, ""
+
+
+def test_clocks_are_read_from_samples_under_load():
+    s = bench.ClockSampler(0)
+    s.proc = _FakeSmi(
+        "1000, 2070, 100.0, 0, Not Active, Not Active, Not Active, Not Active\n"
+        "2070, 2070, 900.0, 100, Not Active, Not Active, Not Active, Active\n"
+        "2040, 2070, 910.0, 98, Not Active, Not Active, Not Active, Not Active\n"
+        "not a sample\n")
+    c = s.stop()
+    # the idle sample (utilisation 0) is left out of the median and of the reasons
+    assert c["sm_mhz"] == 2055.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]
+    assert c["samples"] == 3 and c["samples_under_load"] == 2
+
+
+def test_throttle_reasons_that_reject_a_run_are_reported():
+    s = bench.ClockSampler(0)
+    s.proc = _FakeSmi("1500, 2070, 1300.0, 100, Active, Not Active, Active, Not Active\n")
+    c = s.stop()
+    assert c["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    s = bench.ClockSampler(0)
+    s.proc = _FakeSmi("")
+    assert s.stop()["reasons"] == ["no samples"]
+    s = bench.ClockSampler(0)  # nvidia-smi could not be started
+    assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
