@@ -3,7 +3,12 @@
  *
  * One verify step = tree attention of the flattened candidate tree against the KV
  * prefix (sv_tree_attention), token acceptance over the vocabulary (sv_accept_chain /
- * sv_accept_tree) and the KV commit of the accepted path (sv_commit_kv).
+ * sv_accept_tree) and the KV commit of the accepted path (sv_commit_kv); the fused
+ * calls sv_accept_chain_commit / sv_accept_tree_commit do the last two in one launch
+ * pair.  sv_accept_tree_recursive is the tree acceptance that tries a node's children
+ * in turn (siblings drawn from q keep the target's distribution), sv_accept_tree_noalloc
+ * the tree acceptance without a workspace, and sv_ngram_draft proposes prompt-lookup
+ * drafts on the device.
  *
  * Conventions shared by every entry point
  *  - Every tensor argument is caller-owned DEVICE memory, dense row-major in the layout
