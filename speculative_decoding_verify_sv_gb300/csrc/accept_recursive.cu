@@ -25,8 +25,6 @@
 // by warp 0 from a scan of the chunk sums, then the token inside it by warp-wide
 // inclusive scans in token order.  No waits on other CTAs or on memory barriers: every
 // loop is bounded by the vocabulary or the tree size.
-#include <climits>
-
 #include "row_stat.cuh"
 #include "sv_common.cuh"
 #include "sv_internal.h"
