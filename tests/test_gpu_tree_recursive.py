@@ -39,6 +39,19 @@ def test_chain(cuda_ok, dtype, T, top_k):
     assert sv.sv_read_device_status() == 0
 
 
+def test_chain_large_vocab(cuda_ok):
+    """152064-entry rows (the ragged-paged workload's vocabulary): the final sample's 149
+    chunk sums are split five to a lane of the search."""
+    B, gamma, V = 16, 4, 152064
+    lg = wl.chain_logits(B, gamma, V, sigma=3.0, draft_sigma=1.0, dtype=torch.bfloat16, seed=13)
+    toks = torch.zeros((B, gamma + 1), dtype=torch.int32)
+    toks[:, 1:] = lg["draft_tokens"]
+    out, ref = _run(lg["target_logits"], lg["draft_logits"], sv.Q_LOGITS, wl.chain_parent(gamma),
+                    toks, seed=9, round_=4)
+    _compare(out, ref, KEYS, max_exempt_frac=0.15)
+    assert sv.sv_read_device_status() == 0
+
+
 @pytest.mark.parametrize("parent", [wl.TREE_T26, wl.TREE_T64, wl.TREE_EXAMPLE7])
 def test_medusa_trees(cuda_ok, parent):
     B = 64
