@@ -28,6 +28,12 @@
  *    parent's p and the q of its depth; the chosen node is the deepest one whose whole
  *    root path is accepted (ties: smallest row index); the final token is sampled
  *    from norm([p_a - q_{d+1}]+) if that node has children, else the bonus from p_a.
+ *  - tree acceptance with siblings tried in turn (orc_accept_tree_recursive): the
+ *    children of the current node in row order; after a rejected child the target
+ *    becomes norm([r - q]+) (kept, as a near tie, when that has no mass); after the
+ *    last rejection the token is drawn from norm([r - q]+) of the last r.
+ *  - LM head (orc_lm_head): z = h W^T with no bias, h already normalised; the result is
+ *    read by the acceptance functions as double logits (dtype ORC_F64).
  *  - top-k ties at the k-th value keep the lower token ids; argmax ties pick the
  *    lowest token id; temperature T == 0 means greedy.
  *  - top-p (nucleus; named as a sampling knob by the jennyma11 blog, section
