@@ -29,6 +29,15 @@
  *    trap: the kernel skips the offending access, ORs an SV_DEV_* bit into a sticky
  *    device status word and carries on.  Read (and clear) it with
  *    sv_read_device_status().
+ *  - Near ties.  Every acceptance call can report, per sequence, the decisions and
+ *    samples that lie so close to their threshold that another rounding of the same
+ *    arithmetic could take them the other way (reported, not hidden).  out_near_ties[b]
+ *    packs two counts: bits 0-15 count DECISION ties (a decision with |u_acc - ratio| <
+ *    1e-6 whose parent lies on an accepted path, a top-p cut within 1e-6 of top_p, and
+ *    for the sibling rule an empty residual handed to the next sibling: any of these may
+ *    change which nodes are accepted), bits 16-31 count SAMPLE ties (the final token's
+ *    u_smp * sum(w) within the window of a CDF boundary, or its residual empty: only the
+ *    last emitted token is in doubt).  SV_NEAR_DECISIONS() / SV_NEAR_SAMPLES() unpack it.
  */
 #ifndef SV_H
 #define SV_H
@@ -56,6 +65,10 @@ typedef int32_t sv_status;
                                       outputs of that call are not valid */
 #define SV_DEV_LAYOUT 0x20u        /* shared memory was not 1024-byte aligned; the call
                                       did nothing (outputs not valid) */
+
+/* The two counts of a packed near-tie word (see "Near ties" above). */
+#define SV_NEAR_DECISIONS(w) ((uint32_t)(w) & 0xFFFFu)
+#define SV_NEAR_SAMPLES(w) ((uint32_t)(w) >> 16)
 
 #define SV_MAX_TREE_NODES 64 /* one 64-bit ancestor word per node */
 #define SV_MAX_TOP_K 1024
@@ -135,9 +148,10 @@ size_t sv_tree_attention_workspace_size(sv_dtype dt, int B, int N, int Hq, int H
  * [B,gamma,V] (row i-1 = draft distribution of draft i; unused in greedy mode, may be
  * NULL); draft_tokens [B,gamma] int32.
  * Outputs: out_tokens [B,gamma+1] (accepted drafts then the sampled token, -1 after),
- * out_num_emitted [B] (= accepted + 1), out_num_accepted [B], out_near_ties [B] (count
- * of decisions with |u_acc - ratio| < 1e-6 and samples within 1e-6 of a CDF
- * boundary: reported, not hidden; may be NULL).
+ * out_num_emitted [B] (= accepted + 1), out_num_accepted [B], out_near_ties [B] (the
+ * packed near-tie word: decisions with |u_acc - ratio| < 1e-6 and near top-p cuts in
+ * bits 0-15, a final sample within 1e-6 (probability units) of a CDF boundary or with
+ * an empty residual in bits 16-31; may be NULL).
  * logit_dt: SV_BF16 or SV_F32.  V % 8 == 0, 1 <= gamma <= 63, 0 <= top_k <= 1024
  * (0 = off).  top_p in (0, 1], 1 = off: below 1 the nucleus of the top-k distribution
  * is kept (top-k first, then top-p; needs 0 < top_k < V, else SV_ERR_UNSUPPORTED): in the
@@ -190,10 +204,13 @@ sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
  * target's; with one child per node it equals sv_accept_chain.
  * Exact mode only: temperature must be > 0 (else SV_ERR_UNSUPPORTED; greedy trees use
  * sv_accept_tree).  Every other argument, the outputs, the uniforms, the workspace
- * (sv_accept_workspace_size(B, N, V, Dq)) and the errors as sv_accept_tree; near ties
- * count decisions with |u_acc - ratio| < 1e-6, empty residuals, a sample within 1e-6 of a
- * CDF boundary (in units of the normalised residual) and one for a near top-p cut on a
- * visited row.  Launches: the statistics kernel, then one CTA per sequence. */
+ * (sv_accept_workspace_size(B, N, V, Dq)) and the errors as sv_accept_tree; the packed
+ * near-tie word counts, as decision ties, decisions with |u_acc - ratio| within 1e-6 (or
+ * within the float error bound of the residual's mass, when that is wider), residuals
+ * handed to a sibling with no mass (or less than that error bound) and one near top-p
+ * cut on a visited row; and as sample ties a final sample within 1e-6 of a CDF boundary
+ * (in units of the normalised residual, or the error bound when wider) or with an empty
+ * residual.  Launches: the statistics kernel, then one CTA per sequence. */
 sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const int32_t *parent,
                                    const int32_t *node_tokens, const void *target_logits,
                                    const void *q, sv_q_kind q_kind, int Dq, float temperature,

@@ -49,6 +49,11 @@
  *    matters (its parent lies on an accepted path), or u*sum(w) within 1e-6 of a CDF
  *    boundary around the chosen token (w is in probability units: p and q are
  *    normalised, so the window is absolute), or sum(w) == 0 (then sample from p).
+ *    The count is reported in two classes packed in one word: decision ties (a near
+ *    decision, a near top-p cut, and for the sibling rule an empty residual handed to
+ *    the next sibling: anything that can change which nodes are accepted) in the low 16
+ *    bits, and sample ties (a near CDF boundary or an empty residual in the final
+ *    sample: only the last emitted token is in doubt) times 65536 in the high 16 bits.
  *
  * Build: gcc -O2 -fPIC -shared -fopenmp -o liboracle.so oracle.c -lm
  */
@@ -69,6 +74,8 @@
 #define ORC_Q_PROBS_F32 0
 #define ORC_Q_LOGITS 1
 #define ORC_NEAR_TIE 1e-6
+/* weight of one sample-class near tie in the packed near-tie word */
+#define ORC_SAMPLE_TIE 65536u
 
 /* Host memory for scratch; a failed allocation stops the process with a message. */
 static void *orc_alloc(size_t n) {
@@ -508,8 +515,9 @@ int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *par
       } else {
         tok = orc_sample_residual(pa, NULL, V, u_smp, &near_s);
       }
-      near += (uint32_t)near_s + (uint32_t)nuc_near;
+      near += (uint32_t)near_s * ORC_SAMPLE_TIE;
     }
+    near += (uint32_t)nuc_near;
 
     /* outputs: path nodes root..best in depth order, their tokens, then the sample */
     int D = depth[best];
@@ -603,7 +611,7 @@ int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *t
       orc_uniforms(seed, round, 0u, b, i - 1, &ua, &us);
       int near_s = 0;
       tok = orc_sample_residual(p, qi, V, us, &near_s);
-      near += (uint32_t)near_s;
+      near += (uint32_t)near_s * ORC_SAMPLE_TIE;
       break;
     }
     if (i > gamma) { /* all drafts accepted: bonus from the last row (node gamma) */
@@ -616,7 +624,7 @@ int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *t
         orc_uniforms(seed, round, 0u, b, gamma, &ua, &us);
         int near_s = 0;
         tok = orc_sample_residual(p, NULL, V, us, &near_s);
-        near += (uint32_t)near_s;
+        near += (uint32_t)near_s * ORC_SAMPLE_TIE;
       }
     }
     near += (uint32_t)nuc_near;
@@ -779,7 +787,7 @@ int orc_accept_tree_recursive(int dtype, int B, int N, int V, const int32_t *par
       int near_s = 0;
       if (first < 0) { /* a leaf: the bonus from its p */
         tok = orc_sample_residual(pc, NULL, V, us, &near_s);
-        near += (uint32_t)near_s;
+        near += (uint32_t)near_s * ORC_SAMPLE_TIE;
         break;
       }
       orc_q_row(q, q_kind, dtype, b, Dq, depth[node] + 1, V, T, top_k, top_p, z, qd, &nuc_near);
@@ -821,7 +829,7 @@ int orc_accept_tree_recursive(int dtype, int B, int N, int V, const int32_t *par
         continue;
       }
       tok = orc_sample_residual(pc, qd, V, us, &near_s);
-      near += (uint32_t)near_s;
+      near += (uint32_t)near_s * ORC_SAMPLE_TIE;
       break;
     }
     near += (uint32_t)nuc_near;

@@ -49,6 +49,8 @@ constexpr int kMaxTopkBatches = 32;
 // its own).
 constexpr int kMaxGatherList = 2048;
 constexpr double kNearTie = 1e-6;
+// weight of one sample-class near tie in the packed near-tie word (decision ties count 1)
+constexpr uint32_t kSampleTie = 65536u;
 constexpr float kNearTieF = 1e-6f;
 
 // ------------------------------------------------- float-pair arithmetic
@@ -1488,7 +1490,8 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
     tk[depth] = s_tok;
     p.out_num_emitted[b] = depth + 1;
     p.out_num_accepted[b] = depth;
-    if (p.out_near_ties) p.out_near_ties[b] = (uint32_t)(s_nd + s_snear + nuc_near);
+    if (p.out_near_ties)
+      p.out_near_ties[b] = (uint32_t)(s_nd + nuc_near) + (uint32_t)s_snear * kSampleTie;
     if (p.commit && commit_L >= 0) p.cm.prefix_len[b] = commit_L + commit_count;
   }
 }

@@ -37,6 +37,13 @@ constexpr int kRecThreads = 512;
 constexpr int kRecWarps = kRecThreads / 32;
 constexpr int kRecMaxChunks = 1024;  // chunk sums kept by a CTA (chunks >= 1024 entries)
 constexpr double kRecNearTie = 1e-6;
+// Error bound of a residual mass formed here, in units of the target's probabilities:
+// each entry [p_j - c q_j]+ is formed in float from p_j and q_j that carry a few float
+// roundings each, so the sum over the vocabulary is off by at most about
+// kRecEntryErr * (1 + c) (the entries' magnitudes sum to 1 + c).  After rejections the
+// residual mass n can be small, and the relative error of anything divided by n grows
+// as (1 + c) / n: the near-tie windows widen by that bound where it exceeds 1e-6.
+constexpr double kRecEntryErr = 4.0 * 1.1920928955078125e-7;  // 4 float epsilons
 
 // One sequence's view of the current node's target row and the depth's q row.
 template <typename T>
@@ -121,7 +128,10 @@ __device__ int decide_child(const AcceptParams &p, const RowPair<T> &r, int b, i
     set_status(p.status, SV_DEV_ZERO_DRAFT_PROB);
     ratio = rx > 0.0 ? INFINITY : 0.0;
   }
-  return (u < ratio ? 1 : 0) | (fabs(u - ratio) < kRecNearTie ? 2 : 0);
+  // after a rejection (c > 0) the ratio divides by the float-formed residual mass n
+  const double win =
+      kRecNearTie + (c > 0.0 ? kRecEntryErr * (1.0 + c) / n * fmax(ratio, 1.0) : 0.0);
+  return (u < ratio ? 1 : 0) | (fabs(u - ratio) < win ? 2 : 0);
 }
 
 template <typename T>
@@ -137,8 +147,9 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
   const RowStat *tstat = p.stats + (size_t)b * N;
   const RowStat *qstat = p.stats + (size_t)p.B * N + (size_t)b * p.Dq;
 
-  // thread 0's running counts (near ties of decisions and empty residuals; nucleus cuts)
-  unsigned near = 0u;
+  // thread 0's running counts: near ties that can change a decision (near decisions,
+  // empty residuals handed to a sibling; nucleus cuts) and those of the final sample
+  unsigned near = 0u, near_smp = 0u;
   bool nuc = false;
 
   RowPair<T> r;
@@ -198,11 +209,13 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
       double part = 0.0;
       for (int j = tid; j < V; j += kRecThreads) part += (double)w_at<T>(r, j, c1f);
       const double tot = block_sum_d(part, s_red);
-      if (tot > 0.0) {
+      if (tot > kRecEntryErr * (1.0 + c1)) {
         c = c1;
         n = tot;
       } else if (tid == 0) {
-        ++near;  // no mass left: the residual stays as it was
+        // no mass left, or less than the rounding error of its sum: the residual stays
+        // as it was (a near tie: in exact arithmetic it may hold a little mass)
+        ++near;
       }
     }
     if (next >= 0) {
@@ -217,7 +230,9 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
   const int CH = max(1024, ((V + kRecMaxChunks - 1) / kRecMaxChunks + 31) / 32 * 32);
   const int nch = (V + CH - 1) / CH;
   float cf = (float)c_fin;
-  double tol = kRecNearTie * n;  // the page's 1e-6 window, in units of the normalised w
+  // the 1e-6 window in units of the normalised residual, or the rounding bound of the
+  // float-formed w (kRecEntryErr per unit of the entries' magnitudes) when that is wider
+  const double tol = fmax(kRecNearTie * n, kRecEntryErr * (1.0 + c_fin));
   for (int attempt = 0; attempt < 2; ++attempt) {
     for (int k = warp; k < nch; k += kRecWarps) {
       double s = 0.0;
@@ -234,9 +249,9 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
       if (lane == 0) s_total = s;
     }
     __syncthreads();
-    if (s_total > 0.0 || attempt == 1) break;
+    if (s_total > kRecEntryErr * (1.0 + (double)cf) || attempt == 1) break;
     // the residual has no mass: sample from the last residual itself
-    if (tid == 0) ++near;
+    if (tid == 0) ++near_smp;
     cf = (float)c;
     __syncthreads();  // s_total and s_chunk are rewritten by the second attempt
   }
@@ -305,7 +320,8 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
   __syncthreads();
 
   if (tid == 0) {
-    near += (unsigned)s_near + (nuc ? 1u : 0u);
+    near += nuc ? 1u : 0u;
+    near_smp += (unsigned)s_near;
     const int W = p.tree.Dmax + 1;
     const int D = p.tree.depth[node];
     int32_t *pn = p.out_path_nodes ? p.out_path_nodes + (size_t)b * W : nullptr;
@@ -322,7 +338,7 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
     tk[D] = s_tok;
     p.out_num_emitted[b] = D + 1;
     p.out_num_accepted[b] = D;
-    if (p.out_near_ties) p.out_near_ties[b] = near;
+    if (p.out_near_ties) p.out_near_ties[b] = near + near_smp * 65536u;
   }
 }
 

@@ -1,8 +1,10 @@
 """GPU token acceptance vs the CPU oracle, through the C ABI.
 
 Accepted lengths, paths and emitted token ids must be bit-identical on every sequence
-that neither side reports as a near tie (|u - p/q| < 1e-6 for a decision that
-matters, or a sample within 1e-6 of a CDF boundary); near ties are counted and bounded.
+that neither side reports as a decision near tie (|u - p/q| < 1e-6 for a decision that
+matters, or a near top-p cut); a sequence with only a sample near tie (the final sample
+within 1e-6 of a CDF boundary) is still compared on everything but its last token.
+Near ties are counted and bounded.
 """
 import math
 
@@ -13,30 +15,16 @@ from scipy import stats
 
 import oracle
 import speculative_decoding_verify_sv_gb300 as sv
+from accept_parity import compare
 from speculative_decoding_verify_sv_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
 
-def _compare(gpu, ref, keys, max_exempt_frac=0.01):
-    g = {k: v.cpu() for k, v in gpu.items()}
-    exempt = (g["near_ties"] > 0) | (ref["near_ties"] > 0)
-    keep = ~exempt
-    for k in keys:
-        a, b = g[k][keep], ref[k][keep]
-        if not torch.equal(a, b):
-            bad = torch.nonzero((g[k] != ref[k]).reshape(g[k].shape[0], -1).any(1) & keep).flatten()
-            raise AssertionError(f"{k} differs on sequences {bad[:10].tolist()}: "
-                                 f"gpu {g[k][bad[:3]].tolist()} oracle {ref[k][bad[:3]].tolist()}")
-    n_ex = int(exempt.sum())
-    assert n_ex <= max(2, max_exempt_frac * exempt.numel()), f"{n_ex} near-tie sequences"
-    if n_ex >= 5:
-        # the window is a worst-case bound: most flagged sequences still agree exactly
-        same = torch.ones(exempt.shape[0], dtype=torch.bool)
-        for k in keys:
-            same &= (g[k] == ref[k]).reshape(g[k].shape[0], -1).all(1)
-        assert int(same[exempt].sum()) >= 0.8 * n_ex, "near-tie sequences mostly disagree"
-    return n_ex
+def _compare(gpu, ref, keys, max_exempt_frac=0.01, max_sample_frac=None):
+    """Exact agreement outside the near ties each side reports (see accept_parity)."""
+    return compare(gpu, ref, keys, max_exempt_frac=max_exempt_frac,
+                   max_sample_frac=max_sample_frac)
 
 
 def _chain(mode, lg, q_kind=sv.Q_LOGITS, T=1.0, top_k=0, seed=3, rnd=1, q=None, top_p=1.0):
@@ -123,7 +111,7 @@ def test_select_ring_layouts(cuda_ok, dtype, V, B, q_probs):
         out, ref = _chain(sv.EXACT, lg, q_kind=sv.Q_PROBS_F32, q=qp, seed=8, rnd=5)
     else:
         out, ref = _chain(sv.EXACT, lg, seed=8, rnd=5)
-    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"], max_exempt_frac=0.15)
+    _compare(out, ref, ["tokens", "num_emitted", "num_accepted"], max_sample_frac=0.15)
     assert sv.sv_read_device_status() == 0
 
 
@@ -273,5 +261,5 @@ def test_full_size_workloads(cuda_ok, cfg):
                                      temperature=c["temperature"], top_k=c["top_k"],
                                      seed=w["seed"], round_=0)
             keys = ["tokens", "num_emitted", "num_accepted", "path_nodes"]
-        _compare(out, ref, keys, max_exempt_frac=0.05 if c["V"] <= 32000 else 0.15)
+        _compare(out, ref, keys, max_sample_frac=0.05 if c["V"] <= 32000 else 0.15)
     assert sv.sv_read_device_status() == 0

@@ -1,6 +1,7 @@
 """Exact tree acceptance with siblings tried in turn, on the GPU against the oracle: the
 emitted tokens, counts and path must be identical except on sequences that either side
-reports as a near tie (bounded, as for the other acceptance tests)."""
+reports as a decision near tie; with only a sample near tie, everything but the last
+token (bounded, as for the other acceptance tests)."""
 import numpy as np
 import pytest
 import torch
@@ -48,7 +49,7 @@ def test_chain_large_vocab(cuda_ok):
     toks[:, 1:] = lg["draft_tokens"]
     out, ref = _run(lg["target_logits"], lg["draft_logits"], sv.Q_LOGITS, wl.chain_parent(gamma),
                     toks, seed=9, round_=4)
-    _compare(out, ref, KEYS, max_exempt_frac=0.15)
+    _compare(out, ref, KEYS, max_sample_frac=0.15)
     assert sv.sv_read_device_status() == 0
 
 
@@ -113,3 +114,27 @@ def test_bad_token_is_rejected_and_reported(cuda_ok):
     _compare(out, ref, KEYS, max_exempt_frac=1.0)
     assert torch.all(out["path_nodes"][:, 1].cpu() != 1)
     assert sv.sv_read_device_status() & sv.SV_DEV_BAD_TOKEN
+
+
+def test_siblings_with_small_residuals(cuda_ok):
+    """q close to p (draft logits = target logits + N(0, 0.05)): a rejection leaves a
+    residual of small mass (the total variation between p and q, a few percent), and the
+    next siblings are decided against it.  The kernel forms each residual entry in float,
+    so its near-tie windows widen with (1 + c) / n; outside them every output equals the
+    oracle's, taken in double."""
+    B, m, V = 2048, 4, 4000
+    g = torch.Generator().manual_seed(41)
+    z = torch.randn((B, 1, V), generator=g) * 3.0
+    zq = z + torch.randn((B, 1, V), generator=g) * 0.05
+    tl = torch.cat([z, torch.randn((B, m, V), generator=g) * 3.0], dim=1).to(torch.bfloat16)
+    ql = zq.to(torch.bfloat16)
+    qprob = torch.softmax(ql.float().double(), dim=-1)[:, 0]
+    toks = torch.zeros((B, m + 1), dtype=torch.int32)
+    toks[:, 1:] = torch.multinomial(qprob, m, replacement=True, generator=g).to(torch.int32)
+    out, ref = _run(tl, ql, sv.Q_LOGITS, [-1] + [0] * m, toks, seed=13, round_=2)
+    n_dec, n_smp = _compare(out, ref, KEYS, max_exempt_frac=0.02, max_sample_frac=0.05)
+    taken = ref["path_nodes"][:, 1]
+    # most first children pass; some sequences reach the later siblings through small
+    # residuals
+    assert int((taken == 1).sum()) > 0.8 * B
+    assert int(((taken > 1) | (taken == -1)).sum()) > 20
