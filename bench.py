@@ -3,8 +3,10 @@
 
 A step is one pass of the whole hot path over one batch: tree attention (one layer),
 token acceptance over the vocabulary, and the KV commit of the accepted path.
-Default workload: the 64-node Medusa tree, bf16, B=8, 32 heads x 128, prefix 2048,
-vocab 32000, exact sampling at T=1.
+Default workload (the headline line): ragged-paged, the largest of the five -- B=256
+chains of 4 drafts, GQA 32q/8kv x 128, prefixes U{512..8192} in a paged cache of
+16-token blocks, vocab 152064, exact sampling at T=1.  The other four workloads follow
+under "per_workload" (device-timed, fewer steps).
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides; each step is timed with CUDA events on the
@@ -39,6 +41,7 @@ if ROOT not in sys.path:
 import torch  # noqa: E402
 
 METRIC = "verified candidate tokens/s at 1 GB300; verify-step HBM GB/s vs peak"
+ALL_CONFIGS = (1, 2, 3, 4, 5)
 UNIT = "candidate tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -51,7 +54,13 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, help="workload id 1..5 (default 2)")
+    ap.add_argument("--config", type=int, default=5,
+                    help="workload id 1..5 (default 5, ragged-paged: the largest)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (small profiling captures)")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time only --config (no per_workload lines for the others)")
+    ap.add_argument("--per-workload-steps", type=int, default=30)
     ap.add_argument("--mode", choices=["exact", "greedy"], default=None)
     ap.add_argument("--preheat-s", type=float, default=1.0,
                     help="untimed seconds of steps before warm-up (clock ramp)")
@@ -185,13 +194,15 @@ def committed_traffic(kernel_file: str, workload: str):
     return None
 
 
-def attention_bytes(w) -> int:
+def attention_bytes(w, prefix_len=None) -> int:
     """Algorithmic bytes of one tree-attention launch: prefix K and V read once, tree
-    Q/K/V read, O written."""
+    Q/K/V read, O written.  prefix_len: the lengths the launch reads (default: the
+    workload's, as generated)."""
     c = w["cfg"]
     es = 4 if c["dtype"] == torch.float32 else 2
     B, N, Hq, Hkv, D = c["B"], w["N"], c["Hq"], c["Hkv"], c["D"]
-    prefix = int(w["prefix_len"].sum().item()) * Hkv * D * es * 2
+    lens = w["prefix_len"] if prefix_len is None else prefix_len
+    prefix = int(lens.sum().item()) * Hkv * D * es * 2
     tree = B * N * (2 * Hq + 2 * Hkv) * D * es
     return prefix + tree
 
@@ -204,27 +215,35 @@ def accept_bytes(w) -> int:
     return B * (N + w["Dmax"]) * V * es
 
 
-def attention_flops(w) -> int:
+def attention_flops(w, prefix_len=None) -> int:
     """Algorithmic flops of one tree-attention launch: 4*D per (query row, attended key);
     a node attends to the prefix and to its root path (depth + 1 tree keys)."""
     from speculative_decoding_verify_sv_gb300 import workloads as wl
     c = w["cfg"]
     B, N, Hq, D = c["B"], w["N"], c["Hq"], c["D"]
+    lens = w["prefix_len"] if prefix_len is None else prefix_len
     path_keys = sum(d + 1 for d in wl.depths(w["parent"]))
-    keys = int(w["prefix_len"].sum().item()) * N * Hq + B * Hq * path_keys
+    keys = int(lens.sum().item()) * N * Hq + B * Hq * path_keys
     return 4 * keys * D
+
+
+def workload_name(c, cfg_id) -> str:
+    return f"{c['name']} (config {cfg_id})"
 
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args, dist: Dist):
+def time_workload(args, dist: Dist, cfg_id: int, K: int, warmup: int, preheat_s: float,
+                  batch=None):
+    """Time K verify steps of workload cfg_id on this rank's GPU (device time, CUDA events
+    on the launch stream, L2 flushed between steps).  Returns the measurements and the
+    objects the end-to-end leg reuses."""
     import speculative_decoding_verify_sv_gb300 as sv
     from speculative_decoding_verify_sv_gb300 import workloads as wl
     from speculative_decoding_verify_sv_gb300.step import VerifyStep
 
     dev = torch.device("cuda", dist.local_rank)
-    torch.cuda.set_device(dev)
-    w = wl.make_workload(args.config, device=dev)
+    w = wl.make_workload(cfg_id, device=dev, B=batch)
     c = w["cfg"]
     mode_name = args.mode or c["mode"]
     mode = sv.EXACT if mode_name == "exact" else sv.GREEDY
@@ -235,7 +254,10 @@ def run_ours(args, dist: Dist):
                       dtype=c["dtype"], mode=mode, q_kind=sv.Q_LOGITS,
                       temperature=c["temperature"], top_k=c["top_k"], chain=chain, device=dev)
     toks = w["draft_tokens"] if chain else w["node_tokens"]
+    # every step starts from these lengths (the commit advances them; prepare() restores)
     prefix0 = w["prefix_len"].clone()
+    a_bytes = attention_bytes(w, prefix0)
+    a_flops = attention_flops(w, prefix0)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 1 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -262,7 +284,7 @@ def run_ours(args, dist: Dist):
     # pre-heat (clock ramp), then the warm-up steps
     sampler = ClockSampler(dev.index)
     sampler.start()
-    t_end = time.perf_counter() + args.preheat_s
+    t_end = time.perf_counter() + preheat_s
     i = 0
     while time.perf_counter() < t_end:
         prepare()
@@ -270,7 +292,7 @@ def run_ours(args, dist: Dist):
         i += 1
         if i % 20 == 0:
             torch.cuda.synchronize()
-    for j in range(args.warmup):
+    for j in range(warmup):
         prepare()
         device_step(j)
     torch.cuda.synchronize()
@@ -311,7 +333,6 @@ def run_ours(args, dist: Dist):
             g.replay()
         ev[2].record(stream)
 
-    K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     dist.barrier()
     torch.cuda.synchronize()
@@ -333,22 +354,65 @@ def run_ours(args, dist: Dist):
     tot = [e[0].elapsed_time(e[2]) for e in evs]
     att = [e[0].elapsed_time(e[1]) for e in evs]
     acc = [e[1].elapsed_time(e[2]) for e in evs]
-    dev_ms = dist.max(sum(tot))
+    tc = sv.sv_tree_attention_path(c["dtype"], w["N"], c["Hq"], c["Hkv"], c["D"],
+                                   w.get("block_size", 16) if c["paged"] else 0) == 1
+    return dict(w=w, c=c, step=step, toks=toks, prepare=prepare, stream=stream,
+                mode=mode, mode_name=mode_name, launch_mode=launch_mode, tot=tot, att=att,
+                acc=acc, wall=wall, launches=launches, clocks=clocks, status=status,
+                emitted=float(emitted.sum().item()), a_bytes=a_bytes, a_flops=a_flops,
+                acc_bytes=accept_bytes(w), tc=tc, name=workload_name(c, cfg_id))
+
+
+def _kernel_figures(r):
+    """Mean attention and acceptance times (ms) of one run and their algorithmic GB/s."""
+    a_ms = statistics.mean(r["att"])
+    c_ms = statistics.mean(r["acc"])
+    a_gbs = r["a_bytes"] / (a_ms / 1e3) / 1e9
+    c_gbs = r["acc_bytes"] / (c_ms / 1e3) / 1e9
+    return a_ms, c_ms, a_gbs, c_gbs
+
+
+def per_workload_line(args, dist, cfg_id, K, peak):
+    """Device-timed figures of one more workload (no end-to-end or CPU leg)."""
+    r = time_workload(args, dist, cfg_id, K, max(3, min(args.warmup, 5)), 0.3)
+    a_ms, c_ms, a_gbs, c_gbs = _kernel_figures(r)
+    c = r["c"]
+    cand = c["B"] * (r["w"]["N"] - 1)
+    dev_ms = dist.max(sum(r["tot"]))
+    out = {
+        "workload": r["name"], "steps": K, "ms_per_step": dev_ms / K,
+        "value": dist.sum(cand * K) / (dev_ms / 1e3), "unit": UNIT,
+        "attention_us": 1e3 * a_ms, "attention_gbs": a_gbs, "attention_frac": a_gbs / peak,
+        "attention_tflops": r["a_flops"] / (a_ms / 1e3) / 1e12,
+        "attention_kernel": "attn_tc_kernel" if r["tc"] else "general (mma.sync / FFMA)",
+        "accept_us": 1e3 * c_ms, "accept_gbs": c_gbs, "accept_frac": c_gbs / peak,
+        "algorithmic_bytes": {"attention": r["a_bytes"], "accept": r["acc_bytes"]},
+        "clocks": r["clocks"], "device_status": r["status"],
+    }
+    del r
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, dist: Dist):
+    import speculative_decoding_verify_sv_gb300 as sv  # noqa: F401 (fails loudly if missing)
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = measured_peaks()
+    K = args.steps
+    r = time_workload(args, dist, args.config, K, args.warmup, args.preheat_s, args.batch)
+    w, c = r["w"], r["c"]
+    dev_ms = dist.max(sum(r["tot"]))
     cand = c["B"] * (w["N"] - 1)
     units = dist.sum(cand * K)
     value = units / (dev_ms / 1e3)
-    emitted_total = dist.sum(float(emitted.sum().item()))
-
-    peak, peak_kind = measured_peaks()
-    a_bytes = attention_bytes(w)
-    a_ms = statistics.mean(att)
-    achieved = a_bytes / (a_ms / 1e3) / 1e9
-    workload_name = f"{c['name']} (config {args.config})"
-    tc = sv.sv_tree_attention_path(c["dtype"], w["N"], c["Hq"], c["Hkv"], c["D"],
-                                   w.get("block_size", 16) if c["paged"] else 0) == 1
-    kernel_file = "attention_tc.cu" if tc else "attention.cu"
-    kernel_name = ("attn_tc_kernel (the one kernel of a sv_tree_attention call)" if tc else
+    emitted_total = dist.sum(r["emitted"])
+    a_ms, c_ms, achieved, c_gbs = _kernel_figures(r)
+    kernel_file = "attention_tc.cu" if r["tc"] else "attention.cu"
+    kernel_name = ("attn_tc_kernel (the one kernel of a sv_tree_attention call)" if r["tc"] else
                    "attn_mma_kernel / attn_f32_kernel + split merge")
+    name = r["name"] if args.batch is None else f"{r['name']} with B={c['B']}"
 
     result = {
         "metric": METRIC,
@@ -364,41 +428,55 @@ def run_ours(args, dist: Dist):
         "dtype": "bf16" if c["dtype"] == torch.bfloat16 else "f32",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
         "config": {
-            "workload": workload_name,
+            "workload": name,
             "B": c["B"], "tree_nodes": w["N"], "candidates_per_step": cand,
             "Hq": c["Hq"], "Hkv": c["Hkv"], "D": c["D"], "V": c["V"],
             "prefix": c["L"] if not isinstance(c["L"], tuple) else f"U{{{c['L'][0]}..{c['L'][1]}}}",
-            "paged": c["paged"], "mode": mode_name, "temperature": c["temperature"],
+            "paged": c["paged"], "mode": r["mode_name"], "temperature": c["temperature"],
             "top_k": c["top_k"], "l2": "flushed between steps: 2x L2 written, then another 2x L2 read, outside events",
             "timing": "CUDA events per step on the launch stream; sum over K steps",
-            "launch": launch_mode,
+            "launch": r["launch_mode"],
             "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU",
         },
         "roofline": {
             "kernel": kernel_name,
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
-            "algorithmic_bytes_per_launch": a_bytes,
-            "traffic": committed_traffic(kernel_file, workload_name),
+            "algorithmic_bytes_per_launch": r["a_bytes"],
+            "traffic": committed_traffic(kernel_file, name),
+        },
+        "roofline_accept": {
+            "kernel": "accept_stats_kernel + accept_select_kernel (KV commit fused)",
+            "bound": "hbm", "achieved": c_gbs, "peak": peak, "unit": "GB/s",
+            "frac": c_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
+            "algorithmic_bytes_per_launch": r["acc_bytes"],
+            "traffic": committed_traffic("accept.cu", name),
         },
         "breakdown_us": {
-            "attention": 1e3 * a_ms, "accept_and_commit": 1e3 * statistics.mean(acc),
-            "accept_gbs": accept_bytes(w) / (statistics.mean(acc) / 1e3) / 1e9,
-            "attention_tflops": attention_flops(w) / (a_ms / 1e3) / 1e12,
+            "attention": 1e3 * a_ms, "accept_and_commit": 1e3 * c_ms,
+            "accept_gbs": c_gbs,
+            "attention_tflops": r["a_flops"] / (a_ms / 1e3) / 1e12,
         },
         "emitted_tokens_per_s": emitted_total / (dev_ms / 1e3),
         "mean_accepted": emitted_total / (c["B"] * K * dist.world) - 1.0,
         "acceptance_rate": (emitted_total / (c["B"] * K * dist.world) - 1.0) / max(1, w["Dmax"]),
-        "wall_s_timed_region": wall,
-        "gpu_launches": launches,
-        "device_status": status,
-        "clocks": clocks,
+        "wall_s_timed_region": r["wall"],
+        "gpu_launches": r["launches"],
+        "device_status": r["status"],
+        "clocks": r["clocks"],
     }
 
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, dist, w, step, prepare, stream, toks, cand)
+        result["e2e"] = run_e2e(args, dist, w, r["step"], r["prepare"], r["stream"], r["toks"],
+                                cand)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, mode)
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, r["mode"])
+    if not args.no_per_workload and args.batch is None:
+        del r, w
+        torch.cuda.empty_cache()
+        K_pw = max(3, min(K, args.per_workload_steps))
+        result["per_workload"] = [per_workload_line(args, dist, i, K_pw, peak)
+                                  for i in sorted(ALL_CONFIGS) if i != args.config]
     return result
 
 

@@ -9,7 +9,8 @@
 // A unit's keys are tiles of BN: tile 0 = the tree nodes (masked by ancestor bits),
 // tiles 1.. = the prefix.  The flattened (unit, tile) space is split evenly over one
 // persistent CTA per SM (stream-K); a unit cut by a CTA boundary is written as fp32
-// partials and merged by a second kernel with log-sum-exp weights.
+// partials by the CTAs holding its later tiles, and the CTA holding its first tiles merges
+// them with log-sum-exp weights in the same launch (cooperative, so all CTAs are resident).
 //
 // Per CTA, warp roles:
 //   producer warp   TMA loads of Q (per piece) and K/V tiles into a STAGES-deep ring;
@@ -88,6 +89,16 @@ struct TcLayout {
   static constexpr int THREADS = 32 * (NSW + 2);
   static_assert(NEED_COLS <= 512, "TMEM columns");
 };
+
+// Byte offset of 16-byte unit `rem` (of the KB * 8 in a row) of row r of a K/V tile, before
+// the swizzle.  Plain layout: one block of BN rows x 128 bytes per 64-column half.  Grouped
+// layout (pages loaded with both halves in one copy; D = 128): 8-row groups of 2 KB, each
+// holding the 8 rows of the first half, then of the second.
+template <class Lay>
+__device__ __forceinline__ int kv_unit_offset(bool grouped, int r, int rem) {
+  return grouped ? (r >> 3) * (Lay::KB * 1024) + (rem >> 3) * 1024 + (r & 7) * 128 + (rem & 7) * 16
+                 : (rem >> 3) * Lay::KV_BLOCK + r * 128 + (rem & 7) * 16;
+}
 
 // Iterator over the pieces (unit, tile range) of one CTA's share of the work.
 struct PieceIter {
@@ -184,6 +195,7 @@ __device__ __forceinline__ long long block_scan(long long x, long long *red, lon
 // it.  Kept out of line so that the row loop's code stays small.  False if a wait gave up.
 template <class Lay, int BN, int STAGES, int PBUF>
 __device__ __noinline__ bool idle_piece(int N, int t0, int n, bool publish, int g, int qi, int L,
+                                        bool grouped,
                                         uint64_t *s_full, uint64_t *s_free, uint64_t *v_full,
                                         uint64_t *p_full, uint64_t *o_free, uint64_t *pub, uint8_t *sV,
                                         volatile int *abort_flag) {
@@ -200,8 +212,7 @@ __device__ __noinline__ bool idle_piece(int N, int t0, int n, bool publish, int 
       constexpr int per_row = Lay::KB * 8;
       for (int i = threadIdx.x; i < (BN - nvalid) * per_row; i += 32 * Lay::NSW) {
         const int r = nvalid + i / per_row, rem = i % per_row;
-        *reinterpret_cast<uint4 *>(vt + (rem >> 3) * Lay::KV_BLOCK + r * 128 + (rem & 7) * 16) =
-            make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(vt + kv_unit_offset<Lay>(grouped, r, rem)) = make_uint4(0, 0, 0, 0);
       }
     }
     if (gk >= PBUF && !mbar_wait(&p_full[pb], ((gk / PBUF) - 1) & 1, abort_flag)) return false;
@@ -460,9 +471,16 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         if (valid) {
           const int pos = src.pos0 + lane * p.page_rows;
           const int prow = src.blk * p.block_size + pos % p.block_size;
-          for (int kb = 0; kb < Lay::KB; ++kb)
-            tma_load_3d_hint(dst + kb * Lay::KV_BLOCK + lane * p.page_rows * 128, map, kb * 64,
-                             src.kvh, prow, full, stream_policy);
+          if (p.pg_grouped) {
+            // both halves of the page in one copy: rows prow .. prow + page_rows (a multiple
+            // of 8) land as page_rows / 8 groups of 2 KB
+            tma_load_5d_hint(dst + lane * p.page_rows * (Lay::KB * 128), is_v ? &p.tm_vc5 : &p.tm_kc5,
+                             0, 0, 0, prow >> 3, src.kvh, full, stream_policy);
+          } else {
+            for (int kb = 0; kb < Lay::KB; ++kb)
+              tma_load_3d_hint(dst + kb * Lay::KV_BLOCK + lane * p.page_rows * 128, map, kb * 64,
+                               src.kvh, prow, full, stream_policy);
+          }
         }
       }
       return true;
@@ -620,11 +638,15 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       const uint64_t dk = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dp = sdesc_sw128(smem_u32(sP), 16, 1024);
       const uint64_t dv = sdesc_sw128(smem_u32(sV), Lay::KV_BLOCK, 1024);
+      // the grouped layout of paged prefix tiles: 8-row groups 2 KB apart, the second
+      // 64-column half 1 KB after the first
+      const uint64_t dk_g = sdesc_sw128(smem_u32(sK), 16, Lay::KB * 1024);
+      const uint64_t dv_g = sdesc_sw128(smem_u32(sV), 1024, Lay::KB * 1024);
       PieceIter its = it;  // S side of the walk over this CTA's tiles
       Piece pcs;
       int s_qi = -1, s_rem = 0, gs = 0, gp = 0;
       bool s_first = false, s_done = false;
-      uint8_t m_first[4];
+      uint8_t m_first[4], m_grp[4];
       int m_qi[4];
       unsigned long long idle_t0 = 0;
       uint32_t idle_n = 0;
@@ -633,6 +655,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         if (gp < gs) {
           const int gk = gp, s = gk % STAGES, pb = gk % PBUF;
           const bool first = m_first[gk & 3];
+          const bool grp = m_grp[gk & 3];
           const int qi = m_qi[gk & 3];
           if (mbar_test(&p_full[pb], (gk / PBUF) & 1) &&
               (!first || qi == 0 || mbar_test(o_free, (qi - 1) & 1)) &&
@@ -644,7 +667,9 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
               for (int kk = 0; kk < BN / 16; ++kk) {
                 const uint64_t a = dp + (uint64_t)((pb * Lay::P_BYTES + m * Lay::P_TILE +
                                                      (kk >> 2) * Lay::P_BLOCK + (kk & 3) * 32) >> 4);
-                const uint64_t bd = dv + (uint64_t)((s * Lay::KV_BYTES + kk * 16 * 128) >> 4);
+                const uint64_t bd =
+                    grp ? dv_g + (uint64_t)((s * Lay::KV_BYTES + kk * 2 * (Lay::KB * 1024)) >> 4)
+                        : dv + (uint64_t)((s * Lay::KV_BYTES + kk * 16 * 128) >> 4);
                 umma_bf16(tmem + (uint32_t)(Lay::S_COLS + m * D), a, bd, idO,
                           (!first || kk > 0) ? 1u : 0u);
               }
@@ -670,6 +695,8 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
               mbar_test(&k_full[s], (gk / STAGES) & 1) &&
               (gk < 2 || mbar_test(&s_free[j], ((gk >> 1) - 1) & 1))) {
             tc_fence_after();
+            // tile pcs.t1 - s_rem of its unit; tile 0 holds the tree nodes (plain layout)
+            const bool grp = p.pg_grouped && pcs.t1 - s_rem != 0;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
 #pragma unroll
@@ -677,7 +704,8 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
                 const uint64_t a = dq + (uint64_t)((qb * Lay::Q_BYTES + (kk >> 2) * Lay::Q_BLOCK +
                                                      m * kRows * 128 + (kk & 3) * 32) >> 4);
                 const uint64_t bd =
-                    dk + (uint64_t)((s * Lay::KV_BYTES + (kk >> 2) * Lay::KV_BLOCK + (kk & 3) * 32) >> 4);
+                    grp ? dk_g + (uint64_t)((s * Lay::KV_BYTES + (kk >> 2) * 1024 + (kk & 3) * 32) >> 4)
+                        : dk + (uint64_t)((s * Lay::KV_BYTES + (kk >> 2) * Lay::KV_BLOCK + (kk & 3) * 32) >> 4);
                 umma_bf16(tmem + (uint32_t)((j * MT + m) * BN), a, bd, idS, kk > 0);
               }
             }
@@ -685,6 +713,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
             umma_commit(&k_empty[s]);
             if (s_rem == 1) umma_commit(&q_empty[qb]);
             m_first[gk & 3] = s_first;
+            m_grp[gk & 3] = grp;
             m_qi[gk & 3] = s_qi;
             s_first = false;
             --s_rem;
@@ -759,7 +788,8 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       const bool warp_idle = CP == 1 && __all_sync(0xFFFFFFFFu, !valid_row);
       const int L = clamp_len(p, pc.b);
       if (warp_idle) {  // every row of this warp is padding: barriers only
-        if (!idle_piece<Lay, BN, STAGES, PBUF>(p.N, pc.t0, n, pc.t0 > 0, g, qi, L, s_full, s_free, v_full,
+        if (!idle_piece<Lay, BN, STAGES, PBUF>(p.N, pc.t0, n, pc.t0 > 0, g, qi, L, p.pg_grouped != 0,
+                                              s_full, s_free, v_full,
                                               p_full, o_free, pub, sV, abort_flag)) {
           ok = false;
           break;
@@ -785,10 +815,10 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           if (!mbar_wait(&v_full[s], (gk / STAGES) & 1, abort_flag)) return false;
           uint8_t *vt = sV + s * Lay::KV_BYTES;
           constexpr int per_row = Lay::KB * 8;
+          const bool grouped = p.pg_grouped != 0;  // (a prefix tile)
           for (int i = tid_sm; i < (BN - nvalid) * per_row; i += 32 * NSW) {
             const int r = nvalid + i / per_row, rem = i % per_row;
-            *reinterpret_cast<uint4 *>(vt + (rem >> 3) * Lay::KV_BLOCK + r * 128 + (rem & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(vt + kv_unit_offset<Lay>(grouped, r, rem)) = make_uint4(0, 0, 0, 0);
           }
           return true;
         };
@@ -1219,6 +1249,24 @@ bool map3d(CUtensorMap *m, const void *base, int D, int heads, long long rows, i
          CUDA_SUCCESS;
 }
 
+// The pages of a paged cache as a 5-D bf16 view (64 columns, 8 rows, 2 column halves,
+// groups of 8 rows, heads) with a (64, 8, 2, page_rows / 8, 1) box, 128-byte swizzle: one
+// copy brings both 64-column halves of a page, as page_rows / 8 groups of 2 KB (the grouped
+// tile layout).  D = 128 only.  rows must be a multiple of 8.
+bool map5d_pages(CUtensorMap *m, const void *base, int heads, long long rows, int page_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc || rows % 8 != 0 || page_rows % 8 != 0 || page_rows / 8 > 256) return false;
+  const cuuint64_t row_bytes = (cuuint64_t)128 * 2 * heads;  // one position, all heads
+  cuuint64_t dims[5] = {64, 8, 2, (cuuint64_t)(rows / 8), (cuuint64_t)heads};
+  cuuint64_t strides[4] = {row_bytes, 128, 8 * row_bytes, 256};
+  cuuint32_t box[5] = {64u, 8u, 2u, (cuuint32_t)(page_rows / 8), 1u};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool tc_eligible(sv_dtype dt, int N, int Hq, int Hkv, int D, int paged_block_size) {
@@ -1280,6 +1328,11 @@ cudaError_t launch_attention_tc(const AttnParams &a, const TcPlan &pl, void *ws,
         !map3d(&p.tm_vc, a.cache_v, a.D, a.Hkv, rows, 1, p.page_rows))
       return cudaErrorInvalidValue;
     p.paged = 1;
+    // pages shorter than a tile: one copy per page (both column halves) instead of two,
+    // into the grouped layout; the plain layout stays when the 5-D view is not available
+    p.pg_grouped = a.D == 128 && p.page_rows < BN &&
+                   map5d_pages(&p.tm_kc5, a.cache_k, a.Hkv, rows, p.page_rows) &&
+                   map5d_pages(&p.tm_vc5, a.cache_v, a.Hkv, rows, p.page_rows);
   }
   uint8_t *w = static_cast<uint8_t *>(ws);
   p.hdr = reinterpret_cast<unsigned long long *>(w + pl.off_hdr);

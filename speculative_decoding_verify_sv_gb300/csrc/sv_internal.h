@@ -54,6 +54,10 @@ cudaError_t launch_attention(sv_dtype dt, const AttnParams &p, cudaStream_t s);
 // flattened (unit, key tile) space.
 struct TcParams {
   CUtensorMap tm_q, tm_kt, tm_vt, tm_kc, tm_vc;  // Q, tree K/V, cache K/V (128B swizzle)
+  // paged cache pages as (64, 8, 2, rows/8, Hkv) boxes: both 64-column halves of a page in
+  // one copy, into the grouped tile layout (used when pg_grouped != 0)
+  CUtensorMap tm_kc5, tm_vc5;
+  int pg_grouped;
   const int32_t *prefix_len;
   const int32_t *block_table;
   void *out;

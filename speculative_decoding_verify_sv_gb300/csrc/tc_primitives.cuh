@@ -104,6 +104,17 @@ __device__ __forceinline__ void tma_load_3d_hint(void *smem_dst, const CUtensorM
       : "memory");
 }
 // L2 policy under which every line is evicted first (streamed, read-once data).
+// 5-D tiled load (used for pages whose two 64-column halves land in one box).
+__device__ __forceinline__ void tma_load_5d_hint(void *smem_dst, const CUtensorMap *map, int c0,
+                                                 int c1, int c2, int c3, int c4, uint64_t *bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));

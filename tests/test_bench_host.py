@@ -137,3 +137,15 @@ def test_throttle_reasons_that_reject_a_run_are_reported():
     assert s.stop()["reasons"] == ["no samples"]
     s = bench.ClockSampler(0)  # nvidia-smi could not be started
     assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_attention_bytes_use_the_lengths_the_launch_reads():
+    """The commit advances prefix_len after every step; the roofline counts the lengths
+    each timed launch starts from (restored between steps), passed explicitly."""
+    w = _shape_only(2)
+    start = w["prefix_len"].clone()
+    advanced = start + 5  # what prefix_len holds after a step that emitted 5 tokens
+    w["prefix_len"] = advanced
+    assert bench.attention_bytes(w, start) == HAND[2][0]
+    assert bench.attention_bytes(w) == HAND[2][0] + 8 * 5 * 32 * 128 * 2 * 2
+    assert bench.attention_flops(w, start) == 4 * 128 * (8 * 64 * 32 * 2048 + 8 * 32 * 256)
