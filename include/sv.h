@@ -77,8 +77,13 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 typedef enum { SV_GREEDY = 0, SV_EXACT = 1 } sv_mode;
 /* How the draft distribution q is given: as float32 probabilities used as they are,
  * or as draft logits (dtype of the target logits) to which the same temperature and
- * top-k are applied as to the target. */
-typedef enum { SV_Q_PROBS_F32 = 0, SV_Q_LOGITS = 1 } sv_q_kind;
+ * top-k are applied as to the target, or -- for deterministic drafts such as prompt-lookup
+ * copies (jennyma11 blog, section "Prompt Lookup / N-gram": the copied tokens still go to
+ * the target's verification) -- as a one-hot row at each draft token: q(x) = 1 for the
+ * draft x and 0 elsewhere, so a draft is accepted iff u_acc < p(x) and the token after a
+ * rejection comes from norm([p - e_x]+), p without x.  With SV_Q_DRAFT_ONEHOT no q rows
+ * exist (the q pointer is not read and may be NULL); chains only. */
+typedef enum { SV_Q_PROBS_F32 = 0, SV_Q_LOGITS = 1, SV_Q_DRAFT_ONEHOT = 2 } sv_q_kind;
 
 /* The KV prefix cache of one attention layer.
  *  contiguous (block_table == NULL): k, v are [B, Lmax, Hkv, D]; sequence b's prefix
@@ -145,8 +150,12 @@ size_t sv_tree_attention_workspace_size(sv_dtype dt, int B, int N, int Hq, int H
  * Uniforms: Philox4x32-10 with key (seed_lo, seed_hi) and counter (node, b, round_lo,
  * round_hi); u_acc = word0, u_smp = word1, u = ((w >> 8) + 0.5) * 2^-24.
  * target_logits [B,gamma+1,V] (row i = target distribution after node i); q
- * [B,gamma,V] (row i-1 = draft distribution of draft i; unused in greedy mode, may be
- * NULL); draft_tokens [B,gamma] int32.
+ * [B,gamma,V] (row i-1 = draft distribution of draft i; unused in greedy mode and with
+ * SV_Q_DRAFT_ONEHOT, may then be NULL); draft_tokens [B,gamma] int32.  A draft token of
+ * -1 ends that sequence's chain: a sequence with k < gamma drafts has -1 from position k
+ * on (what sv_ngram_draft writes), and when its k drafts are all accepted the bonus is
+ * drawn from row k.  (Tokens after the first -1 are not decided; values outside [0, V)
+ * other than -1 are bad tokens.)
  * Outputs: out_tokens [B,gamma+1] (accepted drafts then the sampled token, -1 after),
  * out_num_emitted [B] (= accepted + 1), out_num_accepted [B], out_near_ties [B] (the
  * packed near-tie word: decisions with |u_acc - ratio| < 1e-6 and near top-p cuts in
@@ -177,7 +186,8 @@ sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int
  * The emitted tokens are those of the path nodes 1..a*, then a token sampled with
  * u_smp(b, a*) from norm([p_{a*} - q_{d(a*)+1}]+) if a* has children, else from p_{a*}.
  * parent [N] host; node_tokens [B,N] (column 0, the root, is not read);
- * target_logits [B,N,V]; q [B,Dq,V] with row d-1 = depth d (Dq >= tree depth).
+ * target_logits [B,N,V]; q [B,Dq,V] with row d-1 = depth d (Dq >= tree depth); q_kind
+ * SV_Q_PROBS_F32 or SV_Q_LOGITS (SV_Q_DRAFT_ONEHOT: SV_ERR_UNSUPPORTED in exact mode).
  * temperature, top_k, top_p, the uniforms and the near-tie reports as sv_accept_chain.
  * Outputs (Dmax = tree depth): out_path_nodes [B,Dmax+1] (root..a*, -1 after),
  * out_tokens [B,Dmax+1], out_num_emitted [B], out_num_accepted [B], out_near_ties [B].

@@ -27,7 +27,8 @@ _lib = None
 
 F32, BF16, F64 = 0, 1, 2
 GREEDY, EXACT = 0, 1
-Q_PROBS_F32, Q_LOGITS = 0, 1
+Q_PROBS_F32, Q_LOGITS, Q_DRAFT_ONEHOT = 0, 1, 2
+SAMPLE_TIE = 65536  # weight of a sample-class near tie in the packed near-tie word
 
 
 def build(force: bool = False) -> str:
@@ -181,7 +182,7 @@ def tree_attention(q, k_tree, v_tree, cache_k, cache_v, prefix_len, parent, scal
 # ---------------------------------------------------------------- acceptance
 
 def _q_args(q, q_kind):
-    if q is None:
+    if q is None or q_kind == Q_DRAFT_ONEHOT:
         return None, 0
     q = _cpu(q)
     if q_kind == Q_PROBS_F32 and q.dtype != torch.float32:
@@ -226,7 +227,10 @@ def accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperature
 def accept_chain(mode, target_logits, q, q_kind, draft_tokens, temperature=1.0, top_k=0,
                  seed=0, round_=0, top_p=1.0):
     """Chain acceptance as the left-to-right procedure; returns a dict of CPU tensors.
-    top_p < 1 keeps the nucleus of the top-k distribution (needs 0 < top_k < V)."""
+    top_p < 1 keeps the nucleus of the top-k distribution (needs 0 < top_k < V).  A draft
+    of -1 ends a sequence's chain; q_kind Q_DRAFT_ONEHOT takes q = e_x at each draft (q
+    may be None).  near_ties packs decision ties (low 16 bits) and sample ties (times
+    SAMPLE_TIE)."""
     tl = _cpu(target_logits)
     dt = _dtype_code(tl)
     B, W, V = tl.shape

@@ -73,6 +73,7 @@
 #define ORC_EXACT 1
 #define ORC_Q_PROBS_F32 0
 #define ORC_Q_LOGITS 1
+#define ORC_Q_DRAFT_ONEHOT 2 /* deterministic drafts: q = e_x at each draft token x */
 #define ORC_NEAR_TIE 1e-6
 /* weight of one sample-class near tie in the packed near-tie word */
 #define ORC_SAMPLE_TIE 65536u
@@ -433,6 +434,10 @@ int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *par
     free(depth);
     return 2;
   }
+  if (!greedy && q_kind == ORC_Q_DRAFT_ONEHOT) { /* one-hot drafts: chains only */
+    free(depth);
+    return 4;
+  }
   int W = Dmax + 1;
 #pragma omp parallel for schedule(dynamic)
   for (int b = 0; b < B; ++b) {
@@ -553,7 +558,11 @@ int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *par
  * norm([p_{i-1} - q_i]+) and stop; if all pass, sample the bonus from p_gamma.
  * Greedy: accept while x_i == argmax z_{i-1}; then emit argmax of that row.
  * target_logits [B,gamma+1,V]; q [B,gamma,V]; draft_tokens [B,gamma];
- * out_tokens [B,gamma+1] (unused -1).  Node ids for the uniforms: draft i is node i. */
+ * out_tokens [B,gamma+1] (unused -1).  Node ids for the uniforms: draft i is node i.
+ * A draft of -1 ends the sequence's chain (a prompt lookup may propose fewer than gamma
+ * tokens): if the k drafts before it pass, the bonus comes from p_k.  q_kind
+ * ORC_Q_DRAFT_ONEHOT takes q_i = e_{x_i} (deterministic drafts: accept iff u < p(x_i), and
+ * after a rejection norm([p - e_x]+) is p without x); q is then not read. */
 int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *target_logits,
                      const void *q, int q_kind, const int32_t *draft_tokens, double T,
                      int top_k, double top_p, uint64_t seed, uint64_t round, int32_t *out_tokens,
@@ -570,9 +579,13 @@ int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *t
     uint32_t near = 0, flags = 0;
     int nuc_near = 0;  /* a nucleus cut of one of the rows used was a near tie */
     for (int i = 0; i < W; ++i) tk[i] = -1;
-    int i = 1, tok = -1;
+    int i = 1, tok = -1, ended = 0;
     for (; i <= gamma; ++i) {
       int x = draft_tokens[(size_t)b * gamma + (i - 1)];
+      if (x == -1) { /* no more drafts: the bonus is taken below */
+        ended = 1;
+        break;
+      }
       orc_load_row(target_logits, dtype, (size_t)b * W + (i - 1), V, z);
       if (greedy) {
         int amax = orc_argmax(z, V);
@@ -585,7 +598,11 @@ int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *t
         break;
       }
       orc_effective_dist(z, V, T, top_k, top_p, p, &nuc_near);
-      orc_q_row(q, q_kind, dtype, b, gamma, i, V, T, top_k, top_p, z, qi, &nuc_near);
+      if (q_kind == ORC_Q_DRAFT_ONEHOT) {
+        for (int j = 0; j < V; ++j) qi[j] = (j == x) ? 1.0 : 0.0;
+      } else {
+        orc_q_row(q, q_kind, dtype, b, gamma, i, V, T, top_k, top_p, z, qi, &nuc_near);
+      }
       double u_acc, u_smp;
       orc_uniforms(seed, round, 0u, b, i, &u_acc, &u_smp);
       int accepted = 0;
@@ -614,14 +631,15 @@ int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *t
       near += (uint32_t)near_s * ORC_SAMPLE_TIE;
       break;
     }
-    if (i > gamma) { /* all drafts accepted: bonus from the last row (node gamma) */
-      orc_load_row(target_logits, dtype, (size_t)b * W + gamma, V, z);
+    if (i > gamma || ended) { /* every draft present accepted: bonus from row (node) i-1 */
+      int last = i - 1;
+      orc_load_row(target_logits, dtype, (size_t)b * W + last, V, z);
       if (greedy) {
         tok = orc_argmax(z, V);
       } else {
         orc_effective_dist(z, V, T, top_k, top_p, p, &nuc_near);
         double ua, us;
-        orc_uniforms(seed, round, 0u, b, gamma, &ua, &us);
+        orc_uniforms(seed, round, 0u, b, last, &ua, &us);
         int near_s = 0;
         tok = orc_sample_residual(p, NULL, V, us, &near_s);
         near += (uint32_t)near_s * ORC_SAMPLE_TIE;
@@ -760,7 +778,7 @@ int orc_accept_tree_recursive(int dtype, int B, int N, int V, const int32_t *par
     depth[n] = orc_depth(parent, n);
     if (depth[n] > Dmax) Dmax = depth[n];
   }
-  if (Dq < Dmax) {
+  if (Dq < Dmax || q_kind == ORC_Q_DRAFT_ONEHOT) {
     free(depth);
     return 2;
   }

@@ -21,7 +21,7 @@ __all__ = [
     "sv_tree_attention_workspace_size", "sv_tree_attention_path", "sv_accept_chain", "sv_accept_tree",
     "sv_accept_workspace_size", "sv_accept_tree_noalloc", "sv_commit_kv", "sv_accept_tree_commit",
     "sv_accept_chain_commit", "sv_accept_tree_recursive", "sv_ngram_draft", "sv_tree_prepare", "sv_read_device_status",
-    "sv_version", "sv_kernel_launches", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "SV_MAX_TREE_NODES",
+    "sv_version", "sv_kernel_launches", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "Q_DRAFT_ONEHOT", "SV_MAX_TREE_NODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +30,7 @@ _LIB_PATH = os.path.join(_PKG, "_build", "libsv.so")
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_WORKSPACE, SV_ERR_CUDA = 0, 1, 2, 3, 4
 SV_F32, SV_BF16 = 0, 1
 GREEDY, EXACT = 0, 1
-Q_PROBS_F32, Q_LOGITS = 0, 1
+Q_PROBS_F32, Q_LOGITS, Q_DRAFT_ONEHOT = 0, 1, 2  # q as probabilities, draft logits, one-hot drafts
 SV_MAX_TREE_NODES = 64
 SV_DEV_BAD_TOKEN, SV_DEV_BAD_BLOCK, SV_DEV_BAD_PREFIX, SV_DEV_ZERO_DRAFT_PROB = 1, 2, 4, 8
 SV_DEV_TIMEOUT, SV_DEV_LAYOUT = 0x10, 0x20
@@ -263,12 +263,15 @@ def _accept_outputs(B, W, device, outs):
 def sv_accept_chain(mode, target_logits, q, q_kind, draft_tokens, temperature=1.0, top_k=0,
                     seed=0, round_=0, outs=None, workspace=None, stream=None, top_p=1.0) -> dict:
     """Chain acceptance; target_logits [B,gamma+1,V], q [B,gamma,V] (or None in greedy
-    mode), draft_tokens [B,gamma] int32.  Returns dict of device tensors."""
+    mode or with q_kind Q_DRAFT_ONEHOT), draft_tokens [B,gamma] int32 (-1 ends a sequence's
+    drafts).  Returns dict of device tensors."""
     lib = load_library()
     _dev(target_logits, "target_logits", (torch.bfloat16, torch.float32))
     B, W, V = target_logits.shape
     gamma = W - 1
     _dev(draft_tokens, "draft_tokens", torch.int32, (B, gamma))
+    if q_kind == Q_DRAFT_ONEHOT:
+        q = None  # one-hot drafts have no q rows
     if q is not None:
         if q_kind == Q_LOGITS:
             _dev(q, "q", target_logits.dtype, (B, gamma, V))
@@ -420,6 +423,8 @@ def sv_accept_chain_commit(mode, target_logits, q, q_kind, draft_tokens, k_tree,
     B, W, V = target_logits.shape
     gamma = W - 1
     _dev(draft_tokens, "draft_tokens", torch.int32, (B, gamma))
+    if q_kind == Q_DRAFT_ONEHOT:
+        q = None  # one-hot drafts have no q rows
     if q is not None:
         _dev(q, "q", target_logits.dtype if q_kind == Q_LOGITS else torch.float32, (B, gamma, V))
     if k_tree.shape[:2] != (B, W):

@@ -853,7 +853,8 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
   constexpr int NW = NT / 32;
   constexpr int QV = VEC / 4;  // 16-byte vectors of f32 q probabilities per VEC entries
   __shared__ int8_t s_par[kMaxNodes], s_dep[kMaxNodes], s_hc[kMaxNodes];
-  __shared__ uint8_t s_acc[kMaxNodes], s_dnear[kMaxNodes];
+  __shared__ uint8_t s_acc[kMaxNodes], s_dnear[kMaxNodes], s_end[kMaxNodes];
+  __shared__ int s_xtok[kMaxNodes];
   __shared__ int s_best, s_nd;
   __shared__ F2 seg_sum[NW];
   __shared__ F2 s_slice[2];  // this CTA's slice total, per attempt (read by peers)
@@ -880,6 +881,8 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
     s_hc[tid] = p.tree.has_child[tid];
     s_acc[tid] = 0;
     s_dnear[tid] = 0;
+    s_end[tid] = 0;
+    s_xtok[tid] = -1;
   }
   __syncthreads();
 
@@ -893,16 +896,25 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
   const int cnode = tid, a_par = has_node ? s_par[cnode] : 0, d_node = has_node ? s_dep[cnode] : 1;
   const int xt = has_node ? p.tokens[(size_t)b * p.tok_stride + cnode - p.tok_offset] : -1;
   const bool tok_ok = xt >= 0 && xt < V;
+  // a chain's draft of -1: this sequence has fewer drafts (no decision, no status)
+  const bool absent = has_node && p.chain_end && xt == -1;
   const bool logits = p.q_kind == SV_Q_LOGITS;
+  const bool onehot = p.q_kind == SV_Q_DRAFT_ONEHOT;  // q(x) = 1 at the draft token
   float zp = 0.f, zq = 0.f, qprob = 0.f;
   uint32_t k_node = 0u, k_unused = 0u;
   if (!GREEDY && has_node && tok_ok) {
     zp = Elem<T>::load(row_ptr<T>(p.target, (size_t)b * N + a_par, V) + xt);
     if (logits)
       zq = Elem<T>::load(row_ptr<T>(p.q, (size_t)b * p.Dq + d_node - 1, V) + xt);
+    else if (onehot)
+      qprob = 1.f;
     else
       qprob = static_cast<const float *>(p.q)[((size_t)b * p.Dq + d_node - 1) * V + xt];
     verify_uniform_ints(p.seed, p.round, b, cnode, &k_node, &k_unused);
+  }
+  if (has_node) {
+    s_end[cnode] = absent ? 1 : 0;
+    s_xtok[cnode] = xt;
   }
   const int commit_L = p.commit ? p.cm.prefix_len[b] : -1;
 
@@ -928,7 +940,7 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
     const int a = a_par, d = d_node;
     uint8_t acc = 0, dn = 0;
     if (!tok_ok) {
-      if (rank == 0) set_status(p.status, SV_DEV_BAD_TOKEN);
+      if (rank == 0 && !absent) set_status(p.status, SV_DEV_BAD_TOKEN);
     } else if (GREEDY) {
       acc = xt == __ldcg(&tstat[a].argmax);
     } else {
@@ -1021,10 +1033,17 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
   if constexpr (GREEDY) {
     if (tid == 0) s_tok = __ldcg(&tstat[best].argmax);
   } else {
-    // final sample: w = [p_best - q_{d+1}]+ if best has children, else p_best
+    // final sample: w = [p_best - q_{d+1}]+ if best has children, else p_best (a chain
+    // whose drafts end after best: best is its leaf)
     const RowStat sp = load_stat(tstat + best);
     const uint4 *pv = reinterpret_cast<const uint4 *>(row_ptr<T>(p.target, (size_t)b * N + best, V));
-    bool use_q = s_hc[best] != 0;
+    bool use_q = s_hc[best] != 0 && !(p.chain_end && s_end[best + 1]);
+    // one-hot drafts: [p - e_x]+ is p without the rejected draft x (no q row is read)
+    int x_excl = -1;
+    if (use_q && onehot) {
+      x_excl = s_xtok[best + 1];  // a chain: the child of best is best + 1
+      use_q = false;
+    }
     const int qrow = s_dep[best];  // q row of depth d+1
     const bool q_probs = p.q_kind == SV_Q_PROBS_F32;
     RowStat sq{};
@@ -1091,6 +1110,11 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
         const float2 x = mul2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), ip2);
         w[e] = x.x;
         w[e + 1] = x.y;
+      }
+      if (x_excl >= 0) {  // one-hot q: [p - e_x]+ is 0 at x
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+          if (v * VEC + e == x_excl) w[e] = 0.f;
       }
       if (TOPK) {
 #pragma unroll
@@ -1307,6 +1331,7 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
       if (s_rstar >= 0) break;
       // the residual has no mass: sample from p instead (reported)
       use_q = false;
+      x_excl = -1;
       if (tid == 0) s_snear = 1;
     }
     // this CTA has read its peers' totals for the last time: let them go once all have

@@ -277,10 +277,12 @@ sv_status accept_common(sv_mode mode, sv_dtype dt, int B, int V, const void *tar
   if (!target) return fail(SV_ERR_INVALID_ARG, "target_logits is NULL");
   if (!aligned16(target)) return fail(SV_ERR_INVALID_ARG, "target_logits not 16-byte aligned");
   if (!*greedy) {
-    if (q_kind != SV_Q_PROBS_F32 && q_kind != SV_Q_LOGITS)
+    if (q_kind != SV_Q_PROBS_F32 && q_kind != SV_Q_LOGITS && q_kind != SV_Q_DRAFT_ONEHOT)
       return fail(SV_ERR_INVALID_ARG, "q_kind %d", (int)q_kind);
-    if (!q) return fail(SV_ERR_INVALID_ARG, "q is NULL in exact mode");
-    if (!aligned16(q)) return fail(SV_ERR_INVALID_ARG, "q not 16-byte aligned");
+    if (q_kind != SV_Q_DRAFT_ONEHOT) {  // one-hot drafts have no q rows
+      if (!q) return fail(SV_ERR_INVALID_ARG, "q is NULL in exact mode");
+      if (!aligned16(q)) return fail(SV_ERR_INVALID_ARG, "q not 16-byte aligned");
+    }
   }
   if (!out_tokens || !out_num_emitted || !out_num_accepted)
     return fail(SV_ERR_INVALID_ARG, "an output pointer is NULL");
@@ -337,6 +339,7 @@ sv_status chain_params(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
   p.tokens = draft_tokens;
   p.tok_stride = gamma;
   p.tok_offset = 1;
+  p.chain_end = 1;  // a draft of -1 ends the sequence's chain
   p.temperature = temperature;
   p.top_k = top_k;
   p.top_p = top_p;
@@ -365,6 +368,8 @@ sv_status tree_params(sv_mode mode, sv_dtype logit_dt, int B, int N, int V, cons
   if (!out_path_nodes) return fail(SV_ERR_INVALID_ARG, "out_path_nodes is NULL");
   if (!*greedy && Dq < p.tree.Dmax)
     return fail(SV_ERR_INVALID_ARG, "q has %d depth rows, the tree is %d deep", Dq, p.tree.Dmax);
+  if (!*greedy && q_kind == SV_Q_DRAFT_ONEHOT)
+    return fail(SV_ERR_UNSUPPORTED, "one-hot draft q is supported for chains only");
   if (Dq < 0) return fail(SV_ERR_INVALID_ARG, "Dq < 0");
   p.B = B;
   p.N = N;

@@ -120,6 +120,7 @@ struct AcceptParams {
   const void *q;             // [B,Dq,V]
   const int32_t *tokens;     // token of node c of seq b = tokens[b*tok_stride + c - tok_offset]
   int tok_stride, tok_offset;
+  int chain_end;             // chains: a token of -1 ends the sequence's drafts
   float temperature;
   float c_log2;              // log2(e) / T
   int top_k;                 // 0 = off
