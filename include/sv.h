@@ -14,10 +14,16 @@
  *  - Every tensor argument is caller-owned DEVICE memory, dense row-major in the layout
  *    given next to it, 16-byte aligned.  The library never allocates device memory:
  *    scratch comes from a caller workspace sized by the matching *_workspace_size().
- *  - `parent` arguments are HOST arrays: the candidate tree is shared by all sequences
- *    of the batch (a static Medusa tree or a chain), BFS ordered: parent[0] = -1 and
- *    0 <= parent[i] < i, at most SV_MAX_TREE_NODES nodes.  They are validated and
- *    copied at the call, so the host array may be reused as soon as the call returns.
+ *  - Trees: `parent` (BFS ordered: parent[0] = -1 and 0 <= parent[i] < i, at most
+ *    SV_MAX_TREE_NODES nodes) with `parent_stride`.  parent_stride == 0: `parent` is a
+ *    HOST array [N], one tree shared by every sequence of the batch (a static Medusa tree
+ *    or a chain); it is validated and copied at the call, so the host array may be reused
+ *    as soon as the call returns.  parent_stride >= N: `parent` is a DEVICE array
+ *    [B, parent_stride] int32, row b the tree of sequence b (trees pruned or built per
+ *    request, all with N rows); the kernels read and check it (a row that is not a
+ *    BFS-ordered tree sets SV_DEV_BAD_TREE), so it must stay valid until the call's work
+ *    on the stream is done.  With per-sequence trees the path and token outputs have N
+ *    columns (the deepest possible path) instead of tree depth + 1.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only enqueue
  *    work and return without synchronising.
  *  - Arguments are validated on the host before anything is launched; a failed check
@@ -65,6 +71,10 @@ typedef int32_t sv_status;
                                       outputs of that call are not valid */
 #define SV_DEV_LAYOUT 0x20u        /* shared memory was not 1024-byte aligned; the call
                                       did nothing (outputs not valid) */
+#define SV_DEV_BAD_TREE 0x40u      /* a per-sequence parent row is not a BFS-ordered tree
+                                      (or, in exact acceptance, deeper than q's Dq rows):
+                                      that sequence's outputs are not meaningful (its
+                                      acceptance keeps the root alone) */
 
 /* The two counts of a packed near-tie word (see "Near ties" above). */
 #define SV_NEAR_DECISIONS(w) ((uint32_t)(w) & 0xFFFFu)
@@ -113,7 +123,8 @@ typedef struct {
  *   keys  = prefix positions [0, prefix_len[b])  U  tree nodes j on n's root path,
  *   out   = softmax(scale * q . K^T) V over those keys.
  * q [B,N,Hq,D]; k_tree, v_tree [B,N,Hkv,D] (the candidates' fresh K/V, root = node 0);
- * cache as above (read only); parent [N] host; out [B,N,Hq,D].
+ * cache as above (read only); parent, parent_stride as under "Trees" above; out
+ * [B,N,Hq,D].
  * dt: SV_BF16 (fp32 accumulation, bf16 output) or SV_F32 (fp32 throughout).
  * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= N <= 64; block_size % 16 == 0 for
  * paged caches.  Workspace: sv_tree_attention_workspace_size() bytes (may be 0).  The
@@ -123,8 +134,8 @@ typedef struct {
  * SV_DEV_TIMEOUT.  Calls sharing one workspace must be stream-ordered. */
 sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, const void *q,
                             const void *k_tree, const void *v_tree, sv_kv_cache cache,
-                            const int32_t *parent, float scale, void *out, void *workspace,
-                            size_t workspace_bytes, void *stream);
+                            const int32_t *parent, int parent_stride, float scale, void *out,
+                            void *workspace, size_t workspace_bytes, void *stream);
 
 /* Which kernel sv_tree_attention runs for these sizes: 1 = the tensor-core kernel
  * (tcgen05 MMA into TMEM, TMA-fed), 0 = the general kernel (mma.sync for bf16, FFMA for
@@ -185,15 +196,17 @@ sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int
  * node a* is the deepest node whose whole root path is accepted (ties: smallest row).
  * The emitted tokens are those of the path nodes 1..a*, then a token sampled with
  * u_smp(b, a*) from norm([p_{a*} - q_{d(a*)+1}]+) if a* has children, else from p_{a*}.
- * parent [N] host; node_tokens [B,N] (column 0, the root, is not read);
+ * parent, parent_stride as under "Trees" above (per-sequence trees: a node deeper than
+ * Dq sets SV_DEV_BAD_TREE in exact mode); node_tokens [B,N] (column 0, the root, is not
+ * read);
  * target_logits [B,N,V]; q [B,Dq,V] with row d-1 = depth d (Dq >= tree depth); q_kind
  * SV_Q_PROBS_F32 or SV_Q_LOGITS (SV_Q_DRAFT_ONEHOT: SV_ERR_UNSUPPORTED in exact mode).
  * temperature, top_k, top_p, the uniforms and the near-tie reports as sv_accept_chain.
- * Outputs (Dmax = tree depth): out_path_nodes [B,Dmax+1] (root..a*, -1 after),
- * out_tokens [B,Dmax+1], out_num_emitted [B], out_num_accepted [B], out_near_ties [B].
+ * Outputs (W = tree depth + 1; N with per-sequence trees): out_path_nodes [B,W] (root..a*,
+ * -1 after), out_tokens [B,W], out_num_emitted [B], out_num_accepted [B], out_near_ties [B].
  * Workspace: sv_accept_workspace_size(B, N, V, Dq). */
 sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
-                         const int32_t *parent, const int32_t *node_tokens,
+                         const int32_t *parent, int parent_stride, const int32_t *node_tokens,
                          const void *target_logits, const void *q, sv_q_kind q_kind, int Dq,
                          float temperature, int top_k, float top_p, uint64_t seed, uint64_t round,
                          int32_t *out_path_nodes, int32_t *out_tokens,
@@ -222,6 +235,7 @@ sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
  * (in units of the normalised residual, or the error bound when wider) or with an empty
  * residual.  Launches: the statistics kernel, then one CTA per sequence. */
 sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const int32_t *parent,
+                                   int parent_stride,
                                    const int32_t *node_tokens, const void *target_logits,
                                    const void *q, sv_q_kind q_kind, int Dq, float temperature,
                                    int top_k, float top_p, uint64_t seed, uint64_t round,
@@ -248,7 +262,7 @@ size_t sv_accept_workspace_size(int B, int N, int V, int Dq);
  * clearing between calls. */
 #define SV_NOALLOC_ACCEPT_ROWS 65536
 sv_status sv_accept_tree_noalloc(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
-                                 const int32_t *parent, const int32_t *node_tokens,
+                                 const int32_t *parent, int parent_stride, const int32_t *node_tokens,
                                  const void *target_logits, const void *q, sv_q_kind q_kind,
                                  int Dq, float temperature, int top_k, float top_p, uint64_t seed,
                                  uint64_t round, int32_t *out_path_nodes, int32_t *out_tokens,
@@ -297,7 +311,7 @@ sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_
  * checks); the acceptance arguments, outputs and workspace are those of the separate
  * call.  prefix_len[b] is read before any K/V is written and advanced once, after. */
 sv_status sv_accept_tree_commit(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
-                                const int32_t *parent, const int32_t *node_tokens,
+                                const int32_t *parent, int parent_stride, const int32_t *node_tokens,
                                 const void *target_logits, const void *q, sv_q_kind q_kind,
                                 int Dq, float temperature, int top_k, float top_p, uint64_t seed,
                                 uint64_t round, sv_dtype kv_dt, int Hkv, int D,

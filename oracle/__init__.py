@@ -58,17 +58,17 @@ def _load():
             lib.orc_check_tree.restype = I
             lib.orc_tree_mask.argtypes = [I, P, P]
             lib.orc_tree_attention.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, I, I, I,
-                                               P, Dbl, I, I, P]
-            lib.orc_accept_tree.argtypes = [I, I, I, I, I, P, P, P, P, I, I, Dbl, I, Dbl, U64, U64,
-                                            P, P, P, P, P, P, P, P]
+                                               P, I, Dbl, I, I, P]
+            lib.orc_accept_tree.argtypes = [I, I, I, I, I, P, I, P, P, P, I, I, Dbl, I, Dbl, U64,
+                                            U64, P, P, P, P, P, P, P, P]
             lib.orc_accept_tree.restype = I
             lib.orc_accept_chain.argtypes = [I, I, I, I, I, P, P, I, P, Dbl, I, Dbl, U64, U64,
                                              P, P, P, P, P]
             lib.orc_accept_chain.restype = I
             lib.orc_commit_kv.argtypes = [I, I, I, I, I, P, P, P, I, P, P, P, P, P, I, I, I]
             lib.orc_ngram_draft.argtypes = [I, I, P, P, I, I, I, P, P]
-            lib.orc_accept_tree_recursive.argtypes = [I, I, I, I, P, P, P, P, I, I, Dbl, I, Dbl,
-                                                      U64, U64, P, P, P, P, P, P]
+            lib.orc_accept_tree_recursive.argtypes = [I, I, I, I, P, I, P, P, P, I, I, Dbl, I,
+                                                      Dbl, U64, U64, P, P, P, P, P, P]
             lib.orc_accept_tree_recursive.restype = I
             lib.orc_lm_head.argtypes = [I, I, I, P, I, P, I, P]
             lib.orc_set_threads.argtypes = [I]
@@ -114,6 +114,17 @@ def _i32(x):
     return _cpu(torch.as_tensor(x, dtype=torch.int32))
 
 
+def _parents(parent, B):
+    """(int32 tensor, stride, N, per-sequence?) of a tree argument: one parent list [N]
+    shared by the batch, or [B, N] with sequence b's tree in row b."""
+    par = _i32(parent)
+    if par.dim() == 2:
+        if par.shape[0] != B:
+            raise ValueError(f"per-sequence parents must have B = {B} rows")
+        return par, par.shape[1], par.shape[1], True
+    return par, 0, par.numel(), False
+
+
 # ------------------------------------------------------------------- Philox
 
 def philox4x32_10(counter, key):
@@ -156,14 +167,15 @@ def tree_attention(q, k_tree, v_tree, cache_k, cache_v, prefix_len, parent, scal
     """Tree attention by definition; returns float64 [nb,N,Hq,D] for b in b_range.
 
     Contiguous cache [B,Lmax,Hkv,D] when block_table is None, else a paged pool
-    [num_blocks,block_size,Hkv,D] addressed by block_table [B,max_blocks]."""
+    [num_blocks,block_size,Hkv,D] addressed by block_table [B,max_blocks].  parent: one
+    tree [N] for the batch, or [B,N] with one tree per sequence."""
     q, k_tree, v_tree = _cpu(q), _cpu(k_tree), _cpu(v_tree)
     cache_k, cache_v = _cpu(cache_k), _cpu(cache_v)
     dt = _dtype_code(q)
     B, N, Hq, D = q.shape
     Hkv = k_tree.shape[2]
     pl = _i32(prefix_len)
-    par = _i32(parent)
+    par, pstride, _, _ = _parents(parent, B)
     if block_table is None:
         bt, max_blocks, Lmax = None, 0, cache_k.shape[1]
     else:
@@ -175,7 +187,7 @@ def tree_attention(q, k_tree, v_tree, cache_k, cache_v, prefix_len, parent, scal
     out = torch.zeros((b1 - b0, N, Hq, D), dtype=torch.float64)
     _load().orc_tree_attention(dt, B, N, Hq, Hkv, D, _ptr(q), _ptr(k_tree), _ptr(v_tree),
                                _ptr(cache_k), _ptr(cache_v), _ptr(pl), _ptr(bt), max_blocks,
-                               block_size, Lmax, _ptr(par), float(scale), b0, b1, _ptr(out))
+                               block_size, Lmax, _ptr(par), pstride, float(scale), b0, b1, _ptr(out))
     return out
 
 
@@ -199,11 +211,10 @@ def accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperature
     tl = _cpu(target_logits)
     dt = _dtype_code(tl)
     B, N, V = tl.shape
-    par = _i32(parent)
+    par, pstride, _, per_seq = _parents(parent, B)
     toks = _i32(node_tokens)
     qq, Dq = _q_args(q, q_kind)
-    depth = _depths(par.tolist())
-    W = max(depth) + 1
+    W = N if per_seq else max(_depths(par.tolist())) + 1
     out = {
         "path_nodes": torch.full((B, W), -1, dtype=torch.int32),
         "tokens": torch.full((B, W), -1, dtype=torch.int32),
@@ -215,7 +226,7 @@ def accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperature
         "flags": torch.zeros(B, dtype=torch.int32),
     }
     rc = _load().orc_accept_tree(
-        mode, dt, B, N, V, _ptr(par), _ptr(toks), _ptr(tl), _ptr(qq), q_kind, Dq,
+        mode, dt, B, N, V, _ptr(par), pstride, _ptr(toks), _ptr(tl), _ptr(qq), q_kind, Dq,
         float(temperature), int(top_k), float(np.float32(top_p)), int(seed), int(round_), _ptr(out["path_nodes"]),
         _ptr(out["tokens"]), _ptr(out["num_emitted"]), _ptr(out["num_accepted"]),
         _ptr(out["near_ties"]), _ptr(out["acc"]), _ptr(out["ratio"]), _ptr(out["flags"]))
@@ -305,10 +316,10 @@ def accept_tree_recursive(target_logits, q, q_kind, parent, node_tokens, tempera
     tl = _cpu(target_logits)
     dt = _dtype_code(tl)
     B, N, V = tl.shape
-    par = _i32(parent)
+    par, pstride, _, per_seq = _parents(parent, B)
     toks = _i32(node_tokens)
     qq, Dq = _q_args(q, q_kind)
-    W = max(_depths(par.tolist())) + 1
+    W = N if per_seq else max(_depths(par.tolist())) + 1
     out = {
         "path_nodes": torch.full((B, W), -1, dtype=torch.int32),
         "tokens": torch.full((B, W), -1, dtype=torch.int32),
@@ -318,7 +329,7 @@ def accept_tree_recursive(target_logits, q, q_kind, parent, node_tokens, tempera
         "flags": torch.zeros(B, dtype=torch.int32),
     }
     rc = _load().orc_accept_tree_recursive(
-        dt, B, N, V, _ptr(par), _ptr(toks), _ptr(tl), _ptr(qq), q_kind, Dq, float(temperature),
+        dt, B, N, V, _ptr(par), pstride, _ptr(toks), _ptr(tl), _ptr(qq), q_kind, Dq, float(temperature),
         int(top_k), float(np.float32(top_p)), int(seed), int(round_), _ptr(out["path_nodes"]),
         _ptr(out["tokens"]), _ptr(out["num_emitted"]), _ptr(out["num_accepted"]),
         _ptr(out["near_ties"]), _ptr(out["flags"]))

@@ -207,13 +207,14 @@ static size_t orc_cache_row(int b, int pos, const int32_t *block_table, int max_
  *   keys = prefix positions 0..L_b-1 of the cache  U  tree nodes on n's root path,
  *   s_j  = scale * <q, k_j>,  o = sum_j softmax(s)_j v_j.
  * q [B,N,Hq,D]; k_tree, v_tree [B,N,Hkv,D]; cache [B,Lmax,Hkv,D] (block_table NULL)
- * or [num_blocks,block_size,Hkv,D]; out [(b_end-b_begin),N,Hq,D] in double. */
+ * or [num_blocks,block_size,Hkv,D]; out [(b_end-b_begin),N,Hq,D] in double.  The tree of
+ * sequence b is parent[b * parent_stride .. + N): parent_stride 0 shares one tree. */
 void orc_tree_attention(int dtype, int B, int N, int Hq, int Hkv, int D, const void *q,
                         const void *k_tree, const void *v_tree, const void *cache_k,
                         const void *cache_v, const int32_t *prefix_len,
                         const int32_t *block_table, int max_blocks, int block_size, int Lmax,
-                        const int32_t *parent, double scale, int b_begin, int b_end,
-                        double *out) {
+                        const int32_t *parent, int parent_stride, double scale, int b_begin,
+                        int b_end, double *out) {
   (void)B;
   int G = Hq / Hkv;
   int rows = (b_end - b_begin) * N * Hq;
@@ -225,6 +226,7 @@ void orc_tree_attention(int dtype, int B, int N, int Hq, int Hkv, int D, const v
     int g = h / G;
     int L = prefix_len[b];
     int nk = L + N;
+    const int32_t *par = parent + (size_t)b * parent_stride; /* this sequence's tree */
     double *s = (double *)orc_alloc(sizeof(double) * (size_t)nk);
     size_t qoff = (((size_t)b * N + n) * Hq + h) * D;
     double smax = -INFINITY;
@@ -237,7 +239,7 @@ void orc_tree_attention(int dtype, int B, int N, int Hq, int Hkv, int D, const v
         kb = cache_k;
       } else {
         int t = j - L;
-        if (!orc_on_root_path(parent, n, t)) continue;
+        if (!orc_on_root_path(par, n, t)) continue;
         koff = (((size_t)b * N + t) * Hkv + g) * D;
         kb = k_tree;
       }
@@ -416,31 +418,31 @@ static void orc_q_row(const void *q, int q_kind, int dtype, int b, int Dq, int d
  * q [B,Dq,V] with row d-1 for depth d.  Outputs have Dmax+1 columns, unused -1.
  * out_acc / out_ratio [B,N] are optional (per-node decision and p/q, root = 1 / nan).
  * out_flags [B] optional: bit0 = a draft had q(x)=0, bit1 = token id out of range. */
-int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *parent,
-                    const int32_t *node_tokens, const void *target_logits, const void *q,
+int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *parent_all,
+                    int parent_stride, const int32_t *node_tokens, const void *target_logits, const void *q,
                     int q_kind, int Dq, double T, int top_k, double top_p, uint64_t seed,
                     uint64_t round, int32_t *out_path_nodes, int32_t *out_tokens, int32_t *out_num_emitted,
                     int32_t *out_num_accepted, uint32_t *out_near_ties, uint8_t *out_acc,
                     double *out_ratio, uint32_t *out_flags) {
-  if (orc_check_tree(N, parent)) return 1;
   int Dmax = 0;
-  int *depth = (int *)orc_alloc(sizeof(int) * (size_t)N);
-  for (int n = 0; n < N; ++n) {
-    depth[n] = orc_depth(parent, n);
-    if (depth[n] > Dmax) Dmax = depth[n];
+  for (int b = 0; b < (parent_stride ? B : 1); ++b) {
+    const int32_t *par = parent_all + (size_t)b * parent_stride;
+    if (orc_check_tree(N, par)) return 1;
+    for (int n = 0; n < N; ++n) {
+      int d = orc_depth(par, n);
+      if (d > Dmax) Dmax = d;
+    }
   }
   int greedy = (mode == ORC_GREEDY) || (T == 0.0);
-  if (!greedy && Dq < Dmax) {
-    free(depth);
-    return 2;
-  }
-  if (!greedy && q_kind == ORC_Q_DRAFT_ONEHOT) { /* one-hot drafts: chains only */
-    free(depth);
-    return 4;
-  }
-  int W = Dmax + 1;
+  if (!greedy && Dq < Dmax) return 2;
+  if (!greedy && q_kind == ORC_Q_DRAFT_ONEHOT) return 4; /* one-hot drafts: chains only */
+  /* output columns: the deepest path + 1 (per-sequence trees: N, the deepest possible) */
+  int W = parent_stride ? N : Dmax + 1;
 #pragma omp parallel for schedule(dynamic)
   for (int b = 0; b < B; ++b) {
+    const int32_t *parent = parent_all + (size_t)b * parent_stride; /* this sequence's tree */
+    int *depth = (int *)orc_alloc(sizeof(int) * (size_t)N);
+    for (int n = 0; n < N; ++n) depth[n] = orc_depth(parent, n);
     double *z = (double *)orc_alloc(sizeof(double) * (size_t)V);
     double *pa = (double *)orc_alloc(sizeof(double) * (size_t)V);
     double *qd = (double *)orc_alloc(sizeof(double) * (size_t)V);
@@ -545,9 +547,8 @@ int orc_accept_tree(int mode, int dtype, int B, int N, int V, const int32_t *par
     if (out_ratio)
       for (int c = 0; c < N; ++c) out_ratio[(size_t)b * N + c] = ratio[c];
     if (out_flags) out_flags[b] = flags;
-    free(z); free(pa); free(qd); free(acc); free(ok); free(ratio); free(dec_near);
+    free(z); free(pa); free(qd); free(acc); free(ok); free(ratio); free(dec_near); free(depth);
   }
-  free(depth);
   return 0;
 }
 
@@ -763,28 +764,30 @@ void orc_ngram_draft(int B, int Lmax, const int32_t *history, const int32_t *len
  * from q this keeps the output distributed as p; with one child per node it is the chain
  * procedure.  Exact mode only (greedy: orc_accept_tree).  Arguments and outputs as
  * orc_accept_tree (no per-node decision outputs). */
-int orc_accept_tree_recursive(int dtype, int B, int N, int V, const int32_t *parent,
-                              const int32_t *node_tokens, const void *target_logits,
+int orc_accept_tree_recursive(int dtype, int B, int N, int V, const int32_t *parent_all,
+                              int parent_stride, const int32_t *node_tokens, const void *target_logits,
                               const void *q, int q_kind, int Dq, double T, int top_k,
                               double top_p, uint64_t seed, uint64_t round,
                               int32_t *out_path_nodes, int32_t *out_tokens,
                               int32_t *out_num_emitted, int32_t *out_num_accepted,
                               uint32_t *out_near_ties, uint32_t *out_flags) {
-  if (orc_check_tree(N, parent)) return 1;
   if (T == 0.0) return 3;
   int Dmax = 0;
-  int *depth = (int *)orc_alloc(sizeof(int) * (size_t)N);
-  for (int n = 0; n < N; ++n) {
-    depth[n] = orc_depth(parent, n);
-    if (depth[n] > Dmax) Dmax = depth[n];
+  for (int b = 0; b < (parent_stride ? B : 1); ++b) {
+    const int32_t *par = parent_all + (size_t)b * parent_stride;
+    if (orc_check_tree(N, par)) return 1;
+    for (int n = 0; n < N; ++n) {
+      int d = orc_depth(par, n);
+      if (d > Dmax) Dmax = d;
+    }
   }
-  if (Dq < Dmax || q_kind == ORC_Q_DRAFT_ONEHOT) {
-    free(depth);
-    return 2;
-  }
-  int W = Dmax + 1;
+  if (Dq < Dmax || q_kind == ORC_Q_DRAFT_ONEHOT) return 2;
+  int W = parent_stride ? N : Dmax + 1;
 #pragma omp parallel for schedule(dynamic)
   for (int b = 0; b < B; ++b) {
+    const int32_t *parent = parent_all + (size_t)b * parent_stride; /* this sequence's tree */
+    int *depth = (int *)orc_alloc(sizeof(int) * (size_t)N);
+    for (int n = 0; n < N; ++n) depth[n] = orc_depth(parent, n);
     double *z = (double *)orc_alloc(sizeof(double) * (size_t)V);
     double *pc = (double *)orc_alloc(sizeof(double) * (size_t)V);
     double *qd = (double *)orc_alloc(sizeof(double) * (size_t)V);
@@ -867,8 +870,7 @@ int orc_accept_tree_recursive(int dtype, int B, int N, int V, const int32_t *par
     out_num_accepted[b] = D;
     if (out_near_ties) out_near_ties[b] = near;
     if (out_flags) out_flags[b] = flags;
-    free(z); free(pc); free(qd);
+    free(z); free(pc); free(qd); free(depth);
   }
-  free(depth);
   return 0;
 }

@@ -33,7 +33,7 @@ GREEDY, EXACT = 0, 1
 Q_PROBS_F32, Q_LOGITS, Q_DRAFT_ONEHOT = 0, 1, 2  # q as probabilities, draft logits, one-hot drafts
 SV_MAX_TREE_NODES = 64
 SV_DEV_BAD_TOKEN, SV_DEV_BAD_BLOCK, SV_DEV_BAD_PREFIX, SV_DEV_ZERO_DRAFT_PROB = 1, 2, 4, 8
-SV_DEV_TIMEOUT, SV_DEV_LAYOUT = 0x10, 0x20
+SV_DEV_TIMEOUT, SV_DEV_LAYOUT, SV_DEV_BAD_TREE = 0x10, 0x20, 0x40
 
 _STATUS_NAMES = {1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_WORKSPACE",
                  4: "SV_ERR_CUDA"}
@@ -71,23 +71,23 @@ def load_library():
                                "`python -c 'import __graft_entry__ as g; g.build()'`")
         lib = ctypes.CDLL(_LIB_PATH)
         P, I, F, U64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t
-        lib.sv_tree_attention.argtypes = [I, I, I, I, I, I, P, P, P, _KVCacheC, P, F, P, P, SZ, P]
+        lib.sv_tree_attention.argtypes = [I, I, I, I, I, I, P, P, P, _KVCacheC, P, I, F, P, P, SZ, P]
         lib.sv_tree_attention_workspace_size.argtypes = [I, I, I, I, I, I, I]
         lib.sv_tree_attention_path.argtypes = [I, I, I, I, I, I]
         lib.sv_tree_attention_path.restype = I
         lib.sv_tree_attention_workspace_size.restype = SZ
         lib.sv_accept_chain.argtypes = [I, I, I, I, I, P, P, I, P, F, I, F, U64, U64, P, P, P, P, P,
                                         SZ, P]
-        lib.sv_accept_tree.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, F, U64, U64, P, P, P, P,
+        lib.sv_accept_tree.argtypes = [I, I, I, I, I, P, I, P, P, P, I, I, F, I, F, U64, U64, P, P, P, P,
                                        P, P, SZ, P]
-        lib.sv_accept_tree_recursive.argtypes = [I, I, I, I, P, P, P, P, I, I, F, I, F, U64, U64,
+        lib.sv_accept_tree_recursive.argtypes = [I, I, I, I, P, I, P, P, P, I, I, F, I, F, U64, U64,
                                                  P, P, P, P, P, P, SZ, P]
-        lib.sv_accept_tree_noalloc.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, F, U64, U64, P,
+        lib.sv_accept_tree_noalloc.argtypes = [I, I, I, I, I, P, I, P, P, P, I, I, F, I, F, U64, U64, P,
                                                P, P, P, P, P]
         lib.sv_accept_workspace_size.argtypes = [I, I, I, I]
         lib.sv_accept_workspace_size.restype = SZ
         lib.sv_commit_kv.argtypes = [I, I, I, I, I, P, P, P, I, P, _KVCacheC, P]
-        lib.sv_accept_tree_commit.argtypes = [I, I, I, I, I, P, P, P, P, I, I, F, I, F, U64, U64,
+        lib.sv_accept_tree_commit.argtypes = [I, I, I, I, I, P, I, P, P, P, I, I, F, I, F, U64, U64,
                                               I, I, I, P, P, _KVCacheC, P, P, P, P, P, P, SZ, P]
         lib.sv_accept_chain_commit.argtypes = [I, I, I, I, I, P, P, I, P, F, I, F, U64, U64,
                                                I, I, I, P, P, _KVCacheC, P, P, P, P, P, SZ, P]
@@ -155,6 +155,24 @@ def _stream(stream) -> ctypes.c_void_p:
 def _parent_arr(parent: Sequence[int]):
     arr = (ctypes.c_int32 * len(parent))(*[int(x) for x in parent])
     return arr, len(parent)
+
+
+def _tree_arg(parent, B: int, N: int):
+    """The (pointer, parent_stride, output width) of a tree argument: a host sequence [N]
+    shared by the batch (stride 0, width depth + 1), or a CUDA int32 tensor [B, S] (S >= N)
+    with one tree per sequence (stride S, width N)."""
+    if isinstance(parent, torch.Tensor) and parent.is_cuda:
+        if parent.dtype != torch.int32 or parent.dim() != 2 or parent.shape[0] != B:
+            raise ValueError(f"per-sequence parents must be a CUDA int32 tensor [B={B}, >= N]")
+        if parent.stride(1) != 1 or parent.shape[1] < N or parent.stride(0) < N:
+            raise ValueError(f"per-sequence parents need contiguous rows of at least N={N}")
+        return ctypes.c_void_p(parent.data_ptr()), int(parent.stride(0)), N
+    if isinstance(parent, torch.Tensor):
+        parent = parent.tolist()
+    par, n = _parent_arr(parent)
+    if n != N:
+        raise ValueError(f"parent has {n} entries, the tree has {N} rows")
+    return par, 0, _tree_depth(parent) + 1
 
 
 @dataclass
@@ -234,11 +252,9 @@ def sv_tree_attention(q, k_tree, v_tree, cache: KVCache, parent, scale, out=None
     ws_need = sv_tree_attention_workspace_size(q.dtype, B, N, Hq, Hkv, D, cache.max_prefix)
     # a workspace passed in must have been zero-filled before its first use
     workspace, ws_bytes = _workspace(ws_need, q.device, workspace, zero=True)
-    par, n = _parent_arr(parent)
-    if n != N:
-        raise ValueError(f"parent has {n} entries, tree has {N} rows")
+    par, pstride, _ = _tree_arg(parent, B, N)
     _check(lib.sv_tree_attention(_dt(q), B, N, Hq, Hkv, D, _ptr(q), _ptr(k_tree), _ptr(v_tree),
-                                 cs, par, float(scale), _ptr(out), _ptr(workspace), ws_bytes,
+                                 cs, par, pstride, float(scale), _ptr(out), _ptr(workspace), ws_bytes,
                                  _stream(stream)))
     return out
 
@@ -311,15 +327,12 @@ def sv_accept_tree(mode, target_logits, q, q_kind, parent, node_tokens, temperat
             _dev(q, "q", target_logits.dtype, (B, Dq, V))
         else:
             _dev(q, "q", torch.float32, (B, Dq, V))
-    W = _tree_depth(parent) + 1
+    par, pstride, W = _tree_arg(parent, B, N)
     outs = _accept_outputs(B, W, target_logits.device, outs)
     outs.setdefault("path_nodes", torch.empty((B, W), dtype=torch.int32, device=target_logits.device))
     workspace, ws_bytes = _workspace(sv_accept_workspace_size(B, N, V, Dq), target_logits.device,
                                      workspace)
-    par, n = _parent_arr(parent)
-    if n != N:
-        raise ValueError(f"parent has {n} entries, logits have {N} rows")
-    _check(lib.sv_accept_tree(mode, _dt(target_logits), B, N, V, par, _ptr(node_tokens),
+    _check(lib.sv_accept_tree(mode, _dt(target_logits), B, N, V, par, pstride, _ptr(node_tokens),
                               _ptr(target_logits), _ptr(q), q_kind, Dq, float(temperature),
                               int(top_k), float(top_p), int(seed), int(round_), _ptr(outs["path_nodes"]),
                               _ptr(outs["tokens"]), _ptr(outs["num_emitted"]),
@@ -342,15 +355,12 @@ def sv_accept_tree_recursive(target_logits, q, q_kind, parent, node_tokens, temp
         raise ValueError("q is required (exact mode)")
     Dq = q.shape[1]
     _dev(q, "q", target_logits.dtype if q_kind == Q_LOGITS else torch.float32, (B, Dq, V))
-    W = _tree_depth(parent) + 1
+    par, pstride, W = _tree_arg(parent, B, N)
     outs = _accept_outputs(B, W, target_logits.device, outs)
     outs.setdefault("path_nodes", torch.empty((B, W), dtype=torch.int32, device=target_logits.device))
     workspace, ws_bytes = _workspace(sv_accept_workspace_size(B, N, V, Dq), target_logits.device,
                                      workspace)
-    par, n = _parent_arr(parent)
-    if n != N:
-        raise ValueError(f"parent has {n} entries, logits have {N} rows")
-    _check(lib.sv_accept_tree_recursive(_dt(target_logits), B, N, V, par, _ptr(node_tokens),
+    _check(lib.sv_accept_tree_recursive(_dt(target_logits), B, N, V, par, pstride, _ptr(node_tokens),
                                         _ptr(target_logits), _ptr(q), q_kind, Dq,
                                         float(temperature), int(top_k), float(top_p), int(seed),
                                         int(round_), _ptr(outs["path_nodes"]), _ptr(outs["tokens"]),
@@ -375,13 +385,10 @@ def sv_accept_tree_noalloc(mode, target_logits, q, q_kind, parent, node_tokens,
     if q is not None:
         Dq = q.shape[1]
         _dev(q, "q", target_logits.dtype if q_kind == Q_LOGITS else torch.float32, (B, Dq, V))
-    W = _tree_depth(parent) + 1
+    par, pstride, W = _tree_arg(parent, B, N)
     outs = _accept_outputs(B, W, target_logits.device, outs)
     outs.setdefault("path_nodes", torch.empty((B, W), dtype=torch.int32, device=target_logits.device))
-    par, n = _parent_arr(parent)
-    if n != N:
-        raise ValueError(f"parent has {n} entries, logits have {N} rows")
-    _check(lib.sv_accept_tree_noalloc(mode, _dt(target_logits), B, N, V, par, _ptr(node_tokens),
+    _check(lib.sv_accept_tree_noalloc(mode, _dt(target_logits), B, N, V, par, pstride, _ptr(node_tokens),
                                       _ptr(target_logits), _ptr(q), q_kind, Dq, float(temperature),
                                       int(top_k), float(top_p), int(seed), int(round_), _ptr(outs["path_nodes"]),
                                       _ptr(outs["tokens"]), _ptr(outs["num_emitted"]),
@@ -459,15 +466,12 @@ def sv_accept_tree_commit(mode, target_logits, q, q_kind, parent, node_tokens, k
     if k_tree.shape[:2] != (B, N):
         raise ValueError("k_tree must be [B, N, Hkv, D]")
     kv_dt, Hkv, D, cs = _kv_args(k_tree, v_tree, cache)
-    W = _tree_depth(parent) + 1
+    par, pstride, W = _tree_arg(parent, B, N)
     outs = _accept_outputs(B, W, target_logits.device, outs)
     outs.setdefault("path_nodes", torch.empty((B, W), dtype=torch.int32, device=target_logits.device))
     workspace, ws_bytes = _workspace(sv_accept_workspace_size(B, N, V, Dq), target_logits.device,
                                      workspace)
-    par, n = _parent_arr(parent)
-    if n != N:
-        raise ValueError(f"parent has {n} entries, logits have {N} rows")
-    _check(lib.sv_accept_tree_commit(mode, _dt(target_logits), B, N, V, par, _ptr(node_tokens),
+    _check(lib.sv_accept_tree_commit(mode, _dt(target_logits), B, N, V, par, pstride, _ptr(node_tokens),
                                      _ptr(target_logits), _ptr(q), q_kind, Dq, float(temperature),
                                      int(top_k), float(top_p), int(seed), int(round_), kv_dt, Hkv, D,
                                      _ptr(k_tree), _ptr(v_tree), cs, _ptr(outs["path_nodes"]),

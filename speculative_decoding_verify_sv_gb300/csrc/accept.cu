@@ -875,16 +875,40 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
     tc::fence_barrier_init();
     s_abort = 0;
   }
+  // sequence b's tree: the shared one, or its own row checked here (a parent outside
+  // [0, c), a root that is not -1, or a node deeper than the q rows make the sequence keep
+  // its root alone); every row index below is formed from these checked values
+  bool bad_node = false;
   if (tid < kMaxNodes) {
-    s_par[tid] = p.tree.parent[tid];
-    s_dep[tid] = p.tree.depth[tid];
-    s_hc[tid] = p.tree.has_child[tid];
+    int v = -1;
+    if (tid < N) {
+      v = tree_parent(p.tree, b, tid);
+      bad_node = tid == 0 ? v != -1 : (v < 0 || v >= tid);
+      if (bad_node) v = tid == 0 ? -1 : 0;
+    }
+    s_par[tid] = (int8_t)v;
+    s_hc[tid] = 0;
     s_acc[tid] = 0;
     s_dnear[tid] = 0;
     s_end[tid] = 0;
     s_xtok[tid] = -1;
   }
   __syncthreads();
+  if (tid < N) {
+    uint64_t anc_unused;
+    int d = 0;
+    tree_walk(s_par, tid, &anc_unused, &d);  // (s_par holds a valid tree now)
+    s_dep[tid] = (int8_t)d;
+    if (!GREEDY && p.q_kind != SV_Q_DRAFT_ONEHOT && d > p.Dq) bad_node = true;
+    if (tid > 0) s_hc[s_par[tid]] = 1;
+  }
+  const bool seq_bad = __syncthreads_or(bad_node) != 0;
+  if (seq_bad) {
+    // not a usable tree: keep the root alone (no decisions; the bonus from the root row)
+    if (tid < kMaxNodes) s_hc[tid] = 0;
+    if (tid == 0 && rank == 0) set_status(p.status, SV_DEV_BAD_TREE);
+    __syncthreads();
+  }
 
   const RowStat *tstat = p.stats + (size_t)b * N;
   const RowStat *qstat = p.stats + (size_t)p.B * N + (size_t)b * p.Dq;
@@ -892,7 +916,7 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
   // Inputs that do not come from the statistics kernel are read before waiting for it:
   // the candidate token of each non-root node, the two logits at it (the parent's target
   // row, the q row of the node's depth), its uniforms, and the cache length for the commit.
-  const bool has_node = tid >= 1 && tid < N;
+  const bool has_node = tid >= 1 && tid < N && !seq_bad;
   const int cnode = tid, a_par = has_node ? s_par[cnode] : 0, d_node = has_node ? s_dep[cnode] : 1;
   const int xt = has_node ? p.tokens[(size_t)b * p.tok_stride + cnode - p.tok_offset] : -1;
   const bool tok_ok = xt >= 0 && xt < V;

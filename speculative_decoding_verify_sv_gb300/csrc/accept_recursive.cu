@@ -147,6 +147,31 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
   const RowStat *tstat = p.stats + (size_t)b * N;
   const RowStat *qstat = p.stats + (size_t)p.B * N + (size_t)b * p.Dq;
 
+  // sequence b's tree (the shared one, or its own row, checked: a malformed row or a node
+  // deeper than the q rows leaves the root alone, which draws the bonus from its p)
+  __shared__ int s_par[kMaxNodes], s_dep[kMaxNodes];
+  bool bad = false;
+  if (tid < kMaxNodes) {
+    int v = -1;
+    if (tid < N) {
+      v = tree_parent(p.tree, b, tid);
+      bad = tid == 0 ? v != -1 : (v < 0 || v >= tid);
+      if (bad) v = tid == 0 ? -1 : 0;
+    }
+    s_par[tid] = v;
+  }
+  __syncthreads();
+  if (tid < N) {
+    uint64_t anc_unused;
+    int d = 0;
+    tree_walk(s_par, tid, &anc_unused, &d);
+    s_dep[tid] = d;
+    if (d > p.Dq) bad = true;
+  }
+  const bool seq_bad = __syncthreads_or(bad) != 0;
+  if (seq_bad && tid == 0) set_status(p.status, SV_DEV_BAD_TREE);
+  const int Nw = seq_bad ? 1 : N;  // nodes walked: the root alone for a bad tree
+
   // thread 0's running counts: near ties that can change a decision (near decisions,
   // empty residuals handed to a sibling; nucleus cuts) and those of the final sample
   unsigned near = 0u, near_smp = 0u;
@@ -163,8 +188,8 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
   for (int steps = 0; steps < N; ++steps) {
     // the children of the node: rows after it whose parent it is (the same in every thread)
     int first = -1, last = -1;
-    for (int ch = node + 1; ch < N; ++ch)
-      if (p.tree.parent[ch] == node) {
+    for (int ch = node + 1; ch < Nw; ++ch)
+      if (s_par[ch] == node) {
         if (first < 0) first = ch;
         last = ch;
       }
@@ -178,7 +203,7 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
       c_fin = 0.0;
       break;
     }
-    const int drow = p.tree.depth[node];  // q row of the children's depth (depth - 1)
+    const int drow = s_dep[node];  // q row of the children's depth (depth - 1)
     if (logits) {
       r.zq = reinterpret_cast<const T *>(p.q) + ((size_t)b * p.Dq + drow) * V;
       r.sq = load_stat(qstat + drow);
@@ -189,7 +214,7 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
     }
     int next = -1;
     for (int ch = first; ch <= last; ++ch) {
-      if (p.tree.parent[ch] != node) continue;
+      if (s_par[ch] != node) continue;
       if (tid == 0) {
         const int d = decide_child<T>(p, r, b, ch, c, n, logits);
         near += (unsigned)(d >> 1);
@@ -323,7 +348,7 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
     near += nuc ? 1u : 0u;
     near_smp += (unsigned)s_near;
     const int W = p.tree.Dmax + 1;
-    const int D = p.tree.depth[node];
+    const int D = s_dep[node];
     int32_t *pn = p.out_path_nodes ? p.out_path_nodes + (size_t)b * W : nullptr;
     int32_t *tk = p.out_tokens + (size_t)b * W;
     for (int i = 0; i < W; ++i) {
@@ -331,7 +356,7 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
       tk[i] = -1;
     }
     int i = D;
-    for (int a = node; a >= 0 && i >= 0; a = p.tree.parent[a], --i) {
+    for (int a = node; a >= 0 && i >= 0; a = s_par[a], --i) {
       if (pn) pn[i] = a;
       if (i >= 1) tk[i - 1] = p.tokens[(size_t)b * p.tok_stride + a - p.tok_offset];
     }

@@ -76,12 +76,14 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnParams p) 
   const int has_tree = split == 0 ? 1 : 0;
   const int n_tiles = n_pref + has_tree;
 
-  if (tid < kMaxNodes) sPar[tid] = tid < p.tree.N ? (int)p.tree.parent[tid] : -1;
+  // sequence b's tree (shared, or its own row): ancestor masks of its nodes
+  if (tid < kMaxNodes) sPar[tid] = tid < p.tree.N ? tree_parent(p.tree, b, tid) : -1;
   __syncthreads();
   if (tid < kMaxNodes) {
     uint64_t m = 0;
-    if (tid < p.tree.N)
-      for (int a = tid; a >= 0; a = sPar[a]) m |= 1ull << a;
+    int d;
+    if (tid < p.tree.N && !tree_walk(sPar, tid, &m, &d) && split == 0 && kvh == 0 && mt == 0)
+      set_status(p.status, SV_DEV_BAD_TREE);
     sAnc[tid] = m;
   }
 
@@ -310,17 +312,19 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const AttnParams p) 
   __shared__ int sPar[kMaxNodes];
   __shared__ uint64_t sAnc[kMaxNodes];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid < kMaxNodes) sPar[tid] = tid < p.tree.N ? (int)p.tree.parent[tid] : -1;
+  const int b = blockIdx.y;
+  // sequence b's tree (shared, or its own row): ancestor masks of its nodes
+  if (tid < kMaxNodes) sPar[tid] = tid < p.tree.N ? tree_parent(p.tree, b, tid) : -1;
   __syncthreads();
   if (tid < kMaxNodes) {
     uint64_t m = 0;
-    if (tid < p.tree.N)
-      for (int a = tid; a >= 0; a = sPar[a]) m |= 1ull << a;
+    int d;
+    if (tid < p.tree.N && !tree_walk(sPar, tid, &m, &d) && blockIdx.x == 0)
+      set_status(p.status, SV_DEV_BAD_TREE);
     sAnc[tid] = m;
   }
   __syncthreads();
   const int w = blockIdx.x * (kThreads / 32) + warp;
-  const int b = blockIdx.y;
   if (w >= p.N * p.Hq) return;
   const int n = w / p.Hq, hq = w % p.Hq, kvh = hq / p.G;
   const float *gq = static_cast<const float *>(p.q);

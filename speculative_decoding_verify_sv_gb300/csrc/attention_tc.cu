@@ -784,7 +784,16 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       const int R = pc.mg * (MT * kRows) + R_local;
       const bool valid_row = R < p.M;
       const int node = valid_row ? R / p.G : 0;
-      const uint64_t anc = valid_row ? sAnc[node] : 0ull;
+      // the node's ancestor mask: the shared tree's, or a walk of sequence b's own row
+      uint64_t anc = 0ull;
+      if (valid_row) {
+        if (p.tree.rows) {
+          int dep;
+          if (!tree_walk_seq(p.tree, pc.b, node, &anc, &dep)) set_status(p.status, SV_DEV_BAD_TREE);
+        } else {
+          anc = sAnc[node];
+        }
+      }
       const bool warp_idle = CP == 1 && __all_sync(0xFFFFFFFFu, !valid_row);
       const int L = clamp_len(p, pc.b);
       if (warp_idle) {  // every row of this warp is padding: barriers only

@@ -41,17 +41,20 @@ sv_status cuda_fail(cudaError_t e, const char *what) {
 
 constexpr int kMaxDevices = 64;
 
-// Device address of the status word on the current device (looked up once per device).
+// Device address of the status word on the current device (looked up once per device;
+// threads that race on the first lookup store the same address, atomically).
 unsigned int *status_word() {
-  static unsigned int *addr[kMaxDevices] = {nullptr};
+  static std::atomic<unsigned int *> addr[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!addr[dev]) {
+  unsigned int *a = addr[dev].load(std::memory_order_acquire);
+  if (!a) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_sv_status) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<unsigned int *>(p);
+    a = static_cast<unsigned int *>(p);
+    addr[dev].store(a, std::memory_order_release);
   }
-  return addr[dev];
+  return a;
 }
 
 int num_sms() {
@@ -93,6 +96,31 @@ sv_status make_tree(int N, const int32_t *parent, sv::Tree *t) {
     if (t->depth[i] > t->Dmax) t->Dmax = t->depth[i];
   }
   for (int i = N; i < SV_MAX_TREE_NODES; ++i) t->parent[i] = -1;
+  return SV_OK;
+}
+
+// The tree argument of the tree entry points: parent_stride == 0 -> a host array [N]
+// shared by the batch (checked here); parent_stride >= N -> a device array [B,stride], one
+// tree per sequence (checked by the kernels, which report SV_DEV_BAD_TREE); outputs then
+// have N columns (the deepest possible path).
+sv_status tree_arg(int N, const int32_t *parent, int parent_stride, sv::Tree *t) {
+  if (parent_stride == 0) return make_tree(N, parent, t);
+  if (parent == nullptr) return fail(SV_ERR_INVALID_ARG, "parent is NULL");
+  if (N < 1 || N > SV_MAX_TREE_NODES)
+    return fail(N < 1 ? SV_ERR_INVALID_ARG : SV_ERR_UNSUPPORTED,
+                "tree has %d nodes (supported 1..%d)", N, SV_MAX_TREE_NODES);
+  if (parent_stride < N)
+    return fail(SV_ERR_INVALID_ARG, "parent_stride = %d (0 for a shared tree, >= N = %d per sequence)",
+                parent_stride, N);
+  if ((reinterpret_cast<uintptr_t>(parent) & 3u) != 0)
+    return fail(SV_ERR_INVALID_ARG, "per-sequence parent rows must be 4-byte aligned");
+  // the shared fields hold a chain (a valid tree) that no kernel reads for these calls
+  int32_t chain[SV_MAX_TREE_NODES];
+  for (int i = 0; i < N; ++i) chain[i] = i - 1;
+  make_tree(N, chain, t);
+  t->Dmax = N - 1;
+  t->rows = parent;
+  t->stride = parent_stride;
   return SV_OK;
 }
 
@@ -173,14 +201,14 @@ int sv_tree_attention_path(sv_dtype dt, int N, int Hq, int Hkv, int D, int block
 
 sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, const void *q,
                             const void *k_tree, const void *v_tree, sv_kv_cache cache,
-                            const int32_t *parent, float scale, void *out, void *workspace,
-                            size_t workspace_bytes, void *stream) {
+                            const int32_t *parent, int parent_stride, float scale, void *out,
+                            void *workspace, size_t workspace_bytes, void *stream) {
   if (dt != SV_F32 && dt != SV_BF16) return fail(SV_ERR_UNSUPPORTED, "dtype %d not supported", (int)dt);
   if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
     return fail(SV_ERR_INVALID_ARG, "bad sizes B=%d Hq=%d Hkv=%d", B, Hq, Hkv);
   if (D != 64 && D != 128) return fail(SV_ERR_UNSUPPORTED, "head dim %d (supported 64, 128)", D);
   sv::Tree tree;
-  sv_status st = make_tree(N, parent, &tree);
+  sv_status st = tree_arg(N, parent, parent_stride, &tree);
   if (st != SV_OK) return st;
   if (!q || !k_tree || !v_tree || !out) return fail(SV_ERR_INVALID_ARG, "q, k_tree, v_tree or out is NULL");
   if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(out))
@@ -354,7 +382,7 @@ sv_status chain_params(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
 }
 
 sv_status tree_params(sv_mode mode, sv_dtype logit_dt, int B, int N, int V, const int32_t *parent,
-                      const int32_t *node_tokens, const void *target_logits, const void *q,
+                      int parent_stride, const int32_t *node_tokens, const void *target_logits, const void *q,
                       sv_q_kind q_kind, int Dq, float temperature, int top_k, float top_p, uint64_t seed,
                       uint64_t round, int32_t *out_path_nodes, int32_t *out_tokens,
                       int32_t *out_num_emitted, int32_t *out_num_accepted,
@@ -363,11 +391,13 @@ sv_status tree_params(sv_mode mode, sv_dtype logit_dt, int B, int N, int V, cons
                                top_p, out_tokens, out_num_emitted, out_num_accepted, greedy);
   if (st != SV_OK) return st;
   p = sv::AcceptParams{};
-  if ((st = make_tree(N, parent, &p.tree)) != SV_OK) return st;
+  if ((st = tree_arg(N, parent, parent_stride, &p.tree)) != SV_OK) return st;
   if (!node_tokens) return fail(SV_ERR_INVALID_ARG, "node_tokens is NULL");
   if (!out_path_nodes) return fail(SV_ERR_INVALID_ARG, "out_path_nodes is NULL");
-  if (!*greedy && Dq < p.tree.Dmax)
+  if (!*greedy && !p.tree.rows && Dq < p.tree.Dmax)  // (per-sequence trees: checked on the device)
     return fail(SV_ERR_INVALID_ARG, "q has %d depth rows, the tree is %d deep", Dq, p.tree.Dmax);
+  if (!*greedy && p.tree.rows && Dq < 1 && N > 1)
+    return fail(SV_ERR_INVALID_ARG, "q has no depth rows");
   if (!*greedy && q_kind == SV_Q_DRAFT_ONEHOT)
     return fail(SV_ERR_UNSUPPORTED, "one-hot draft q is supported for chains only");
   if (Dq < 0) return fail(SV_ERR_INVALID_ARG, "Dq < 0");
@@ -448,7 +478,7 @@ sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int
 }
 
 sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
-                         const int32_t *parent, const int32_t *node_tokens,
+                         const int32_t *parent, int parent_stride, const int32_t *node_tokens,
                          const void *target_logits, const void *q, sv_q_kind q_kind, int Dq,
                          float temperature, int top_k, float top_p, uint64_t seed, uint64_t round,
                          int32_t *out_path_nodes, int32_t *out_tokens,
@@ -457,7 +487,7 @@ sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
                          void *stream) {
   sv::AcceptParams p;
   bool greedy = false;
-  sv_status st = tree_params(mode, logit_dt, B, N, V, parent, node_tokens, target_logits, q,
+  sv_status st = tree_params(mode, logit_dt, B, N, V, parent, parent_stride, node_tokens, target_logits, q,
                              q_kind, Dq, temperature, top_k, top_p, seed, round, out_path_nodes,
                              out_tokens, out_num_emitted, out_num_accepted, out_near_ties, p,
                              &greedy);
@@ -466,6 +496,7 @@ sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
 }
 
 sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const int32_t *parent,
+                                   int parent_stride,
                                    const int32_t *node_tokens, const void *target_logits,
                                    const void *q, sv_q_kind q_kind, int Dq, float temperature,
                                    int top_k, float top_p, uint64_t seed, uint64_t round,
@@ -475,7 +506,7 @@ sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const
                                    size_t workspace_bytes, void *stream) {
   sv::AcceptParams p;
   bool greedy = false;
-  sv_status st = tree_params(SV_EXACT, logit_dt, B, N, V, parent, node_tokens, target_logits, q,
+  sv_status st = tree_params(SV_EXACT, logit_dt, B, N, V, parent, parent_stride, node_tokens, target_logits, q,
                              q_kind, Dq, temperature, top_k, top_p, seed, round, out_path_nodes,
                              out_tokens, out_num_emitted, out_num_accepted, out_near_ties, p,
                              &greedy);
@@ -521,7 +552,7 @@ sv_status sv_accept_chain_commit(sv_mode mode, sv_dtype logit_dt, int B, int gam
 }
 
 sv_status sv_accept_tree_commit(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
-                                const int32_t *parent, const int32_t *node_tokens,
+                                const int32_t *parent, int parent_stride, const int32_t *node_tokens,
                                 const void *target_logits, const void *q, sv_q_kind q_kind,
                                 int Dq, float temperature, int top_k, float top_p, uint64_t seed,
                                 uint64_t round, sv_dtype kv_dt, int Hkv, int D,
@@ -532,7 +563,7 @@ sv_status sv_accept_tree_commit(sv_mode mode, sv_dtype logit_dt, int B, int N, i
                                 void *stream) {
   sv::AcceptParams p;
   bool greedy = false;
-  sv_status st = tree_params(mode, logit_dt, B, N, V, parent, node_tokens, target_logits, q,
+  sv_status st = tree_params(mode, logit_dt, B, N, V, parent, parent_stride, node_tokens, target_logits, q,
                              q_kind, Dq, temperature, top_k, top_p, seed, round, out_path_nodes,
                              out_tokens, out_num_emitted, out_num_accepted, out_near_ties, p,
                              &greedy);
@@ -602,23 +633,25 @@ namespace {
 // Device address of the scratch array on the current device.  Looked up once per
 // device, with that device current; host code must never pass the array's name.
 void *noalloc_rows_address(sv_status *st) {
-  static void *addr[kMaxDevices] = {nullptr};
+  static std::atomic<void *> addr[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     *st = e != cudaSuccess ? cuda_fail(e, "cudaGetDevice") : fail(SV_ERR_CUDA, "device index out of range");
     return nullptr;
   }
-  if (!addr[dev]) {
+  void *a = addr[dev].load(std::memory_order_acquire);
+  if (!a) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_sv_noalloc_rows);
     if (e != cudaSuccess || p == nullptr) {
       *st = cuda_fail(e, "cudaGetSymbolAddress of the acceptance scratch array");
       return nullptr;
     }
-    addr[dev] = p;
+    a = p;  // threads racing on the first lookup store the same address
+    addr[dev].store(a, std::memory_order_release);
   }
-  return addr[dev];
+  return a;
 }
 
 }  // namespace
@@ -626,7 +659,7 @@ void *noalloc_rows_address(sv_status *st) {
 extern "C" {
 
 sv_status sv_accept_tree_noalloc(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
-                                 const int32_t *parent, const int32_t *node_tokens,
+                                 const int32_t *parent, int parent_stride, const int32_t *node_tokens,
                                  const void *target_logits, const void *q, sv_q_kind q_kind,
                                  int Dq, float temperature, int top_k, float top_p, uint64_t seed,
                                  uint64_t round, int32_t *out_path_nodes, int32_t *out_tokens,
@@ -642,7 +675,7 @@ sv_status sv_accept_tree_noalloc(sv_mode mode, sv_dtype logit_dt, int B, int N, 
   sv_status st = SV_OK;
   void *scratch = noalloc_rows_address(&st);
   if (!scratch) return st;
-  return sv_accept_tree(mode, logit_dt, B, N, V, parent, node_tokens, target_logits, q, q_kind,
+  return sv_accept_tree(mode, logit_dt, B, N, V, parent, parent_stride, node_tokens, target_logits, q, q_kind,
                         Dq, temperature, top_k, top_p, seed, round, out_path_nodes, out_tokens,
                         out_num_emitted, out_num_accepted, out_near_ties, scratch,
                         sizeof(g_sv_noalloc_rows), stream);

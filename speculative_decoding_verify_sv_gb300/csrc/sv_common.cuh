@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "sv.h"
+#include "sv_internal.h"
 
 namespace sv {
 
@@ -15,6 +16,62 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void set_status(unsigned int *status, unsigned int bits) {
   if (status) atomicOr(status, bits);
+}
+
+// ------------------------------------------------------------------ trees
+
+// Parent of node c (< N) of sequence b: the shared tree's, or the sequence's own row.
+__device__ __forceinline__ int tree_parent(const Tree &t, int b, int c) {
+  return t.rows ? __ldg(t.rows + (size_t)b * t.stride + c) : (int)t.parent[c];
+}
+
+// Walk from node c to the root over a parent array par[] (BFS order): the ancestor mask
+// (bit j set iff j is c or one of its ancestors) and the depth.  False when the chain is
+// not that of a BFS-ordered tree (a parent outside [0, i), or par[0] != -1): the walk stops
+// there, with the bits and depth gathered so far.  Per-sequence trees come from device
+// memory unchecked, so every kernel walks them this way; a shared tree was checked on the
+// host and always walks to the root.
+template <typename P>
+__device__ __forceinline__ bool tree_walk(const P *par, int c, uint64_t *anc, int *depth) {
+  uint64_t m = 0;
+  int d = 0, a = c;
+  for (int s = 0; s < kMaxNodes; ++s) {
+    m |= 1ull << a;
+    if (a == 0) {
+      *anc = m;
+      *depth = d;
+      return (int)par[0] == -1;
+    }
+    const int pa = (int)par[a];
+    if (pa < 0 || pa >= a) break;
+    a = pa;
+    ++d;
+  }
+  *anc = m;
+  *depth = d;
+  return false;
+}
+
+// The same walk reading sequence b's parents straight from the tree descriptor.
+__device__ __forceinline__ bool tree_walk_seq(const Tree &t, int b, int c, uint64_t *anc,
+                                              int *depth) {
+  uint64_t m = 0;
+  int d = 0, a = c;
+  for (int s = 0; s < kMaxNodes; ++s) {
+    m |= 1ull << a;
+    if (a == 0) {
+      *anc = m;
+      *depth = d;
+      return tree_parent(t, b, 0) == -1;
+    }
+    const int pa = tree_parent(t, b, a);
+    if (pa < 0 || pa >= a) break;
+    a = pa;
+    ++d;
+  }
+  *anc = m;
+  *depth = d;
+  return false;
 }
 
 // ------------------------------------------------------------ element access

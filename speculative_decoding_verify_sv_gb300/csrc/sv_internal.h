@@ -13,12 +13,17 @@ namespace sv {
 constexpr int kMaxNodes = SV_MAX_TREE_NODES;
 
 // The candidate tree, passed by value: parent (BFS order, parent[0] = -1) and depth.
+// Per-sequence trees (rows != NULL): sequence b's parent array is rows[b*stride ..
+// b*stride + N) in device memory, checked on the device; parent, depth and has_child are
+// then unused and Dmax = N - 1 (the widest path, which sizes the outputs).
 struct Tree {
   int N;
   int Dmax;
   int8_t parent[kMaxNodes];
   int8_t depth[kMaxNodes];
   int8_t has_child[kMaxNodes];
+  const int32_t *rows;
+  int stride;
 };
 
 // ---------------------------------------------------------------- attention

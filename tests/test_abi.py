@@ -70,22 +70,22 @@ def test_attention_rejects_before_launch(lib):
     par = (ctypes.c_int32 * 1)(-1)
     P = ctypes.c_void_p(16)
     # head dim 96 is not compiled
-    assert lib.sv_tree_attention(1, 1, 1, 4, 4, 96, P, P, P, _cache(), par, 0.1, P, None, 0,
+    assert lib.sv_tree_attention(1, 1, 1, 4, 4, 96, P, P, P, _cache(), par, 0, 0.1, P, None, 0,
                                  None) == sv.SV_ERR_UNSUPPORTED
     # Hq not a multiple of Hkv
-    assert lib.sv_tree_attention(1, 1, 1, 6, 4, 128, P, P, P, _cache(), par, 0.1, P, None, 0,
+    assert lib.sv_tree_attention(1, 1, 1, 6, 4, 128, P, P, P, _cache(), par, 0, 0.1, P, None, 0,
                                  None) == sv.SV_ERR_INVALID_ARG
     # misaligned q
-    assert lib.sv_tree_attention(1, 1, 1, 4, 4, 128, ctypes.c_void_p(18), P, P, _cache(), par,
+    assert lib.sv_tree_attention(1, 1, 1, 4, 4, 128, ctypes.c_void_p(18), P, P, _cache(), par, 0,
                                  0.1, P, None, 0, None) == sv.SV_ERR_INVALID_ARG
     # NaN scale
-    assert lib.sv_tree_attention(1, 1, 1, 4, 4, 128, P, P, P, _cache(), par, float("nan"), P,
+    assert lib.sv_tree_attention(1, 1, 1, 4, 4, 128, P, P, P, _cache(), par, 0, float("nan"), P,
                                  None, 0, None) == sv.SV_ERR_INVALID_ARG
     assert "scale" in lib.sv_last_error().decode()
     # missing workspace when the plan needs one (long prefix, small batch -> splits)
     need = lib.sv_tree_attention_workspace_size(1, 1, 1, 4, 4, 128, 32768)
     assert need > 0
-    assert lib.sv_tree_attention(1, 1, 1, 4, 4, 128, P, P, P, _cache(Lmax=32768), par, 0.1, P,
+    assert lib.sv_tree_attention(1, 1, 1, 4, 4, 128, P, P, P, _cache(Lmax=32768), par, 0, 0.1, P,
                                  None, 0, None) == sv.SV_ERR_WORKSPACE
 
 
@@ -105,7 +105,7 @@ def test_accept_rejects_before_launch(lib):
     assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, None, 1, P, 1.0, 0, 1.0, 0, 0, P, P, P, P, P,
                                1 << 20, None) == sv.SV_ERR_INVALID_ARG
     # q rows must cover the tree depth
-    assert lib.sv_accept_tree(1, 1, 1, 3, 1000, par, P, P, P, 1, 0, 1.0, 0, 1.0, 0, 0, P, P, P, P, P,
+    assert lib.sv_accept_tree(1, 1, 1, 3, 1000, par, 0, P, P, P, 1, 0, 1.0, 0, 1.0, 0, 0, P, P, P, P, P,
                               P, 1 << 20, None) == sv.SV_ERR_INVALID_ARG
     # top_p outside (0, 1]; top_p < 1 without top-k in exact mode
     assert lib.sv_accept_chain(1, 1, 1, 4, 1000, P, P, 1, P, 1.0, 5, 0.0, 0, 0, P, P, P, P, P,
@@ -117,7 +117,7 @@ def test_accept_rejects_before_launch(lib):
     # workspace too small
     need = lib.sv_accept_workspace_size(2, 3, 1000, 1)
     assert need > 0
-    assert lib.sv_accept_tree(1, 1, 2, 3, 1000, par, P, P, P, 1, 1, 1.0, 0, 1.0, 0, 0, P, P, P, P, P,
+    assert lib.sv_accept_tree(1, 1, 2, 3, 1000, par, 0, P, P, P, 1, 1, 1.0, 0, 1.0, 0, 0, P, P, P, P, P,
                               P, 16, None) == sv.SV_ERR_WORKSPACE
     del common
 
@@ -133,11 +133,11 @@ def test_fused_accept_commit_rejects_before_launch(lib):
     P = ctypes.c_void_p(16)
     par = (ctypes.c_int32 * 3)(-1, 0, 0)
     # a bad acceptance argument (V not a multiple of 8) is reported as by sv_accept_tree
-    assert lib.sv_accept_tree_commit(1, 1, 1, 3, 1001, par, P, P, P, 1, 2, 1.0, 0, 1.0, 0, 0,
+    assert lib.sv_accept_tree_commit(1, 1, 1, 3, 1001, par, 0, P, P, P, 1, 2, 1.0, 0, 1.0, 0, 0,
                                      1, 4, 128, P, P, _cache(), P, P, P, P, P, P, 1 << 20,
                                      None) == sv.SV_ERR_UNSUPPORTED
     # a bad commit argument (missing tree V) is reported as by sv_commit_kv
-    assert lib.sv_accept_tree_commit(1, 1, 1, 3, 1000, par, P, P, P, 1, 2, 1.0, 0, 1.0, 0, 0,
+    assert lib.sv_accept_tree_commit(1, 1, 1, 3, 1000, par, 0, P, P, P, 1, 2, 1.0, 0, 1.0, 0, 0,
                                      1, 4, 128, P, None, _cache(), P, P, P, P, P, P, 1 << 20,
                                      None) == sv.SV_ERR_INVALID_ARG
     assert "v_tree" in lib.sv_last_error().decode()
@@ -153,7 +153,7 @@ def test_tree_recursive_rejects_before_launch(lib):
     bad = (ctypes.c_int32 * 3)(-1, 2, 0)  # a parent after its child
 
     def call(parent=par, V=1000, q=P, Dq=1, T=1.0, top_k=0, top_p=1.0, ws=1 << 20):
-        return lib.sv_accept_tree_recursive(1, 2, 3, V, parent, P, P, q, 1, Dq, T, top_k, top_p,
+        return lib.sv_accept_tree_recursive(1, 2, 3, V, parent, 0, P, P, q, 1, Dq, T, top_k, top_p,
                                             0, 0, P, P, P, P, P, P, ws, None)
     # greedy (temperature 0) has no sibling residuals: unsupported here
     assert call(T=0.0) == sv.SV_ERR_UNSUPPORTED
@@ -182,3 +182,24 @@ def test_binding_requires_cuda_tensors(lib):
     with pytest.raises(TypeError):
         sv.sv_accept_chain(sv.GREEDY, torch.zeros(1, 2, 8), None, sv.Q_LOGITS,
                            torch.zeros(1, 1, dtype=torch.int32))
+
+
+def test_per_sequence_tree_argument_is_checked_before_launch(lib):
+    """parent_stride: 0 = a host tree shared by the batch; >= N = one device row per
+    sequence.  A stride between 1 and N-1, a NULL or misaligned row pointer are rejected."""
+    P = ctypes.c_void_p(16)
+    rows = ctypes.c_void_p(4096)  # a device address the host never reads
+    def attn(parent, stride):
+        return lib.sv_tree_attention(1, 2, 3, 4, 4, 128, P, P, P, _cache(), parent, stride, 0.1, P,
+                                     P, 1 << 20, None)
+    assert attn(rows, 2) == sv.SV_ERR_INVALID_ARG
+    assert "parent_stride" in lib.sv_last_error().decode()
+    assert attn(None, 3) == sv.SV_ERR_INVALID_ARG
+    assert attn(ctypes.c_void_p(4098), 3) == sv.SV_ERR_INVALID_ARG
+
+    def accept(parent, stride, Dq=2):
+        return lib.sv_accept_tree(1, 1, 2, 3, 1000, parent, stride, P, P, P, 1, Dq, 1.0, 0, 1.0, 0,
+                                  0, P, P, P, P, P, P, 1 << 20, None)
+    assert accept(rows, -1) == sv.SV_ERR_INVALID_ARG
+    assert accept(rows, 1) == sv.SV_ERR_INVALID_ARG
+    assert accept(rows, 3, Dq=0) == sv.SV_ERR_INVALID_ARG  # exact mode needs q rows

@@ -26,7 +26,7 @@ def _noalloc_call(lib, mode, tl, q, parent, toks, seed, rnd, outs):
     Dq = 0 if q is None else q.shape[1]
     P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    return lib.sv_accept_tree_noalloc(mode, 1, B, N, V, par, P(toks), P(tl), P(q), sv.Q_LOGITS, Dq,
+    return lib.sv_accept_tree_noalloc(mode, 1, B, N, V, par, 0, P(toks), P(tl), P(q), sv.Q_LOGITS, Dq,
                                       1.0, 0, 1.0, seed, rnd, P(outs["path_nodes"]), P(outs["tokens"]),
                                       P(outs["num_emitted"]), P(outs["num_accepted"]),
                                       P(outs["near_ties"]), stream)
@@ -63,7 +63,7 @@ def test_noalloc_rejects_rows_beyond_its_scratch(cuda_ok):
     par = (ctypes.c_int32 * 5)(-1, 0, 1, 2, 3)
     P = ctypes.c_void_p(16)
     # 20000 * (5 + 4) rows > 65536: rejected before anything is launched
-    rc = lib.sv_accept_tree_noalloc(sv.EXACT, 1, 20000, 5, 64, par, P, P, P, sv.Q_LOGITS, 4, 1.0,
+    rc = lib.sv_accept_tree_noalloc(sv.EXACT, 1, 20000, 5, 64, par, 0, P, P, P, sv.Q_LOGITS, 4, 1.0,
                                     0, 1.0, 0, 0, P, P, P, P, P, None)
     assert rc == sv.SV_ERR_UNSUPPORTED
     assert "fixed scratch" in lib.sv_last_error().decode()
