@@ -8,7 +8,9 @@
  * pair.  sv_accept_tree_recursive is the tree acceptance that tries a node's children
  * in turn (siblings drawn from q keep the target's distribution), sv_accept_tree_noalloc
  * the tree acceptance without a workspace, and sv_ngram_draft proposes prompt-lookup
- * drafts on the device.
+ * drafts on the device; sv_lm_head is the LM-head projection on the tensor cores, and
+ * sv_accept_chain_lmhead / sv_accept_tree_lmhead fuse it with the acceptance (the target
+ * rows' statistics come from the projection's epilogue).
  *
  * Conventions shared by every entry point
  *  - Every tensor argument is caller-owned DEVICE memory, dense row-major in the layout
@@ -328,6 +330,46 @@ sv_status sv_accept_chain_commit(sv_mode mode, sv_dtype logit_dt, int B, int gam
                                  int32_t *out_tokens, int32_t *out_num_emitted,
                                  int32_t *out_num_accepted, uint32_t *out_near_ties,
                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------ LM head */
+
+/* The LM-head projection ("推测解码技术详解", section "Medusa Heads": the original LM head
+ * and the Medusa heads read the backbone's last hidden states; lpnh.cn walkthrough,
+ * section 3.1: a head is a Linear(H, V) from h_t to V logits): logits[r, v] =
+ * sum_k hidden[r, k] * weight[v, k] with fp32 accumulation on the tensor cores, stored in
+ * bf16.  hidden [R, Dm] bf16, weight [V, Dm] bf16 (row v = token v's output embedding; no
+ * bias), logits [R, V] bf16 (written).  Dm and V positive multiples of 8.  No workspace. */
+sv_status sv_lm_head(int R, int Dm, int V, const void *hidden, const void *weight, void *logits,
+                     void *stream);
+
+/* Acceptance fused with the LM-head projection of the target rows: the projection above
+ * computes the target logits from the hidden states (stored in target_logits, which the
+ * final sample reads) and, without top-k, its epilogue also takes each row's statistics
+ * (max, argmax, softmax sum at the given temperature), so the logits are not read back for
+ * them; with top-k the statistics kernel reads the stored rows.  Then the acceptance of
+ * sv_accept_chain / sv_accept_tree runs on the stored bf16 logits: every argument, output,
+ * uniform and near-tie report as there, with logit_dt = SV_BF16.
+ * hidden [B, gamma+1, Dm] (chain) or [B, N, Dm] (tree) bf16, row order of the target rows;
+ * weight [V, Dm] bf16; target_logits [B, gamma+1 or N, V] bf16 (written).
+ * Workspace: sv_accept_lmhead_workspace_size(B, N, V, Dq) (N = gamma+1, Dq = gamma for a
+ * chain). */
+size_t sv_accept_lmhead_workspace_size(int B, int N, int V, int Dq);
+sv_status sv_accept_chain_lmhead(sv_mode mode, int B, int gamma, int V, int Dm, const void *hidden,
+                                 const void *weight, void *target_logits, const void *q,
+                                 sv_q_kind q_kind, const int32_t *draft_tokens, float temperature,
+                                 int top_k, float top_p, uint64_t seed, uint64_t round,
+                                 int32_t *out_tokens, int32_t *out_num_emitted,
+                                 int32_t *out_num_accepted, uint32_t *out_near_ties,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+sv_status sv_accept_tree_lmhead(sv_mode mode, int B, int N, int V, int Dm, const void *hidden,
+                                const void *weight, void *target_logits, const int32_t *parent,
+                                int parent_stride, const int32_t *node_tokens, const void *q,
+                                sv_q_kind q_kind, int Dq, float temperature, int top_k,
+                                float top_p, uint64_t seed, uint64_t round,
+                                int32_t *out_path_nodes, int32_t *out_tokens,
+                                int32_t *out_num_emitted, int32_t *out_num_accepted,
+                                uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
+                                void *stream);
 
 /* ---------------------------------------------------------------- tree helper */
 

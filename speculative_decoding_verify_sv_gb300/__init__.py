@@ -21,6 +21,7 @@ __all__ = [
     "sv_tree_attention_workspace_size", "sv_tree_attention_path", "sv_accept_chain", "sv_accept_tree",
     "sv_accept_workspace_size", "sv_accept_tree_noalloc", "sv_commit_kv", "sv_accept_tree_commit",
     "sv_accept_chain_commit", "sv_accept_tree_recursive", "sv_ngram_draft", "sv_tree_prepare", "sv_read_device_status",
+    "sv_lm_head", "sv_accept_lmhead_workspace_size", "sv_accept_chain_lmhead", "sv_accept_tree_lmhead",
     "sv_version", "sv_kernel_launches", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "Q_DRAFT_ONEHOT", "SV_MAX_TREE_NODES",
 ]
 
@@ -91,6 +92,13 @@ def load_library():
                                               I, I, I, P, P, _KVCacheC, P, P, P, P, P, P, SZ, P]
         lib.sv_accept_chain_commit.argtypes = [I, I, I, I, I, P, P, I, P, F, I, F, U64, U64,
                                                I, I, I, P, P, _KVCacheC, P, P, P, P, P, SZ, P]
+        lib.sv_lm_head.argtypes = [I, I, I, P, P, P, P]
+        lib.sv_accept_lmhead_workspace_size.argtypes = [I, I, I, I]
+        lib.sv_accept_lmhead_workspace_size.restype = SZ
+        lib.sv_accept_chain_lmhead.argtypes = [I, I, I, I, I, P, P, P, P, I, P, F, I, F, U64, U64,
+                                               P, P, P, P, P, SZ, P]
+        lib.sv_accept_tree_lmhead.argtypes = [I, I, I, I, I, P, P, P, P, I, P, P, I, I, F, I, F,
+                                              U64, U64, P, P, P, P, P, P, SZ, P]
         lib.sv_tree_prepare.argtypes = [I, P, P, P]
         lib.sv_read_device_status.argtypes = [P, P]
         lib.sv_ngram_draft.argtypes = [I, I, P, P, I, I, I, P, P, P]
@@ -499,6 +507,104 @@ def sv_read_device_status(stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check(lib.sv_read_device_status(ctypes.byref(v), _stream(stream)))
     return int(v.value)
+
+
+# ------------------------------------------------------------------- LM head
+
+def sv_lm_head(hidden, weight, out=None, stream=None) -> torch.Tensor:
+    """LM-head projection on the tensor cores: hidden [..., Dm] bf16, weight [V, Dm] bf16
+    -> logits [..., V] bf16 (fp32 accumulation)."""
+    lib = load_library()
+    _dev(hidden, "hidden", torch.bfloat16)
+    _dev(weight, "weight", torch.bfloat16)
+    Dm = hidden.shape[-1]
+    V = weight.shape[0]
+    if weight.dim() != 2 or weight.shape[1] != Dm:
+        raise ValueError(f"weight must be [V, {Dm}]")
+    R = hidden.numel() // Dm
+    if out is None:
+        out = torch.empty(tuple(hidden.shape[:-1]) + (V,), dtype=torch.bfloat16, device=hidden.device)
+    _dev(out, "logits", torch.bfloat16, tuple(hidden.shape[:-1]) + (V,))
+    _check(lib.sv_lm_head(R, Dm, V, _ptr(hidden), _ptr(weight), _ptr(out), _stream(stream)))
+    return out
+
+
+def sv_accept_lmhead_workspace_size(B, N, V, Dq) -> int:
+    return int(load_library().sv_accept_lmhead_workspace_size(B, N, V, Dq))
+
+
+def _lmhead_args(hidden, weight, B, N):
+    _dev(hidden, "hidden", torch.bfloat16)
+    _dev(weight, "weight", torch.bfloat16)
+    if hidden.dim() != 3 or hidden.shape[:2] != (B, N):
+        raise ValueError(f"hidden must be [B={B}, {N}, Dm]")
+    Dm = hidden.shape[2]
+    if weight.dim() != 2 or weight.shape[1] != Dm:
+        raise ValueError(f"weight must be [V, {Dm}]")
+    return Dm, weight.shape[0]
+
+
+def sv_accept_chain_lmhead(mode, hidden, weight, q, q_kind, draft_tokens, temperature=1.0, top_k=0,
+                           seed=0, round_=0, top_p=1.0, outs=None, logits=None, workspace=None,
+                           stream=None) -> dict:
+    """Chain acceptance fused with the LM-head projection of the target rows: hidden
+    [B,gamma+1,Dm] bf16, weight [V,Dm] bf16; the target logits [B,gamma+1,V] (bf16) are
+    returned under "target_logits" with the acceptance outputs."""
+    lib = load_library()
+    _dev(draft_tokens, "draft_tokens", torch.int32)
+    B, gamma = draft_tokens.shape
+    W = gamma + 1
+    Dm, V = _lmhead_args(hidden, weight, B, W)
+    if q_kind == Q_DRAFT_ONEHOT:
+        q = None
+    if q is not None:
+        _dev(q, "q", torch.bfloat16 if q_kind == Q_LOGITS else torch.float32, (B, gamma, V))
+    if logits is None:
+        logits = torch.empty((B, W, V), dtype=torch.bfloat16, device=hidden.device)
+    _dev(logits, "logits", torch.bfloat16, (B, W, V))
+    outs = _accept_outputs(B, W, hidden.device, outs)
+    workspace, ws_bytes = _workspace(sv_accept_lmhead_workspace_size(B, W, V, gamma), hidden.device,
+                                     workspace)
+    _check(lib.sv_accept_chain_lmhead(mode, B, gamma, V, Dm, _ptr(hidden), _ptr(weight), _ptr(logits),
+                                      _ptr(q), q_kind, _ptr(draft_tokens), float(temperature),
+                                      int(top_k), float(top_p), int(seed), int(round_),
+                                      _ptr(outs["tokens"]), _ptr(outs["num_emitted"]),
+                                      _ptr(outs["num_accepted"]), _ptr(outs["near_ties"]),
+                                      _ptr(workspace), ws_bytes, _stream(stream)))
+    outs["target_logits"] = logits
+    return outs
+
+
+def sv_accept_tree_lmhead(mode, hidden, weight, q, q_kind, parent, node_tokens, temperature=1.0,
+                          top_k=0, seed=0, round_=0, top_p=1.0, outs=None, logits=None,
+                          workspace=None, stream=None) -> dict:
+    """Tree acceptance fused with the LM-head projection: hidden [B,N,Dm] bf16, weight
+    [V,Dm] bf16; the target logits [B,N,V] bf16 are returned under "target_logits"."""
+    lib = load_library()
+    _dev(node_tokens, "node_tokens", torch.int32)
+    B, N = node_tokens.shape
+    Dm, V = _lmhead_args(hidden, weight, B, N)
+    Dq = 0
+    if q is not None:
+        Dq = q.shape[1]
+        _dev(q, "q", torch.bfloat16 if q_kind == Q_LOGITS else torch.float32, (B, Dq, V))
+    par, pstride, W = _tree_arg(parent, B, N)
+    if logits is None:
+        logits = torch.empty((B, N, V), dtype=torch.bfloat16, device=hidden.device)
+    _dev(logits, "logits", torch.bfloat16, (B, N, V))
+    outs = _accept_outputs(B, W, hidden.device, outs)
+    outs.setdefault("path_nodes", torch.empty((B, W), dtype=torch.int32, device=hidden.device))
+    workspace, ws_bytes = _workspace(sv_accept_lmhead_workspace_size(B, N, V, Dq), hidden.device,
+                                     workspace)
+    _check(lib.sv_accept_tree_lmhead(mode, B, N, V, Dm, _ptr(hidden), _ptr(weight), _ptr(logits), par,
+                                     pstride, _ptr(node_tokens), _ptr(q), q_kind, Dq,
+                                     float(temperature), int(top_k), float(top_p), int(seed),
+                                     int(round_), _ptr(outs["path_nodes"]), _ptr(outs["tokens"]),
+                                     _ptr(outs["num_emitted"]), _ptr(outs["num_accepted"]),
+                                     _ptr(outs["near_ties"]), _ptr(workspace), ws_bytes,
+                                     _stream(stream)))
+    outs["target_logits"] = logits
+    return outs
 
 
 def sv_ngram_draft(history, length, max_ngram=3, min_ngram=1, gamma=4, out=None,

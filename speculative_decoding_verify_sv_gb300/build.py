@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libsv.so")
 
 SOURCES = ["sv_api.cu", "attention.cu", "attention_tc.cu", "accept.cu", "accept_recursive.cu",
-           "commit.cu", "ngram.cu"]
+           "commit.cu", "ngram.cu", "lm_head.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                  "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]

@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(stat_threads<TOPK>(), 4) accept_stats_kernel(c
   // the select kernel may be scheduled now; it waits for this grid before reading the
   // statistics (programmatic dependent launch)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  row_stats<T, GREEDY, TOPK, stat_threads<TOPK>()>(p, blockIdx.x);
+  row_stats<T, GREEDY, TOPK, stat_threads<TOPK>()>(p, (size_t)p.stat_row0 + blockIdx.x);
 }
 
 // ------------------------------------------------------------ kernel 2
@@ -1671,6 +1671,28 @@ cudaError_t launch_accept(sv_dtype dt, const AcceptParams &p, int num_sms, cudaS
 
 cudaError_t launch_accept_stats(sv_dtype dt, const AcceptParams &p, cudaStream_t s) {
   return dt == SV_F32 ? launch_stats_typed<float>(p, s) : launch_stats_typed<bf16>(p, s);
+}
+
+// The target rows' statistics are already in place (the LM-head projection's epilogue
+// wrote them; no top-k): the statistics kernel over the q rows only when q comes as
+// logits, then the select kernel (its wait for the previous grid then covers either).
+template <typename T>
+cudaError_t launch_given_typed(const AcceptParams &p, int num_sms, cudaStream_t s) {
+  const bool greedy = p.mode == SV_GREEDY;
+  if (!greedy && p.q_kind == SV_Q_LOGITS && p.B * p.Dq > 0) {
+    AcceptParams pq = p;
+    pq.stat_row0 = p.B * p.N;
+    accept_stats_kernel<T, false, false><<<p.B * p.Dq, stat_threads<false>(), 0, s>>>(pq);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (greedy) return launch_select<T, true, false>(p, num_sms, s);
+  return launch_select<T, false, false>(p, num_sms, s);
+}
+
+cudaError_t launch_accept_given_target_stats(sv_dtype dt, const AcceptParams &p, int num_sms,
+                                             cudaStream_t s) {
+  return dt == SV_F32 ? launch_given_typed<float>(p, num_sms, s) : launch_given_typed<bf16>(p, num_sms, s);
 }
 
 }  // namespace sv

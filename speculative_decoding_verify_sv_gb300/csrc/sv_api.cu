@@ -618,6 +618,126 @@ sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_
 
 }  // extern "C"
 
+// ------------------------------------------------- LM head fused with acceptance
+
+namespace {
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+sv_status lm_head_check(int R, int Dm, int V, const void *hidden, const void *weight,
+                        const void *logits) {
+  if (R < 0) return fail(SV_ERR_INVALID_ARG, "rows = %d", R);
+  if (Dm < 8 || Dm % 8 != 0)
+    return fail(SV_ERR_UNSUPPORTED, "hidden size %d must be a positive multiple of 8", Dm);
+  if (V < 8 || V % 8 != 0) return fail(SV_ERR_UNSUPPORTED, "V = %d must be a positive multiple of 8", V);
+  if (!hidden || !weight || !logits) return fail(SV_ERR_INVALID_ARG, "hidden, weight or logits is NULL");
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(logits))
+    return fail(SV_ERR_INVALID_ARG, "hidden, weight and logits must be 16-byte aligned");
+  return SV_OK;
+}
+
+// The projection of the B*N target rows, then the acceptance on the stored logits.  With no
+// top-k / top-p the projection's epilogue gives the target rows' statistics (the statistics
+// kernel then runs over the q rows only); otherwise the statistics kernel reads every row.
+sv_status lm_head_accept_launch(sv::AcceptParams &p, bool greedy, int Dm, const void *hidden,
+                                const void *weight, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+  const size_t st_bytes = up256(sv::accept_ws_bytes(p.B, p.N, p.Dq));
+  const size_t need = st_bytes + sv::lm_head_part_bytes(p.B * p.N, p.V);
+  if (!workspace || workspace_bytes < need)
+    return fail(SV_ERR_WORKSPACE, "LM-head acceptance workspace %zu bytes, need %zu", workspace_bytes, need);
+  if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  p.status = status_word();
+  if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
+  p.mode = greedy ? SV_GREEDY : SV_EXACT;
+  p.c_log2 = greedy ? 0.f : (float)(1.4426950408889634 / (double)p.temperature);
+  if (p.top_k >= p.V) p.top_k = 0;
+  if (greedy) p.top_p = 1.f;
+  p.stats = static_cast<sv::RowStat *>(workspace);
+  if (p.B == 0) return SV_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool epilogue_stats = greedy || p.top_k == 0;  // (top_p < 1 needs top-k)
+  void *part = static_cast<uint8_t *>(workspace) + st_bytes;
+  cudaError_t e = sv::launch_lm_head(hidden, weight, p.B * p.N, Dm, p.V, p.c_log2,
+                                     const_cast<void *>(p.target), epilogue_stats ? part : nullptr,
+                                     epilogue_stats ? p.stats : nullptr, p.status, num_sms(), s);
+  if (e != cudaSuccess) return cuda_fail(e, "LM-head projection launch");
+  sv::count_launches(epilogue_stats ? 2 : 1);
+  if (epilogue_stats) {
+    e = sv::launch_accept_given_target_stats(SV_BF16, p, num_sms(), s);
+    const bool q_stats = !greedy && p.q_kind == SV_Q_LOGITS && p.Dq > 0;
+    if (e == cudaSuccess) sv::count_launches(q_stats ? 2 : 1);
+  } else {
+    e = sv::launch_accept(SV_BF16, p, num_sms(), s);
+    if (e == cudaSuccess) sv::count_launches(2);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "acceptance launch");
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sv_status sv_lm_head(int R, int Dm, int V, const void *hidden, const void *weight, void *logits,
+                     void *stream) {
+  sv_status st = lm_head_check(R, Dm, V, hidden, weight, logits);
+  if (st != SV_OK) return st;
+  unsigned int *status = status_word();
+  if (!status) return fail(SV_ERR_CUDA, "no CUDA device");
+  if (R == 0) return SV_OK;
+  cudaError_t e = sv::launch_lm_head(hidden, weight, R, Dm, V, 0.f, logits, nullptr, nullptr,
+                                     status, num_sms(), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "LM-head projection launch");
+  sv::count_launches(1);
+  return SV_OK;
+}
+
+size_t sv_accept_lmhead_workspace_size(int B, int N, int V, int Dq) {
+  if (B <= 0 || N <= 0 || V <= 0 || Dq < 0) return 0;
+  return up256(sv::accept_ws_bytes(B, N, Dq)) + sv::lm_head_part_bytes(B * N, V);
+}
+
+sv_status sv_accept_chain_lmhead(sv_mode mode, int B, int gamma, int V, int Dm, const void *hidden,
+                                 const void *weight, void *target_logits, const void *q,
+                                 sv_q_kind q_kind, const int32_t *draft_tokens, float temperature,
+                                 int top_k, float top_p, uint64_t seed, uint64_t round,
+                                 int32_t *out_tokens, int32_t *out_num_emitted,
+                                 int32_t *out_num_accepted, uint32_t *out_near_ties,
+                                 void *workspace, size_t workspace_bytes, void *stream) {
+  sv_status st = lm_head_check(B * (gamma + 1), Dm, V, hidden, weight, target_logits);
+  if (st != SV_OK) return st;
+  sv::AcceptParams p;
+  bool greedy = false;
+  st = chain_params(mode, SV_BF16, B, gamma, V, target_logits, q, q_kind, draft_tokens,
+                    temperature, top_k, top_p, seed, round, out_tokens, out_num_emitted,
+                    out_num_accepted, out_near_ties, p, &greedy);
+  if (st != SV_OK) return st;
+  return lm_head_accept_launch(p, greedy, Dm, hidden, weight, workspace, workspace_bytes, stream);
+}
+
+sv_status sv_accept_tree_lmhead(sv_mode mode, int B, int N, int V, int Dm, const void *hidden,
+                                const void *weight, void *target_logits, const int32_t *parent,
+                                int parent_stride, const int32_t *node_tokens, const void *q,
+                                sv_q_kind q_kind, int Dq, float temperature, int top_k,
+                                float top_p, uint64_t seed, uint64_t round,
+                                int32_t *out_path_nodes, int32_t *out_tokens,
+                                int32_t *out_num_emitted, int32_t *out_num_accepted,
+                                uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+  sv_status st = lm_head_check(B * N, Dm, V, hidden, weight, target_logits);
+  if (st != SV_OK) return st;
+  sv::AcceptParams p;
+  bool greedy = false;
+  st = tree_params(mode, SV_BF16, B, N, V, parent, parent_stride, node_tokens, target_logits, q,
+                   q_kind, Dq, temperature, top_k, top_p, seed, round, out_path_nodes, out_tokens,
+                   out_num_emitted, out_num_accepted, out_near_ties, p, &greedy);
+  if (st != SV_OK) return st;
+  return lm_head_accept_launch(p, greedy, Dm, hidden, weight, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
 // ------------------------------------------------- acceptance without allocation
 
 // Scratch of sv_accept_tree_noalloc: the per-row statistics (row max, argmax, top-k

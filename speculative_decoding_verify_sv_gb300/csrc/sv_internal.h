@@ -131,6 +131,7 @@ struct AcceptParams {
   int top_k;                 // 0 = off
   float top_p;               // 1 = off; < 1 only with top-k (the nucleus of its distribution)
   int ring_stages;           // stages of the select kernel's ring (set at its launch)
+  int stat_row0;             // first row of the statistics kernel's grid (q rows only: B*N)
   uint64_t seed, round;
   RowStat *stats;            // [B*N + B*Dq]
   int32_t *out_path_nodes;   // [B,Dmax+1] or NULL
@@ -166,5 +167,27 @@ cudaError_t launch_accept_stats(sv_dtype dt, const AcceptParams &p, cudaStream_t
 cudaError_t launch_accept_recursive(sv_dtype dt, const AcceptParams &p, cudaStream_t s);
 
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
+
+// ---------------------------------------------------------------- LM head
+
+struct LmHeadParams {
+  CUtensorMap tm_h, tm_w;  // hidden [R, Dm] and weight [V, Dm] as K-major operand views
+  void *z;                 // [R, V] bf16 logits (out)
+  float4 *part;            // [R, ntiles] per (row, 256-column tile): max, sum, argmax bits
+  unsigned int *status;
+  int R, V, Dm, mtiles, ntiles;
+  float c_log2;            // log2(e) / T (0: statistics without the softmax sum)
+};
+// Bytes of the per-(row, tile) partial statistics of the projection.
+size_t lm_head_part_bytes(int R, int V);
+// z = hidden W^T (bf16 out), then, when stats is not NULL, the rows' statistics (max,
+// argmax, softmax sum at temperature 1 / (c_log2 ln 2); no top-k) into stats[0..R).
+cudaError_t launch_lm_head(const void *hidden, const void *weight, int R, int Dm, int V,
+                           float c_log2, void *z, void *part, RowStat *stats, unsigned int *status,
+                           int num_sms, cudaStream_t s);
+// The acceptance with the target rows' statistics already in p.stats (from the projection):
+// the statistics kernel over the q rows only (q logits), then the select kernel.
+cudaError_t launch_accept_given_target_stats(sv_dtype dt, const AcceptParams &p, int num_sms,
+                                             cudaStream_t s);
 
 }  // namespace sv

@@ -203,3 +203,25 @@ def test_per_sequence_tree_argument_is_checked_before_launch(lib):
     assert accept(rows, -1) == sv.SV_ERR_INVALID_ARG
     assert accept(rows, 1) == sv.SV_ERR_INVALID_ARG
     assert accept(rows, 3, Dq=0) == sv.SV_ERR_INVALID_ARG  # exact mode needs q rows
+
+
+def test_lm_head_rejects_before_launch(lib):
+    P = ctypes.c_void_p(16)
+    # hidden size not a multiple of 8, V not a multiple of 8, NULL or misaligned operands
+    assert lib.sv_lm_head(4, 100, 1000, P, P, P, None) == sv.SV_ERR_UNSUPPORTED
+    assert lib.sv_lm_head(4, 128, 1001, P, P, P, None) == sv.SV_ERR_UNSUPPORTED
+    assert lib.sv_lm_head(4, 128, 1000, None, P, P, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.sv_lm_head(4, 128, 1000, P, ctypes.c_void_p(24), P, None) == sv.SV_ERR_INVALID_ARG
+    # the fused chain call checks the projection and the acceptance arguments, and its
+    # workspace (statistics plus the projection's per-tile partials)
+    need = lib.sv_accept_lmhead_workspace_size(2, 5, 1000, 4)
+    assert need > lib.sv_accept_workspace_size(2, 5, 1000, 4)
+    assert lib.sv_accept_chain_lmhead(1, 2, 4, 1000, 100, P, P, P, P, 1, P, 1.0, 0, 1.0, 0, 0,
+                                      P, P, P, P, P, need, None) == sv.SV_ERR_UNSUPPORTED
+    assert lib.sv_accept_chain_lmhead(1, 2, 4, 1000, 128, P, P, P, P, 1, P, -1.0, 0, 1.0, 0, 0,
+                                      P, P, P, P, P, need, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.sv_accept_chain_lmhead(1, 2, 4, 1000, 128, P, P, P, P, 1, P, 1.0, 0, 1.0, 0, 0,
+                                      P, P, P, P, P, 16, None) == sv.SV_ERR_WORKSPACE
+    par = (ctypes.c_int32 * 3)(-1, 0, 0)
+    assert lib.sv_accept_tree_lmhead(1, 2, 3, 1000, 128, P, P, P, par, 0, P, P, 1, 0, 1.0, 0, 1.0,
+                                     0, 0, P, P, P, P, P, P, need, None) == sv.SV_ERR_INVALID_ARG
