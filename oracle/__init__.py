@@ -71,6 +71,9 @@ def _load():
                                                       Dbl, U64, U64, P, P, P, P, P, P]
             lib.orc_accept_tree_recursive.restype = I
             lib.orc_lm_head.argtypes = [I, I, I, P, I, P, I, P]
+            lib.orc_accept_typical.argtypes = [I, I, I, I, P, I, P, P, Dbl, Dbl, Dbl, P, P, P, P, P,
+                                               P]
+            lib.orc_accept_typical.restype = I
             lib.orc_set_threads.argtypes = [I]
             lib.orc_get_threads.restype = I
             _lib = lib
@@ -335,6 +338,36 @@ def accept_tree_recursive(target_logits, q, q_kind, parent, node_tokens, tempera
         _ptr(out["near_ties"]), _ptr(out["flags"]))
     if rc != 0:
         raise ValueError(f"oracle accept_tree_recursive rejected its arguments (code {rc})")
+    return out
+
+
+def accept_typical(target_logits, parent, node_tokens, temperature=1.0, epsilon=0.3,
+                   delta=0.09):
+    """Typical acceptance (see oracle.c, orc_accept_typical): node c is accepted iff
+    p_parent(x_c) > min(epsilon, delta * exp(-H(p_parent))); the token after the kept path is
+    the target's argmax.  parent [N] or [B, N]; returns a dict of CPU tensors, with the
+    entropy (nats) of every row under "entropy"."""
+    tl = _cpu(target_logits)
+    dt = _dtype_code(tl)
+    B, N, V = tl.shape
+    par, pstride, _, per_seq = _parents(parent, B)
+    toks = _i32(node_tokens)
+    W = N if per_seq else max(_depths(par.tolist())) + 1
+    out = {
+        "path_nodes": torch.full((B, W), -1, dtype=torch.int32),
+        "tokens": torch.full((B, W), -1, dtype=torch.int32),
+        "num_emitted": torch.zeros(B, dtype=torch.int32),
+        "num_accepted": torch.zeros(B, dtype=torch.int32),
+        "near_ties": torch.zeros(B, dtype=torch.int32),
+        "entropy": torch.zeros((B, N), dtype=torch.float64),
+    }
+    rc = _load().orc_accept_typical(
+        dt, B, N, V, _ptr(par), pstride, _ptr(toks), _ptr(tl), float(temperature),
+        float(np.float32(epsilon)), float(np.float32(delta)), _ptr(out["path_nodes"]),
+        _ptr(out["tokens"]), _ptr(out["num_emitted"]), _ptr(out["num_accepted"]),
+        _ptr(out["near_ties"]), _ptr(out["entropy"]))
+    if rc != 0:
+        raise ValueError(f"oracle accept_typical rejected its arguments (code {rc})")
     return out
 
 

@@ -658,6 +658,92 @@ int orc_accept_chain(int mode, int dtype, int B, int gamma, int V, const void *t
   return 0;
 }
 
+/* ------------------------------------------------ acceptance: typical rule */
+
+/* Typical acceptance (the Medusa paper: T. Cai et al., "Medusa: Simple LLM Inference
+ * Acceleration Framework with Multiple Decoding Heads", 2024, section "Typical Acceptance";
+ * the jennyma11 blog, section "Medusa", names it beside lossless verification without a
+ * rule).  Node c (parent a) is accepted iff p_a(x_c) > min(epsilon, delta * exp(-H(p_a))),
+ * p_a the parent's target distribution at temperature T (T > 0, no top-k), H its entropy in
+ * nats; no draft distribution and no uniforms are used.  The kept node a* is the deepest
+ * one whose whole root path is accepted (ties: smallest row); the tokens of its path are
+ * emitted, then the target's most likely token at a* (argmax, lowest id), so that every
+ * step emits at least one token.  Near ties (decision class): |p_a(x_c) - threshold| <
+ * 1e-6 on a decision whose parent lies on an accepted path.  parent_all / parent_stride
+ * as orc_accept_tree; outputs as orc_accept_tree (W = depth + 1, or N per sequence). */
+int orc_accept_typical(int dtype, int B, int N, int V, const int32_t *parent_all,
+                       int parent_stride, const int32_t *node_tokens, const void *target_logits,
+                       double T, double epsilon, double delta, int32_t *out_path_nodes,
+                       int32_t *out_tokens, int32_t *out_num_emitted, int32_t *out_num_accepted,
+                       uint32_t *out_near_ties, double *out_entropy) {
+  if (!(T > 0.0)) return 3;
+  int Dmax = 0;
+  for (int b = 0; b < (parent_stride ? B : 1); ++b) {
+    const int32_t *par = parent_all + (size_t)b * parent_stride;
+    if (orc_check_tree(N, par)) return 1;
+    for (int n = 0; n < N; ++n) {
+      int d = orc_depth(par, n);
+      if (d > Dmax) Dmax = d;
+    }
+  }
+  int W = parent_stride ? N : Dmax + 1;
+#pragma omp parallel for schedule(dynamic)
+  for (int b = 0; b < B; ++b) {
+    const int32_t *parent = parent_all + (size_t)b * parent_stride;
+    double *z = (double *)orc_alloc(sizeof(double) * (size_t)V);
+    double *pa = (double *)orc_alloc(sizeof(double) * (size_t)V);
+    unsigned char *acc = (unsigned char *)calloc((size_t)N, 1);
+    unsigned char *ok = (unsigned char *)calloc((size_t)N, 1);
+    unsigned char *dec_near = (unsigned char *)calloc((size_t)N, 1);
+    int *depth = (int *)orc_alloc(sizeof(int) * (size_t)N);
+    for (int n = 0; n < N; ++n) depth[n] = orc_depth(parent, n);
+    for (int a = 0; a < N; ++a) {
+      orc_load_row(target_logits, dtype, (size_t)b * N + a, V, z);
+      orc_effective_dist(z, V, T, 0, 1.0, pa, NULL);
+      double H = 0.0; /* entropy in nats */
+      for (int j = 0; j < V; ++j)
+        if (pa[j] > 0.0) H -= pa[j] * log(pa[j]);
+      if (out_entropy) out_entropy[(size_t)b * N + a] = H;
+      double thr = delta * exp(-H);
+      if (epsilon < thr) thr = epsilon;
+      for (int c = a + 1; c < N; ++c) {
+        if (parent[c] != a) continue;
+        int x = node_tokens[(size_t)b * N + c];
+        if (x < 0 || x >= V) continue; /* rejected */
+        acc[c] = pa[x] > thr;
+        dec_near[c] = fabs(pa[x] - thr) < ORC_NEAR_TIE;
+      }
+    }
+    ok[0] = 1;
+    int best = 0;
+    uint32_t near = 0;
+    for (int c = 1; c < N; ++c) {
+      ok[c] = ok[parent[c]] && acc[c];
+      if (ok[parent[c]] && dec_near[c]) ++near;
+      if (ok[c] && depth[c] > depth[best]) best = c;
+    }
+    orc_load_row(target_logits, dtype, (size_t)b * N + best, V, z);
+    int tok = orc_argmax(z, V);
+    int D = depth[best];
+    int32_t *pn = out_path_nodes ? out_path_nodes + (size_t)b * W : NULL;
+    int32_t *tk = out_tokens + (size_t)b * W;
+    for (int i = 0; i < W; ++i) {
+      if (pn) pn[i] = -1;
+      tk[i] = -1;
+    }
+    for (int a = best, i = D; a >= 0; a = parent[a], --i) {
+      if (pn) pn[i] = a;
+      if (i >= 1) tk[i - 1] = node_tokens[(size_t)b * N + a];
+    }
+    tk[D] = tok;
+    out_num_emitted[b] = D + 1;
+    out_num_accepted[b] = D;
+    if (out_near_ties) out_near_ties[b] = near;
+    free(z); free(pa); free(acc); free(ok); free(dec_near); free(depth);
+  }
+  return 0;
+}
+
 /* ------------------------------------------------------------- KV commit */
 
 /* Copy the tree K/V rows of the path nodes (root, then accepted nodes in depth order)
