@@ -246,6 +246,27 @@ sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const
                                    uint32_t *out_near_ties, void *workspace,
                                    size_t workspace_bytes, void *stream);
 
+/* Typical acceptance (named beside lossless verification by the jennyma11 blog, section
+ * "Medusa", without a rule; the rule is the Medusa paper's -- T. Cai et al., "Medusa: Simple
+ * LLM Inference Acceleration Framework with Multiple Decoding Heads", 2024, section
+ * "Typical Acceptance"): node c (parent a) is accepted iff
+ *   p_a(x_c) > min(epsilon, delta * exp(-H(p_a))),
+ * p_a the parent's target distribution at the given temperature (> 0; no top-k), H its
+ * entropy in nats.  No draft distribution and no uniforms: it is not distribution
+ * preserving, it trades exactness for longer accepted runs.  The kept node a* is the
+ * deepest one whose whole root path is accepted (ties: smallest row); the emitted tokens are
+ * those of path nodes 1..a*, then the target's most likely token at a* (argmax, lowest id),
+ * so every call emits at least one token.  Trees, node_tokens, target_logits, the outputs
+ * and the near-tie word as sv_accept_tree (decision ties: |p_a(x_c) - threshold| < 1e-6 on
+ * an accepted path).  Workspace: sv_accept_workspace_size(B, N, V, 0). */
+sv_status sv_accept_typical(sv_dtype logit_dt, int B, int N, int V, const int32_t *parent,
+                           int parent_stride, const int32_t *node_tokens,
+                           const void *target_logits, float temperature, float epsilon,
+                           float delta, int32_t *out_path_nodes, int32_t *out_tokens,
+                           int32_t *out_num_emitted, int32_t *out_num_accepted,
+                           uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
 /* Workspace bytes for sv_accept_chain (N = gamma+1, Dq = gamma) / sv_accept_tree. */
 size_t sv_accept_workspace_size(int B, int N, int V, int Dq);
 
@@ -254,7 +275,7 @@ size_t sv_accept_workspace_size(int B, int N, int V, int Dq);
  * embedded runtimes, callers holding no allocator handle).  No counterpart on the
  * pages: it is a deployment convenience.  Arguments, outputs and results are those of
  * sv_accept_tree; the per-row statistics go to a fixed device array inside the library
- * of SV_NOALLOC_ACCEPT_ROWS rows (24 bytes each, 1.5 MiB), held by every GPU that
+ * of SV_NOALLOC_ACCEPT_ROWS rows (32 bytes each, 2 MiB), held by every GPU that
  * loads the library until the process exits.  B*(N+Dq) logit rows (B*N in greedy
  * mode) must not exceed SV_NOALLOC_ACCEPT_ROWS, else SV_ERR_UNSUPPORTED and nothing is
  * launched.  The first call on a device looks the array's address up on that device

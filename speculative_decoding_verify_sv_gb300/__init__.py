@@ -22,6 +22,7 @@ __all__ = [
     "sv_accept_workspace_size", "sv_accept_tree_noalloc", "sv_commit_kv", "sv_accept_tree_commit",
     "sv_accept_chain_commit", "sv_accept_tree_recursive", "sv_ngram_draft", "sv_tree_prepare", "sv_read_device_status",
     "sv_lm_head", "sv_accept_lmhead_workspace_size", "sv_accept_chain_lmhead", "sv_accept_tree_lmhead",
+    "sv_accept_typical",
     "sv_version", "sv_kernel_launches", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "Q_DRAFT_ONEHOT", "SV_MAX_TREE_NODES",
 ]
 
@@ -93,6 +94,7 @@ def load_library():
         lib.sv_accept_chain_commit.argtypes = [I, I, I, I, I, P, P, I, P, F, I, F, U64, U64,
                                                I, I, I, P, P, _KVCacheC, P, P, P, P, P, SZ, P]
         lib.sv_lm_head.argtypes = [I, I, I, P, P, P, P]
+        lib.sv_accept_typical.argtypes = [I, I, I, I, P, I, P, P, F, F, F, P, P, P, P, P, P, SZ, P]
         lib.sv_accept_lmhead_workspace_size.argtypes = [I, I, I, I]
         lib.sv_accept_lmhead_workspace_size.restype = SZ
         lib.sv_accept_chain_lmhead.argtypes = [I, I, I, I, I, P, P, P, P, I, P, F, I, F, U64, U64,
@@ -507,6 +509,30 @@ def sv_read_device_status(stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check(lib.sv_read_device_status(ctypes.byref(v), _stream(stream)))
     return int(v.value)
+
+
+def sv_accept_typical(target_logits, parent, node_tokens, temperature=1.0, epsilon=0.3,
+                      delta=0.09, outs=None, workspace=None, stream=None) -> dict:
+    """Typical acceptance (the Medusa paper's rule): node c is accepted iff
+    p_parent(x_c) > min(epsilon, delta * exp(-H(p_parent))); then the target's argmax at the
+    kept node.  target_logits [B,N,V], node_tokens [B,N] int32, parent a host sequence [N]
+    or a CUDA int32 tensor [B,N].  Returns dict of device tensors."""
+    lib = load_library()
+    _dev(target_logits, "target_logits", (torch.bfloat16, torch.float32))
+    B, N, V = target_logits.shape
+    _dev(node_tokens, "node_tokens", torch.int32, (B, N))
+    par, pstride, W = _tree_arg(parent, B, N)
+    outs = _accept_outputs(B, W, target_logits.device, outs)
+    outs.setdefault("path_nodes", torch.empty((B, W), dtype=torch.int32, device=target_logits.device))
+    workspace, ws_bytes = _workspace(sv_accept_workspace_size(B, N, V, 0), target_logits.device,
+                                     workspace)
+    _check(lib.sv_accept_typical(_dt(target_logits), B, N, V, par, pstride, _ptr(node_tokens),
+                                 _ptr(target_logits), float(temperature), float(epsilon),
+                                 float(delta), _ptr(outs["path_nodes"]), _ptr(outs["tokens"]),
+                                 _ptr(outs["num_emitted"]), _ptr(outs["num_accepted"]),
+                                 _ptr(outs["near_ties"]), _ptr(workspace), ws_bytes,
+                                 _stream(stream)))
+    return outs
 
 
 # ------------------------------------------------------------------- LM head

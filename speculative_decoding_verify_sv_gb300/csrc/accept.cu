@@ -219,7 +219,7 @@ __device__ __forceinline__ float vec_max(const uint4 &r) {
 // Statistics of one logit row (all NT threads of the CTA): row max and its lowest index,
 // the top-k threshold, and the softmax sum over the kept entries.  Thread 0 writes
 // p.stats[row].  Rows 0..B*N-1 are target rows, then the q rows.
-template <typename T, bool GREEDY, bool TOPK, int NT>
+template <typename T, bool GREEDY, bool TOPK, int NT, bool ENT = false>
 __device__ void row_stats(const AcceptParams &p, size_t row) {
   constexpr int VEC = Elem<T>::kVec;
   __shared__ float sh_v[32];
@@ -240,6 +240,7 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
   int imax = INT_MAX;
   float m = -INFINITY;  // running maximum the partial sum is taken against
   KahanF acc;
+  KahanF ent;  // ENT: sum of 2^t t, t = (z - m) c (the entropy's second term)
   // TOPK: the maxima of this thread's 4 units (fp32: units = element lanes 0..3 of each
   // vector; bf16: the low and high halves of words x, z and of words y, w, kept as two
   // packed pairs), and the top 16 bits of the key of each batch's maximum, so that the
@@ -312,6 +313,12 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
       if (vmax > m) {  // vmax: the largest value this thread has seen
         if (m != -INFINITY) {
           const float sc = ex2_approx((m - vmax) * c);
+          if constexpr (ENT) {
+            // sum 2^(t - d) (t - d) = 2^-d (sum 2^t t - d sum 2^t), d = (vmax - m) c
+            const float d = (vmax - m) * c;
+            ent.s = sc * (ent.value() - d * acc.value());
+            ent.c = 0.f;
+          }
           acc.s *= sc;
           acc.c *= sc;
         }
@@ -321,6 +328,7 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
         // partial sums ps[e & 3] in lane pairs: (z - m) * c and the sums as packed f32x2
         // (the same roundings and order as the scalar form)
         float2 ps01 = make_float2(0.f, 0.f), ps23 = make_float2(0.f, 0.f);
+        float es = 0.f;  // ENT: this batch's sum of 2^t t (2^-inf * -inf counts as 0)
         const float2 m2 = make_float2(m, m), c2 = make_float2(c, c);
 #pragma unroll
         for (int u = 0; u < U; ++u)
@@ -330,8 +338,13 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
             const float2 x = make_float2(ex2_approx(t.x), ex2_approx(t.y));
             if (e & 2) ps23 = add2(ps23, x);
             else ps01 = add2(ps01, x);
+            if constexpr (ENT) {
+              if (x.x > 0.f) es = fmaf(x.x, t.x, es);
+              if (x.y > 0.f) es = fmaf(x.y, t.y, es);
+            }
           }
         acc.add((ps01.x + ps01.y) + (ps23.x + ps23.y));
+        if constexpr (ENT) ent.add(es);
       }
     }
   }
@@ -347,10 +360,20 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
   st.idx_k = INT_MAX;
   st.S = 0.f;
   st.flags = 0u;
+  st.H = 0.f;
+  st.pad = 0u;
 
   if constexpr (!GREEDY && !TOPK) {
-    const float part = m == -INFINITY ? 0.f : acc.value() * exp2f((m - zmax) * c);
+    const float sc = m == -INFINITY ? 0.f : exp2f((m - zmax) * c);
+    const float part = m == -INFINITY ? 0.f : acc.value() * sc;
     st.S = block_sum_f<NT>(part, sh_d);
+    if constexpr (ENT) {
+      // to the row maximum: sum 2^(t + d) (t + d) = 2^d (sum 2^t t + d sum 2^t), d = (m - zmax) c
+      const float epart = m == -INFINITY ? 0.f : sc * (ent.value() + (m - zmax) * c * acc.value());
+      const float E = block_sum_f<NT>(epart, sh_d);
+      // p_j = 2^t_j / S: H = -sum p ln p = ln S - ln 2 * E / S
+      st.H = st.S > 0.f ? (float)(log((double)st.S) - 0.6931471805599453 * (double)E / (double)st.S) : 0.f;
+    }
   }
 
   if constexpr (TOPK) {
@@ -633,12 +656,12 @@ __device__ void row_stats(const AcceptParams &p, size_t row) {
   if (tid == 0) p.stats[row] = st;
 }
 
-template <typename T, bool GREEDY, bool TOPK>
+template <typename T, bool GREEDY, bool TOPK, bool ENT = false>
 __global__ void __launch_bounds__(stat_threads<TOPK>(), 4) accept_stats_kernel(const AcceptParams p) {
   // the select kernel may be scheduled now; it waits for this grid before reading the
   // statistics (programmatic dependent launch)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  row_stats<T, GREEDY, TOPK, stat_threads<TOPK>()>(p, (size_t)p.stat_row0 + blockIdx.x);
+  row_stats<T, GREEDY, TOPK, stat_threads<TOPK>(), ENT>(p, (size_t)p.stat_row0 + blockIdx.x);
 }
 
 // ------------------------------------------------------------ kernel 2
@@ -844,6 +867,18 @@ __device__ __noinline__ int decide_double(uint32_t k_node, float zp, RowStat sa,
   return (u_acc < ratio ? 1 : 0) | (fabs(u_acc - ratio) < kNearTie ? 2 : 0);
 }
 
+// A typical-acceptance decision (the Medusa paper's rule): p(x) > min(eps, delta exp(-H)),
+// taken in double from the parent row's statistics.  Bit 0: accepted; bit 1: a near tie
+// (|p(x) - threshold| within 1e-6, widened by the float error of the entropy).
+__device__ __noinline__ int decide_typical(float zp, RowStat sa, float temperature, float eps,
+                                           float delta) {
+  const double px = exp(((double)zp - (double)sa.zmax) / (double)temperature) / (double)sa.S;
+  const double H = (double)sa.H;
+  const double thr = fmin((double)eps, (double)delta * exp(-H));
+  const double win = kNearTie + 1e-6 * thr * (1.0 + H);
+  return (px > thr ? 1 : 0) | (fabs(px - thr) < win ? 2 : 0);
+}
+
 // Decisions, path, optional commit and final sample of sequence b by the CTA of rank
 // `rank` in a thread-block cluster of C CTAs that split the vocabulary pass and exchange
 // their slice totals through distributed shared memory (C = 1: one CTA, no exchange).
@@ -926,6 +961,8 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
   const bool onehot = p.q_kind == SV_Q_DRAFT_ONEHOT;  // q(x) = 1 at the draft token
   float zp = 0.f, zq = 0.f, qprob = 0.f;
   uint32_t k_node = 0u, k_unused = 0u;
+  if (GREEDY && p.typical && has_node && tok_ok)  // typical acceptance: the parent's p(x)
+    zp = Elem<T>::load(row_ptr<T>(p.target, (size_t)b * N + a_par, V) + xt);
   if (!GREEDY && has_node && tok_ok) {
     zp = Elem<T>::load(row_ptr<T>(p.target, (size_t)b * N + a_par, V) + xt);
     if (logits)
@@ -966,7 +1003,13 @@ __device__ void select_seq(const AcceptParams &p, int b, unsigned rank, unsigned
     if (!tok_ok) {
       if (rank == 0 && !absent) set_status(p.status, SV_DEV_BAD_TOKEN);
     } else if (GREEDY) {
-      acc = xt == __ldcg(&tstat[a].argmax);
+      if (p.typical) {
+        const int r = decide_typical(zp, load_stat(tstat + a), p.temperature, p.typ_eps, p.typ_delta);
+        acc = r & 1;
+        dn = r >> 1;
+      } else {
+        acc = xt == __ldcg(&tstat[a].argmax);
+      }
     } else {
       // u = (k + 0.5) 2^-24 in float (within 2^-25; exact for the k near kNearTie)
       const float u_f = ((float)k_node + 0.5f) * (1.f / 16777216.f);
@@ -1652,6 +1695,14 @@ template <typename T>
 cudaError_t launch_typed(const AcceptParams &p, int num_sms, cudaStream_t s) {
   const bool greedy = p.mode == SV_GREEDY;
   const bool topk = !greedy && p.top_k > 0 && p.top_k < p.V;
+  if (p.typical) {
+    // the target rows' statistics with their entropy, then the greedy-form select kernel
+    // taking the typical decisions (the emitted token after the path is the argmax)
+    accept_stats_kernel<T, false, false, true><<<p.B * p.N, stat_threads<false>(), 0, s>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_select<T, true, false>(p, num_sms, s);
+  }
   cudaError_t e = launch_stats_typed<T>(p, s);
   if (e != cudaSuccess) return e;
   if (greedy) return launch_select<T, true, false>(p, num_sms, s);

@@ -256,6 +256,8 @@ __global__ void lm_head_merge_kernel(const float4 *part, int R, int ntiles, floa
     st.idx_k = INT_MAX;
     st.S = (float)S;
     st.flags = 0u;
+    st.H = 0.f;
+    st.pad = 0u;
     stats[row] = st;
   }
 }

@@ -21,6 +21,8 @@ __device__ __forceinline__ RowStat load_stat(const RowStat *s) {
   r.idx_k = __ldcg(&s->idx_k);
   r.S = __ldcg(&s->S);
   r.flags = __ldcg(&s->flags);
+  r.H = __ldcg(&s->H);
+  r.pad = 0u;
   return r;
 }
 

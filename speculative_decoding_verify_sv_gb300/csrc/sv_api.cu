@@ -531,6 +531,45 @@ sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const
   return SV_OK;
 }
 
+sv_status sv_accept_typical(sv_dtype logit_dt, int B, int N, int V, const int32_t *parent,
+                           int parent_stride, const int32_t *node_tokens,
+                           const void *target_logits, float temperature, float epsilon,
+                           float delta, int32_t *out_path_nodes, int32_t *out_tokens,
+                           int32_t *out_num_emitted, int32_t *out_num_accepted,
+                           uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+  if (!(temperature > 0.f) || !std::isfinite(temperature))
+    return fail(SV_ERR_INVALID_ARG, "typical acceptance needs a finite temperature > 0");
+  if (!(epsilon >= 0.f) || !std::isfinite(epsilon) || !(delta >= 0.f) || !std::isfinite(delta))
+    return fail(SV_ERR_INVALID_ARG, "epsilon and delta must be finite and >= 0");
+  sv::AcceptParams p;
+  bool greedy = false;
+  // the greedy form of the parameters (no q rows, no uniforms); the decisions are typical
+  sv_status st = tree_params(SV_GREEDY, logit_dt, B, N, V, parent, parent_stride, node_tokens,
+                             target_logits, nullptr, SV_Q_LOGITS, 0, temperature, 0, 1.f, 0, 0,
+                             out_path_nodes, out_tokens, out_num_emitted, out_num_accepted,
+                             out_near_ties, p, &greedy);
+  if (st != SV_OK) return st;
+  const size_t need = sv::accept_ws_bytes(p.B, p.N, 0);
+  if (!workspace || workspace_bytes < need)
+    return fail(SV_ERR_WORKSPACE, "acceptance workspace %zu bytes, need %zu", workspace_bytes, need);
+  if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  p.status = status_word();
+  if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
+  p.mode = SV_GREEDY;
+  p.typical = 1;
+  p.typ_eps = epsilon;
+  p.typ_delta = delta;
+  p.temperature = temperature;
+  p.c_log2 = (float)(1.4426950408889634 / (double)temperature);
+  p.stats = static_cast<sv::RowStat *>(workspace);
+  if (p.B == 0) return SV_OK;
+  cudaError_t e = sv::launch_accept(logit_dt, p, num_sms(), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "typical acceptance launch");
+  sv::count_launches(2);
+  return SV_OK;
+}
+
 sv_status sv_accept_chain_commit(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
                                  const void *target_logits, const void *q, sv_q_kind q_kind,
                                  const int32_t *draft_tokens, float temperature, int top_k, float top_p,
@@ -744,7 +783,7 @@ sv_status sv_accept_tree_lmhead(sv_mode mode, int B, int N, int V, int Dm, const
 // threshold, softmax sum) that the first acceptance kernel writes and the second
 // reads.  A fixed array in device memory instead of a caller workspace, so that
 // callers which cannot allocate device memory can still run acceptance.  Every GPU
-// that loads this library holds it (SV_NOALLOC_ACCEPT_ROWS rows of 24 bytes) until
+// that loads this library holds it (SV_NOALLOC_ACCEPT_ROWS rows of 32 bytes) until
 // the process exits.
 static __device__ __align__(256) sv::RowStat g_sv_noalloc_rows[SV_NOALLOC_ACCEPT_ROWS];
 

@@ -100,6 +100,8 @@ struct RowStat {
   int32_t idx_k;
   float S;        // sum over kept entries of exp((z - zmax) / T)
   uint32_t flags; // bit 0: the top-p cut lies within 1e-6 of top_p (a near tie)
+  float H;        // entropy of the row's distribution in nats (typical acceptance only)
+  uint32_t pad;
 };
 
 // ------------------------------------------------------------------- commit
@@ -132,6 +134,10 @@ struct AcceptParams {
   float top_p;               // 1 = off; < 1 only with top-k (the nucleus of its distribution)
   int ring_stages;           // stages of the select kernel's ring (set at its launch)
   int stat_row0;             // first row of the statistics kernel's grid (q rows only: B*N)
+  // typical acceptance (mode SV_GREEDY in the select kernel, entropy in the statistics):
+  // node accepted iff p_parent(x) > min(typ_eps, typ_delta * exp(-H(p_parent)))
+  int typical;
+  float typ_eps, typ_delta;
   uint64_t seed, round;
   RowStat *stats;            // [B*N + B*Dq]
   int32_t *out_path_nodes;   // [B,Dmax+1] or NULL
