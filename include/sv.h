@@ -416,6 +416,16 @@ const char *sv_version(void);
  * all threads); the difference around a region counts the region's launches. */
 uint64_t sv_kernel_launches(void);
 
+/* The time after which a wait for progress inside the tensor-core attention kernel gives
+ * up (a copy, an MMA, or another CTA's piece of a split unit that does not arrive): the
+ * kernel then lets its copies and MMAs in flight land, frees its tensor memory, sets
+ * SV_DEV_TIMEOUT and returns; the workspace stays usable for the next call.  Default 2 s;
+ * 0 restores it.  Process-wide, read at each sv_tree_attention call.  A limit shorter
+ * than the kernel's normal waits makes the calls fail with SV_DEV_TIMEOUT: it exists to
+ * exercise that path. */
+void sv_set_wait_limit_ns(uint64_t ns);
+uint64_t sv_get_wait_limit_ns(void);
+
 #ifdef __cplusplus
 }
 #endif

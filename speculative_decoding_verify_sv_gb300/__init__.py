@@ -22,7 +22,7 @@ __all__ = [
     "sv_accept_workspace_size", "sv_accept_tree_noalloc", "sv_commit_kv", "sv_accept_tree_commit",
     "sv_accept_chain_commit", "sv_accept_tree_recursive", "sv_ngram_draft", "sv_tree_prepare", "sv_read_device_status",
     "sv_lm_head", "sv_accept_lmhead_workspace_size", "sv_accept_chain_lmhead", "sv_accept_tree_lmhead",
-    "sv_accept_typical",
+    "sv_accept_typical", "sv_set_wait_limit_ns", "sv_get_wait_limit_ns",
     "sv_version", "sv_kernel_launches", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "Q_DRAFT_ONEHOT", "SV_MAX_TREE_NODES",
 ]
 
@@ -94,6 +94,9 @@ def load_library():
         lib.sv_accept_chain_commit.argtypes = [I, I, I, I, I, P, P, I, P, F, I, F, U64, U64,
                                                I, I, I, P, P, _KVCacheC, P, P, P, P, P, SZ, P]
         lib.sv_lm_head.argtypes = [I, I, I, P, P, P, P]
+        lib.sv_set_wait_limit_ns.argtypes = [U64]
+        lib.sv_set_wait_limit_ns.restype = None
+        lib.sv_get_wait_limit_ns.restype = U64
         lib.sv_accept_typical.argtypes = [I, I, I, I, P, I, P, P, F, F, F, P, P, P, P, P, P, SZ, P]
         lib.sv_accept_lmhead_workspace_size.argtypes = [I, I, I, I]
         lib.sv_accept_lmhead_workspace_size.restype = SZ
@@ -533,6 +536,15 @@ def sv_accept_typical(target_logits, parent, node_tokens, temperature=1.0, epsil
                                  _ptr(outs["near_ties"]), _ptr(workspace), ws_bytes,
                                  _stream(stream)))
     return outs
+
+
+def sv_set_wait_limit_ns(ns: int) -> None:
+    """Limit of the tensor-core attention kernel's waits for progress (0: the default 2 s)."""
+    load_library().sv_set_wait_limit_ns(int(ns))
+
+
+def sv_get_wait_limit_ns() -> int:
+    return int(load_library().sv_get_wait_limit_ns())
 
 
 # ------------------------------------------------------------------- LM head

@@ -198,16 +198,16 @@ __device__ __noinline__ bool idle_piece(int N, int t0, int n, bool publish, int 
                                         bool grouped,
                                         uint64_t *s_full, uint64_t *s_free, uint64_t *v_full,
                                         uint64_t *p_full, uint64_t *o_free, uint64_t *pub, uint8_t *sV,
-                                        volatile int *abort_flag) {
+                                        volatile int *abort_flag, unsigned long long wlim) {
   const int lane = threadIdx.x & 31;
   for (int k = 0; k < n; ++k) {
     const int gk = g + k, j = gk & 1, s = gk % STAGES, t = t0 + k, pb = gk % PBUF;
-    if (!mbar_wait(&s_full[j], (gk >> 1) & 1, abort_flag)) return false;
+    if (!mbar_wait(&s_full[j], (gk >> 1) & 1, abort_flag, wlim)) return false;
     __syncwarp();
     if (lane == 0) mbar_arrive(&s_free[j]);
     const int nvalid = t == 0 ? N : min(BN, L - (t - 1) * BN);
     if (t != 0 && nvalid < BN) {  // this warp's share of zeroing the V tail (see the row loop)
-      if (!mbar_wait(&v_full[s], (gk / STAGES) & 1, abort_flag)) return false;
+      if (!mbar_wait(&v_full[s], (gk / STAGES) & 1, abort_flag, wlim)) return false;
       uint8_t *vt = sV + s * Lay::KV_BYTES;
       constexpr int per_row = Lay::KB * 8;
       for (int i = threadIdx.x; i < (BN - nvalid) * per_row; i += 32 * Lay::NSW) {
@@ -215,7 +215,7 @@ __device__ __noinline__ bool idle_piece(int N, int t0, int n, bool publish, int 
         *reinterpret_cast<uint4 *>(vt + kv_unit_offset<Lay>(grouped, r, rem)) = make_uint4(0, 0, 0, 0);
       }
     }
-    if (gk >= PBUF && !mbar_wait(&p_full[pb], ((gk / PBUF) - 1) & 1, abort_flag)) return false;
+    if (gk >= PBUF && !mbar_wait(&p_full[pb], ((gk / PBUF) - 1) & 1, abort_flag, wlim)) return false;
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&p_full[pb]);
@@ -225,7 +225,7 @@ __device__ __noinline__ bool idle_piece(int N, int t0, int n, bool publish, int 
     __syncwarp();
     if (lane == 0) mbar_arrive(pub);
   }
-  if (qi > 0 && !mbar_wait(o_free, (qi - 1) & 1, abort_flag)) return false;
+  if (qi > 0 && !mbar_wait(o_free, (qi - 1) & 1, abort_flag, wlim)) return false;
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(o_free);
@@ -263,6 +263,9 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
     finish();
     return;
   }
+  // the limit of every wait for progress (copies, MMAs, other CTAs' pieces); the waits
+  // for work already in flight to land after an abort keep the fixed kWaitLimitNs
+  const unsigned long long wlim = p.wait_ns;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::OFF_BAR);
   uint64_t *k_full = bars;
   uint64_t *k_empty = bars + STAGES;
@@ -437,7 +440,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
     // lane 0 waits; the outcome is shared with the warp
     auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
       int r = 1;
-      if (lane == 0) r = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
+      if (lane == 0) r = mbar_wait(bar, parity, abort_flag, wlim) ? 1 : 0;
       return __shfl_sync(0xFFFFFFFFu, r, 0) != 0;
     };
     auto load = [&](const Src &src, int gi, bool is_v) -> bool {
@@ -583,14 +586,14 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           if (lane == 0) {
             const unsigned long long t0 = global_ns();
             while (ld_acquire_u64(p.flags + sl0) != epoch) {
-              if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
+              if (*abort_flag || global_ns() - t0 > wlim) {
                 *abort_flag = 1;
                 r = 0;
                 break;
               }
             }
-            if (r && !mbar_wait(&k_empty[(g - 1) % STAGES], ((g - 1) / STAGES) & 1, abort_flag)) r = 0;
-            if (r && !mbar_wait(&q_empty[(nq - 1) % QBUF], ((nq - 1) / QBUF) & 1, abort_flag)) r = 0;
+            if (r && !mbar_wait(&k_empty[(g - 1) % STAGES], ((g - 1) / STAGES) & 1, abort_flag, wlim)) r = 0;
+            if (r && !mbar_wait(&q_empty[(nq - 1) % QBUF], ((nq - 1) / QBUF) & 1, abort_flag, wlim)) r = 0;
           }
           if (__shfl_sync(0xFFFFFFFFu, r, 0)) {
             (void)ld_acquire_u64(p.flags + sl0);  // each lane's own acquire of the published rows
@@ -623,6 +626,9 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       settle(v_full, gv, STAGES);
       settle(q_full, nq, QBUF);
     }
+    // this lane's staging copies (a split unit's partial rows) land before the CTA retires,
+    // also when the consumer gave up waiting for them
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == NSW + 1) {
     // -------------------------------------------------------------- MMA issue
     // One thread polls both kinds of work and issues whichever is ready, P V first:
@@ -731,7 +737,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           if (*abort_flag) break;
           const unsigned long long now = global_ns();
           if (idle_n == 64) idle_t0 = now;
-          else if (now - idle_t0 > kWaitLimitNs) {
+          else if (now - idle_t0 > wlim) {
             *abort_flag = 1;
             break;
           }
@@ -799,7 +805,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       if (warp_idle) {  // every row of this warp is padding: barriers only
         if (!idle_piece<Lay, BN, STAGES, PBUF>(p.N, pc.t0, n, pc.t0 > 0, g, qi, L, p.pg_grouped != 0,
                                               s_full, s_free, v_full,
-                                              p_full, o_free, pub, sV, abort_flag)) {
+                                              p_full, o_free, pub, sV, abort_flag, wlim)) {
           ok = false;
           break;
         }
@@ -812,7 +818,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         const int gk = g + k, j = gk & 1, s = gk % STAGES, t = pc.t0 + k, pb = gk % PBUF;
         const bool tree = t == 0;
         const int nvalid = tree ? p.N : min(BN, L - (t - 1) * BN);
-        if (!mbar_wait(&s_full[j], (gk >> 1) & 1, abort_flag)) {
+        if (!mbar_wait(&s_full[j], (gk >> 1) & 1, abort_flag, wlim)) {
           ok = false;
           break;
         }
@@ -821,7 +827,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         // Done by all softmax threads once V has landed, before P is published.
         auto zero_v_tail = [&]() -> bool {
           if (tree || nvalid >= BN) return true;
-          if (!mbar_wait(&v_full[s], (gk / STAGES) & 1, abort_flag)) return false;
+          if (!mbar_wait(&v_full[s], (gk / STAGES) & 1, abort_flag, wlim)) return false;
           uint8_t *vt = sV + s * Lay::KV_BYTES;
           constexpr int per_row = Lay::KB * 8;
           const bool grouped = p.pg_grouped != 0;  // (a prefix tile)
@@ -900,7 +906,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           xb[wq * 32 + lane] = pmax;
           __syncwarp();
           if (lane == 0) mbar_arrive(&xch_full[gk & 1]);
-          if (!mbar_wait(&xch_full[gk & 1], (gk >> 1) & 1, abort_flag)) {
+          if (!mbar_wait(&xch_full[gk & 1], (gk >> 1) & 1, abort_flag, wlim)) {
             ok = false;
             break;
           }
@@ -924,7 +930,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         // this piece must have finished first (P V runs in order, so waiting for the
         // previous tile's buffer release is enough)
         if (owner && __any_sync(0xFFFFFFFFu, rescale)) {
-          if (!mbar_wait(&p_free[(gk - 1) % PBUF], ((gk - 1) / PBUF) & 1, abort_flag)) {
+          if (!mbar_wait(&p_free[(gk - 1) % PBUF], ((gk - 1) / PBUF) & 1, abort_flag, wlim)) {
             ok = false;
             break;
           }
@@ -942,7 +948,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           tmem_wait_st();
         }
         // P buffer gk&1 is free once the P V of tile gk-2 has finished
-        if (gk >= PBUF && !mbar_wait(&p_free[pb], ((gk / PBUF) - 1) & 1, abort_flag)) {
+        if (gk >= PBUF && !mbar_wait(&p_free[pb], ((gk / PBUF) - 1) & 1, abort_flag, wlim)) {
           ok = false;
           break;
         }
@@ -1010,7 +1016,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         xl[wq * 32 + lane] = l;
         __syncwarp();
         if (lane == 0) mbar_arrive(xl_full);
-        if (!mbar_wait(xl_full, qi & 1, abort_flag)) break;
+        if (!mbar_wait(xl_full, qi & 1, abort_flag, wlim)) break;
         if (owner) {
           l = 0.f;
 #pragma unroll
@@ -1025,7 +1031,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       const long long U_end = pc.fs - pc.t0 + pc.T;
       constexpr int ROWS = MT * kRows;
       if (owner && !warp_idle) {
-        if (!mbar_wait(&p_free[gl % PBUF], (gl / PBUF) & 1, abort_flag)) break;
+        if (!mbar_wait(&p_free[gl % PBUF], (gl / PBUF) & 1, abort_flag, wlim)) break;
         tc_fence_after();
         const int hq = pc.kvh * p.G + (valid_row ? R % p.G : 0);
         bf16 *dst = static_cast<bf16 *>(p.out) + (((size_t)pc.b * p.N + node) * p.Hq + hq) * D;
@@ -1054,13 +1060,13 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
             float2 ml;
             if (MT == 1 && j == 0) {
               // staged by the producer warp (after it saw the flag)
-              if (!mbar_wait(stage_full, 0, abort_flag)) return false;
+              if (!mbar_wait(stage_full, 0, abort_flag, wlim)) return false;
               ml = reinterpret_cast<const float2 *>(sQ)[R_local];
             } else {
               const unsigned long long *flag = p.flags + sl;
               const unsigned long long t0 = global_ns();
               while (ld_acquire_u64(flag) != epoch) {
-                if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
+                if (*abort_flag || global_ns() - t0 > wlim) {
                   *abort_flag = 1;
                   return false;
                 }
@@ -1182,7 +1188,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         __threadfence();
         __syncwarp();
         if (lane == 0) mbar_arrive(pub);
-        if (threadIdx.x == 0 && mbar_wait(pub, 0, abort_flag)) {
+        if (threadIdx.x == 0 && mbar_wait(pub, 0, abort_flag, wlim)) {
           __threadfence();
           st_release_u64(p.flags + pc.unit + blockIdx.x, epoch);
         }
@@ -1369,6 +1375,7 @@ cudaError_t launch_attention_tc(const AttnParams &a, const TcPlan &pl, void *ws,
   p.cap = a.cap;
   p.scale_log2 = a.scale_log2;
   p.tree = a.tree;
+  p.wait_ns = a.wait_ns;
   if (a.D == 128) {
     // (two Q buffers paid for with one P buffer measured slower: the softmax then
     // waits for every P V before writing the next P)

@@ -41,6 +41,10 @@ sv_status cuda_fail(cudaError_t e, const char *what) {
 
 constexpr int kMaxDevices = 64;
 
+// The tensor-core attention kernel's limit on a wait for progress (sv_set_wait_limit_ns).
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+
 // Device address of the status word on the current device (looked up once per device;
 // threads that race on the first lookup store the same address, atomically).
 unsigned int *status_word() {
@@ -151,6 +155,12 @@ const char *sv_version(void) { return SV_VERSION_STRING; }
 
 uint64_t sv_kernel_launches(void) { return sv::g_launches.load(std::memory_order_relaxed); }
 
+void sv_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : ns, std::memory_order_relaxed);
+}
+
+uint64_t sv_get_wait_limit_ns(void) { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 sv_status sv_tree_prepare(int N, const int32_t *parent, uint64_t *anc, int32_t *depth) {
   sv::Tree t;
   sv_status st = make_tree(N, parent, &t);
@@ -259,6 +269,7 @@ sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, c
   p.scale = scale;
   p.scale_log2 = scale * sv::kLog2e;
   p.tree = tree;
+  p.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   cudaError_t e;
   if (use_tc) {
     e = sv::launch_attention_tc(p, tplan, workspace, static_cast<cudaStream_t>(stream));

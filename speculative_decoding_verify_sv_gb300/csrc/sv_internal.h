@@ -44,6 +44,7 @@ struct AttnParams {
   float scale_log2;      // softmax scale * log2(e)
   float scale;
   Tree tree;
+  unsigned long long wait_ns;  // limit of the tensor-core kernel's waits for progress
 };
 
 struct AttnPlan {
@@ -76,6 +77,7 @@ struct TcParams {
   int Lmax, block_size, max_blocks, num_blocks, cap, paged, page_rows;
   float scale_log2;
   Tree tree;
+  unsigned long long wait_ns;  // a wait for progress gives up after this long
 };
 
 struct TcPlan {

@@ -61,13 +61,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 
 // Slow path of mbar_wait, kept out of line so that the many wait sites do not fill the
 // instruction cache with copies of the timeout logic.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                   unsigned long long limit_ns) {
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > limit_ns) {
         *abort = 1;
         return false;
       }
@@ -77,9 +78,10 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parit
 
 // Wait for the phase of the given parity to complete.  Returns false if *abort was
 // raised by another thread or the wait ran past the limit (then *abort is raised).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort);
+  return mbar_wait_slow(bar, parity, abort, limit_ns);
 }
 
 // --------------------------------------------------------------------- TMA

@@ -225,3 +225,12 @@ def test_lm_head_rejects_before_launch(lib):
     par = (ctypes.c_int32 * 3)(-1, 0, 0)
     assert lib.sv_accept_tree_lmhead(1, 2, 3, 1000, 128, P, P, P, par, 0, P, P, 1, 0, 1.0, 0, 1.0,
                                      0, 0, P, P, P, P, P, P, need, None) == sv.SV_ERR_INVALID_ARG
+
+
+def test_wait_limit_is_settable_and_restored(lib):
+    default = sv.sv_get_wait_limit_ns()
+    assert default == 2_000_000_000
+    sv.sv_set_wait_limit_ns(1234)
+    assert sv.sv_get_wait_limit_ns() == 1234
+    sv.sv_set_wait_limit_ns(0)  # 0 restores the default
+    assert sv.sv_get_wait_limit_ns() == default
