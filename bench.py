@@ -394,6 +394,75 @@ def per_workload_line(args, dist, cfg_id, K, peak):
     return out
 
 
+def measured_bf16_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (burst)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def lm_head_line(args, dist, K):
+    """The LM-head projection fused with the acceptance (draft-chain shapes: B = 64 chains
+    of 5 drafts, hidden size 4096, V = 128256): the projection alone, projection then
+    acceptance, and the fused call.  Inputs: hidden ~N(0,1), W ~N(0, 3/sqrt(4096)) (logits
+    about N(0,3)), draft rows the projection of perturbed hidden states, random drafts."""
+    import speculative_decoding_verify_sv_gb300 as sv
+    dev = torch.device("cuda", dist.local_rank)
+    B, gamma, Dm, V = 64, 5, 4096, 128256
+    R = B * (gamma + 1)
+    g = torch.Generator(device=dev).manual_seed(4321)
+    h = torch.randn((R, Dm), generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn((V, Dm), generator=g, device=dev) * (3.0 / math.sqrt(Dm))).to(torch.bfloat16)
+    hq = (h.float().view(B, gamma + 1, Dm)[:, :gamma]
+          + 0.3 * torch.randn((B, gamma, Dm), generator=g, device=dev)).to(torch.bfloat16)
+    dl = sv.sv_lm_head(hq, w)
+    toks = torch.randint(0, V, (B, gamma), generator=g, device=dev, dtype=torch.int32)
+    z = torch.empty((R, V), dtype=torch.bfloat16, device=dev)
+    hv = h.view(B, gamma + 1, Dm)
+    ws = torch.zeros(sv.sv_accept_lmhead_workspace_size(B, gamma + 1, V, gamma), dtype=torch.uint8,
+                     device=dev)
+    ws2 = torch.zeros(sv.sv_accept_workspace_size(B, gamma + 1, V, gamma), dtype=torch.uint8, device=dev)
+    outs = sv.sv_accept_chain_lmhead(sv.EXACT, hv, w, dl, sv.Q_LOGITS, toks, workspace=ws)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(flush.numel() // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        for a, b in evs:
+            flush.zero_()
+            torch.sum(flush_read)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    proj = timed(lambda: sv.sv_lm_head(h, w, out=z))
+    unfused = timed(lambda: (sv.sv_lm_head(h, w, out=z),
+                             sv.sv_accept_chain(sv.EXACT, z.view(B, gamma + 1, V), dl, sv.Q_LOGITS,
+                                                toks, outs=outs, workspace=ws2)))
+    fused = timed(lambda: sv.sv_accept_chain_lmhead(sv.EXACT, hv, w, dl, sv.Q_LOGITS, toks,
+                                                    outs=outs, logits=outs["target_logits"],
+                                                    workspace=ws))
+    flops = 2.0 * R * V * Dm
+    peak, kind = measured_bf16_tflops()
+    tf = flops / (proj / 1e6) / 1e12
+    return {
+        "workload": "LM head + acceptance, draft-chain shapes (B=64, gamma=5, hidden 4096, V=128256)",
+        "steps": K, "projection_us": proj, "projection_then_accept_us": unfused,
+        "fused_us": fused, "candidates_per_s_fused": B * gamma / (fused / 1e6),
+        "roofline": {"kernel": "lm_head_kernel (tcgen05 GEMM, statistics epilogue)",
+                     "bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tf / peak, "peak_source": kind, "flops_per_launch": flops},
+    }
+
+
 def run_ours(args, dist: Dist):
     import speculative_decoding_verify_sv_gb300 as sv  # noqa: F401 (fails loudly if missing)
 
@@ -477,6 +546,7 @@ def run_ours(args, dist: Dist):
         K_pw = max(3, min(K, args.per_workload_steps))
         result["per_workload"] = [per_workload_line(args, dist, i, K_pw, peak)
                                   for i in sorted(ALL_CONFIGS) if i != args.config]
+        result["lm_head"] = lm_head_line(args, dist, K_pw)
     return result
 
 

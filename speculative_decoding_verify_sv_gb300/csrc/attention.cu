@@ -304,77 +304,184 @@ __global__ void __launch_bounds__(D) attn_combine_kernel(const AttnParams p) {
   dst[d] = __float2bfloat16(den > 0.f ? acc / den : 0.f);
 }
 
-// fp32 path: one warp per (node, query head); lanes hold D/32 dimensions; keys are
-// consumed one at a time with an online softmax in fp32 (FFMA, no tensor cores).
+// fp32 path (FFMA, no tensor cores): one warp per query row (node, query head), the
+// kThreads / 32 rows of a CTA sharing one kv head.  The keys go in chunks of 32 -- the
+// prefix, then the tree nodes -- copied by the whole CTA with cp.async into a ring of
+// f32_stages() shared-memory stages, so that that many chunks are in flight at once (a short
+// prefix arrives in one round trip).  Lane j scores key j of the chunk (rows of K padded to
+// D + 4 floats: conflict-free 16-byte reads); online softmax in fp32 per row: chunk maximum
+// and sum by warp reductions, then P V with lane i holding dimensions i, i + 32, ... and
+// each key's weight broadcast by a shuffle.
+constexpr int kF32Keys = 32;  // keys per chunk: one per lane
+// stages of the ring: 8 (132 KB) at D = 64, 6 (198 KB) at D = 128
+template <int D>
+__host__ __device__ constexpr int f32_stages() { return D == 64 ? 8 : 6; }
+
+template <int D>
+__host__ __device__ constexpr size_t f32_stage_floats() { return (size_t)kF32Keys * (D + 4) + (size_t)kF32Keys * D; }
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const AttnParams p) {
-  constexpr int PL = D / 32;
+  constexpr int KC = kF32Keys, ST = f32_stages<D>();
+  constexpr int KS = D + 4;                 // K row stride in shared memory (floats)
+  constexpr int PL = D / 32;                // dimensions per lane in P V
+  constexpr int NW = kThreads / 32;         // rows per CTA
+  constexpr int F4 = KC * D / 4;            // float4 per chunk of K (and of V)
+  constexpr int PER = F4 / kThreads;        // float4 of K (and of V) per thread per chunk
+  static_assert(F4 % kThreads == 0, "whole float4 per thread");
+  extern __shared__ __align__(16) float f32_ring[];  // ST x { K [KC][KS], V [KC][D] }
+  __shared__ __align__(16) float sQ[NW][D];
+  __shared__ uint8_t sValid[ST][KC];        // key j of a stage exists (block id checked)
   __shared__ int sPar[kMaxNodes];
   __shared__ uint64_t sAnc[kMaxNodes];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y;
+  const int kvh = blockIdx.y, b = blockIdx.z;
   // sequence b's tree (shared, or its own row): ancestor masks of its nodes
   if (tid < kMaxNodes) sPar[tid] = tid < p.tree.N ? tree_parent(p.tree, b, tid) : -1;
   __syncthreads();
   if (tid < kMaxNodes) {
     uint64_t m = 0;
     int d;
-    if (tid < p.tree.N && !tree_walk(sPar, tid, &m, &d) && blockIdx.x == 0)
+    if (tid < p.tree.N && !tree_walk(sPar, tid, &m, &d) && blockIdx.x == 0 && kvh == 0)
       set_status(p.status, SV_DEV_BAD_TREE);
     sAnc[tid] = m;
   }
-  __syncthreads();
-  const int w = blockIdx.x * (kThreads / 32) + warp;
-  if (w >= p.N * p.Hq) return;
-  const int n = w / p.Hq, hq = w % p.Hq, kvh = hq / p.G;
   const float *gq = static_cast<const float *>(p.q);
   const float *gkt = static_cast<const float *>(p.k_tree);
   const float *gvt = static_cast<const float *>(p.v_tree);
   const float *gkc = static_cast<const float *>(p.cache_k);
   const float *gvc = static_cast<const float *>(p.cache_v);
   const int L = clamp_prefix(p, b);
+  // this warp's row: query rows of the kv head are (node, group head), node-major
+  const int R = blockIdx.x * NW + warp;
+  const bool live = R < p.M;
+  const int n = live ? R / p.G : 0, hq = kvh * p.G + (live ? R % p.G : 0);
 
-  float qv[PL], o[PL];
+  // chunk c: prefix positions [32c, 32c + 32) for c < nP, then tree nodes from 32 (c - nP)
+  const int nP = (L + KC - 1) / KC, nT = (p.N + KC - 1) / KC, nC = nP + nT;
+  auto stage_k = [&](int st) { return f32_ring + (size_t)st * f32_stage_floats<D>(); };
+  auto stage_v = [&](int st) { return f32_ring + (size_t)st * f32_stage_floats<D>() + KC * KS; };
+  auto issue = [&](int c, int st) {
+    float *sk = stage_k(st), *sv = stage_v(st);
 #pragma unroll
-  for (int i = 0; i < PL; ++i) {
-    qv[i] = gq[(((size_t)b * p.N + n) * p.Hq + hq) * D + lane + 32 * i];
-    o[i] = 0.f;
-  }
-  float m = -INFINITY, l = 0.f;
-  auto consume = [&](const float *kr, const float *vr) {
-    float part = 0.f;
-#pragma unroll
-    for (int i = 0; i < PL; ++i) part = fmaf(qv[i], kr[lane + 32 * i], part);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
-    const float s = part * p.scale;
-    const float m_new = fmaxf(m, s);
-    const float alpha = expf(m - m_new);
-    const float pe = expf(s - m_new);
-    l = l * alpha + pe;
-#pragma unroll
-    for (int i = 0; i < PL; ++i) o[i] = fmaf(o[i], alpha, pe * vr[lane + 32 * i]);
-    m = m_new;
-  };
-  for (int pos = 0; pos < L; ++pos) {
-    long long row = cache_row(p, b, pos);
-    if (row < 0) {
-      set_status(p.status, SV_DEV_BAD_BLOCK);
-      continue;
+    for (int k = 0; k < PER; ++k) {
+      const int f = tid + k * kThreads, key = f / (D / 4), d4 = f % (D / 4);
+      const float *srck = gkc, *srcv = gvc;  // any valid address when nothing is read
+      bool ok = false;
+      if (c < nP) {
+        const int pos = c * KC + key;
+        if (pos < L) {
+          const long long row = cache_row(p, b, pos);
+          if (row >= 0) {
+            const size_t off = ((size_t)row * p.Hkv + kvh) * D + 4 * d4;
+            srck = gkc + off;
+            srcv = gvc + off;
+            ok = true;
+          } else if (d4 == 0) {
+            set_status(p.status, SV_DEV_BAD_BLOCK);
+          }
+        }
+      } else {
+        const int j = (c - nP) * KC + key;
+        if (j < p.N) {
+          const size_t off = (((size_t)b * p.N + j) * p.Hkv + kvh) * D + 4 * d4;
+          srck = gkt + off;
+          srcv = gvt + off;
+          ok = true;
+        }
+      }
+      cp_async_16(sk + key * KS + 4 * d4, srck, ok);
+      cp_async_16(sv + key * D + 4 * d4, srcv, ok);
+      if (d4 == 0) sValid[st][key] = ok ? 1 : 0;
     }
-    const size_t off = ((size_t)row * p.Hkv + kvh) * D;
-    consume(gkc + off, gvc + off);
+  };
+  // the first ST chunks in flight together; one commit group per chunk (empty past the end)
+#pragma unroll 1
+  for (int st = 0; st < ST; ++st) {
+    if (st < nC) issue(st, st);
+    cp_async_commit();
   }
+  // the row's q while the chunks are in flight
+  for (int i = lane; i < D; i += 32)
+    sQ[warp][i] = live ? gq[(((size_t)b * p.N + n) * p.Hq + hq) * D + i] : 0.f;
+  __syncthreads();  // sQ, sAnc
   const uint64_t anc = sAnc[n];
-  for (int j = 0; j < p.N; ++j) {
-    if (!((anc >> j) & 1ull)) continue;
-    const size_t off = (((size_t)b * p.N + j) * p.Hkv + kvh) * D;
-    consume(gkt + off, gvt + off);
+  float m = -INFINITY, l = 0.f, o[PL];
+#pragma unroll
+  for (int i = 0; i < PL; ++i) o[i] = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < nC; ++c) {
+    const int st = c % ST;
+    cp_async_wait<ST - 1>();  // chunk c's group has landed (later ones may still be in flight)
+    __syncthreads();
+    if (live) {
+      const float *sk = stage_k(st), *sv = stage_v(st);
+      // lane j scores key j of the chunk
+      const bool tree_chunk = c >= nP;
+      const int j = tree_chunk ? (c - nP) * KC + lane : c * KC + lane;
+      bool vis = sValid[st][lane] != 0;
+      if (tree_chunk) vis = vis && ((anc >> j) & 1ull);
+      const float4 *kr = reinterpret_cast<const float4 *>(sk + lane * KS);
+      const float4 *qr = reinterpret_cast<const float4 *>(sQ[warp]);
+      float dot = 0.f;
+#pragma unroll 8
+      for (int d4 = 0; d4 < D / 4; ++d4) {
+        const float4 kv = kr[d4], qv = qr[d4];
+        dot = fmaf(qv.x, kv.x, dot);
+        dot = fmaf(qv.y, kv.y, dot);
+        dot = fmaf(qv.z, kv.z, dot);
+        dot = fmaf(qv.w, kv.w, dot);
+      }
+      const float sc = vis ? dot * p.scale : -INFINITY;
+      float cm = sc;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, off));
+      const float m_new = fmaxf(m, cm);
+      if (m_new != -INFINITY) {
+        const float alpha = m == -INFINITY ? 0.f : expf(m - m_new);
+        const float pe = vis ? expf(sc - m_new) : 0.f;
+        float ps = pe;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
+        l = l * alpha + ps;
+#pragma unroll
+        for (int i = 0; i < PL; ++i) o[i] *= alpha;
+#pragma unroll 8
+        for (int jj = 0; jj < KC; ++jj) {
+          const float w = __shfl_sync(0xFFFFFFFFu, pe, jj);
+#pragma unroll
+          for (int i = 0; i < PL; ++i) o[i] = fmaf(w, sv[jj * D + lane + 32 * i], o[i]);
+        }
+        m = m_new;
+      }
+    }
+    __syncthreads();  // every warp is done with this stage before it is refilled
+    if (c + ST < nC) issue(c + ST, st);
+    cp_async_commit();
   }
+  cp_async_wait<0>();
+  if (!live) return;
   float *dst = static_cast<float *>(p.out) + (((size_t)b * p.N + n) * p.Hq + hq) * D;
-  const float inv = 1.f / l;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
   for (int i = 0; i < PL; ++i) dst[lane + 32 * i] = o[i] * inv;
+}
+
+template <int D>
+cudaError_t launch_f32(const AttnParams &p, cudaStream_t s) {
+  const size_t smem = (size_t)f32_stages<D>() * f32_stage_floats<D>() * sizeof(float);
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(attn_f32_kernel<D>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  dim3 grid((p.M + kThreads / 32 - 1) / (kThreads / 32), p.Hkv, p.B);
+  attn_f32_kernel<D><<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
 }
 
 template <int D>
@@ -425,14 +532,7 @@ AttnPlan attn_plan(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, int max_pr
 }
 
 cudaError_t launch_attention(sv_dtype dt, const AttnParams &p, cudaStream_t s) {
-  if (dt == SV_F32) {
-    dim3 grid((p.N * p.Hq + kThreads / 32 - 1) / (kThreads / 32), p.B);
-    if (p.D == 64)
-      attn_f32_kernel<64><<<grid, kThreads, 0, s>>>(p);
-    else
-      attn_f32_kernel<128><<<grid, kThreads, 0, s>>>(p);
-    return cudaGetLastError();
-  }
+  if (dt == SV_F32) return p.D == 64 ? launch_f32<64>(p, s) : launch_f32<128>(p, s);
   return p.D == 64 ? launch_mma<64>(p, s) : launch_mma<128>(p, s);
 }
 
