@@ -23,6 +23,13 @@
 // When all query rows fit in 128/CP lanes (CP = 2 or 4 row copies), the rows are
 // loaded CP times into the A tile so that every TMEM lane quarter, and so every SM
 // sub-partition's exponential unit, holds a copy; the copies split each tile's columns.
+//
+// Two M tiles (129..256 rows) run as a ping-pong instead: each M tile m has one S region
+// in TMEM, and its softmax warps write P (bf16) over that S in TMEM, from where P V takes
+// its A operand; S[m] is free again once P V of m has completed.  The tensor pipe then
+// alternates between the M tiles (Q K^T of one while the other's softmax runs), no P
+// passes through shared memory, and the keys come in tiles of 128, so that Q (both M
+// tiles, 64 KB at D = 128) is read by the tensor core once per 128 keys.
 #include <cudaTypedefs.h>
 
 #include <cfloat>
@@ -64,7 +71,9 @@ struct TcLayout {
   static constexpr int PB = BN / 64;                     // 64-key column blocks of P
   static constexpr int P_BLOCK = kRows * 128;
   static constexpr int P_TILE = PB * P_BLOCK;            // P of one M tile
-  static constexpr int P_BYTES = MT * P_TILE;            // one P buffer (PBUF are used)
+  // two M tiles keep P in TMEM (over S): no P buffers in shared memory
+  static constexpr bool PT = MT == 2;
+  static constexpr int P_BYTES = PT ? 0 : MT * P_TILE;   // one P buffer (PBUF are used)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + QBUF * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
@@ -82,7 +91,8 @@ struct TcLayout {
   static constexpr int OFF_PAR = OFF_ANC + kMaxNodes * 8;
   static constexpr int BYTES = OFF_PAR + kMaxNodes * 4;
   static constexpr int SMEM = BYTES;  // the dynamic window starts 1024-aligned (checked)
-  static constexpr int S_COLS = 2 * MT * BN;
+  // S: two buffers per M tile, or (P in TMEM) one region per M tile
+  static constexpr int S_COLS = (PT ? 1 : 2) * MT * BN;
   static constexpr int NEED_COLS = S_COLS + MT * D;
   static constexpr uint32_t TMEM_COLS = NEED_COLS <= 256 ? 256 : 512;
   static constexpr int NSW = 4 * MT;  // softmax warps
@@ -192,33 +202,41 @@ __device__ __forceinline__ long long block_scan(long long x, long long *red, lon
 // warp whose rows are all padding.  It reads no S and writes no P or O, but takes its part
 // in every barrier and in zeroing the V rows past the prefix end.  Each arrival waits for
 // the previous phase of its barrier to be complete, since no write of this warp orders
-// it.  Kept out of line so that the row loop's code stays small.  False if a wait gave up.
+// it (with P in TMEM the wait for S of M tile mt orders it).  Kept out of line so that
+// the row loop's code stays small.  False if a wait gave up.
 template <class Lay, int BN, int STAGES, int PBUF>
 __device__ __noinline__ bool idle_piece(int N, int t0, int n, bool publish, int g, int qi, int L,
-                                        bool grouped,
+                                        bool grouped, int mt,
                                         uint64_t *s_full, uint64_t *s_free, uint64_t *v_full,
                                         uint64_t *p_full, uint64_t *o_free, uint64_t *pub, uint8_t *sV,
                                         volatile int *abort_flag, unsigned long long wlim) {
   const int lane = threadIdx.x & 31;
   for (int k = 0; k < n; ++k) {
     const int gk = g + k, j = gk & 1, s = gk % STAGES, t = t0 + k, pb = gk % PBUF;
-    if (!mbar_wait(&s_full[j], (gk >> 1) & 1, abort_flag, wlim)) return false;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&s_free[j]);
+    if constexpr (Lay::PT) {
+      if (!mbar_wait(&s_full[mt], gk & 1, abort_flag, wlim)) return false;
+    } else {
+      if (!mbar_wait(&s_full[j], (gk >> 1) & 1, abort_flag, wlim)) return false;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[j]);
+    }
     const int nvalid = t == 0 ? N : min(BN, L - (t - 1) * BN);
-    if (t != 0 && nvalid < BN) {  // this warp's share of zeroing the V tail (see the row loop)
+    // this warp's share of zeroing the V tail (see the row loop)
+    if (t != 0 && nvalid < BN && (!Lay::PT || mt == 0)) {
       if (!mbar_wait(&v_full[s], (gk / STAGES) & 1, abort_flag, wlim)) return false;
       uint8_t *vt = sV + s * Lay::KV_BYTES;
       constexpr int per_row = Lay::KB * 8;
-      for (int i = threadIdx.x; i < (BN - nvalid) * per_row; i += 32 * Lay::NSW) {
+      constexpr int stride = 32 * (Lay::PT ? 4 : Lay::NSW);
+      for (int i = threadIdx.x; i < (BN - nvalid) * per_row; i += stride) {
         const int r = nvalid + i / per_row, rem = i % per_row;
         *reinterpret_cast<uint4 *>(vt + kv_unit_offset<Lay>(grouped, r, rem)) = make_uint4(0, 0, 0, 0);
       }
     }
-    if (gk >= PBUF && !mbar_wait(&p_full[pb], ((gk / PBUF) - 1) & 1, abort_flag, wlim)) return false;
+    if (!Lay::PT && gk >= PBUF && !mbar_wait(&p_full[pb], ((gk / PBUF) - 1) & 1, abort_flag, wlim))
+      return false;
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&p_full[pb]);
+    if (lane == 0) mbar_arrive(&p_full[Lay::PT ? mt : pb]);
   }
   if (publish) {
     __threadfence();
@@ -364,10 +382,12 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
+    // with P in TMEM, index j is the M tile: S[j] full and free (its P V done) are MMA
+    // commits, P[j] written is the arrival of that M tile's four softmax warps
     for (int j = 0; j < 2; ++j) {
       mbar_init(&s_full[j], 1);
-      mbar_init(&s_free[j], NSW);
-      mbar_init(&p_full[j], NSW);
+      mbar_init(&s_free[j], Lay::PT ? 1 : NSW);
+      mbar_init(&p_full[j], Lay::PT ? 4 : NSW);
       mbar_init(&p_free[j], 1);
       mbar_init(&xch_full[j], NSW);
     }
@@ -634,7 +654,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
     // One thread polls both kinds of work and issues whichever is ready, P V first:
     // P V of a tile as soon as its P is written, and S = Q K^T up to two tiles ahead of
     // P V (S is double buffered), across piece boundaries.  A late K never holds back
-    // a P V that is ready.
+    // a P V that is ready.  Two M tiles (P in TMEM) take the ping-pong order below.
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(kRows, BN, 0, 0);
       constexpr uint32_t idO = idesc_bf16(kRows, D, 0, 1);
@@ -648,63 +668,82 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       // 64-column half 1 KB after the first
       const uint64_t dk_g = sdesc_sw128(smem_u32(sK), 16, Lay::KB * 1024);
       const uint64_t dv_g = sdesc_sw128(smem_u32(sV), 1024, Lay::KB * 1024);
-      PieceIter its = it;  // S side of the walk over this CTA's tiles
-      Piece pcs;
-      int s_qi = -1, s_rem = 0, gs = 0, gp = 0;
-      bool s_first = false, s_done = false;
-      uint8_t m_first[4], m_grp[4];
-      int m_qi[4];
+      // the idle poll: gives up after the wait limit (or when another role gave up)
       unsigned long long idle_t0 = 0;
       uint32_t idle_n = 0;
-      while (true) {
-        bool prog = false;
-        if (gp < gs) {
-          const int gk = gp, s = gk % STAGES, pb = gk % PBUF;
-          const bool first = m_first[gk & 3];
-          const bool grp = m_grp[gk & 3];
-          const int qi = m_qi[gk & 3];
-          if (mbar_test(&p_full[pb], (gk / PBUF) & 1) &&
-              (!first || qi == 0 || mbar_test(o_free, (qi - 1) & 1)) &&
-              mbar_test(&v_full[s], (gk / STAGES) & 1)) {
-            tc_fence_after();
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
+      auto idle = [&]() -> bool {
+        if ((++idle_n & 63u) == 0) {
+          if (*abort_flag) return false;
+          const unsigned long long now = global_ns();
+          if (idle_n == 64) idle_t0 = now;
+          else if (now - idle_t0 > wlim) {
+            *abort_flag = 1;
+            return false;
+          }
+        }
+        // a short sleep keeps the poll from taking issue slots from the softmax warps
+        // that share this SM sub-partition
+        __nanosleep(kPollSleepNs);
+        return true;
+      };
+      if constexpr (Lay::PT) {
+        // Ping-pong of the two M tiles.  Per tile: S[0] = Q[0] K^T, S[1] = Q[1] K^T, then
+        // P V of M tile 0 once its P is in TMEM, then of M tile 1.  S[m] of the next tile
+        // waits for P V of m to complete (P lives over S[m]), so one M tile's Q K^T and
+        // P V run while the other M tile's softmax works.  P V of a ready M tile first.
+        PieceIter its = it;
+        Piece pcs;
+        int s_qi = -1, s_rem = 0, gs = 0, sm_ = 0, gp = 0, pm_ = 0;
+        bool s_first = false, s_done = false;
+        uint8_t m_first[4], m_grp[4];
+        int m_qi[4];
+        while (true) {
+          bool prog = false;
+          if (gp < gs || (gp == gs && pm_ < sm_)) {  // S of (gp, pm_) was issued
+            const int gk = gp, s = gk % STAGES, m = pm_;
+            const bool first = m_first[gk & 3];
+            const bool grp = m_grp[gk & 3];
+            const int qi = m_qi[gk & 3];
+            if (mbar_test(&p_full[m], gk & 1) &&
+                (!first || qi == 0 || mbar_test(o_free, (qi - 1) & 1)) &&
+                mbar_test(&v_full[s], (gk / STAGES) & 1)) {
+              tc_fence_after();
 #pragma unroll
               for (int kk = 0; kk < BN / 16; ++kk) {
-                const uint64_t a = dp + (uint64_t)((pb * Lay::P_BYTES + m * Lay::P_TILE +
-                                                     (kk >> 2) * Lay::P_BLOCK + (kk & 3) * 32) >> 4);
                 const uint64_t bd =
                     grp ? dv_g + (uint64_t)((s * Lay::KV_BYTES + kk * 2 * (Lay::KB * 1024)) >> 4)
                         : dv + (uint64_t)((s * Lay::KV_BYTES + kk * 16 * 128) >> 4);
-                umma_bf16(tmem + (uint32_t)(Lay::S_COLS + m * D), a, bd, idO,
-                          (!first || kk > 0) ? 1u : 0u);
+                // 16 keys of P per MMA: 8 TMEM columns of bf16 pairs
+                umma_bf16_ts(tmem + (uint32_t)(Lay::S_COLS + m * D), tmem + (uint32_t)(m * BN + kk * 8),
+                             bd, idO, (!first || kk > 0) ? 1u : 0u);
+              }
+              umma_commit(&s_free[m]);
+              if (m == MT - 1) {
+                umma_commit(&v_empty[s]);
+                ++gp;
+                pm_ = 0;
+              } else {
+                ++pm_;
+              }
+              prog = true;
+            }
+          }
+          if (!s_done) {
+            if (sm_ == 0 && s_rem == 0) {
+              if (piece_next(its, p, pcs)) {
+                ++s_qi;
+                s_rem = pcs.t1 - pcs.t0;
+                s_first = true;
+              } else {
+                s_done = true;
               }
             }
-            umma_commit(&v_empty[s]);
-            umma_commit(&p_free[pb]);
-            ++gp;
-            prog = true;
-          }
-        }
-        if (!s_done && gs < gp + 2) {
-          if (s_rem == 0) {
-            if (piece_next(its, p, pcs)) {
-              ++s_qi;
-              s_rem = pcs.t1 - pcs.t0;
-              s_first = true;
-            } else {
-              s_done = true;
-            }
-          }
-          const int gk = gs, s = gk % STAGES, j = gk & 1, qb = s_qi % QBUF;
-          if (!s_done && (!s_first || mbar_test(&q_full[qb], (s_qi / QBUF) & 1)) &&
-              mbar_test(&k_full[s], (gk / STAGES) & 1) &&
-              (gk < 2 || mbar_test(&s_free[j], ((gk >> 1) - 1) & 1))) {
-            tc_fence_after();
-            // tile pcs.t1 - s_rem of its unit; tile 0 holds the tree nodes (plain layout)
-            const bool grp = p.pg_grouped && pcs.t1 - s_rem != 0;
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
+            const int gk = gs, s = gk % STAGES, m = sm_, qb = s_qi % QBUF;
+            if (!s_done && (!s_first || mbar_test(&q_full[qb], (s_qi / QBUF) & 1)) &&
+                mbar_test(&k_full[s], (gk / STAGES) & 1) &&
+                (gk == 0 || mbar_test(&s_free[m], (gk - 1) & 1))) {
+              tc_fence_after();
+              const bool grp = p.pg_grouped && pcs.t1 - s_rem != 0;
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t a = dq + (uint64_t)((qb * Lay::Q_BYTES + (kk >> 2) * Lay::Q_BLOCK +
@@ -712,39 +751,120 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
                 const uint64_t bd =
                     grp ? dk_g + (uint64_t)((s * Lay::KV_BYTES + (kk >> 2) * 1024 + (kk & 3) * 32) >> 4)
                         : dk + (uint64_t)((s * Lay::KV_BYTES + (kk >> 2) * Lay::KV_BLOCK + (kk & 3) * 32) >> 4);
-                umma_bf16(tmem + (uint32_t)((j * MT + m) * BN), a, bd, idS, kk > 0);
+                umma_bf16(tmem + (uint32_t)(m * BN), a, bd, idS, kk > 0);
+              }
+              umma_commit(&s_full[m]);
+              if (m == 0) {
+                m_first[gk & 3] = s_first;
+                m_grp[gk & 3] = grp;
+                m_qi[gk & 3] = s_qi;
+              }
+              if (m == MT - 1) {
+                umma_commit(&k_empty[s]);
+                if (s_rem == 1) umma_commit(&q_empty[qb]);
+                s_first = false;
+                --s_rem;
+                ++gs;
+                sm_ = 0;
+              } else {
+                ++sm_;
+              }
+              prog = true;
+            }
+          }
+          if (s_done && gp == gs) break;
+          if (prog) {
+            idle_n = 0;
+            continue;
+          }
+          if (!idle()) break;
+        }
+      } else {
+        PieceIter its = it;  // S side of the walk over this CTA's tiles
+        Piece pcs;
+        int s_qi = -1, s_rem = 0, gs = 0, gp = 0;
+        bool s_first = false, s_done = false;
+        uint8_t m_first[4], m_grp[4];
+        int m_qi[4];
+        while (true) {
+          bool prog = false;
+          if (gp < gs) {
+            const int gk = gp, s = gk % STAGES, pb = gk % PBUF;
+            const bool first = m_first[gk & 3];
+            const bool grp = m_grp[gk & 3];
+            const int qi = m_qi[gk & 3];
+            if (mbar_test(&p_full[pb], (gk / PBUF) & 1) &&
+                (!first || qi == 0 || mbar_test(o_free, (qi - 1) & 1)) &&
+                mbar_test(&v_full[s], (gk / STAGES) & 1)) {
+              tc_fence_after();
+#pragma unroll
+              for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                  const uint64_t a = dp + (uint64_t)((pb * Lay::P_BYTES + m * Lay::P_TILE +
+                                                       (kk >> 2) * Lay::P_BLOCK + (kk & 3) * 32) >> 4);
+                  const uint64_t bd =
+                      grp ? dv_g + (uint64_t)((s * Lay::KV_BYTES + kk * 2 * (Lay::KB * 1024)) >> 4)
+                          : dv + (uint64_t)((s * Lay::KV_BYTES + kk * 16 * 128) >> 4);
+                  umma_bf16(tmem + (uint32_t)(Lay::S_COLS + m * D), a, bd, idO,
+                            (!first || kk > 0) ? 1u : 0u);
+                }
+              }
+              umma_commit(&v_empty[s]);
+              umma_commit(&p_free[pb]);
+              ++gp;
+              prog = true;
+            }
+          }
+          if (!s_done && gs < gp + 2) {
+            if (s_rem == 0) {
+              if (piece_next(its, p, pcs)) {
+                ++s_qi;
+                s_rem = pcs.t1 - pcs.t0;
+                s_first = true;
+              } else {
+                s_done = true;
               }
             }
-            umma_commit(&s_full[j]);
-            umma_commit(&k_empty[s]);
-            if (s_rem == 1) umma_commit(&q_empty[qb]);
-            m_first[gk & 3] = s_first;
-            m_grp[gk & 3] = grp;
-            m_qi[gk & 3] = s_qi;
-            s_first = false;
-            --s_rem;
-            ++gs;
-            prog = true;
+            const int gk = gs, s = gk % STAGES, j = gk & 1, qb = s_qi % QBUF;
+            if (!s_done && (!s_first || mbar_test(&q_full[qb], (s_qi / QBUF) & 1)) &&
+                mbar_test(&k_full[s], (gk / STAGES) & 1) &&
+                (gk < 2 || mbar_test(&s_free[j], ((gk >> 1) - 1) & 1))) {
+              tc_fence_after();
+              // tile pcs.t1 - s_rem of its unit; tile 0 holds the tree nodes (plain layout)
+              const bool grp = p.pg_grouped && pcs.t1 - s_rem != 0;
+#pragma unroll
+              for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                  const uint64_t a = dq + (uint64_t)((qb * Lay::Q_BYTES + (kk >> 2) * Lay::Q_BLOCK +
+                                                       m * kRows * 128 + (kk & 3) * 32) >> 4);
+                  const uint64_t bd =
+                      grp ? dk_g + (uint64_t)((s * Lay::KV_BYTES + (kk >> 2) * 1024 + (kk & 3) * 32) >> 4)
+                          : dk + (uint64_t)((s * Lay::KV_BYTES + (kk >> 2) * Lay::KV_BLOCK + (kk & 3) * 32) >> 4);
+                  umma_bf16(tmem + (uint32_t)((j * MT + m) * BN), a, bd, idS, kk > 0);
+                }
+              }
+              umma_commit(&s_full[j]);
+              umma_commit(&k_empty[s]);
+              if (s_rem == 1) umma_commit(&q_empty[qb]);
+              m_first[gk & 3] = s_first;
+              m_grp[gk & 3] = grp;
+              m_qi[gk & 3] = s_qi;
+              s_first = false;
+              --s_rem;
+              ++gs;
+              prog = true;
+            }
           }
-        }
-        if (s_done && gp == gs) break;
-        if (prog) {
-          idle_n = 0;
-          continue;
-        }
-        // nothing ready: give up after the wait limit (or when another role gave up)
-        if ((++idle_n & 63u) == 0) {
-          if (*abort_flag) break;
-          const unsigned long long now = global_ns();
-          if (idle_n == 64) idle_t0 = now;
-          else if (now - idle_t0 > wlim) {
-            *abort_flag = 1;
-            break;
+          if (s_done && gp == gs) break;
+          if (prog) {
+            idle_n = 0;
+            continue;
           }
+          // nothing ready: give up after the wait limit (or when another role gave up)
+          if (!idle()) break;
         }
-        // a short sleep keeps the poll from taking issue slots from the softmax warp
-        // that shares this SM sub-partition
-        __nanosleep(kPollSleepNs);
       }
       // every MMA issued must complete before TMEM is released
       umma_commit(drain);
@@ -803,7 +923,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       const bool warp_idle = CP == 1 && __all_sync(0xFFFFFFFFu, !valid_row);
       const int L = clamp_len(p, pc.b);
       if (warp_idle) {  // every row of this warp is padding: barriers only
-        if (!idle_piece<Lay, BN, STAGES, PBUF>(p.N, pc.t0, n, pc.t0 > 0, g, qi, L, p.pg_grouped != 0,
+        if (!idle_piece<Lay, BN, STAGES, PBUF>(p.N, pc.t0, n, pc.t0 > 0, g, qi, L, p.pg_grouped != 0, mt,
                                               s_full, s_free, v_full,
                                               p_full, o_free, pub, sV, abort_flag, wlim)) {
           ok = false;
@@ -818,20 +938,24 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         const int gk = g + k, j = gk & 1, s = gk % STAGES, t = pc.t0 + k, pb = gk % PBUF;
         const bool tree = t == 0;
         const int nvalid = tree ? p.N : min(BN, L - (t - 1) * BN);
-        if (!mbar_wait(&s_full[j], (gk >> 1) & 1, abort_flag, wlim)) {
+        // S of this tile: buffer j, or (P in TMEM) this M tile's region, one phase per tile
+        if (!(Lay::PT ? mbar_wait(&s_full[mt], gk & 1, abort_flag, wlim)
+                      : mbar_wait(&s_full[j], (gk >> 1) & 1, abort_flag, wlim))) {
           ok = false;
           break;
         }
         tc_fence_after();
         // V rows past the prefix end may hold anything: zero them so that 0 * V stays 0.
-        // Done by all softmax threads once V has landed, before P is published.
+        // Done by all softmax threads once V has landed, before P is published.  With P in
+        // TMEM, by the warps of M tile 0, whose P V is issued first.
         auto zero_v_tail = [&]() -> bool {
-          if (tree || nvalid >= BN) return true;
+          if (tree || nvalid >= BN || (Lay::PT && mt != 0)) return true;
           if (!mbar_wait(&v_full[s], (gk / STAGES) & 1, abort_flag, wlim)) return false;
           uint8_t *vt = sV + s * Lay::KV_BYTES;
           constexpr int per_row = Lay::KB * 8;
+          constexpr int stride = 32 * (Lay::PT ? 4 : NSW);
           const bool grouped = p.pg_grouped != 0;  // (a prefix tile)
-          for (int i = tid_sm; i < (BN - nvalid) * per_row; i += 32 * NSW) {
+          for (int i = tid_sm; i < (BN - nvalid) * per_row; i += stride) {
             const int r = nvalid + i / per_row, rem = i % per_row;
             *reinterpret_cast<uint4 *>(vt + kv_unit_offset<Lay>(grouped, r, rem)) = make_uint4(0, 0, 0, 0);
           }
@@ -842,7 +966,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         const uint64_t anc_s = (tree && valid_row && col0 < 64) ? (anc >> col0) : 0ull;
         const int nv_rel = (tree || !valid_row) ? 0 : nvalid - col0;
         const bool full = !tree && valid_row && nv_rel >= CW;
-        const uint32_t ta0 = t_lane + (uint32_t)((j * MT + mt) * BN + col0);
+        const uint32_t ta0 = t_lane + (uint32_t)(((Lay::PT ? 0 : j * MT) + mt) * BN + col0);
 
         // bit c of visible(h) <=> column h*CH + c of this warp's slice is a key the row sees.
         // Padding rows (past the unit's rows) see every column: their results are never
@@ -864,7 +988,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
           if (km == kAll) {
 #pragma unroll
-            for (int c = 0; c < CH; ++c) mx[c & 7] = fmaxf(mx[c & 7], v[c]);
+            for (int c = 0; c < CH; c += 2) mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], v[c], v[c + 1]);
           } else {
 #pragma unroll
             for (int c = 0; c < CH; ++c) mx[c & 7] = fmaxf(mx[c & 7], ((km >> c) & 1u) ? v[c] : -INFINITY);
@@ -872,11 +996,11 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                        fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         };
-        // With two M tiles (a 64-column slice per warp) the slice is read from TMEM once,
-        // into registers, and the S buffer is released at once.  Otherwise it is read twice
-        // (max, then P) and S is released with P: releasing it early lets the next S take
-        // the tensor pipe ahead of this tile's P V, which costs more than it gains there.
-        constexpr bool kOnePass = MT == 2 && CW <= 64;
+        // The row's columns are read from TMEM twice (max, then P), 32 at a time, and S is
+        // released with P: releasing it early lets the next S take the tensor pipe ahead
+        // of this tile's P V, which costs more than it gains.  (With P in TMEM, P goes over
+        // columns already read in the second pass, and S is free once P V has completed.)
+        constexpr bool kOnePass = false;
         float vs[kOnePass ? CW : 1];
         auto vchunk = [&](int h) -> float (&)[CH] { return *reinterpret_cast<float(*)[CH]>(vs + h * CH); };
         float pmax = -INFINITY;
@@ -887,9 +1011,6 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
             else tmem_ld16(ta0 + h * CH, vchunk(h));
           }
           tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_free[j]);
 #pragma unroll
           for (int h = 0; h < NCH; ++h) pmax = fmaxf(pmax, chunk_max(h, vchunk(h)));
         } else {
@@ -928,9 +1049,11 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
 
         // O is rescaled in place only when the running max jumped: all earlier P V of
         // this piece must have finished first (P V runs in order, so waiting for the
-        // previous tile's buffer release is enough)
+        // previous tile's buffer release is enough; with P in TMEM, this tile's S was
+        // computed only after the previous P V of this M tile completed)
         if (owner && __any_sync(0xFFFFFFFFu, rescale)) {
-          if (!mbar_wait(&p_free[(gk - 1) % PBUF], ((gk - 1) / PBUF) & 1, abort_flag, wlim)) {
+          if (!Lay::PT &&
+              !mbar_wait(&p_free[(gk - 1) % PBUF], ((gk - 1) / PBUF) & 1, abort_flag, wlim)) {
             ok = false;
             break;
           }
@@ -948,21 +1071,35 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           tmem_wait_st();
         }
         // P buffer gk&1 is free once the P V of tile gk-2 has finished
-        if (gk >= PBUF && !mbar_wait(&p_free[pb], ((gk / PBUF) - 1) & 1, abort_flag, wlim)) {
+        if (!Lay::PT && gk >= PBUF && !mbar_wait(&p_free[pb], ((gk / PBUF) - 1) & 1, abort_flag, wlim)) {
           ok = false;
           break;
         }
+        // 2^(s*scale - max) of a whole chunk, the scale and the subtraction on fp32 pairs;
+        // partial row sums in rs (pairs of lanes 0/1 and 2/3)
+        auto exp_pairs = [&](float (&v)[CH], float (&rs)[4]) {
+          const float2 sc2 = make_float2(sc, sc), nmu2 = make_float2(-mu, -mu);
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < CH; c += 2) {
+            const float2 x = __ffma2_rn(make_float2(v[c], v[c + 1]), sc2, nmu2);
+            v[c] = ex2(x.x);
+            v[c + 1] = ex2(x.y);
+            if ((c >> 1) & 1) acc1 = __fadd2_rn(acc1, make_float2(v[c], v[c + 1]));
+            else acc0 = __fadd2_rn(acc0, make_float2(v[c], v[c + 1]));
+          }
+          rs[0] += acc0.x;
+          rs[1] += acc0.y;
+          rs[2] += acc1.x;
+          rs[3] += acc1.y;
+        };
         // P = 2^(s*scale - max) in bf16 into this warp's slice of the P row
         uint8_t *ptile = sP + pb * Lay::P_BYTES + mt * Lay::P_TILE;
         auto chunk_exp = [&](int h, float (&v)[CH]) -> float {
           const uint32_t km = visible(h);
           float rs[4] = {0.f, 0.f, 0.f, 0.f};
           if (km == kAll) {
-#pragma unroll
-            for (int c = 0; c < CH; ++c) {
-              v[c] = ex2(fmaf(v[c], sc, -mu));
-              rs[c & 3] += v[c];
-            }
+            exp_pairs(v, rs);
           } else {
 #pragma unroll
             for (int c = 0; c < CH; ++c) {
@@ -983,6 +1120,27 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           }
           return (rs[0] + rs[1]) + (rs[2] + rs[3]);
         };
+        // With P in TMEM: P of chunk h as bf16 pairs over TMEM columns [h*CH/2, (h+1)*CH/2)
+        // of this row's S region, which hold S columns of chunks h/2 and earlier, already read
+        auto chunk_exp_tmem = [&](int h, float (&v)[CH]) -> float {
+          static_assert(CH == 32, "P in TMEM takes 32-column chunks");
+          const uint32_t km = visible(h);
+          float rs[4] = {0.f, 0.f, 0.f, 0.f};
+          if (km == kAll) {
+            exp_pairs(v, rs);
+          } else {
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+              v[c] = ((km >> c) & 1u) ? ex2(fmaf(v[c], sc, -mu)) : 0.f;
+              rs[c & 3] += v[c];
+            }
+          }
+          float pw[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) pw[c] = __uint_as_float(pack_bf16x2(v[2 * c], v[2 * c + 1]));
+          tmem_st16(ta0 + (uint32_t)(h * 16), pw);
+          return (rs[0] + rs[1]) + (rs[2] + rs[3]);
+        };
         float rsum = 0.f;
         if constexpr (kOnePass) {
 #pragma unroll
@@ -992,7 +1150,8 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           for (int h = 0; h < NCH; ++h) {
             float v[CH];
             read_chunk(ta0 + h * CH, v);
-            rsum += chunk_exp(h, v);
+            if constexpr (Lay::PT) rsum += chunk_exp_tmem(h, v);
+            else rsum += chunk_exp(h, v);
           }
         }
         l = l * alpha + rsum;
@@ -1000,12 +1159,13 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           ok = false;
           break;
         }
+        if constexpr (Lay::PT) tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (!kOnePass) mbar_arrive(&s_free[j]);
-          mbar_arrive(&p_full[pb]);
+          if (!kOnePass && !Lay::PT) mbar_arrive(&s_free[j]);
+          mbar_arrive(&p_full[Lay::PT ? mt : pb]);
         }
       }
       if (!ok) break;
@@ -1031,7 +1191,10 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       const long long U_end = pc.fs - pc.t0 + pc.T;
       constexpr int ROWS = MT * kRows;
       if (owner && !warp_idle) {
-        if (!mbar_wait(&p_free[gl % PBUF], (gl / PBUF) & 1, abort_flag, wlim)) break;
+        // the piece's last P V has completed (with P in TMEM: that of this M tile)
+        if (!(Lay::PT ? mbar_wait(&s_free[mt], gl & 1, abort_flag, wlim)
+                      : mbar_wait(&p_free[gl % PBUF], (gl / PBUF) & 1, abort_flag, wlim)))
+          break;
         tc_fence_after();
         const int hq = pc.kvh * p.G + (valid_row ? R % p.G : 0);
         bf16 *dst = static_cast<bf16 *>(p.out) + (((size_t)pc.b * p.N + node) * p.Hq + hq) * D;
@@ -1305,7 +1468,7 @@ TcPlan tc_plan(int B, int N, int Hq, int Hkv, int D, int num_sms) {
   pl.CP = 1;
   if (pl.MT == 1 && M <= 32 && 32 % G == 0) pl.CP = 4;
   else if (pl.MT == 1 && M <= 64 && 64 % G == 0) pl.CP = 2;
-  pl.BN = pl.MT == 1 ? 128 : 64;  // keys per tile
+  pl.BN = 128;  // keys per tile
   pl.m_groups = (M + pl.MT * kRows - 1) / (pl.MT * kRows);
   pl.grid = num_sms > 0 ? num_sms : 152;
   const long long units = (long long)B * Hkv * pl.m_groups;
@@ -1379,12 +1542,12 @@ cudaError_t launch_attention_tc(const AttnParams &a, const TcPlan &pl, void *ws,
   if (a.D == 128) {
     // (two Q buffers paid for with one P buffer measured slower: the softmax then
     // waits for every P V before writing the next P)
-    if (pl.MT == 2) return launch_tc_typed<128, 2, 1, 64, 3, 1, 2>(p, pl.grid, s);
+    if (pl.MT == 2) return launch_tc_typed<128, 2, 1, 128, 2, 1, 1>(p, pl.grid, s);
     if (pl.CP == 4) return launch_tc_typed<128, 1, 4, 128, 2, 1, 2>(p, pl.grid, s);
     if (pl.CP == 2) return launch_tc_typed<128, 1, 2, 128, 2, 1, 2>(p, pl.grid, s);
     return launch_tc_typed<128, 1, 1, 128, 2, 1, 2>(p, pl.grid, s);
   }
-  if (pl.MT == 2) return launch_tc_typed<64, 2, 1, 64, 4, 2, 2>(p, pl.grid, s);
+  if (pl.MT == 2) return launch_tc_typed<64, 2, 1, 128, 4, 2, 1>(p, pl.grid, s);
   if (pl.CP == 4) return launch_tc_typed<64, 1, 4, 128, 3, 2, 2>(p, pl.grid, s);
   if (pl.CP == 2) return launch_tc_typed<64, 1, 2, 128, 3, 2, 2>(p, pl.grid, s);
   return launch_tc_typed<64, 1, 1, 128, 3, 2, 2>(p, pl.grid, s);

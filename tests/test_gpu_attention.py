@@ -45,7 +45,7 @@ def test_chain_gqa_ragged(cuda_ok, lens):
 
 
 def test_tree26_gqa64_multi_mtile(cuda_ok):
-    """26 nodes x 8 group heads = 208 query rows: four 64-row tiles per KV head."""
+    """26 nodes x 8 group heads = 208 query rows: two 128-row M tiles per KV head."""
     par = wl.TREE_T26
     inp = wl.attention_inputs(3, 26, 64, 8, 128, [777, 0, 1500], dtype=torch.bfloat16, seed=2)
     _check(inp, par, torch.bfloat16)
@@ -176,11 +176,34 @@ def test_paged_block32_64_128_256(cuda_ok):
 
 
 def test_paged_block128_two_mma_tiles(cuda_ok):
-    """Pages of 128 rows cut into 64-key tiles (the 256-row kernel)."""
+    """Pages of 128 rows, one per 128-key tile, with two M tiles (208 rows)."""
     par = wl.TREE_T26
     inp = wl.attention_inputs(2, 26, 64, 8, 128, [600, 129], dtype=torch.bfloat16, paged=True,
                               block_size=128, seed=17)
     _check(inp, par, torch.bfloat16, block_size=128)
+
+
+@pytest.mark.parametrize("D,paged,bs,lens", [(64, False, 16, [333, 1200, 128]),
+                                          (128, True, 16, [600, 129, 1]),
+                                          (64, True, 32, [257, 40, 1000])])
+def test_two_mma_tiles_head_dim_and_pages(cuda_ok, D, paged, bs, lens):
+    """Two M tiles (26 nodes x 8 group heads) with D = 64, and with pages shorter than a
+    tile (16-row pages: one copy per page into the grouped layout at D = 128); ragged ends
+    of the last tile (prefix lengths not multiples of 128)."""
+    par = wl.TREE_T26
+    inp = wl.attention_inputs(len(lens), 26, 64, 8, D, lens, dtype=torch.bfloat16, paged=paged,
+                              block_size=bs, seed=31 + D + bs)
+    _check(inp, par, torch.bfloat16, block_size=bs)
+
+
+def test_two_mma_tiles_many_units_repeatable(cuda_ok):
+    """More units than CTAs with two M tiles; three calls give identical outputs."""
+    par = wl.TREE_T26
+    inp = wl.attention_inputs(40, 26, 64, 8, 128, [64 * (i % 7) + 5 * i for i in range(40)],
+                              dtype=torch.bfloat16, seed=37)
+    out, _ = _check(inp, par, torch.bfloat16, b_range=(0, 6))
+    for _ in range(2):
+        assert torch.equal(_run(inp, par, torch.bfloat16), out)
 
 
 def test_workspace_reused_across_calls_and_shapes(cuda_ok):
