@@ -687,97 +687,88 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         return true;
       };
       if constexpr (Lay::PT) {
-        // Ping-pong of the two M tiles.  Per tile: S[0] = Q[0] K^T, S[1] = Q[1] K^T, then
-        // P V of M tile 0 once its P is in TMEM, then of M tile 1.  S[m] of the next tile
-        // waits for P V of m to complete (P lives over S[m]), so one M tile's Q K^T and
-        // P V run while the other M tile's softmax works.  P V of a ready M tile first.
+        // Ping-pong of the two M tiles, in a fixed order: S[0] and S[1] of the first tile,
+        // then per tile k: P V of M tile 0, S[0] of tile k+1 (once that P V has completed:
+        // P lives over S[0]), P V of M tile 1, S[1] of tile k+1.  One M tile's Q K^T and
+        // P V run while the other M tile's softmax works.  Each step waits on its own
+        // barrier (a blocking wait wakes as soon as the phase completes).
         PieceIter its = it;
         Piece pcs;
-        int s_qi = -1, s_rem = 0, gs = 0, sm_ = 0, gp = 0, pm_ = 0;
-        bool s_first = false, s_done = false;
-        uint8_t m_first[4], m_grp[4];
-        int m_qi[4];
-        while (true) {
-          bool prog = false;
-          if (gp < gs || (gp == gs && pm_ < sm_)) {  // S of (gp, pm_) was issued
-            const int gk = gp, s = gk % STAGES, m = pm_;
-            const bool first = m_first[gk & 3];
-            const bool grp = m_grp[gk & 3];
-            const int qi = m_qi[gk & 3];
-            if (mbar_test(&p_full[m], gk & 1) &&
-                (!first || qi == 0 || mbar_test(o_free, (qi - 1) & 1)) &&
-                mbar_test(&v_full[s], (gk / STAGES) & 1)) {
-              tc_fence_after();
+        struct TileInfo {
+          bool first, last, grp;
+          int qi;
+        };
+        int s_qi = -1, s_rem = 0;
+        bool first_flag = false;
+        auto next_tile = [&](TileInfo &ti) -> bool {
+          if (s_rem == 0) {
+            if (!piece_next(its, p, pcs)) return false;
+            ++s_qi;
+            s_rem = pcs.t1 - pcs.t0;
+            first_flag = true;
+          }
+          ti.first = first_flag;
+          first_flag = false;
+          ti.qi = s_qi;
+          // tile pcs.t1 - s_rem of its unit; tile 0 holds the tree nodes (plain layout)
+          ti.grp = p.pg_grouped && pcs.t1 - s_rem != 0;
+          ti.last = s_rem == 1;
+          --s_rem;
+          return true;
+        };
+        auto issue_qk = [&](const TileInfo &ti, int gk, int m) -> bool {
+          const int s = gk % STAGES, qb = ti.qi % QBUF;
+          if (m == 0 && ti.first && !mbar_wait(&q_full[qb], (ti.qi / QBUF) & 1, abort_flag, wlim))
+            return false;
+          if (m == 0 && !mbar_wait(&k_full[s], (gk / STAGES) & 1, abort_flag, wlim)) return false;
+          if (gk > 0 && !mbar_wait(&s_free[m], (gk - 1) & 1, abort_flag, wlim)) return false;
+          tc_fence_after();
 #pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk) {
-                const uint64_t bd =
-                    grp ? dv_g + (uint64_t)((s * Lay::KV_BYTES + kk * 2 * (Lay::KB * 1024)) >> 4)
-                        : dv + (uint64_t)((s * Lay::KV_BYTES + kk * 16 * 128) >> 4);
-                // 16 keys of P per MMA: 8 TMEM columns of bf16 pairs
-                umma_bf16_ts(tmem + (uint32_t)(Lay::S_COLS + m * D), tmem + (uint32_t)(m * BN + kk * 8),
-                             bd, idO, (!first || kk > 0) ? 1u : 0u);
-              }
-              umma_commit(&s_free[m]);
-              if (m == MT - 1) {
-                umma_commit(&v_empty[s]);
-                ++gp;
-                pm_ = 0;
-              } else {
-                ++pm_;
-              }
-              prog = true;
-            }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = dq + (uint64_t)((qb * Lay::Q_BYTES + (kk >> 2) * Lay::Q_BLOCK +
+                                                 m * kRows * 128 + (kk & 3) * 32) >> 4);
+            const uint64_t bd =
+                ti.grp ? dk_g + (uint64_t)((s * Lay::KV_BYTES + (kk >> 2) * 1024 + (kk & 3) * 32) >> 4)
+                       : dk + (uint64_t)((s * Lay::KV_BYTES + (kk >> 2) * Lay::KV_BLOCK + (kk & 3) * 32) >> 4);
+            umma_bf16(tmem + (uint32_t)(m * BN), a, bd, idS, kk > 0);
           }
-          if (!s_done) {
-            if (sm_ == 0 && s_rem == 0) {
-              if (piece_next(its, p, pcs)) {
-                ++s_qi;
-                s_rem = pcs.t1 - pcs.t0;
-                s_first = true;
-              } else {
-                s_done = true;
-              }
-            }
-            const int gk = gs, s = gk % STAGES, m = sm_, qb = s_qi % QBUF;
-            if (!s_done && (!s_first || mbar_test(&q_full[qb], (s_qi / QBUF) & 1)) &&
-                mbar_test(&k_full[s], (gk / STAGES) & 1) &&
-                (gk == 0 || mbar_test(&s_free[m], (gk - 1) & 1))) {
-              tc_fence_after();
-              const bool grp = p.pg_grouped && pcs.t1 - s_rem != 0;
+          umma_commit(&s_full[m]);
+          if (m == MT - 1) {
+            umma_commit(&k_empty[s]);
+            if (ti.last) umma_commit(&q_empty[qb]);
+          }
+          return true;
+        };
+        auto issue_pv = [&](const TileInfo &ti, int gk, int m) -> bool {
+          const int s = gk % STAGES;
+          if (!mbar_wait(&p_full[m], gk & 1, abort_flag, wlim)) return false;
+          // the first P V of a piece overwrites O: the previous piece's readout is done
+          if (m == 0 && ti.first && ti.qi > 0 && !mbar_wait(o_free, (ti.qi - 1) & 1, abort_flag, wlim))
+            return false;
+          if (m == 0 && !mbar_wait(&v_full[s], (gk / STAGES) & 1, abort_flag, wlim)) return false;
+          tc_fence_after();
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t a = dq + (uint64_t)((qb * Lay::Q_BYTES + (kk >> 2) * Lay::Q_BLOCK +
-                                                     m * kRows * 128 + (kk & 3) * 32) >> 4);
-                const uint64_t bd =
-                    grp ? dk_g + (uint64_t)((s * Lay::KV_BYTES + (kk >> 2) * 1024 + (kk & 3) * 32) >> 4)
-                        : dk + (uint64_t)((s * Lay::KV_BYTES + (kk >> 2) * Lay::KV_BLOCK + (kk & 3) * 32) >> 4);
-                umma_bf16(tmem + (uint32_t)(m * BN), a, bd, idS, kk > 0);
-              }
-              umma_commit(&s_full[m]);
-              if (m == 0) {
-                m_first[gk & 3] = s_first;
-                m_grp[gk & 3] = grp;
-                m_qi[gk & 3] = s_qi;
-              }
-              if (m == MT - 1) {
-                umma_commit(&k_empty[s]);
-                if (s_rem == 1) umma_commit(&q_empty[qb]);
-                s_first = false;
-                --s_rem;
-                ++gs;
-                sm_ = 0;
-              } else {
-                ++sm_;
-              }
-              prog = true;
-            }
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t bd =
+                ti.grp ? dv_g + (uint64_t)((s * Lay::KV_BYTES + kk * 2 * (Lay::KB * 1024)) >> 4)
+                       : dv + (uint64_t)((s * Lay::KV_BYTES + kk * 16 * 128) >> 4);
+            // 16 keys of P per MMA: 8 TMEM columns of bf16 pairs
+            umma_bf16_ts(tmem + (uint32_t)(Lay::S_COLS + m * D), tmem + (uint32_t)(m * BN + kk * 8), bd,
+                         idO, (!ti.first || kk > 0) ? 1u : 0u);
           }
-          if (s_done && gp == gs) break;
-          if (prog) {
-            idle_n = 0;
-            continue;
-          }
-          if (!idle()) break;
+          umma_commit(&s_free[m]);
+          if (m == MT - 1) umma_commit(&v_empty[s]);
+          return true;
+        };
+        TileInfo cur, nxt;
+        bool have = next_tile(cur);
+        bool ok = !have || (issue_qk(cur, 0, 0) && issue_qk(cur, 0, 1));
+        for (int gk = 0; ok && have; ++gk) {
+          const bool more = next_tile(nxt);
+          ok = issue_pv(cur, gk, 0) && (!more || issue_qk(nxt, gk + 1, 0)) && issue_pv(cur, gk, 1) &&
+               (!more || issue_qk(nxt, gk + 1, 1));
+          cur = nxt;
+          have = more;
         }
       } else {
         PieceIter its = it;  // S side of the walk over this CTA's tiles
