@@ -72,6 +72,82 @@ __device__ __forceinline__ float w_at(const RowPair<T> &r, int j, float c) {
   return fmaxf(pj - c * qj, 0.f);
 }
 
+// The 8 entries w_j = [p_j - c q_j]+ of group g (entries 8g .. 8g+7), each formed in
+// float exactly as w_at forms it, from 16-byte loads of the two rows.
+template <typename T>
+__device__ __forceinline__ void w_group(const RowPair<T> &r, int g, float c, float w[8]) {
+  constexpr int kv = Elem<T>::kVec;  // entries per 16-byte vector
+  float z[8], zq[8];
+#pragma unroll
+  for (int i = 0; i < 8 / kv; ++i)
+    Elem<T>::unpack(__ldg(reinterpret_cast<const uint4 *>(r.zt + (size_t)g * 8) + i), z + i * kv);
+  if (c != 0.f) {
+    if (r.zq != nullptr) {
+#pragma unroll
+      for (int i = 0; i < 8 / kv; ++i)
+        Elem<T>::unpack(__ldg(reinterpret_cast<const uint4 *>(r.zq + (size_t)g * 8) + i), zq + i * kv);
+    } else {
+      const float4 a = __ldg(reinterpret_cast<const float4 *>(r.qp + (size_t)g * 8));
+      const float4 b = __ldg(reinterpret_cast<const float4 *>(r.qp + (size_t)g * 8) + 1);
+      zq[0] = a.x, zq[1] = a.y, zq[2] = a.z, zq[3] = a.w;
+      zq[4] = b.x, zq[5] = b.y, zq[6] = b.z, zq[7] = b.w;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int j = g * 8 + i;
+    const float pj = kept<T>(z[i], j, r.sa) ? exp2f((z[i] - r.sa.zmax) * r.c_log2) * r.inv_sa : 0.f;
+    if (c == 0.f) {
+      w[i] = pj;
+      continue;
+    }
+    float qj;
+    if (r.zq != nullptr)
+      qj = kept<T>(zq[i], j, r.sq) ? exp2f((zq[i] - r.sq.zmax) * r.c_log2) * r.inv_sq : 0.f;
+    else
+      qj = zq[i];
+    w[i] = fmaxf(pj - c * qj, 0.f);
+  }
+}
+
+// A running sum carried as hi + lo of two floats: each addition is exact up to the
+// final rounding of hi + lo (Knuth's TwoSum), so the sum of float entries is as good as
+// a double accumulation, without the part's slow FP64 adds.
+struct SumF2 {
+  float hi = 0.f, lo = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float s = hi + x;
+    const float bb = s - hi;
+    lo += (hi - (s - bb)) + (x - bb);
+    hi = s;
+  }
+  __device__ __forceinline__ double value() const { return (double)hi + (double)lo; }
+};
+
+// This thread's sum of w over groups g0, g0 + stride, ... below g_end, two groups'
+// loads in flight at a time.
+template <typename T>
+__device__ __forceinline__ double w_sum(const RowPair<T> &r, int g0, int g_end, int stride, float c) {
+  SumF2 acc;
+  int g = g0;
+  for (; g + stride < g_end; g += 2 * stride) {
+    float a[8], b[8];
+    w_group<T>(r, g, c, a);
+    w_group<T>(r, g + stride, c, b);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc.add(a[i]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc.add(b[i]);
+  }
+  if (g < g_end) {
+    float a[8];
+    w_group<T>(r, g, c, a);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc.add(a[i]);
+  }
+  return acc.value();
+}
+
 // Sum over the CTA of one double per thread; every thread returns the same value (the
 // warp sums are added in warp order by each thread).
 __device__ __forceinline__ double block_sum_d(double v, double *sh) {
@@ -231,8 +307,7 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
       // the next sibling sees the residual [p - (c + n) q]+ / its mass
       const double c1 = c + n;
       const float c1f = (float)c1;
-      double part = 0.0;
-      for (int j = tid; j < V; j += kRecThreads) part += (double)w_at<T>(r, j, c1f);
+      const double part = w_sum<T>(r, tid, V / 8, kRecThreads, c1f);
       const double tot = block_sum_d(part, s_red);
       if (tot > kRecEntryErr * (1.0 + c1)) {
         c = c1;
@@ -252,7 +327,8 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
   }
 
   // ---- final sample: inverse CDF of w = [p - c_fin q]+ in token order, with u_smp(b, node)
-  const int CH = max(1024, ((V + kRecMaxChunks - 1) / kRecMaxChunks + 31) / 32 * 32);
+  // chunks of whole 256-entry warp steps (8 entries per lane)
+  const int CH = max(1024, ((V + kRecMaxChunks - 1) / kRecMaxChunks + 255) / 256 * 256);
   const int nch = (V + CH - 1) / CH;
   float cf = (float)c_fin;
   // the 1e-6 window in units of the normalised residual, or the rounding bound of the
@@ -260,10 +336,8 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
   const double tol = fmax(kRecNearTie * n, kRecEntryErr * (1.0 + c_fin));
   for (int attempt = 0; attempt < 2; ++attempt) {
     for (int k = warp; k < nch; k += kRecWarps) {
-      double s = 0.0;
-      const int j_end = min(V, (k + 1) * CH);
-      for (int j = k * CH + lane; j < j_end; j += 32) s += (double)w_at<T>(r, j, cf);
-      s = warp_sum_d(s);
+      const int g_end = min(V, (k + 1) * CH) / 8;
+      const double s = warp_sum_d(w_sum<T>(r, k * (CH / 8) + lane, g_end, 32, cf));
       if (lane == 0) s_chunk[k] = s;
     }
     __syncthreads();
