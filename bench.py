@@ -463,6 +463,105 @@ def lm_head_line(args, dist, K):
     }
 
 
+def next_rows_lines(args, dist, K, peak):
+    """The widened rows on synthetic inputs of the workloads' shapes, each timed with L2
+    flushed before every call (median of K): bytes are the rows each call must read at
+    least once, so GB/s is a lower bound of the achieved traffic.
+
+    F2 sibling-recursive tree acceptance and F3 typical acceptance: the medusa-t64 shapes
+    (B = 8, 64-node tree, V = 32000; target rows near the head rows, so paths get
+    accepted).  F3 top-p: the draft-chain shapes (B = 64, gamma = 5, V = 128256, T = 0.7,
+    top-k 50, top-p 0.9).  F4: prompt-lookup drafting over 256 histories of 8192 tokens,
+    and exact verification of its deterministic drafts (no q rows) at the ragged-paged
+    acceptance shapes (B = 256, gamma = 4, V = 152064)."""
+    import speculative_decoding_verify_sv_gb300 as sv
+    from speculative_decoding_verify_sv_gb300 import workloads as wl
+    dev = torch.device("cuda", dist.local_rank)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(flush.numel() // 4, dtype=torch.int32, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        for a, b in evs:
+            flush.zero_()
+            torch.sum(flush_read)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    def line(row, what, us, nbytes, extra=None):
+        gbs = nbytes / (us / 1e6) / 1e9
+        d = {"row": row, "workload": what, "us": us, "bytes": nbytes, "gbs": gbs,
+             "frac_of_hbm": gbs / peak}
+        d.update(extra or {})
+        return d
+
+    out = []
+    # F2 and F3 typical: medusa-t64 shapes
+    B, parent, V = 8, wl.TREE_T64, 32000
+    N = len(parent)
+    lg = wl.medusa_logits(B, parent, V, sigma=3.0, seed=77, coverage=True, coverage_sigma=0.7)
+    tl, q, nt = lg["target_logits"].to(dev), lg["draft_logits"].to(dev), lg["node_tokens"].to(dev)
+    Dq = q.shape[1]
+    ws = torch.empty(sv.sv_accept_workspace_size(B, N, V, Dq), dtype=torch.uint8, device=dev)
+    o_ind = sv.sv_accept_tree(sv.EXACT, tl, q, sv.Q_LOGITS, parent, nt, seed=3, workspace=ws)
+    o_rec = sv.sv_accept_tree_recursive(tl, q, sv.Q_LOGITS, parent, nt, seed=3, workspace=ws)
+    o_typ = sv.sv_accept_typical(tl, parent, nt, workspace=ws)
+    t_ind = timed(lambda: sv.sv_accept_tree(sv.EXACT, tl, q, sv.Q_LOGITS, parent, nt, seed=3,
+                                            outs=o_ind, workspace=ws))
+    t_rec = timed(lambda: sv.sv_accept_tree_recursive(tl, q, sv.Q_LOGITS, parent, nt, seed=3,
+                                                      outs=o_rec, workspace=ws))
+    t_typ = timed(lambda: sv.sv_accept_typical(tl, parent, nt, outs=o_typ, workspace=ws))
+    rows_b = B * (N + Dq) * V * tl.element_size()
+    out.append(line("F2", "sibling-recursive tree acceptance, medusa-t64 shapes", t_rec, rows_b,
+                    {"independent_rule_us": t_ind,
+                     "mean_accepted": float(o_rec["num_accepted"].float().mean())}))
+    out.append(line("F3", "typical acceptance, medusa-t64 shapes", t_typ, B * N * V * tl.element_size(),
+                    {"mean_accepted": float(o_typ["num_accepted"].float().mean())}))
+    del tl, q, nt, lg, ws
+    # F3 top-p: draft-chain shapes
+    B, gamma, V = 64, 5, 128256
+    g = torch.Generator(device=dev).manual_seed(78)
+    tl = (3.0 * torch.randn((B, gamma + 1, V), generator=g, device=dev)).to(torch.bfloat16)
+    dl = (tl[:, :gamma].float() + torch.randn((B, gamma, V), generator=g, device=dev)).to(torch.bfloat16)
+    toks = torch.argmax(dl.float(), dim=-1).to(torch.int32)
+    ws = torch.empty(sv.sv_accept_workspace_size(B, gamma + 1, V, gamma), dtype=torch.uint8, device=dev)
+    o = sv.sv_accept_chain(sv.EXACT, tl, dl, sv.Q_LOGITS, toks, temperature=0.7, top_k=50, top_p=0.9,
+                           seed=5, workspace=ws)
+    t_tp = timed(lambda: sv.sv_accept_chain(sv.EXACT, tl, dl, sv.Q_LOGITS, toks, temperature=0.7,
+                                            top_k=50, top_p=0.9, seed=5, outs=o, workspace=ws))
+    out.append(line("F3", "top-p 0.9 within top-k 50, T = 0.7, draft-chain shapes", t_tp,
+                    B * (2 * gamma + 1) * V * 2))
+    del tl, dl, toks, ws, o
+    # F4: drafting over histories, then verifying the deterministic drafts
+    B, L, gamma, V = 256, 8192, 4, 152064
+    hist = torch.randint(0, 32000, (B, L), generator=g, device=dev, dtype=torch.int32)
+    hist[:, L - 3:] = hist[:, 1000:1003]  # the last trigram occurs earlier: drafts exist
+    lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+    drafts, num = sv.sv_ngram_draft(hist, lens, max_ngram=3, min_ngram=1, gamma=gamma)
+    t_ng = timed(lambda: sv.sv_ngram_draft(hist, lens, max_ngram=3, min_ngram=1, gamma=gamma,
+                                           out=(drafts, num)))
+    out.append(line("F4", "prompt-lookup drafts, 256 histories of 8192 tokens, n = 3..1", t_ng,
+                    B * L * 4, {"mean_drafts": float(num.float().mean())}))
+    tl = (3.0 * torch.randn((B, gamma + 1, V), generator=g, device=dev)).to(torch.bfloat16)
+    ws = torch.empty(sv.sv_accept_workspace_size(B, gamma + 1, V, gamma), dtype=torch.uint8, device=dev)
+    o = sv.sv_accept_chain(sv.EXACT, tl, None, sv.Q_DRAFT_ONEHOT, drafts, seed=6, workspace=ws)
+    t_oh = timed(lambda: sv.sv_accept_chain(sv.EXACT, tl, None, sv.Q_DRAFT_ONEHOT, drafts, seed=6,
+                                            outs=o, workspace=ws))
+    out.append(line("F4", "exact verification of the drafts (q one-hot), ragged-paged acceptance shapes",
+                    t_oh, B * (gamma + 1) * V * 2))
+    del tl, ws, o, hist
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, dist: Dist):
     import speculative_decoding_verify_sv_gb300 as sv  # noqa: F401 (fails loudly if missing)
 
@@ -547,6 +646,7 @@ def run_ours(args, dist: Dist):
         result["per_workload"] = [per_workload_line(args, dist, i, K_pw, peak)
                                   for i in sorted(ALL_CONFIGS) if i != args.config]
         result["lm_head"] = lm_head_line(args, dist, K_pw)
+        result["next_rows"] = next_rows_lines(args, dist, K_pw, peak)
     return result
 
 
