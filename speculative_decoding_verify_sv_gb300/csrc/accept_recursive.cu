@@ -18,13 +18,19 @@
 // of the current node's target row and the depth's q row, and the final sample is one
 // inverse-CDF pass over w = [p - c q]+.
 //
-// One CTA per sequence walks the tree; thread 0 takes each decision in double from the
-// two logits at the candidate and the rows' statistics (kernel 1 of the acceptance);
-// the block sums the residual masses (each entry formed in float, summed in double).
-// The final sample: per-chunk sums of w by the warps, the chunk holding u * sum(w) found
-// by warp 0 from a scan of the chunk sums, then the token inside it by warp-wide
-// inclusive scans in token order.  No waits on other CTAs or on memory barriers: every
-// loop is bounded by the vocabulary or the tree size.
+// A thread-block cluster of C CTAs per sequence walks the tree, every CTA alike: thread 0
+// of each takes each decision in double from the two logits at the candidate and the
+// rows' statistics (kernel 1 of the acceptance), so all CTAs follow the same path.  Each
+// CTA owns a slice of the vocabulary: a residual mass is the sum of the CTAs' slice sums
+// (entries formed in float, summed exactly as float pairs, then in double), exchanged
+// through distributed shared memory and added in rank order, identically in every CTA.
+// The final sample: per-chunk sums of w in each slice, the slice holding u * sum(w) found
+// from the slice totals, then in that CTA the chunk (a scan of its chunk sums) and the
+// token inside it (warp-wide inclusive scans in token order).  The cluster barriers are
+// reached by every CTA (their branches depend only on values all CTAs compute alike); no
+// other wait: every loop is bounded by the vocabulary or the tree size.
+#include <atomic>
+
 #include "row_stat.cuh"
 #include "sv_common.cuh"
 #include "sv_internal.h"
@@ -35,7 +41,8 @@ namespace {
 
 constexpr int kRecThreads = 512;
 constexpr int kRecWarps = kRecThreads / 32;
-constexpr int kRecMaxChunks = 1024;  // chunk sums kept by a CTA (chunks >= 1024 entries)
+constexpr int kRecMaxChunks = 1024;  // chunk sums kept by a CTA
+constexpr int kRecMaxCluster = 16;   // CTAs per sequence
 constexpr double kRecNearTie = 1e-6;
 // Error bound of a residual mass formed here, in units of the target's probabilities:
 // each entry [p_j - c q_j]+ is formed in float from p_j and q_j that carry a few float
@@ -162,6 +169,54 @@ __device__ __forceinline__ double block_sum_d(double v, double *sh) {
   return t;
 }
 
+__device__ __forceinline__ unsigned rec_cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ unsigned rec_cluster_size() {
+  unsigned n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+__device__ __forceinline__ void rec_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// The same shared-memory variable in CTA `rank` of this cluster.
+__device__ __forceinline__ double ld_peer_d(const double *local, unsigned rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(remote) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_peer_i(int *local, unsigned rank, int v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+
+// The cluster-wide total of one double per CTA (v, as written to slot[k & 1] by the
+// caller's thread 0 before): after a cluster barrier warp 0 reads the C values, lane r
+// that of rank r, and sums them in a fixed order; every CTA gets the same total, also
+// each rank's value (in `mine` of lane r).  Slots alternate, so that the next write to a
+// slot follows the barrier after every peer's read of it.
+__device__ double cluster_total(double *slot, int k, unsigned C, double *s_bcast, double *lane_val) {
+  rec_cluster_sync();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    const double x = lane < (int)C ? ld_peer_d(&slot[k & 1], (unsigned)lane) : 0.0;
+    if (lane_val) *lane_val = x;
+    const double t = warp_sum_d(x);
+    if (lane == 0) *s_bcast = t;
+  }
+  __syncthreads();
+  const double t = *s_bcast;
+  __syncthreads();
+  return t;
+}
+
 __device__ __forceinline__ double warp_incl_scan_d(double v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -172,34 +227,48 @@ __device__ __forceinline__ double warp_incl_scan_d(double v) {
   return v;
 }
 
-// The decision on candidate child ch of the current node (thread 0 only), in double:
-// ratio = [p(x) - c q(x)]+ / (n q(x)).  Returns bit 0: accepted, bit 1: near tie.
+// What the decision on candidate child ch of the current node needs, in double: p(x) and
+// q(x) of its token x, and u_acc(b, ch).  Computed for all children of a node at once (one
+// thread each); flags: bit 0 the token is out of range, bit 1 q(x) = 0.
+struct ChildIn {
+  double px, qx, u;
+  int flags;
+};
 template <typename T>
-__device__ int decide_child(const AcceptParams &p, const RowPair<T> &r, int b, int ch, double c,
-                            double n, bool logits) {
+__device__ ChildIn child_inputs(const AcceptParams &p, const RowPair<T> &r, int b, int ch, bool logits) {
+  ChildIn ci{0.0, 0.0, 1.0, 0};
   const int x = p.tokens[(size_t)b * p.tok_stride + ch - p.tok_offset];
   if (x < 0 || x >= p.V) {
-    set_status(p.status, SV_DEV_BAD_TOKEN);
-    return 0;
+    ci.flags = 1;
+    return ci;
   }
   const double temp = (double)p.temperature;
   const float zp = Elem<T>::load(r.zt + x);
-  const double px =
-      kept<T>(zp, x, r.sa) ? exp(((double)zp - (double)r.sa.zmax) / temp) / (double)r.sa.S : 0.0;
-  double qx;
+  ci.px = kept<T>(zp, x, r.sa) ? exp(((double)zp - (double)r.sa.zmax) / temp) / (double)r.sa.S : 0.0;
   if (logits) {
     const float zq = Elem<T>::load(r.zq + x);
-    qx = kept<T>(zq, x, r.sq) ? exp(((double)zq - (double)r.sq.zmax) / temp) / (double)r.sq.S : 0.0;
+    ci.qx = kept<T>(zq, x, r.sq) ? exp(((double)zq - (double)r.sq.zmax) / temp) / (double)r.sq.S : 0.0;
   } else {
-    qx = (double)r.qp[x];
+    ci.qx = (double)r.qp[x];
   }
-  const double rx = fmax(px - c * qx, 0.0) / n;
+  if (!(ci.qx > 0.0)) ci.flags |= 2;
   uint32_t k_acc = 0u, k_smp = 0u;
   verify_uniform_ints(p.seed, p.round, b, ch, &k_acc, &k_smp);
-  const double u = ((double)k_acc + 0.5) * (1.0 / 16777216.0);
+  ci.u = ((double)k_acc + 0.5) * (1.0 / 16777216.0);
+  return ci;
+}
+
+// The decision on a child against the current residual [p - c q]+ / n (thread 0):
+// ratio = [p(x) - c q(x)]+ / (n q(x)).  Returns bit 0: accepted, bit 1: near tie.
+__device__ int decide_child(const AcceptParams &p, const ChildIn &ci, double c, double n) {
+  if (ci.flags & 1) {
+    set_status(p.status, SV_DEV_BAD_TOKEN);
+    return 0;
+  }
+  const double rx = fmax(ci.px - c * ci.qx, 0.0) / n;
   double ratio;
-  if (qx > 0.0) {
-    ratio = rx / qx;
+  if (ci.qx > 0.0) {
+    ratio = rx / ci.qx;
   } else {
     set_status(p.status, SV_DEV_ZERO_DRAFT_PROB);
     ratio = rx > 0.0 ? INFINITY : 0.0;
@@ -207,21 +276,36 @@ __device__ int decide_child(const AcceptParams &p, const RowPair<T> &r, int b, i
   // after a rejection (c > 0) the ratio divides by the float-formed residual mass n
   const double win =
       kRecNearTie + (c > 0.0 ? kRecEntryErr * (1.0 + c) / n * fmax(ratio, 1.0) : 0.0);
-  return (u < ratio ? 1 : 0) | (fabs(u - ratio) < win ? 2 : 0);
+  return (ci.u < ratio ? 1 : 0) | (fabs(ci.u - ratio) < win ? 2 : 0);
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const AcceptParams p) {
   __shared__ double s_red[kRecWarps];
   __shared__ double s_chunk[kRecMaxChunks];
-  __shared__ double s_total;
+  __shared__ double s_slot[2], s_bcast;
   __shared__ int s_dec, s_tok, s_near;
+  __shared__ ChildIn s_cin[kMaxNodes];
 
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned C = rec_cluster_size(), rank = rec_cluster_rank();
+  const int b = blockIdx.x / (int)C, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int N = p.tree.N, V = p.V;
   const bool logits = p.q_kind == SV_Q_LOGITS;
   const RowStat *tstat = p.stats + (size_t)b * N;
   const RowStat *qstat = p.stats + (size_t)p.B * N + (size_t)b * p.Dq;
+
+  // this CTA's slice of the vocabulary: chunks [ch_lo, ch_hi) of CH entries (whole 256-entry
+  // warp steps; at most kRecMaxChunks per CTA), in 8-entry groups [g_lo, g_hi)
+  const int ng = V / 8;
+  const int per_cta = (V + (int)C - 1) / (int)C;
+  const int CH = max(256, ((per_cta + kRecMaxChunks - 1) / kRecMaxChunks + 255) / 256 * 256);
+  const int CHG = CH / 8;
+  const int nch_all = (V + CH - 1) / CH;
+  const int ch_per = (nch_all + (int)C - 1) / (int)C;
+  const int ch_lo = min(nch_all, (int)rank * ch_per), ch_hi = min(nch_all, ch_lo + ch_per);
+  const int nloc = ch_hi - ch_lo;
+  const int g_lo = ch_lo * CHG, g_hi = min(ng, ch_hi * CHG);
+  int xk = 0;  // cluster exchanges so far (slot parity)
 
   // sequence b's tree (the shared one, or its own row, checked: a malformed row or a node
   // deeper than the q rows leaves the root alone, which draws the bonus from its p)
@@ -245,7 +329,7 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
     if (d > p.Dq) bad = true;
   }
   const bool seq_bad = __syncthreads_or(bad) != 0;
-  if (seq_bad && tid == 0) set_status(p.status, SV_DEV_BAD_TREE);
+  if (seq_bad && tid == 0 && rank == 0) set_status(p.status, SV_DEV_BAD_TREE);
   const int Nw = seq_bad ? 1 : N;  // nodes walked: the root alone for a bad tree
 
   // thread 0's running counts: near ties that can change a decision (near decisions,
@@ -288,11 +372,14 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
     } else {
       r.qp = static_cast<const float *>(p.q) + ((size_t)b * p.Dq + drow) * V;
     }
+    // every child's p(x), q(x) and u at once, one thread each
+    if (tid >= first && tid <= last && s_par[tid] == node) s_cin[tid] = child_inputs<T>(p, r, b, tid, logits);
+    __syncthreads();
     int next = -1;
     for (int ch = first; ch <= last; ++ch) {
       if (s_par[ch] != node) continue;
       if (tid == 0) {
-        const int d = decide_child<T>(p, r, b, ch, c, n, logits);
+        const int d = decide_child(p, s_cin[ch], c, n);
         near += (unsigned)(d >> 1);
         s_dec = d & 1;
       }
@@ -307,8 +394,9 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
       // the next sibling sees the residual [p - (c + n) q]+ / its mass
       const double c1 = c + n;
       const float c1f = (float)c1;
-      const double part = w_sum<T>(r, tid, V / 8, kRecThreads, c1f);
-      const double tot = block_sum_d(part, s_red);
+      const double part = block_sum_d(w_sum<T>(r, g_lo + tid, g_hi, kRecThreads, c1f), s_red);
+      if (tid == 0) s_slot[xk & 1] = part;
+      const double tot = cluster_total(s_slot, xk++, C, &s_bcast, nullptr);
       if (tot > kRecEntryErr * (1.0 + c1)) {
         c = c1;
         n = tot;
@@ -327,98 +415,109 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
   }
 
   // ---- final sample: inverse CDF of w = [p - c_fin q]+ in token order, with u_smp(b, node)
-  // chunks of whole 256-entry warp steps (8 entries per lane)
-  const int CH = max(1024, ((V + kRecMaxChunks - 1) / kRecMaxChunks + 255) / 256 * 256);
-  const int nch = (V + CH - 1) / CH;
   float cf = (float)c_fin;
   // the 1e-6 window in units of the normalised residual, or the rounding bound of the
   // float-formed w (kRecEntryErr per unit of the entries' magnitudes) when that is wider
   const double tol = fmax(kRecNearTie * n, kRecEntryErr * (1.0 + c_fin));
+  double total = 0.0, slice_tot = 0.0;  // slice_tot: rank `lane`'s slice total (warp 0)
   for (int attempt = 0; attempt < 2; ++attempt) {
-    for (int k = warp; k < nch; k += kRecWarps) {
-      const int g_end = min(V, (k + 1) * CH) / 8;
-      const double s = warp_sum_d(w_sum<T>(r, k * (CH / 8) + lane, g_end, 32, cf));
-      if (lane == 0) s_chunk[k] = s;
+    for (int k = warp; k < nloc; k += kRecWarps) {
+      const int kg = ch_lo + k;
+      const double sk = warp_sum_d(w_sum<T>(r, kg * CHG + lane, min(ng, (kg + 1) * CHG), 32, cf));
+      if (lane == 0) s_chunk[k] = sk;
     }
     __syncthreads();
     if (warp == 0) {
-      double s = 0.0;
-      for (int k = lane; k < nch; k += 32) s += s_chunk[k];
-      s = warp_sum_d(s);
-      if (lane == 0) s_total = s;
+      double sl = 0.0;
+      for (int k = lane; k < nloc; k += 32) sl += s_chunk[k];
+      sl = warp_sum_d(sl);
+      if (lane == 0) s_slot[xk & 1] = sl;
     }
     __syncthreads();
-    if (s_total > kRecEntryErr * (1.0 + (double)cf) || attempt == 1) break;
+    total = cluster_total(s_slot, xk++, C, &s_bcast, &slice_tot);
+    if (total > kRecEntryErr * (1.0 + (double)cf) || attempt == 1) break;
     // the residual has no mass: sample from the last residual itself
     if (tid == 0) ++near_smp;
     cf = (float)c;
-    __syncthreads();  // s_total and s_chunk are rewritten by the second attempt
+    __syncthreads();  // s_chunk is rewritten by the second attempt
   }
 
   if (warp == 0) {
     uint32_t k_acc = 0u, k_smp = 0u;
     verify_uniform_ints(p.seed, p.round, b, node, &k_acc, &k_smp);
     const double u = ((double)k_smp + 0.5) * (1.0 / 16777216.0);
-    // lane l owns chunks [l * per, (l + 1) * per): its sum, then a scan over the lanes
-    const int per = (nch + 31) / 32;
-    const int k0 = min(nch, lane * per), k1 = min(nch, k0 + per);
-    double ls = 0.0;
-    for (int k = k0; k < k1; ++k) ls += s_chunk[k];
-    const double incl = warp_incl_scan_d(ls);
-    const double total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    const double t = u * total;
-    unsigned hit = __ballot_sync(0xFFFFFFFFu, k1 > k0 && incl > t);
-    if (hit == 0u) {  // t at or past the end (rounding): start at the last lane with mass
-      const unsigned m = __ballot_sync(0xFFFFFFFFu, ls > 0.0);
+    // the slice holding u * sum(w): lane r holds rank r's slice total (the same in every
+    // CTA); the sum is the scan's end, as the prefixes are
+    const double sincl = warp_incl_scan_d(slice_tot);
+    const double t = u * __shfl_sync(0xFFFFFFFFu, sincl, 31);
+    unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < (int)C && sincl > t);
+    if (hit == 0u) {  // t at or past the end (rounding): the last slice with mass
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, lane < (int)C && slice_tot > 0.0);
       hit = m != 0u ? 1u << (31 - __clz(m)) : 1u;
     }
-    const int L = __ffs(hit) - 1;
-    // lane L finds its first chunk whose end passes t (else its last chunk)
-    int my_start = k1 - 1;
-    double my_base = incl - ls;
-    if (lane == L) {
-      for (int k = k0; k < k1; ++k) {
-        if (my_base + s_chunk[k] > t) {
-          my_start = k;
+    const int owner = __ffs(hit) - 1;
+    const double sbase = __shfl_sync(0xFFFFFFFFu, sincl - slice_tot, owner);
+    if ((int)rank == owner) {
+      // lane l owns local chunks [l * per, (l + 1) * per): its sum, then a scan over the lanes
+      const int per = (nloc + 31) / 32;
+      const int k0 = min(nloc, lane * per), k1 = min(nloc, k0 + per);
+      double ls = 0.0;
+      for (int k = k0; k < k1; ++k) ls += s_chunk[k];
+      const double incl = sbase + warp_incl_scan_d(ls);
+      unsigned hit2 = __ballot_sync(0xFFFFFFFFu, k1 > k0 && incl > t);
+      if (hit2 == 0u) {
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, ls > 0.0);
+        hit2 = m != 0u ? 1u << (31 - __clz(m)) : 1u;
+      }
+      const int L = __ffs(hit2) - 1;
+      // lane L finds its first chunk whose end passes t (else its last chunk)
+      int my_start = k1 - 1;
+      double my_base = incl - ls;
+      if (lane == L) {
+        for (int k = k0; k < k1; ++k) {
+          if (my_base + s_chunk[k] > t) {
+            my_start = k;
+            break;
+          }
+          if (k + 1 < k1) my_base += s_chunk[k];
+        }
+      }
+      const int start = max(0, __shfl_sync(0xFFFFFFFFu, my_start, L));
+      const double base = __shfl_sync(0xFFFFFFFFu, my_base, L);
+      // the token: warp-wide scans in token order from the start chunk to the slice end
+      const int j_end = min(V, g_hi * 8);
+      int tok = -1, last_pos = -1, nearf = 0;
+      double run = base;
+      for (int j0 = (ch_lo + start) * CH; j0 < j_end; j0 += 32) {
+        const int j = j0 + lane;
+        const double w = j < j_end ? (double)w_at<T>(r, j, cf) : 0.0;
+        const double ci = warp_incl_scan_d(w);
+        const double cum = run + ci, prev = cum - w;
+        const unsigned h = __ballot_sync(0xFFFFFFFFu, w > 0.0 && cum > t);
+        const unsigned pos = __ballot_sync(0xFFFFFFFFu, w > 0.0);
+        if (h != 0u) {
+          const int lh = __ffs(h) - 1;
+          const int nr = (t - prev < tol || cum - t < tol) ? 1 : 0;
+          nearf = __shfl_sync(0xFFFFFFFFu, nr, lh);
+          tok = j0 + lh;
           break;
         }
-        if (k + 1 < k1) my_base += s_chunk[k];
+        if (pos != 0u) last_pos = j0 + 31 - __clz(pos);
+        run += __shfl_sync(0xFFFFFFFFu, ci, 31);
       }
-    }
-    const int start = max(0, __shfl_sync(0xFFFFFFFFu, my_start, L));
-    const double base = __shfl_sync(0xFFFFFFFFu, my_base, L);
-    // the token: warp-wide scans in token order from the start chunk onwards
-    int tok = -1, last_pos = -1, nearf = 0;
-    double run = base;
-    for (int j0 = start * CH; j0 < V; j0 += 32) {
-      const int j = j0 + lane;
-      const double w = j < V ? (double)w_at<T>(r, j, cf) : 0.0;
-      const double ci = warp_incl_scan_d(w);
-      const double cum = run + ci, prev = cum - w;
-      const unsigned h = __ballot_sync(0xFFFFFFFFu, w > 0.0 && cum > t);
-      const unsigned pos = __ballot_sync(0xFFFFFFFFu, w > 0.0);
-      if (h != 0u) {
-        const int lh = __ffs(h) - 1;
-        const int nr = (t - prev < tol || cum - t < tol) ? 1 : 0;
-        nearf = __shfl_sync(0xFFFFFFFFu, nr, lh);
-        tok = j0 + lh;
-        break;
+      if (tok < 0) {  // rounding put u * sum(w) at or past the end: the last token with mass
+        tok = last_pos >= 0 ? last_pos : 0;
+        nearf = 1;
       }
-      if (pos != 0u) last_pos = j0 + 31 - __clz(pos);
-      run += __shfl_sync(0xFFFFFFFFu, ci, 31);
-    }
-    if (tok < 0) {  // rounding put u * sum(w) at or past the end: the last token with mass
-      tok = last_pos >= 0 ? last_pos : 0;
-      nearf = 1;
-    }
-    if (lane == 0) {
-      s_tok = tok;
-      s_near = nearf;
+      if (lane == 0) {  // to rank 0, which writes the outputs
+        st_peer_i(&s_tok, 0u, tok);
+        st_peer_i(&s_near, 0u, nearf);
+      }
     }
   }
-  __syncthreads();
+  rec_cluster_sync();  // the token is in rank 0's shared memory
 
-  if (tid == 0) {
+  if (tid == 0 && rank == 0) {
     near += nuc ? 1u : 0u;
     near_smp += (unsigned)s_near;
     const int W = p.tree.Dmax + 1;
@@ -441,10 +540,45 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
   }
 }
 
+// CTAs per sequence: the largest power of two up to kRecMaxCluster that keeps the grid
+// within one CTA per SM and each CTA's slice at least 2048 entries.
+int recursive_cluster(int B, int V, int num_sms) {
+  int C = 1;
+  while (C < kRecMaxCluster && (long long)B * C * 2 <= num_sms && V / (C * 2) >= 2048) C *= 2;
+  return C;
+}
+
 template <typename T>
 cudaError_t launch_recursive_typed(const AcceptParams &p, cudaStream_t s) {
-  accept_recursive_kernel<T><<<p.B, kRecThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  auto kern = accept_recursive_kernel<T>;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int C = recursive_cluster(p.B, p.V, sms);
+  if (C > 8) {
+    static std::atomic<int> big_ok[64];  // 0 untried, 1 allowed, 2 refused
+    const bool dev_ok = dev >= 0 && dev < 64;
+    if (dev_ok && big_ok[dev].load() == 0) {
+      const bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                      cudaSuccess;
+      cudaGetLastError();
+      big_ok[dev].store(ok ? 1 : 2);
+    }
+    if (!dev_ok || big_ok[dev].load() != 1) C = 8;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * C));
+  cfg.blockDim = dim3(kRecThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
