@@ -22,6 +22,7 @@
 // the vocabulary (long slices streamed through a shared-memory ring of bulk copies),
 // slice totals exchanged through distributed shared memory, then one warp of the CTA
 // whose slice holds the target finds the chunk and, in it, the inverse-CDF token.
+#include <atomic>
 #include <algorithm>
 #include <cfloat>
 #include <climits>
@@ -1616,14 +1617,15 @@ cudaError_t launch_select_kernel(AcceptParams pl, int C, cudaStream_t s) {
   cudaGetDevice(&dev);
   const bool dev_ok = dev >= 0 && dev < 64;
   if (C > 8) {
-    static bool big_ok[64] = {false}, tried[64] = {false};
-    if (dev_ok && !tried[dev]) {
-      tried[dev] = true;
-      big_ok[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-                    cudaSuccess;
+    // per device: 0 untried, 1 allowed, 2 refused (atomic: host threads may launch at once)
+    static std::atomic<int> big_ok[64];
+    if (dev_ok && big_ok[dev].load() == 0) {
+      const bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                      cudaSuccess;
       cudaGetLastError();
+      big_ok[dev].store(ok ? 1 : 2);
     }
-    if (!dev_ok || !big_ok[dev]) C = 8;
+    if (!dev_ok || big_ok[dev].load() != 1) C = 8;
   }
   size_t dyn = 0;
   if constexpr (RING) {
@@ -1632,13 +1634,13 @@ cudaError_t launch_select_kernel(AcceptParams pl, int C, cudaStream_t s) {
     const int per_cta = ((nvec + C - 1) / C + 31) / 32 * 32;
     pl.ring_stages = std::max(1, std::min(kRingStages, (per_cta + kRingVec - 1) / kRingVec));
     dyn = (size_t)pl.ring_stages * ring_stage_bytes<T>(pl.q_kind == SV_Q_PROBS_F32);
-    static bool attr_ok[64] = {false};
-    if (!dev_ok || !attr_ok[dev]) {
+    static std::atomic<bool> attr_ok[64];
+    if (!dev_ok || !attr_ok[dev].load()) {
       const cudaError_t e = cudaFuncSetAttribute(
           kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
           (int)((size_t)kRingStages * ring_stage_bytes<T>(true)));
       if (e != cudaSuccess) return e;
-      if (dev_ok) attr_ok[dev] = true;
+      if (dev_ok) attr_ok[dev].store(true);
     }
   }
   cudaLaunchConfig_t cfg = {};

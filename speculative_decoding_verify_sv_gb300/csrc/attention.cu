@@ -11,6 +11,7 @@
 // cp.async pipeline and both products run on bf16 tensor cores with fp32 accumulators
 // and an online softmax.  Splits of the prefix merge in a second kernel by
 // log-sum-exp weights.
+#include <atomic>
 #include <cfloat>
 
 #include "sv_common.cuh"
@@ -470,14 +471,14 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const AttnParams p) 
 template <int D>
 cudaError_t launch_f32(const AttnParams &p, cudaStream_t s) {
   const size_t smem = (size_t)f32_stages<D>() * f32_stage_floats<D>() * sizeof(float);
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load()) {
     const cudaError_t e = cudaFuncSetAttribute(attn_f32_kernel<D>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true);
   }
   dim3 grid((p.M + kThreads / 32 - 1) / (kThreads / 32), p.Hkv, p.B);
   attn_f32_kernel<D><<<grid, kThreads, smem, s>>>(p);
@@ -487,12 +488,14 @@ cudaError_t launch_f32(const AttnParams &p, cudaStream_t s) {
 template <int D>
 cudaError_t launch_mma(const AttnParams &p, cudaStream_t s) {
   const size_t smem = attn_smem_bytes<D>();
-  static bool attr_set = false;  // per process; the attribute is per device function
-  if (!attr_set) {
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true);
   }
   dim3 grid(p.m_tiles * p.splits, p.Hkv, p.B);
   attn_mma_kernel<D><<<grid, kThreads, smem, s>>>(p);

@@ -30,6 +30,7 @@
 // alternates between the M tiles (Q K^T of one while the other's softmax runs), no P
 // passes through shared memory, and the keys come in tiles of 128, so that Q (both M
 // tiles, 64 KB at D = 128) is read by the tensor core once per 128 keys.
+#include <atomic>
 #include <cudaTypedefs.h>
 
 #include <cfloat>
@@ -1367,14 +1368,14 @@ template <int D, int MT, int CP, int BN, int STAGES, int QBUF, int PBUF>
 cudaError_t launch_tc_typed(const TcParams &p, int grid, cudaStream_t s) {
   using Lay = TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>;
   static_assert(Lay::SMEM <= 232448, "shared memory layout exceeds 227 KB");
-  static bool attr[64] = {false};
+  static std::atomic<bool> attr[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr[dev]) {
+  if (dev < 0 || dev >= 64 || !attr[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, MT, CP, BN, STAGES, QBUF, PBUF>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::SMEM);
     if (e != cudaSuccess) return e;
-    attr[dev] = true;
+    if (dev >= 0 && dev < 64) attr[dev].store(true);
   }
   // all CTAs must be resident together: a CTA may wait for pieces of later CTAs
   cudaLaunchConfig_t cfg = {};

@@ -19,6 +19,7 @@
 // accumulators of 256 columns let the epilogue of one tile overlap the MMAs of the next.
 // Tiles are numbered rows-fastest, so the CTAs that read the same W tile run at the same
 // time and W comes from HBM about once.  Every wait is bounded (SV_DEV_TIMEOUT).
+#include <atomic>
 #include <cudaTypedefs.h>
 
 #include <cfloat>
@@ -311,13 +312,13 @@ cudaError_t launch_lm_head(const void *hidden, const void *weight, int R, int Dm
   p.mtiles = (R + kBM - 1) / kBM;
   p.ntiles = (V + kBN - 1) / kBN;
   p.c_log2 = c_log2;
-  static bool attr[64] = {false};
+  static std::atomic<bool> attr[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr[dev]) {
+  if (dev < 0 || dev >= 64 || !attr[dev].load()) {
     const cudaError_t e = cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    attr[dev] = true;
+    if (dev >= 0 && dev < 64) attr[dev].store(true);
   }
   const int tiles = p.mtiles * p.ntiles;
   const int grid = tiles < num_sms ? tiles : num_sms;

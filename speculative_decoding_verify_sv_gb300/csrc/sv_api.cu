@@ -62,7 +62,7 @@ unsigned int *status_word() {
 }
 
 int num_sms() {
-  static int sms[kMaxDevices] = {0};
+  static std::atomic<int> sms[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
