@@ -22,8 +22,8 @@
 // the vocabulary (long slices streamed through a shared-memory ring of bulk copies),
 // slice totals exchanged through distributed shared memory, then one warp of the CTA
 // whose slice holds the target finds the chunk and, in it, the inverse-CDF token.
-#include <atomic>
 #include <algorithm>
+#include <atomic>
 #include <cfloat>
 #include <climits>
 
