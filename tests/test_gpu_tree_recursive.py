@@ -53,6 +53,18 @@ def test_chain_large_vocab(cuda_ok):
     assert sv.sv_read_device_status() == 0
 
 
+def test_tree_sixteen_cta_cluster(cuda_ok):
+    """Eight sequences of a 26-node tree with 131072-entry rows: each sequence runs on a
+    cluster of 16 CTAs (slices of 8192 entries), so the residual masses and the final
+    sample's slice totals cross 16 CTAs."""
+    B, parent, V = 8, wl.TREE_T26, 131072
+    lg = wl.medusa_logits(B, parent, V, sigma=3.0, seed=41, coverage=True, coverage_sigma=0.7)
+    out, ref = _run(lg["target_logits"], lg["draft_logits"], sv.Q_LOGITS, parent, lg["node_tokens"],
+                    seed=21, round_=2)
+    _compare(out, ref, KEYS, max_exempt_frac=0.25, max_sample_frac=0.5)
+    assert sv.sv_read_device_status() == 0
+
+
 @pytest.mark.parametrize("parent", [wl.TREE_T26, wl.TREE_T64, wl.TREE_EXAMPLE7])
 def test_medusa_trees(cuda_ok, parent):
     B = 64
