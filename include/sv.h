@@ -235,7 +235,8 @@ sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
  * handed to a sibling with no mass (or less than that error bound) and one near top-p
  * cut on a visited row; and as sample ties a final sample within 1e-6 of a CDF boundary
  * (in units of the normalised residual, or the error bound when wider) or with an empty
- * residual.  Launches: the statistics kernel, then one CTA per sequence. */
+ * residual.  Launches: the statistics kernel, then one thread-block cluster of up to 16
+ * CTAs per sequence (each on a slice of the vocabulary). */
 sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const int32_t *parent,
                                    int parent_stride,
                                    const int32_t *node_tokens, const void *target_logits,
