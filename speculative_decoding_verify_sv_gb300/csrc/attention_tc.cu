@@ -624,9 +624,10 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
             for (int row = lane; row < kRows; row += 32) {
               // 16-byte unit i of row r at r * (D / 4) + (i ^ (r % (D / 4))): a warp reading
               // one unit of 32 rows meets no bank conflict
-              const float4 *src = reinterpret_cast<const float4 *>(p.part_o + ((size_t)sl0 * kRows + row) * D);
+              // (partial O is stored by 16-byte unit: unit i of all rows, then unit i + 1)
+              const float4 *src = reinterpret_cast<const float4 *>(p.part_o) + (size_t)sl0 * (D / 4) * kRows + row;
               for (int i = 0; i < D / 4; ++i)
-                cp_async_16(stage + (size_t)row * (D / 4) + (i ^ (row % (D / 4))), src + i, true);
+                cp_async_16(stage + (size_t)row * (D / 4) + (i ^ (row % (D / 4))), src + (size_t)i * kRows, true);
               cp_async_8(mls + row, p.part_ml + ((size_t)sl0 * kRows + row) * 2);
             }
             cp_async_mbar_arrive(stage_full);
@@ -1264,7 +1265,12 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           stage = reinterpret_cast<float4 *>(sK) + (size_t)R_local * (D / 4);
         __syncwarp();  // tcgen05.ld below is warp-collective
         const long long slot = pc.unit + blockIdx.x;
-        float *pdst = p.part_o + ((size_t)slot * ROWS + R_local) * D;
+        // partial O by 16-byte unit (unit i of all ROWS rows, then unit i + 1): a warp's
+        // stores and loads of one unit cover 32 consecutive rows, 512 contiguous bytes
+        float4 *pdst = reinterpret_cast<float4 *>(p.part_o) + (size_t)slot * (D / 4) * ROWS + R_local;
+        auto punit = [&](long long sl, int i) -> const float4 * {
+          return reinterpret_cast<const float4 *>(p.part_o) + ((size_t)sl * (D / 4) + i) * ROWS + R_local;
+        };
 #pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
           float4 cur[8];
@@ -1279,8 +1285,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           if (pc.t0 > 0) {
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
-              *reinterpret_cast<float4 *>(pdst + ch * 32 + c4 * 4) =
-                  make_float4(o[c4 * 4], o[c4 * 4 + 1], o[c4 * 4 + 2], o[c4 * 4 + 3]);
+              pdst[(size_t)(ch * 8 + c4) * ROWS] = make_float4(o[c4 * 4], o[c4 * 4 + 1], o[c4 * 4 + 2], o[c4 * 4 + 3]);
             continue;
           }
           if (head) {
@@ -1300,11 +1305,9 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
 #pragma unroll
             for (int k = stage ? 1 : 0; k < kPre; ++k) {
               if (k < np) {
-                const float4 *src =
-                    reinterpret_cast<const float4 *>(p.part_o + ((size_t)pslot[k] * ROWS + R_local) * D + ch * 32);
                 float4 x[8];
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) x[c4] = __ldcg(src + c4);
+                for (int c4 = 0; c4 < 8; ++c4) x[c4] = __ldcg(punit(pslot[k], ch * 8 + c4));
                 add(pw[k], x);
               }
             }
@@ -1314,10 +1317,9 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
                 const size_t row = (size_t)sl * ROWS + R_local;
                 const float m2 = __ldcg(p.part_ml + row * 2);
                 if (m2 == -INFINITY) return true;
-                const float4 *src = reinterpret_cast<const float4 *>(p.part_o + row * D + ch * 32);
                 float4 x[8];
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) x[c4] = __ldcg(src + c4);
+                for (int c4 = 0; c4 < 8; ++c4) x[c4] = __ldcg(punit(sl, ch * 8 + c4));
                 add(exp2f(m2 - m_ref), x);
                 return true;
               });
