@@ -239,8 +239,7 @@ __device__ __noinline__ bool idle_piece(int N, int t0, int n, bool publish, int 
     __syncwarp();
     if (lane == 0) mbar_arrive(&p_full[Lay::PT ? mt : pb]);
   }
-  if (publish) {
-    __threadfence();
+  if (publish) {  // (nothing written: the arrival only completes the barrier)
     __syncwarp();
     if (lane == 0) mbar_arrive(pub);
   }
@@ -1341,8 +1340,9 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         }
       }
       if (pc.t0 > 0) {
-        // publish this piece once every softmax warp has written its rows
-        __threadfence();
+        // publish this piece once every softmax warp has written its rows: the arrivals
+        // (release, CTA scope) order each warp's writes before thread 0's wait, and thread
+        // 0's fence and release store make them visible with the flag (cumulatively)
         __syncwarp();
         if (lane == 0) mbar_arrive(pub);
         if (threadIdx.x == 0 && mbar_wait(pub, 0, abort_flag, wlim)) {
