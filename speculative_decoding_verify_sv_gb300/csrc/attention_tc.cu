@@ -1339,6 +1339,11 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           ml[1] = l;
         }
       }
+      // O has been read out of TMEM: the next piece's P V may overwrite it (before the
+      // publication below, which touches global memory only)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
       if (pc.t0 > 0) {
         // publish this piece once every softmax warp has written its rows: the arrivals
         // (release, CTA scope) order each warp's writes before thread 0's wait, and thread
@@ -1350,9 +1355,6 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           st_release_u64(p.flags + pc.unit + blockIdx.x, epoch);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
       g += n;
       ++qi;
     }
