@@ -155,20 +155,6 @@ __device__ __forceinline__ double w_sum(const RowPair<T> &r, int g0, int g_end, 
   return acc.value();
 }
 
-// Sum over the CTA of one double per thread; every thread returns the same value (the
-// warp sums are added in warp order by each thread).
-__device__ __forceinline__ double block_sum_d(double v, double *sh) {
-  v = warp_sum_d(v);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) sh[warp] = v;
-  __syncthreads();
-  double t = 0.0;
-#pragma unroll
-  for (int i = 0; i < kRecWarps; ++i) t += sh[i];
-  __syncthreads();  // sh may be rewritten by the next call
-  return t;
-}
-
 __device__ __forceinline__ unsigned rec_cluster_rank() {
   unsigned r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -197,24 +183,28 @@ __device__ __forceinline__ void st_peer_i(int *local, unsigned rank, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
 }
 
-// The cluster-wide total of one double per CTA (v, as written to slot[k & 1] by the
-// caller's thread 0 before): after a cluster barrier warp 0 reads the C values, lane r
-// that of rank r, and sums them in a fixed order; every CTA gets the same total, also
-// each rank's value (in `mine` of lane r).  Slots alternate, so that the next write to a
-// slot follows the barrier after every peer's read of it.
-__device__ double cluster_total(double *slot, int k, unsigned C, double *s_bcast, double *lane_val) {
-  rec_cluster_sync();
+// The cluster-wide sum of one double per thread (v): each warp's sum goes to
+// parts[k & 1][warp]; after one cluster barrier warp 0 of every CTA reads all C ranks'
+// warp sums (lane r those of rank r, added in warp order) and sums the ranks in a fixed
+// order, so every CTA gets the same total; lane r of warp 0 also gets rank r's total in
+// *lane_val.  The slots alternate with k (and so does the broadcast), so that a slot is
+// rewritten only after the next cluster barrier, which every peer reaches after its reads.
+__device__ double cluster_sum(double v, double (*parts)[kRecWarps], double *bcast, int k, unsigned C,
+                              double *lane_val) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum_d(v);
+  if (lane == 0) parts[k & 1][warp] = v;
+  rec_cluster_sync();  // (also orders this CTA's writes of parts before warp 0's reads)
   if (warp == 0) {
-    const double x = lane < (int)C ? ld_peer_d(&slot[k & 1], (unsigned)lane) : 0.0;
+    double x = 0.0;
+    if (lane < (int)C)
+      for (int w = 0; w < kRecWarps; ++w) x += ld_peer_d(&parts[k & 1][w], (unsigned)lane);
     if (lane_val) *lane_val = x;
     const double t = warp_sum_d(x);
-    if (lane == 0) *s_bcast = t;
+    if (lane == 0) bcast[k & 1] = t;
   }
   __syncthreads();
-  const double t = *s_bcast;
-  __syncthreads();
-  return t;
+  return bcast[k & 1];
 }
 
 __device__ __forceinline__ double warp_incl_scan_d(double v) {
@@ -281,10 +271,10 @@ __device__ int decide_child(const AcceptParams &p, const ChildIn &ci, double c, 
 
 template <typename T>
 __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const AcceptParams p) {
-  __shared__ double s_red[kRecWarps];
   __shared__ double s_chunk[kRecMaxChunks];
-  __shared__ double s_slot[2], s_bcast;
-  __shared__ int s_dec, s_tok, s_near;
+  __shared__ double s_parts[2][kRecWarps], s_bcast[2];
+  __shared__ int s_dec[2], s_tok, s_near;
+  int ndec = 0;  // decisions so far (parity of the s_dec slot)
   __shared__ ChildIn s_cin[kMaxNodes];
 
   const unsigned C = rec_cluster_size(), rank = rec_cluster_rank();
@@ -381,11 +371,12 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
       if (tid == 0) {
         const int d = decide_child(p, s_cin[ch], c, n);
         near += (unsigned)(d >> 1);
-        s_dec = d & 1;
+        s_dec[ndec & 1] = d & 1;
       }
       __syncthreads();
-      const int acc = s_dec;
-      __syncthreads();  // s_dec is rewritten only after every thread has read it
+      // (two slots: a slot is rewritten two decisions later, past another barrier)
+      const int acc = s_dec[ndec & 1];
+      ++ndec;
       if (acc) {
         next = ch;
         break;
@@ -394,9 +385,8 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
       // the next sibling sees the residual [p - (c + n) q]+ / its mass
       const double c1 = c + n;
       const float c1f = (float)c1;
-      const double part = block_sum_d(w_sum<T>(r, g_lo + tid, g_hi, kRecThreads, c1f), s_red);
-      if (tid == 0) s_slot[xk & 1] = part;
-      const double tot = cluster_total(s_slot, xk++, C, &s_bcast, nullptr);
+      const double tot = cluster_sum(w_sum<T>(r, g_lo + tid, g_hi, kRecThreads, c1f), s_parts, s_bcast,
+                                     xk++, C, nullptr);
       if (tot > kRecEntryErr * (1.0 + c1)) {
         c = c1;
         n = tot;
@@ -421,20 +411,14 @@ __global__ void __launch_bounds__(kRecThreads) accept_recursive_kernel(const Acc
   const double tol = fmax(kRecNearTie * n, kRecEntryErr * (1.0 + c_fin));
   double total = 0.0, slice_tot = 0.0;  // slice_tot: rank `lane`'s slice total (warp 0)
   for (int attempt = 0; attempt < 2; ++attempt) {
+    double wpart = 0.0;  // this warp's chunks (every lane holds it)
     for (int k = warp; k < nloc; k += kRecWarps) {
       const int kg = ch_lo + k;
       const double sk = warp_sum_d(w_sum<T>(r, kg * CHG + lane, min(ng, (kg + 1) * CHG), 32, cf));
       if (lane == 0) s_chunk[k] = sk;
+      wpart += sk;
     }
-    __syncthreads();
-    if (warp == 0) {
-      double sl = 0.0;
-      for (int k = lane; k < nloc; k += 32) sl += s_chunk[k];
-      sl = warp_sum_d(sl);
-      if (lane == 0) s_slot[xk & 1] = sl;
-    }
-    __syncthreads();
-    total = cluster_total(s_slot, xk++, C, &s_bcast, &slice_tot);
+    total = cluster_sum(lane == 0 ? wpart : 0.0, s_parts, s_bcast, xk++, C, &slice_tot);
     if (total > kRecEntryErr * (1.0 + (double)cf) || attempt == 1) break;
     // the residual has no mass: sample from the last residual itself
     if (tid == 0) ++near_smp;
