@@ -60,9 +60,12 @@ constexpr float kNearTieF = 1e-6f;
 // sums and prefixes that need more than float precision (the inverse-CDF search) carry
 // a value as an unevaluated sum hi + lo of two floats (Knuth's TwoSum, then a
 // renormalising Fast2Sum): about 2^-44 relative, from a few FP32 operations.
-struct F2 {
+// 8-byte aligned: a pair is read from a peer CTA's shared memory as one 64-bit load
+// (ld.shared::cluster.v2.f32), which faults on a 4-byte boundary
+struct __align__(8) F2 {
   float hi, lo;
 };
+static_assert(sizeof(F2) == 8 && alignof(F2) == 8, "one 64-bit word per pair");
 __device__ __forceinline__ F2 f2(float x) { return F2{x, 0.f}; }
 __device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
   const float s = a.hi + b.hi;
