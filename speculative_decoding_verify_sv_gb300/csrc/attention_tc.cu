@@ -13,12 +13,15 @@
 // them with log-sum-exp weights in the same launch (cooperative, so all CTAs are resident).
 //
 // Per CTA, warp roles:
-//   producer warp   TMA loads of Q (per piece) and K/V tiles into a STAGES-deep ring;
+//   producer warp   TMA loads of Q (per piece) and K/V tiles into rings of STAGES K and
+//                   VST V stages (a single M tile with one P buffer spends the second
+//                   P buffer's room on a third V stage: V is held until P V completes,
+//                   K only until S = Q K^T does);
 //   MMA warp        one thread issues P V as soon as P is written and keeps S = Q K^T
 //                   two tiles ahead (S in TMEM, double buffered; O accumulates in TMEM);
 //   4*MT softmax warps, one thread per query row: read S from TMEM, mask, online
-//                   softmax in log2 units, write P (bf16, 128B-swizzled, double
-//                   buffered) to shared memory, rescale O in TMEM only when the running
+//                   softmax in log2 units, write P (bf16, 128B-swizzled, PBUF
+//                   buffers) to shared memory, rescale O in TMEM only when the running
 //                   max grows by more than 2^8, and write the normalised row at the end.
 // When all query rows fit in 128/CP lanes (CP = 2 or 4 row copies), the rows are
 // loaded CP times into the A tile so that every TMEM lane quarter, and so every SM
@@ -77,12 +80,14 @@ struct TcLayout {
   static constexpr int P_BYTES = PT ? 0 : MT * P_TILE;   // one P buffer (PBUF are used)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + QBUF * Q_BYTES;
+  // V stages: one more than K's when a single M tile keeps one P buffer
+  static constexpr int VST = (MT == 1 && PBUF == 1) ? STAGES + 1 : STAGES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + VST * KV_BYTES;
   static constexpr int OFF_BAR = OFF_P + PBUF * P_BYTES;
-  // k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], s_free[2], p_full[2], p_free[2], o_free, drain,
+  // k_full[S], k_empty[S], v_full[VST], v_empty[VST], s_full[2], s_free[2], p_full[2], p_free[2], o_free, drain,
   // xch_full[2], xl_full, pub, q_full[QBUF], q_empty[QBUF], stage_full (one M tile only)
-  static constexpr int NBAR = 4 * STAGES + 14 + 2 * QBUF + (MT == 1 ? 1 : 0);
+  static constexpr int NBAR = 2 * STAGES + 2 * VST + 14 + 2 * QBUF + (MT == 1 ? 1 : 0);
   // row copies exchange partial row maxima [2][4][32] and row sums [4][32] (f32)
   static constexpr int OFF_XCH = OFF_BAR + NBAR * 8;
   static constexpr int OFF_XL = OFF_XCH + (CP > 1 ? 2 * 4 * 32 * 4 : 0);
@@ -205,7 +210,7 @@ __device__ __forceinline__ long long block_scan(long long x, long long *red, lon
 // the previous phase of its barrier to be complete, since no write of this warp orders
 // it (with P in TMEM the wait for S of M tile mt orders it).  Kept out of line so that
 // the row loop's code stays small.  False if a wait gave up.
-template <class Lay, int BN, int STAGES, int PBUF>
+template <class Lay, int BN, int PBUF>
 __device__ __noinline__ bool idle_piece(int N, int t0, int n, bool publish, int g, int qi, int L,
                                         bool grouped, int mt,
                                         uint64_t *s_full, uint64_t *s_free, uint64_t *v_full,
@@ -213,7 +218,7 @@ __device__ __noinline__ bool idle_piece(int N, int t0, int n, bool publish, int 
                                         volatile int *abort_flag, unsigned long long wlim) {
   const int lane = threadIdx.x & 31;
   for (int k = 0; k < n; ++k) {
-    const int gk = g + k, j = gk & 1, s = gk % STAGES, t = t0 + k, pb = gk % PBUF;
+    const int gk = g + k, j = gk & 1, s = gk % Lay::VST, t = t0 + k, pb = gk % PBUF;
     if constexpr (Lay::PT) {
       if (!mbar_wait(&s_full[mt], gk & 1, abort_flag, wlim)) return false;
     } else {
@@ -224,7 +229,7 @@ __device__ __noinline__ bool idle_piece(int N, int t0, int n, bool publish, int 
     const int nvalid = t == 0 ? N : min(BN, L - (t - 1) * BN);
     // this warp's share of zeroing the V tail (see the row loop)
     if (t != 0 && nvalid < BN && (!Lay::PT || mt == 0)) {
-      if (!mbar_wait(&v_full[s], (gk / STAGES) & 1, abort_flag, wlim)) return false;
+      if (!mbar_wait(&v_full[s], (gk / Lay::VST) & 1, abort_flag, wlim)) return false;
       uint8_t *vt = sV + s * Lay::KV_BYTES;
       constexpr int per_row = Lay::KB * 8;
       constexpr int stride = 32 * (Lay::PT ? 4 : Lay::NSW);
@@ -287,9 +292,10 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::OFF_BAR);
   uint64_t *k_full = bars;
   uint64_t *k_empty = bars + STAGES;
+  constexpr int VST = Lay::VST;
   uint64_t *v_full = bars + 2 * STAGES;
-  uint64_t *v_empty = bars + 3 * STAGES;
-  uint64_t *s_full = bars + 4 * STAGES;
+  uint64_t *v_empty = bars + 2 * STAGES + VST;
+  uint64_t *s_full = bars + 2 * STAGES + 2 * VST;
   uint64_t *s_free = s_full + 2;
   uint64_t *p_full = s_free + 2;
   uint64_t *p_free = p_full + 2;
@@ -376,11 +382,13 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
   if (threadIdx.x < kMaxNodes)
     sPar[threadIdx.x] = threadIdx.x < p.tree.N ? (int)p.tree.parent[threadIdx.x] : -1;
   if (threadIdx.x == 0) {
+    for (int i = 0; i < VST; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
     }
     // with P in TMEM, index j is the M tile: S[j] full and free (its P V done) are MMA
     // commits, P[j] written is the arrival of that M tile's four softmax warps
@@ -464,10 +472,11 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       return __shfl_sync(0xFFFFFFFFu, r, 0) != 0;
     };
     auto load = [&](const Src &src, int gi, bool is_v) -> bool {
-      const int s = gi % STAGES;
+      const int NS = is_v ? VST : STAGES;
+      const int s = gi % NS;
       uint64_t *full = is_v ? &v_full[s] : &k_full[s];
-      if (gi >= STAGES &&
-          !wait_all(is_v ? &v_empty[s] : &k_empty[s], ((gi / STAGES) - 1) & 1))
+      if (gi >= NS &&
+          !wait_all(is_v ? &v_empty[s] : &k_empty[s], ((gi / NS) - 1) & 1))
         return false;
       uint8_t *dst = (is_v ? sV : sK) + s * Lay::KV_BYTES;
       const CUtensorMap *map =
@@ -644,7 +653,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           }
       };
       settle(k_full, g, STAGES);
-      settle(v_full, gv, STAGES);
+      settle(v_full, gv, VST);
       settle(q_full, nq, QBUF);
     }
     // this lane's staging copies (a split unit's partial rows) land before the CTA retires,
@@ -741,12 +750,12 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
           return true;
         };
         auto issue_pv = [&](const TileInfo &ti, int gk, int m) -> bool {
-          const int s = gk % STAGES;
+          const int s = gk % VST;
           if (!mbar_wait(&p_full[m], gk & 1, abort_flag, wlim)) return false;
           // the first P V of a piece overwrites O: the previous piece's readout is done
           if (m == 0 && ti.first && ti.qi > 0 && !mbar_wait(o_free, (ti.qi - 1) & 1, abort_flag, wlim))
             return false;
-          if (m == 0 && !mbar_wait(&v_full[s], (gk / STAGES) & 1, abort_flag, wlim)) return false;
+          if (m == 0 && !mbar_wait(&v_full[s], (gk / VST) & 1, abort_flag, wlim)) return false;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
@@ -781,13 +790,13 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         while (true) {
           bool prog = false;
           if (gp < gs) {
-            const int gk = gp, s = gk % STAGES, pb = gk % PBUF;
+            const int gk = gp, s = gk % VST, pb = gk % PBUF;
             const bool first = m_first[gk & 3];
             const bool grp = m_grp[gk & 3];
             const int qi = m_qi[gk & 3];
             if (mbar_test(&p_full[pb], (gk / PBUF) & 1) &&
                 (!first || qi == 0 || mbar_test(o_free, (qi - 1) & 1)) &&
-                mbar_test(&v_full[s], (gk / STAGES) & 1)) {
+                mbar_test(&v_full[s], (gk / VST) & 1)) {
               tc_fence_after();
 #pragma unroll
               for (int m = 0; m < MT; ++m) {
@@ -915,7 +924,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       const bool warp_idle = CP == 1 && __all_sync(0xFFFFFFFFu, !valid_row);
       const int L = clamp_len(p, pc.b);
       if (warp_idle) {  // every row of this warp is padding: barriers only
-        if (!idle_piece<Lay, BN, STAGES, PBUF>(p.N, pc.t0, n, pc.t0 > 0, g, qi, L, p.pg_grouped != 0, mt,
+        if (!idle_piece<Lay, BN, PBUF>(p.N, pc.t0, n, pc.t0 > 0, g, qi, L, p.pg_grouped != 0, mt,
                                               s_full, s_free, v_full,
                                               p_full, o_free, pub, sV, abort_flag, wlim)) {
           ok = false;
@@ -927,7 +936,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
       }
       float m_ref = -INFINITY, l = 0.f;
       for (int k = 0; k < n; ++k) {
-        const int gk = g + k, j = gk & 1, s = gk % STAGES, t = pc.t0 + k, pb = gk % PBUF;
+        const int gk = g + k, j = gk & 1, s = gk % VST, t = pc.t0 + k, pb = gk % PBUF;
         const bool tree = t == 0;
         const int nvalid = tree ? p.N : min(BN, L - (t - 1) * BN);
         // S of this tile: buffer j, or (P in TMEM) this M tile's region, one phase per tile
@@ -942,7 +951,7 @@ __global__ void __launch_bounds__(TcLayout<D, MT, CP, BN, STAGES, QBUF, PBUF>::T
         // TMEM, by the warps of M tile 0, whose P V is issued first.
         auto zero_v_tail = [&]() -> bool {
           if (tree || nvalid >= BN || (Lay::PT && mt != 0)) return true;
-          if (!mbar_wait(&v_full[s], (gk / STAGES) & 1, abort_flag, wlim)) return false;
+          if (!mbar_wait(&v_full[s], (gk / VST) & 1, abort_flag, wlim)) return false;
           uint8_t *vt = sV + s * Lay::KV_BYTES;
           constexpr int per_row = Lay::KB * 8;
           constexpr int stride = 32 * (Lay::PT ? 4 : NSW);
@@ -1536,12 +1545,13 @@ cudaError_t launch_attention_tc(const AttnParams &a, const TcPlan &pl, void *ws,
   p.tree = a.tree;
   p.wait_ns = a.wait_ns;
   if (a.D == 128) {
-    // (two Q buffers paid for with one P buffer measured slower: the softmax then
-    // waits for every P V before writing the next P)
+    // One M tile: one P buffer, its room spent on a third V stage (ragged-paged 763 us
+    // against 775 with two P buffers; the other shapes time the same).  Two Q buffers paid
+    // for with the P buffer measured slower (the Q load is not the late one).
     if (pl.MT == 2) return launch_tc_typed<128, 2, 1, 128, 2, 1, 1>(p, pl.grid, s);
-    if (pl.CP == 4) return launch_tc_typed<128, 1, 4, 128, 2, 1, 2>(p, pl.grid, s);
-    if (pl.CP == 2) return launch_tc_typed<128, 1, 2, 128, 2, 1, 2>(p, pl.grid, s);
-    return launch_tc_typed<128, 1, 1, 128, 2, 1, 2>(p, pl.grid, s);
+    if (pl.CP == 4) return launch_tc_typed<128, 1, 4, 128, 2, 1, 1>(p, pl.grid, s);
+    if (pl.CP == 2) return launch_tc_typed<128, 1, 2, 128, 2, 1, 1>(p, pl.grid, s);
+    return launch_tc_typed<128, 1, 1, 128, 2, 1, 1>(p, pl.grid, s);
   }
   if (pl.MT == 2) return launch_tc_typed<64, 2, 1, 128, 4, 2, 1>(p, pl.grid, s);
   if (pl.CP == 4) return launch_tc_typed<64, 1, 4, 128, 3, 2, 2>(p, pl.grid, s);
