@@ -13,10 +13,11 @@
 // them with log-sum-exp weights in the same launch (cooperative, so all CTAs are resident).
 //
 // Per CTA, warp roles:
-//   producer warp   TMA loads of Q (per piece) and K/V tiles into rings of STAGES K and
-//                   VST V stages (a single M tile with one P buffer spends the second
-//                   P buffer's room on a third V stage: V is held until P V completes,
-//                   K only until S = Q K^T does);
+//   producer warp   TMA loads of Q (per piece, QBUF buffers) and K/V tiles into rings
+//                   of STAGES K and VST V stages (a single M tile with one P buffer
+//                   spends the second P buffer's room on a third V stage -- V is held
+//                   until P V completes, K only until S = Q K^T does -- or on a
+//                   second Q buffer);
 //   MMA warp        one thread issues P V as soon as P is written and keeps S = Q K^T
 //                   two tiles ahead (S in TMEM, double buffered; O accumulates in TMEM);
 //   4*MT softmax warps, one thread per query row: read S from TMEM, mask, online
@@ -80,8 +81,8 @@ struct TcLayout {
   static constexpr int P_BYTES = PT ? 0 : MT * P_TILE;   // one P buffer (PBUF are used)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + QBUF * Q_BYTES;
-  // V stages: one more than K's when a single M tile keeps one P buffer
-  static constexpr int VST = (MT == 1 && PBUF == 1) ? STAGES + 1 : STAGES;
+  // V stages: one more than K's when a single M tile keeps one P buffer and one Q buffer
+  static constexpr int VST = (MT == 1 && PBUF == 1 && QBUF == 1) ? STAGES + 1 : STAGES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_P = OFF_V + VST * KV_BYTES;
   static constexpr int OFF_BAR = OFF_P + PBUF * P_BYTES;
@@ -1546,11 +1547,13 @@ cudaError_t launch_attention_tc(const AttnParams &a, const TcPlan &pl, void *ws,
   p.wait_ns = a.wait_ns;
   if (a.D == 128) {
     // One M tile: one P buffer, its room spent on a third V stage (ragged-paged 763 us
-    // against 775 with two P buffers; the other shapes time the same).  Two Q buffers paid
-    // for with the P buffer measured slower (the Q load is not the late one).
+    // against 775 with two P buffers) or, with two row copies, on a second Q buffer, so
+    // that the next piece's Q is loaded before the current piece ends (medusa-t64 66.7
+    // us against 68.2 with the third V stage; ragged-paged, four row copies, 774 against
+    // 764 the other way round).
     if (pl.MT == 2) return launch_tc_typed<128, 2, 1, 128, 2, 1, 1>(p, pl.grid, s);
     if (pl.CP == 4) return launch_tc_typed<128, 1, 4, 128, 2, 1, 1>(p, pl.grid, s);
-    if (pl.CP == 2) return launch_tc_typed<128, 1, 2, 128, 2, 1, 1>(p, pl.grid, s);
+    if (pl.CP == 2) return launch_tc_typed<128, 1, 2, 128, 2, 2, 1>(p, pl.grid, s);
     return launch_tc_typed<128, 1, 1, 128, 2, 1, 1>(p, pl.grid, s);
   }
   if (pl.MT == 2) return launch_tc_typed<64, 2, 1, 128, 4, 2, 1>(p, pl.grid, s);
