@@ -27,7 +27,9 @@
  *    on the stream is done.  With per-sequence trees the path and token outputs have N
  *    columns (the deepest possible path) instead of tree depth + 1.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only enqueue
- *    work and return without synchronising.
+ *    work and return without synchronising.  Each call that launches work opens an NVTX
+ *    range named after it (e.g. "sv_accept_chain_commit") for the duration of the host
+ *    call, so profiler timelines attribute the kernels to the call.
  *  - Arguments are validated on the host before anything is launched; a failed check
  *    returns SV_ERR_INVALID_ARG / SV_ERR_UNSUPPORTED / SV_ERR_WORKSPACE and launches
  *    nothing.  A launch failure returns SV_ERR_CUDA.  sv_last_error() gives the

@@ -6,6 +6,8 @@
 #include <cstring>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "sv_common.cuh"
 #include "sv_internal.h"
 
@@ -44,6 +46,16 @@ constexpr int kMaxDevices = 64;
 // The tensor-core attention kernel's limit on a wait for progress (sv_set_wait_limit_ns).
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
 std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+// An NVTX range named after the entry point for the duration of the host call, so that a
+// profiler's timeline (and ncu's --nvtx filters) show which call enqueued which kernels.
+// Without a profiler attached a push or a pop costs a few nanoseconds.
+struct CallRange {
+  explicit CallRange(const char *name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange &) = delete;
+  CallRange &operator=(const CallRange &) = delete;
+};
 
 // Device address of the status word on the current device (looked up once per device;
 // threads that race on the first lookup store the same address, atomically).
@@ -213,6 +225,7 @@ sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, c
                             const void *k_tree, const void *v_tree, sv_kv_cache cache,
                             const int32_t *parent, int parent_stride, float scale, void *out,
                             void *workspace, size_t workspace_bytes, void *stream) {
+  const CallRange range("sv_tree_attention");
   if (dt != SV_F32 && dt != SV_BF16) return fail(SV_ERR_UNSUPPORTED, "dtype %d not supported", (int)dt);
   if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
     return fail(SV_ERR_INVALID_ARG, "bad sizes B=%d Hq=%d Hkv=%d", B, Hq, Hkv);
@@ -479,6 +492,7 @@ sv_status sv_accept_chain(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int
                           int32_t *out_num_emitted, int32_t *out_num_accepted,
                           uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
                           void *stream) {
+  const CallRange range("sv_accept_chain");
   sv::AcceptParams p;
   bool greedy = false;
   sv_status st = chain_params(mode, logit_dt, B, gamma, V, target_logits, q, q_kind, draft_tokens,
@@ -496,6 +510,7 @@ sv_status sv_accept_tree(sv_mode mode, sv_dtype logit_dt, int B, int N, int V,
                          int32_t *out_num_emitted, int32_t *out_num_accepted,
                          uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
                          void *stream) {
+  const CallRange range("sv_accept_tree");
   sv::AcceptParams p;
   bool greedy = false;
   sv_status st = tree_params(mode, logit_dt, B, N, V, parent, parent_stride, node_tokens, target_logits, q,
@@ -515,6 +530,7 @@ sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const
                                    int32_t *out_num_emitted, int32_t *out_num_accepted,
                                    uint32_t *out_near_ties, void *workspace,
                                    size_t workspace_bytes, void *stream) {
+  const CallRange range("sv_accept_tree_recursive");
   sv::AcceptParams p;
   bool greedy = false;
   sv_status st = tree_params(SV_EXACT, logit_dt, B, N, V, parent, parent_stride, node_tokens, target_logits, q,
@@ -549,6 +565,7 @@ sv_status sv_accept_typical(sv_dtype logit_dt, int B, int N, int V, const int32_
                            int32_t *out_num_emitted, int32_t *out_num_accepted,
                            uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
                            void *stream) {
+  const CallRange range("sv_accept_typical");
   if (!(temperature > 0.f) || !std::isfinite(temperature))
     return fail(SV_ERR_INVALID_ARG, "typical acceptance needs a finite temperature > 0");
   if (!(epsilon >= 0.f) || !std::isfinite(epsilon) || !(delta >= 0.f) || !std::isfinite(delta))
@@ -589,6 +606,7 @@ sv_status sv_accept_chain_commit(sv_mode mode, sv_dtype logit_dt, int B, int gam
                                  int32_t *out_tokens, int32_t *out_num_emitted,
                                  int32_t *out_num_accepted, uint32_t *out_near_ties,
                                  void *workspace, size_t workspace_bytes, void *stream) {
+  const CallRange range("sv_accept_chain_commit");
   sv::AcceptParams p;
   bool greedy = false;
   sv_status st = chain_params(mode, logit_dt, B, gamma, V, target_logits, q, q_kind, draft_tokens,
@@ -611,6 +629,7 @@ sv_status sv_accept_tree_commit(sv_mode mode, sv_dtype logit_dt, int B, int N, i
                                 int32_t *out_num_emitted, int32_t *out_num_accepted,
                                 uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
                                 void *stream) {
+  const CallRange range("sv_accept_tree_commit");
   sv::AcceptParams p;
   bool greedy = false;
   sv_status st = tree_params(mode, logit_dt, B, N, V, parent, parent_stride, node_tokens, target_logits, q,
@@ -628,6 +647,7 @@ sv_status sv_accept_tree_commit(sv_mode mode, sv_dtype logit_dt, int B, int N, i
 sv_status sv_ngram_draft(int B, int Lmax, const int32_t *history, const int32_t *length,
                          int max_ngram, int min_ngram, int gamma, int32_t *out_drafts,
                          int32_t *out_num_drafts, void *stream) {
+  const CallRange range("sv_ngram_draft");
   if (B < 0 || Lmax < 1) return fail(SV_ERR_INVALID_ARG, "B = %d, Lmax = %d", B, Lmax);
   if (min_ngram < 1 || max_ngram < min_ngram || max_ngram > SV_MAX_NGRAM)
     return fail(SV_ERR_INVALID_ARG, "n-gram sizes %d..%d (1 <= min <= max <= %d)", min_ngram,
@@ -651,6 +671,7 @@ sv_status sv_ngram_draft(int B, int Lmax, const int32_t *history, const int32_t 
 sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_tree,
                        const void *v_tree, const int32_t *path_nodes, int path_stride,
                        const int32_t *num_accepted, sv_kv_cache cache, void *stream) {
+  const CallRange range("sv_commit_kv");
   if (path_stride < 1) return fail(SV_ERR_INVALID_ARG, "path_stride = %d", path_stride);
   if (!path_nodes || !num_accepted) return fail(SV_ERR_INVALID_ARG, "path_nodes or num_accepted is NULL");
   sv::CommitParams p;
@@ -731,6 +752,7 @@ extern "C" {
 
 sv_status sv_lm_head(int R, int Dm, int V, const void *hidden, const void *weight, void *logits,
                      void *stream) {
+  const CallRange range("sv_lm_head");
   sv_status st = lm_head_check(R, Dm, V, hidden, weight, logits);
   if (st != SV_OK) return st;
   unsigned int *status = status_word();
@@ -755,6 +777,7 @@ sv_status sv_accept_chain_lmhead(sv_mode mode, int B, int gamma, int V, int Dm, 
                                  int32_t *out_tokens, int32_t *out_num_emitted,
                                  int32_t *out_num_accepted, uint32_t *out_near_ties,
                                  void *workspace, size_t workspace_bytes, void *stream) {
+  const CallRange range("sv_accept_chain_lmhead");
   sv_status st = lm_head_check(B * (gamma + 1), Dm, V, hidden, weight, target_logits);
   if (st != SV_OK) return st;
   sv::AcceptParams p;
@@ -775,6 +798,7 @@ sv_status sv_accept_tree_lmhead(sv_mode mode, int B, int N, int V, int Dm, const
                                 int32_t *out_num_emitted, int32_t *out_num_accepted,
                                 uint32_t *out_near_ties, void *workspace, size_t workspace_bytes,
                                 void *stream) {
+  const CallRange range("sv_accept_tree_lmhead");
   sv_status st = lm_head_check(B * N, Dm, V, hidden, weight, target_logits);
   if (st != SV_OK) return st;
   sv::AcceptParams p;
@@ -835,6 +859,7 @@ sv_status sv_accept_tree_noalloc(sv_mode mode, sv_dtype logit_dt, int B, int N, 
                                  uint64_t round, int32_t *out_path_nodes, int32_t *out_tokens,
                                  int32_t *out_num_emitted, int32_t *out_num_accepted,
                                  uint32_t *out_near_ties, void *stream) {
+  const CallRange range("sv_accept_tree_noalloc");
   const bool greedy = mode == SV_GREEDY || temperature == 0.f;
   const long long rows = (long long)B * ((long long)N + (greedy ? 0 : (Dq > 0 ? Dq : 0)));
   if (rows > SV_NOALLOC_ACCEPT_ROWS)
