@@ -429,6 +429,14 @@ uint64_t sv_kernel_launches(void);
 void sv_set_wait_limit_ns(uint64_t ns);
 uint64_t sv_get_wait_limit_ns(void);
 
+/* Failure injection on the host, for tests of a caller's error handling: the next n kernel
+ * launch requests of the library (process-wide, each entry point's launches counted in
+ * order) report a launch failure instead of launching -- the call returns SV_ERR_CUDA with
+ * its message in sv_last_error(), and neither that launch nor any later one of the same
+ * call is enqueued (a call stops at its first failed launch).  No kernel runs and no GPU
+ * state changes.  n <= 0 clears the count. */
+void sv_inject_launch_failures(int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,7 @@ __all__ = [
     "sv_accept_workspace_size", "sv_accept_tree_noalloc", "sv_commit_kv", "sv_accept_tree_commit",
     "sv_accept_chain_commit", "sv_accept_tree_recursive", "sv_ngram_draft", "sv_tree_prepare", "sv_read_device_status",
     "sv_lm_head", "sv_accept_lmhead_workspace_size", "sv_accept_chain_lmhead", "sv_accept_tree_lmhead",
-    "sv_accept_typical", "sv_set_wait_limit_ns", "sv_get_wait_limit_ns",
+    "sv_accept_typical", "sv_set_wait_limit_ns", "sv_get_wait_limit_ns", "sv_inject_launch_failures",
     "sv_version", "sv_kernel_launches", "GREEDY", "EXACT", "Q_PROBS_F32", "Q_LOGITS", "Q_DRAFT_ONEHOT", "SV_MAX_TREE_NODES",
 ]
 
@@ -97,6 +97,8 @@ def load_library():
         lib.sv_set_wait_limit_ns.argtypes = [U64]
         lib.sv_set_wait_limit_ns.restype = None
         lib.sv_get_wait_limit_ns.restype = U64
+        lib.sv_inject_launch_failures.argtypes = [I]
+        lib.sv_inject_launch_failures.restype = None
         lib.sv_accept_typical.argtypes = [I, I, I, I, P, I, P, P, F, F, F, P, P, P, P, P, P, SZ, P]
         lib.sv_accept_lmhead_workspace_size.argtypes = [I, I, I, I]
         lib.sv_accept_lmhead_workspace_size.restype = SZ
@@ -545,6 +547,12 @@ def sv_set_wait_limit_ns(ns: int) -> None:
 
 def sv_get_wait_limit_ns() -> int:
     return int(load_library().sv_get_wait_limit_ns())
+
+
+def sv_inject_launch_failures(n: int) -> None:
+    """Test hook: the library's next n launch requests fail (SV_ERR_CUDA) without
+    launching; 0 clears."""
+    load_library().sv_inject_launch_failures(int(n))
 
 
 # ------------------------------------------------------------------- LM head

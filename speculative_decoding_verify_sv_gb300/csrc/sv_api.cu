@@ -47,6 +47,16 @@ constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
 std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 
+// Launch failures injected on the host (sv_inject_launch_failures): the next n launch
+// requests report cudaErrorLaunchFailure instead of launching.
+std::atomic<int> g_injected_failures{0};
+bool take_injected_failure() {
+  int n = g_injected_failures.load(std::memory_order_relaxed);
+  while (n > 0)
+    if (g_injected_failures.compare_exchange_weak(n, n - 1, std::memory_order_relaxed)) return true;
+  return false;
+}
+
 // An NVTX range named after the entry point for the duration of the host call, so that a
 // profiler's timeline (and ncu's --nvtx filters) show which call enqueued which kernels.
 // Without a profiler attached a push or a pop costs a few nanoseconds.
@@ -167,6 +177,8 @@ const char *sv_version(void) { return SV_VERSION_STRING; }
 
 uint64_t sv_kernel_launches(void) { return sv::g_launches.load(std::memory_order_relaxed); }
 
+void sv_inject_launch_failures(int n) { g_injected_failures.store(n > 0 ? n : 0, std::memory_order_relaxed); }
+
 void sv_set_wait_limit_ns(uint64_t ns) {
   g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : ns, std::memory_order_relaxed);
 }
@@ -285,14 +297,15 @@ sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, c
   p.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   cudaError_t e;
   if (use_tc) {
-    e = sv::launch_attention_tc(p, tplan, workspace, static_cast<cudaStream_t>(stream));
+    e = take_injected_failure() ? cudaErrorLaunchFailure
+                                  : sv::launch_attention_tc(p, tplan, workspace, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) sv::count_launches(1);
   } else {
     if (plan.ws_bytes > 0) {
       p.part_o = static_cast<float *>(workspace);
       p.part_ml = p.part_o + (size_t)B * Hkv * plan.splits * plan.Mpad * D;
     }
-    e = sv::launch_attention(dt, p, static_cast<cudaStream_t>(stream));
+    e = take_injected_failure() ? cudaErrorLaunchFailure : sv::launch_attention(dt, p, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) sv::count_launches(dt == SV_BF16 && plan.splits > 1 ? 2 : 1);
   }
   if (e != cudaSuccess) return cuda_fail(e, "tree attention launch");
@@ -355,7 +368,8 @@ sv_status accept_launch(sv_dtype dt, sv::AcceptParams &p, bool greedy, void *wor
   if (greedy) p.top_p = 1.f;
   p.stats = static_cast<sv::RowStat *>(workspace);
   if (p.B == 0) return SV_OK;
-  cudaError_t e = sv::launch_accept(dt, p, num_sms(), static_cast<cudaStream_t>(stream));
+  cudaError_t e = take_injected_failure() ? cudaErrorLaunchFailure
+                                          : sv::launch_accept(dt, p, num_sms(), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "acceptance launch");
   sv::count_launches(2);
   return SV_OK;
@@ -552,7 +566,8 @@ sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const
   if (p.top_k >= p.V) p.top_k = 0;
   p.stats = static_cast<sv::RowStat *>(workspace);
   if (p.B == 0) return SV_OK;
-  cudaError_t e = sv::launch_accept_recursive(logit_dt, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = take_injected_failure() ? cudaErrorLaunchFailure
+                                          : sv::launch_accept_recursive(logit_dt, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "recursive tree acceptance launch");
   sv::count_launches(2);
   return SV_OK;
@@ -592,7 +607,8 @@ sv_status sv_accept_typical(sv_dtype logit_dt, int B, int N, int V, const int32_
   p.c_log2 = (float)(1.4426950408889634 / (double)temperature);
   p.stats = static_cast<sv::RowStat *>(workspace);
   if (p.B == 0) return SV_OK;
-  cudaError_t e = sv::launch_accept(logit_dt, p, num_sms(), static_cast<cudaStream_t>(stream));
+  cudaError_t e = take_injected_failure() ? cudaErrorLaunchFailure
+                                          : sv::launch_accept(logit_dt, p, num_sms(), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "typical acceptance launch");
   sv::count_launches(2);
   return SV_OK;
@@ -660,7 +676,8 @@ sv_status sv_ngram_draft(int B, int Lmax, const int32_t *history, const int32_t 
                     out_num_drafts, status_word()};
   if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
   if (B == 0) return SV_OK;
-  const cudaError_t e = sv::launch_ngram(p, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = take_injected_failure() ? cudaErrorLaunchFailure
+                                                : sv::launch_ngram(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "n-gram draft launch");
   sv::count_launches(1);
   return SV_OK;
@@ -681,7 +698,7 @@ sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_
   p.path_nodes = path_nodes;
   p.path_stride = path_stride;
   p.num_accepted = num_accepted;
-  cudaError_t e = sv::launch_commit(p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = take_injected_failure() ? cudaErrorLaunchFailure : sv::launch_commit(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "commit launch");
   sv::count_launches(1);
   return SV_OK;
@@ -729,17 +746,17 @@ sv_status lm_head_accept_launch(sv::AcceptParams &p, bool greedy, int Dm, const 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool epilogue_stats = greedy || p.top_k == 0;  // (top_p < 1 needs top-k)
   void *part = static_cast<uint8_t *>(workspace) + st_bytes;
-  cudaError_t e = sv::launch_lm_head(hidden, weight, p.B * p.N, Dm, p.V, p.c_log2,
+  cudaError_t e = take_injected_failure() ? cudaErrorLaunchFailure : sv::launch_lm_head(hidden, weight, p.B * p.N, Dm, p.V, p.c_log2,
                                      const_cast<void *>(p.target), epilogue_stats ? part : nullptr,
                                      epilogue_stats ? p.stats : nullptr, p.status, num_sms(), s);
   if (e != cudaSuccess) return cuda_fail(e, "LM-head projection launch");
   sv::count_launches(epilogue_stats ? 2 : 1);
   if (epilogue_stats) {
-    e = sv::launch_accept_given_target_stats(SV_BF16, p, num_sms(), s);
+    e = take_injected_failure() ? cudaErrorLaunchFailure : sv::launch_accept_given_target_stats(SV_BF16, p, num_sms(), s);
     const bool q_stats = !greedy && p.q_kind == SV_Q_LOGITS && p.Dq > 0;
     if (e == cudaSuccess) sv::count_launches(q_stats ? 2 : 1);
   } else {
-    e = sv::launch_accept(SV_BF16, p, num_sms(), s);
+    e = take_injected_failure() ? cudaErrorLaunchFailure : sv::launch_accept(SV_BF16, p, num_sms(), s);
     if (e == cudaSuccess) sv::count_launches(2);
   }
   if (e != cudaSuccess) return cuda_fail(e, "acceptance launch");
@@ -758,7 +775,7 @@ sv_status sv_lm_head(int R, int Dm, int V, const void *hidden, const void *weigh
   unsigned int *status = status_word();
   if (!status) return fail(SV_ERR_CUDA, "no CUDA device");
   if (R == 0) return SV_OK;
-  cudaError_t e = sv::launch_lm_head(hidden, weight, R, Dm, V, 0.f, logits, nullptr, nullptr,
+  cudaError_t e = take_injected_failure() ? cudaErrorLaunchFailure : sv::launch_lm_head(hidden, weight, R, Dm, V, 0.f, logits, nullptr, nullptr,
                                      status, num_sms(), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "LM-head projection launch");
   sv::count_launches(1);
