@@ -356,7 +356,15 @@ def time_workload(args, dist: Dist, cfg_id: int, K: int, warmup: int, preheat_s:
     acc = [e[1].elapsed_time(e[2]) for e in evs]
     tc = sv.sv_tree_attention_path(c["dtype"], w["N"], c["Hq"], c["Hkv"], c["D"],
                                    w.get("block_size", 16) if c["paged"] else 0) == 1
-    return dict(w=w, c=c, step=step, toks=toks, prepare=prepare, stream=stream,
+    # every timed step verifies the same inputs with the same round: the last step's
+    # accepted lengths and near-tie words are those of every step
+    na = step.outs["num_accepted"].cpu().to(torch.int64)
+    nt = step.outs["near_ties"].cpu().to(torch.int64) & 0xFFFFFFFF
+    outcome = dict(
+        accepted_length_histogram=torch.bincount(na.clamp(0, w["Dmax"]), minlength=w["Dmax"] + 1).tolist(),
+        sequences_with_decision_near_ties=int(((nt & 0xFFFF) > 0).sum()),
+        sequences_with_sample_near_ties=int(((nt >> 16) > 0).sum()))
+    return dict(w=w, c=c, step=step, toks=toks, prepare=prepare, stream=stream, outcome=outcome,
                 mode=mode, mode_name=mode_name, launch_mode=launch_mode, tot=tot, att=att,
                 acc=acc, wall=wall, launches=launches, clocks=clocks, status=status,
                 emitted=float(emitted.sum().item()), a_bytes=a_bytes, a_flops=a_flops,
@@ -633,6 +641,8 @@ def run_ours(args, dist: Dist):
         },
         "emitted_tokens_per_s": emitted_total / (dev_ms / 1e3),
         "mean_accepted": emitted_total / (c["B"] * K * dist.world) - 1.0,
+        "outcome_per_step": dict(r["outcome"], note="sequences of one step (rank 0); every timed "
+                                 "step verifies the same inputs with the same round"),
         "acceptance_rate": (emitted_total / (c["B"] * K * dist.world) - 1.0) / max(1, w["Dmax"]),
         "wall_s_timed_region": r["wall"],
         "gpu_launches": r["launches"],
