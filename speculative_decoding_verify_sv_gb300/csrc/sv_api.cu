@@ -154,9 +154,10 @@ int max_prefix_of(const sv_kv_cache &c) {
   return c.block_table ? c.max_blocks * c.block_size : c.Lmax;
 }
 
-sv_status check_cache(const sv_kv_cache &c, bool writable) {
+sv_status check_cache(const sv_kv_cache &c, bool writable, int B) {
   (void)writable;
-  if (!c.k || !c.v || !c.prefix_len) return fail(SV_ERR_INVALID_ARG, "cache k, v or prefix_len is NULL");
+  if (B > 0 && (!c.k || !c.v || !c.prefix_len))
+    return fail(SV_ERR_INVALID_ARG, "cache k, v or prefix_len is NULL");
   if (!aligned16(c.k) || !aligned16(c.v)) return fail(SV_ERR_INVALID_ARG, "cache k/v not 16-byte aligned");
   if (c.block_table) {
     if (c.block_size < 1 || c.max_blocks < 1 || c.num_blocks < 1)
@@ -245,10 +246,11 @@ sv_status sv_tree_attention(sv_dtype dt, int B, int N, int Hq, int Hkv, int D, c
   sv::Tree tree;
   sv_status st = tree_arg(N, parent, parent_stride, &tree);
   if (st != SV_OK) return st;
-  if (!q || !k_tree || !v_tree || !out) return fail(SV_ERR_INVALID_ARG, "q, k_tree, v_tree or out is NULL");
+  if (B > 0 && (!q || !k_tree || !v_tree || !out))
+    return fail(SV_ERR_INVALID_ARG, "q, k_tree, v_tree or out is NULL");
   if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(out))
     return fail(SV_ERR_INVALID_ARG, "q, k_tree, v_tree and out must be 16-byte aligned");
-  if ((st = check_cache(cache, false)) != SV_OK) return st;
+  if ((st = check_cache(cache, false, B)) != SV_OK) return st;
   if (!std::isfinite(scale)) return fail(SV_ERR_INVALID_ARG, "scale is not finite");
   if (B == 0) return SV_OK;
   const int max_prefix = max_prefix_of(cache);
@@ -339,17 +341,17 @@ sv_status accept_common(sv_mode mode, sv_dtype dt, int B, int V, const void *tar
   *greedy = mode == SV_GREEDY || temperature == 0.f;
   if (!*greedy && top_p < 1.f && !(top_k > 0 && top_k < V))
     return fail(SV_ERR_UNSUPPORTED, "top_p < 1 is applied within top-k: needs 0 < top_k < V");
-  if (!target) return fail(SV_ERR_INVALID_ARG, "target_logits is NULL");
+  if (B > 0 && !target) return fail(SV_ERR_INVALID_ARG, "target_logits is NULL");
   if (!aligned16(target)) return fail(SV_ERR_INVALID_ARG, "target_logits not 16-byte aligned");
   if (!*greedy) {
     if (q_kind != SV_Q_PROBS_F32 && q_kind != SV_Q_LOGITS && q_kind != SV_Q_DRAFT_ONEHOT)
       return fail(SV_ERR_INVALID_ARG, "q_kind %d", (int)q_kind);
     if (q_kind != SV_Q_DRAFT_ONEHOT) {  // one-hot drafts have no q rows
-      if (!q) return fail(SV_ERR_INVALID_ARG, "q is NULL in exact mode");
+      if (B > 0 && !q) return fail(SV_ERR_INVALID_ARG, "q is NULL in exact mode");
       if (!aligned16(q)) return fail(SV_ERR_INVALID_ARG, "q not 16-byte aligned");
     }
   }
-  if (!out_tokens || !out_num_emitted || !out_num_accepted)
+  if (B > 0 && (!out_tokens || !out_num_emitted || !out_num_accepted))
     return fail(SV_ERR_INVALID_ARG, "an output pointer is NULL");
   return SV_OK;
 }
@@ -357,7 +359,7 @@ sv_status accept_common(sv_mode mode, sv_dtype dt, int B, int V, const void *tar
 sv_status accept_launch(sv_dtype dt, sv::AcceptParams &p, bool greedy, void *workspace,
                         size_t workspace_bytes, void *stream) {
   const size_t need = sv::accept_ws_bytes(p.B, p.N, p.Dq);
-  if (!workspace || workspace_bytes < need)
+  if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(SV_ERR_WORKSPACE, "acceptance workspace %zu bytes, need %zu", workspace_bytes, need);
   if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
   p.status = status_word();
@@ -390,7 +392,7 @@ sv_status chain_params(sv_mode mode, sv_dtype logit_dt, int B, int gamma, int V,
   if (st != SV_OK) return st;
   if (gamma < 1 || gamma >= SV_MAX_TREE_NODES)
     return fail(SV_ERR_UNSUPPORTED, "gamma = %d (supported 1..%d)", gamma, SV_MAX_TREE_NODES - 1);
-  if (!draft_tokens) return fail(SV_ERR_INVALID_ARG, "draft_tokens is NULL");
+  if (B > 0 && !draft_tokens) return fail(SV_ERR_INVALID_ARG, "draft_tokens is NULL");
   int32_t parent[SV_MAX_TREE_NODES];
   for (int i = 0; i <= gamma; ++i) parent[i] = i - 1;
   p = sv::AcceptParams{};
@@ -430,8 +432,8 @@ sv_status tree_params(sv_mode mode, sv_dtype logit_dt, int B, int N, int V, cons
   if (st != SV_OK) return st;
   p = sv::AcceptParams{};
   if ((st = tree_arg(N, parent, parent_stride, &p.tree)) != SV_OK) return st;
-  if (!node_tokens) return fail(SV_ERR_INVALID_ARG, "node_tokens is NULL");
-  if (!out_path_nodes) return fail(SV_ERR_INVALID_ARG, "out_path_nodes is NULL");
+  if (B > 0 && !node_tokens) return fail(SV_ERR_INVALID_ARG, "node_tokens is NULL");
+  if (B > 0 && !out_path_nodes) return fail(SV_ERR_INVALID_ARG, "out_path_nodes is NULL");
   if (!*greedy && !p.tree.rows && Dq < p.tree.Dmax)  // (per-sequence trees: checked on the device)
     return fail(SV_ERR_INVALID_ARG, "q has %d depth rows, the tree is %d deep", Dq, p.tree.Dmax);
   if (!*greedy && p.tree.rows && Dq < 1 && N > 1)
@@ -472,9 +474,9 @@ sv_status commit_params(sv_dtype dt, int B, int N, int Hkv, int D, const void *k
   const int esize = dt == SV_F32 ? 4 : 2;
   if (((size_t)Hkv * D * esize) % 16 != 0)
     return fail(SV_ERR_UNSUPPORTED, "Hkv*D*elem bytes must be a multiple of 16");
-  if (!k_tree || !v_tree) return fail(SV_ERR_INVALID_ARG, "k_tree or v_tree is NULL");
+  if (B > 0 && (!k_tree || !v_tree)) return fail(SV_ERR_INVALID_ARG, "k_tree or v_tree is NULL");
   if (!aligned16(k_tree) || !aligned16(v_tree)) return fail(SV_ERR_INVALID_ARG, "k_tree/v_tree not 16-byte aligned");
-  sv_status st = check_cache(cache, true);
+  sv_status st = check_cache(cache, true, B);
   if (st != SV_OK) return st;
   p = sv::CommitParams{};
   p.k_tree = k_tree;
@@ -556,7 +558,7 @@ sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const
     return fail(SV_ERR_UNSUPPORTED,
                 "siblings tried in turn need temperature > 0 (greedy: sv_accept_tree)");
   const size_t need = sv::accept_ws_bytes(p.B, p.N, p.Dq);
-  if (!workspace || workspace_bytes < need)
+  if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(SV_ERR_WORKSPACE, "acceptance workspace %zu bytes, need %zu", workspace_bytes, need);
   if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
   p.status = status_word();
@@ -594,7 +596,7 @@ sv_status sv_accept_typical(sv_dtype logit_dt, int B, int N, int V, const int32_
                              out_near_ties, p, &greedy);
   if (st != SV_OK) return st;
   const size_t need = sv::accept_ws_bytes(p.B, p.N, 0);
-  if (!workspace || workspace_bytes < need)
+  if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(SV_ERR_WORKSPACE, "acceptance workspace %zu bytes, need %zu", workspace_bytes, need);
   if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
   p.status = status_word();
@@ -670,7 +672,7 @@ sv_status sv_ngram_draft(int B, int Lmax, const int32_t *history, const int32_t 
                 max_ngram, SV_MAX_NGRAM);
   if (gamma < 1 || gamma >= SV_MAX_TREE_NODES)
     return fail(SV_ERR_UNSUPPORTED, "gamma = %d (supported 1..%d)", gamma, SV_MAX_TREE_NODES - 1);
-  if (!history || !length || !out_drafts || !out_num_drafts)
+  if (B > 0 && (!history || !length || !out_drafts || !out_num_drafts))
     return fail(SV_ERR_INVALID_ARG, "a pointer argument is NULL");
   sv::NgramParams p{history, length, B, Lmax, max_ngram, min_ngram, gamma, out_drafts,
                     out_num_drafts, status_word()};
@@ -690,7 +692,8 @@ sv_status sv_commit_kv(sv_dtype dt, int B, int N, int Hkv, int D, const void *k_
                        const int32_t *num_accepted, sv_kv_cache cache, void *stream) {
   const CallRange range("sv_commit_kv");
   if (path_stride < 1) return fail(SV_ERR_INVALID_ARG, "path_stride = %d", path_stride);
-  if (!path_nodes || !num_accepted) return fail(SV_ERR_INVALID_ARG, "path_nodes or num_accepted is NULL");
+  if (B > 0 && (!path_nodes || !num_accepted))
+    return fail(SV_ERR_INVALID_ARG, "path_nodes or num_accepted is NULL");
   sv::CommitParams p;
   sv_status st = commit_params(dt, B, N, Hkv, D, k_tree, v_tree, cache, p);
   if (st != SV_OK) return st;
@@ -718,7 +721,8 @@ sv_status lm_head_check(int R, int Dm, int V, const void *hidden, const void *we
   if (Dm < 8 || Dm % 8 != 0)
     return fail(SV_ERR_UNSUPPORTED, "hidden size %d must be a positive multiple of 8", Dm);
   if (V < 8 || V % 8 != 0) return fail(SV_ERR_UNSUPPORTED, "V = %d must be a positive multiple of 8", V);
-  if (!hidden || !weight || !logits) return fail(SV_ERR_INVALID_ARG, "hidden, weight or logits is NULL");
+  if (R > 0 && (!hidden || !weight || !logits))
+    return fail(SV_ERR_INVALID_ARG, "hidden, weight or logits is NULL");
   if (!aligned16(hidden) || !aligned16(weight) || !aligned16(logits))
     return fail(SV_ERR_INVALID_ARG, "hidden, weight and logits must be 16-byte aligned");
   return SV_OK;
@@ -732,7 +736,7 @@ sv_status lm_head_accept_launch(sv::AcceptParams &p, bool greedy, int Dm, const 
                                 void *stream) {
   const size_t st_bytes = up256(sv::accept_ws_bytes(p.B, p.N, p.Dq));
   const size_t need = st_bytes + sv::lm_head_part_bytes(p.B * p.N, p.V);
-  if (!workspace || workspace_bytes < need)
+  if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(SV_ERR_WORKSPACE, "LM-head acceptance workspace %zu bytes, need %zu", workspace_bytes, need);
   if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
   p.status = status_word();
