@@ -33,8 +33,8 @@
  *  - Arguments are validated on the host before anything is launched; a failed check
  *    returns SV_ERR_INVALID_ARG / SV_ERR_UNSUPPORTED / SV_ERR_WORKSPACE and launches
  *    nothing.  An empty batch (B = 0, or R = 0 rows for sv_lm_head) validates the other
- *    arguments and returns SV_OK without launching or reading any tensor: its tensor
- *    pointers and workspace may be NULL.  A launch failure returns SV_ERR_CUDA.  sv_last_error() gives the
+ *    arguments and returns SV_OK without launching, reading any tensor or calling the
+ *    CUDA runtime: its tensor pointers and workspace may be NULL.  A launch failure returns SV_ERR_CUDA.  sv_last_error() gives the
  *    message of the last failure in the calling thread.
  *  - Data-dependent problems found on the device (a token id outside [0,V), a block
  *    id outside the pool, a prefix longer than the cache, a draft with q(x) = 0) never

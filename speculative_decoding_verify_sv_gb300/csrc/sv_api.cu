@@ -362,6 +362,7 @@ sv_status accept_launch(sv_dtype dt, sv::AcceptParams &p, bool greedy, void *wor
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(SV_ERR_WORKSPACE, "acceptance workspace %zu bytes, need %zu", workspace_bytes, need);
   if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  if (p.B == 0) return SV_OK;  // an empty batch: nothing to launch, no device needed
   p.status = status_word();
   if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
   p.mode = greedy ? SV_GREEDY : SV_EXACT;
@@ -369,7 +370,6 @@ sv_status accept_launch(sv_dtype dt, sv::AcceptParams &p, bool greedy, void *wor
   if (p.top_k >= p.V) p.top_k = 0;
   if (greedy) p.top_p = 1.f;
   p.stats = static_cast<sv::RowStat *>(workspace);
-  if (p.B == 0) return SV_OK;
   cudaError_t e = take_injected_failure() ? cudaErrorLaunchFailure
                                           : sv::launch_accept(dt, p, num_sms(), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "acceptance launch");
@@ -494,6 +494,7 @@ sv_status commit_params(sv_dtype dt, int B, int N, int Hkv, int D, const void *k
   p.block_size = cache.block_size;
   p.max_blocks = cache.max_blocks;
   p.num_blocks = cache.num_blocks;
+  if (B == 0) return SV_OK;  // an empty batch launches nothing: no device needed
   p.status = status_word();
   if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
   return SV_OK;
@@ -561,13 +562,13 @@ sv_status sv_accept_tree_recursive(sv_dtype logit_dt, int B, int N, int V, const
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(SV_ERR_WORKSPACE, "acceptance workspace %zu bytes, need %zu", workspace_bytes, need);
   if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  if (p.B == 0) return SV_OK;  // an empty batch: nothing to launch, no device needed
   p.status = status_word();
   if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
   p.mode = SV_EXACT;
   p.c_log2 = (float)(1.4426950408889634 / (double)p.temperature);
   if (p.top_k >= p.V) p.top_k = 0;
   p.stats = static_cast<sv::RowStat *>(workspace);
-  if (p.B == 0) return SV_OK;
   cudaError_t e = take_injected_failure() ? cudaErrorLaunchFailure
                                           : sv::launch_accept_recursive(logit_dt, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "recursive tree acceptance launch");
@@ -599,6 +600,7 @@ sv_status sv_accept_typical(sv_dtype logit_dt, int B, int N, int V, const int32_
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(SV_ERR_WORKSPACE, "acceptance workspace %zu bytes, need %zu", workspace_bytes, need);
   if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  if (p.B == 0) return SV_OK;  // an empty batch: nothing to launch, no device needed
   p.status = status_word();
   if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
   p.mode = SV_GREEDY;
@@ -608,7 +610,6 @@ sv_status sv_accept_typical(sv_dtype logit_dt, int B, int N, int V, const int32_
   p.temperature = temperature;
   p.c_log2 = (float)(1.4426950408889634 / (double)temperature);
   p.stats = static_cast<sv::RowStat *>(workspace);
-  if (p.B == 0) return SV_OK;
   cudaError_t e = take_injected_failure() ? cudaErrorLaunchFailure
                                           : sv::launch_accept(logit_dt, p, num_sms(), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "typical acceptance launch");
@@ -674,10 +675,10 @@ sv_status sv_ngram_draft(int B, int Lmax, const int32_t *history, const int32_t 
     return fail(SV_ERR_UNSUPPORTED, "gamma = %d (supported 1..%d)", gamma, SV_MAX_TREE_NODES - 1);
   if (B > 0 && (!history || !length || !out_drafts || !out_num_drafts))
     return fail(SV_ERR_INVALID_ARG, "a pointer argument is NULL");
+  if (B == 0) return SV_OK;  // an empty batch: nothing to launch, no device needed
   sv::NgramParams p{history, length, B, Lmax, max_ngram, min_ngram, gamma, out_drafts,
                     out_num_drafts, status_word()};
   if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
-  if (B == 0) return SV_OK;
   const cudaError_t e = take_injected_failure() ? cudaErrorLaunchFailure
                                                 : sv::launch_ngram(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "n-gram draft launch");
@@ -739,6 +740,7 @@ sv_status lm_head_accept_launch(sv::AcceptParams &p, bool greedy, int Dm, const 
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(SV_ERR_WORKSPACE, "LM-head acceptance workspace %zu bytes, need %zu", workspace_bytes, need);
   if (!aligned16(workspace)) return fail(SV_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  if (p.B == 0) return SV_OK;  // an empty batch: nothing to launch, no device needed
   p.status = status_word();
   if (!p.status) return fail(SV_ERR_CUDA, "no CUDA device");
   p.mode = greedy ? SV_GREEDY : SV_EXACT;
@@ -746,7 +748,6 @@ sv_status lm_head_accept_launch(sv::AcceptParams &p, bool greedy, int Dm, const 
   if (p.top_k >= p.V) p.top_k = 0;
   if (greedy) p.top_p = 1.f;
   p.stats = static_cast<sv::RowStat *>(workspace);
-  if (p.B == 0) return SV_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool epilogue_stats = greedy || p.top_k == 0;  // (top_p < 1 needs top-k)
   void *part = static_cast<uint8_t *>(workspace) + st_bytes;
@@ -776,9 +777,9 @@ sv_status sv_lm_head(int R, int Dm, int V, const void *hidden, const void *weigh
   const CallRange range("sv_lm_head");
   sv_status st = lm_head_check(R, Dm, V, hidden, weight, logits);
   if (st != SV_OK) return st;
+  if (R == 0) return SV_OK;  // no rows: nothing to launch, no device needed
   unsigned int *status = status_word();
   if (!status) return fail(SV_ERR_CUDA, "no CUDA device");
-  if (R == 0) return SV_OK;
   cudaError_t e = take_injected_failure() ? cudaErrorLaunchFailure : sv::launch_lm_head(hidden, weight, R, Dm, V, 0.f, logits, nullptr, nullptr,
                                      status, num_sms(), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "LM-head projection launch");
@@ -889,12 +890,15 @@ sv_status sv_accept_tree_noalloc(sv_mode mode, sv_dtype logit_dt, int B, int N, 
                 "%d rows; use sv_accept_tree with a workspace",
                 rows, SV_NOALLOC_ACCEPT_ROWS);
   sv_status st = SV_OK;
-  void *scratch = noalloc_rows_address(&st);
-  if (!scratch) return st;
+  void *scratch = nullptr;  // (an empty batch needs none, and no device)
+  if (B > 0) {
+    scratch = noalloc_rows_address(&st);
+    if (!scratch) return st;
+  }
   return sv_accept_tree(mode, logit_dt, B, N, V, parent, parent_stride, node_tokens, target_logits, q, q_kind,
                         Dq, temperature, top_k, top_p, seed, round, out_path_nodes, out_tokens,
                         out_num_emitted, out_num_accepted, out_near_ties, scratch,
-                        sizeof(g_sv_noalloc_rows), stream);
+                        scratch ? sizeof(g_sv_noalloc_rows) : 0, stream);
 }
 
 }  // extern "C"

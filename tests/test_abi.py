@@ -234,3 +234,52 @@ def test_wait_limit_is_settable_and_restored(lib):
     assert sv.sv_get_wait_limit_ns() == 1234
     sv.sv_set_wait_limit_ns(0)  # 0 restores the default
     assert sv.sv_get_wait_limit_ns() == default
+
+
+def test_empty_batch_needs_no_device(lib):
+    """B = 0 sequences (R = 0 rows for the projection): every entry point that launches work
+    validates its other arguments and returns SV_OK with NULL tensors and no workspace,
+    before any CUDA runtime call (this runs on a machine without a GPU)."""
+    par = (ctypes.c_int32 * 3)(-1, 0, 0)
+    E, G, BF, QL = sv.EXACT, sv.GREEDY, sv.SV_BF16, sv.Q_LOGITS
+    empty_cache = _cache(k=None, v=None, prefix_len=None)
+    calls = {
+        "sv_tree_attention": lambda: lib.sv_tree_attention(BF, 0, 3, 8, 2, 128, None, None, None,
+                                                           empty_cache, par, 0, 0.1, None, None, 0, None),
+        "sv_accept_chain": lambda: lib.sv_accept_chain(E, BF, 0, 4, 1000, None, None, QL, None, 1.0, 0,
+                                                       1.0, 0, 0, None, None, None, None, None, 0, None),
+        "sv_accept_tree": lambda: lib.sv_accept_tree(E, BF, 0, 3, 1000, par, 0, None, None, None, QL, 1,
+                                                     1.0, 0, 1.0, 0, 0, None, None, None, None, None,
+                                                     None, 0, None),
+        "sv_accept_tree_noalloc": lambda: lib.sv_accept_tree_noalloc(
+            G, BF, 0, 3, 1000, par, 0, None, None, None, QL, 1, 1.0, 0, 1.0, 0, 0, None, None, None,
+            None, None, None),
+        "sv_accept_tree_recursive": lambda: lib.sv_accept_tree_recursive(
+            BF, 0, 3, 1000, par, 0, None, None, None, QL, 1, 1.0, 0, 1.0, 0, 0, None, None, None, None,
+            None, None, 0, None),
+        "sv_accept_typical": lambda: lib.sv_accept_typical(BF, 0, 3, 1000, par, 0, None, None, 1.0, 0.3,
+                                                           0.09, None, None, None, None, None, None, 0,
+                                                           None),
+        "sv_commit_kv": lambda: lib.sv_commit_kv(BF, 0, 3, 2, 128, None, None, None, 2, None,
+                                                 empty_cache, None),
+        "sv_accept_tree_commit": lambda: lib.sv_accept_tree_commit(
+            E, BF, 0, 3, 1000, par, 0, None, None, None, QL, 1, 1.0, 0, 1.0, 0, 0, BF, 2, 128, None, None,
+            empty_cache, None, None, None, None, None, None, 0, None),
+        "sv_accept_chain_commit": lambda: lib.sv_accept_chain_commit(
+            E, BF, 0, 4, 1000, None, None, QL, None, 1.0, 0, 1.0, 0, 0, BF, 2, 128, None, None,
+            empty_cache, None, None, None, None, None, 0, None),
+        "sv_ngram_draft": lambda: lib.sv_ngram_draft(0, 256, None, None, 3, 1, 4, None, None, None),
+        "sv_lm_head": lambda: lib.sv_lm_head(0, 128, 1024, None, None, None, None),
+        "sv_accept_chain_lmhead": lambda: lib.sv_accept_chain_lmhead(
+            E, 0, 4, 1024, 128, None, None, None, None, QL, None, 1.0, 0, 1.0, 0, 0, None, None, None,
+            None, None, 0, None),
+        "sv_accept_tree_lmhead": lambda: lib.sv_accept_tree_lmhead(
+            E, 0, 3, 1024, 128, None, None, None, par, 0, None, None, QL, 1, 1.0, 0, 1.0, 0, 0, None,
+            None, None, None, None, None, 0, None),
+    }
+    for name, call in calls.items():
+        assert call() == sv.SV_OK, (name, lib.sv_last_error().decode())
+    # the other arguments are still checked: a bad V with B = 0 is refused
+    assert lib.sv_accept_chain(E, BF, 0, 4, 1001, None, None, QL, None, 1.0, 0, 1.0, 0, 0, None, None,
+                               None, None, None, 0, None) == sv.SV_ERR_UNSUPPORTED
+    assert lib.sv_ngram_draft(0, 256, None, None, 3, 1, 0, None, None, None) == sv.SV_ERR_UNSUPPORTED
