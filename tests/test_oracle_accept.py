@@ -301,6 +301,32 @@ def test_all_argmax_drafts_give_bonus_argmax():
     assert torch.equal(out["tokens"], am)
 
 
+
+@pytest.mark.parametrize("T", [1.0, 0.5])
+def test_exact_with_top_1_is_greedy(T):
+    """Exact sampling with top-k = 1 on both sides is greedy decoding: p and q are point
+    masses at their argmaxes, so the drafter proposes q's argmax, the ratio p(x)/q(x) is 1 or
+    0 (accepted iff x is p's argmax, for every uniform), and the residual [p - q]+ of a
+    rejection, like the bonus, is p's argmax.  No decision or sample is a near tie."""
+    B, gamma, V = 48, 4, 64
+    g = torch.Generator().manual_seed(12)
+    tl = torch.randn(B, gamma + 1, V, generator=g) * 3
+    dl = torch.randn(B, gamma, V, generator=g) * 3
+    # the draft row agrees with the target's argmax for a seeded number of positions
+    keep = torch.randint(0, gamma + 1, (B,), generator=g)
+    am = tl.argmax(-1)
+    for b in range(B):
+        for i in range(int(keep[b])):
+            dl[b, i, am[b, i]] = dl[b, i].max() + 1.0
+    toks = dl.argmax(-1).int()
+    ex = oracle.accept_chain(oracle.EXACT, tl, dl, oracle.Q_LOGITS, toks, temperature=T, top_k=1,
+                             seed=5, round_=3)
+    gr = oracle.accept_chain(oracle.GREEDY, tl, None, oracle.Q_LOGITS, toks)
+    for k in ("tokens", "num_emitted", "num_accepted"):
+        assert torch.equal(ex[k], gr[k]), k
+    assert int(ex["near_ties"].sum()) == 0
+    assert sorted(set(ex["num_accepted"].tolist())) == list(range(gamma + 1))
+
 # ------------------------------------------------- ratio and sampling formulas
 
 def test_ratio_orientation_and_residual():
